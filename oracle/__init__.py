@@ -1,0 +1,14 @@
+"""CPU oracle for the MX block-scaled NT GEMM.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the CPU-baseline leg of ``bench.py``.  The product path (the package
+``mx_block_scaled_gb300``) never imports it, and it never imports the package.
+"""
+from .mxref import (  # noqa: F401
+    FMT_MXFP8,
+    FMT_MXFP4,
+    build,
+    decode_table,
+    gemm,
+    num_threads,
+)

@@ -1,0 +1,224 @@
+/*
+ * mxref.c -- CPU oracle for the MX block-scaled NT GEMM.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the tests, the package's smoke check and the bench's
+ * CPU-baseline leg do.  It shares no code, table or header with the CUDA path.
+ *
+ * What it computes (the plain definition, written out):
+ *
+ *   C[m,n] = sum_{j=0}^{K/32-1} 2^(SA[m,j]-127) * 2^(SB[n,j]-127)
+ *                               * sum_{t=0}^{31} dec(A[m,32j+t]) * dec(B[n,32j+t])
+ *
+ *   S[m,n] = the same sum with every product replaced by its absolute value
+ *            (the scale of the rounding-error bound used by the parity tests).
+ *
+ * Sources:
+ *  - "Accelerating PyTorch on AMD GPUs with FlyDSL" (English digest), section
+ *    "API compatibility is not universal input coverage": MXFP scaled GEMM takes
+ *    one E8M0 scale per 32 values along K, and K divisible by 128.
+ *  - AI-compiler daily digest of 2026-10-22, item 1 (FlyDSL): MXFP8/MXFP4 scaled
+ *    GEMM is "BlockWise1x32, E8M0 scale, FP32 accumulation".
+ *  - Same digest, item 2 ("Deciding Scale Placement in MXFP4 Dot Products"):
+ *    applying the scale before or after the dot product can round differently.
+ *    This oracle evaluates each 32-block's inner sum exactly (see below), so both
+ *    placements give the same value here and no placement choice is made.
+ *  - The element formats (OCP MX): E4M3 for MXFP8, E2M1 (two codes per byte)
+ *    for MXFP4, E8M0 scales with code 0xFF = NaN.  The pages name only "MXFP8"
+ *    and "MXFP4"; these encodings are the reading this build takes.
+ *
+ * Exactness: an E4M3 product has at most 8 significant bits and lies in
+ * [2^-18, 448^2]; an E2M1 product is a multiple of 1/4 of magnitude <= 36.  Any
+ * 32-term sum of such products is exact in binary64, and so is its scaling by a
+ * power of two in [2^-254, 2^254].  The only rounding left is the binary64
+ * accumulation across blocks, in increasing j (relative error <= (K/32)*2^-53
+ * of S, far below the 1e-5*S tolerance the parity tests use).
+ *
+ * Element order inside an MXFP4 byte: element 2i is the low nibble, element
+ * 2i+1 the high nibble.  Decoding is by table (16 entries for E2M1, 256 for
+ * E4M3 and E8M0); NaN codes decode to NaN and propagate through the sums.
+ *
+ * Built with: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (oracle/build.py).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define MXREF_FMT_MXFP8 1
+#define MXREF_FMT_MXFP4 2
+
+static double tab_e2m1[16];
+static double tab_e4m3[256];
+static double tab_e8m0[256];
+static int tables_ready = 0;
+
+/* E2M1 (OCP FP4): sign bit 3, exponent bits 2..1, mantissa bit 0, bias 1.
+ * The eight magnitudes are listed outright: 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ * No infinities and no NaN; code 0x8 is -0. */
+static void fill_e2m1(void)
+{
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    for (int c = 0; c < 16; ++c)
+        tab_e2m1[c] = (c & 8) ? -mag[c & 7] : mag[c & 7];
+}
+
+/* E4M3 (OCP FP8 "E4M3FN"): sign bit 7, exponent bits 6..3 (bias 7), mantissa
+ * bits 2..0.  Exponent field 0 is subnormal: m/8 * 2^-6.  Otherwise
+ * (1 + m/8) * 2^(e-7).  e=15,m=7 (0x7F / 0xFF) is NaN; there is no infinity,
+ * so 0x7E = 448 is the largest finite value. */
+static void fill_e4m3(void)
+{
+    for (int c = 0; c < 256; ++c) {
+        int s = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+        double v;
+        if (e == 15 && m == 7)
+            v = NAN;
+        else if (e == 0)
+            v = ldexp((double)m, -9);          /* m/8 * 2^-6 */
+        else
+            v = ldexp(8.0 + m, e - 10);        /* (8+m)/8 * 2^(e-7) */
+        tab_e4m3[c] = s ? -v : v;
+    }
+}
+
+/* E8M0: unsigned power-of-two exponent, value 2^(c-127) for c in 0..254;
+ * c = 255 is NaN.  There is no zero and no sign. */
+static void fill_e8m0(void)
+{
+    for (int c = 0; c < 255; ++c)
+        tab_e8m0[c] = ldexp(1.0, c - 127);
+    tab_e8m0[255] = NAN;
+}
+
+void mxref_init(void)
+{
+    if (tables_ready)
+        return;
+    fill_e2m1();
+    fill_e4m3();
+    fill_e8m0();
+    tables_ready = 1;
+}
+
+/* Copy a decode table out (which: 1 = E4M3, 2 = E2M1, 3 = E8M0).
+ * Returns the number of entries written, or -1 for an unknown table. */
+int mxref_decode_table(int which, double *out)
+{
+    mxref_init();
+    switch (which) {
+    case 1: memcpy(out, tab_e4m3, sizeof tab_e4m3); return 256;
+    case 2: memcpy(out, tab_e2m1, sizeof tab_e2m1); return 16;
+    case 3: memcpy(out, tab_e8m0, sizeof tab_e8m0); return 256;
+    default: return -1;
+    }
+}
+
+/* Decode one packed operand row (codes only, no scale) into K doubles. */
+static void decode_row(int fmt, const uint8_t *row, int64_t K, double *dst)
+{
+    if (fmt == MXREF_FMT_MXFP8) {
+        for (int64_t k = 0; k < K; ++k)
+            dst[k] = tab_e4m3[row[k]];
+    } else {
+        for (int64_t k = 0; k < K; k += 2) {
+            uint8_t byte = row[k >> 1];
+            dst[k] = tab_e2m1[byte & 15];
+            dst[k + 1] = tab_e2m1[byte >> 4];
+        }
+    }
+}
+
+/*
+ * Reference GEMM over a set of output rows and columns.
+ *
+ *   fmt          1 = MXFP8 (E4M3, one byte per code), 2 = MXFP4 (E2M1, two codes/byte)
+ *   A, SA        M x K codes (row-major, K or K/2 bytes per row) and M x K/32 scales
+ *   B, SB        N x K codes and N x K/32 scales (B is the "T" operand: C = A * B^T)
+ *   rows, nrows  which rows of C to compute (NULL: all M, in order)
+ *   cols, ncols  which columns of C to compute (NULL: all N, in order)
+ *   C, S         nrows x ncols binary64 outputs (S may be NULL)
+ *   nthreads     OpenMP threads (<= 0: the runtime default)
+ *
+ * Returns 0, or -1 for bad arguments (K not a positive multiple of 32, unknown
+ * fmt, out-of-range row or column index).
+ */
+int mxref_gemm(int fmt, int64_t M, int64_t N, int64_t K,
+               const uint8_t *A, const uint8_t *SA,
+               const uint8_t *B, const uint8_t *SB,
+               const int64_t *rows, int64_t nrows,
+               const int64_t *cols, int64_t ncols,
+               double *C, double *S, int nthreads)
+{
+    mxref_init();
+    if ((fmt != MXREF_FMT_MXFP8 && fmt != MXREF_FMT_MXFP4) || K <= 0 || K % 32 != 0 ||
+        M < 0 || N < 0)
+        return -1;
+    if (rows == NULL) nrows = M;
+    if (cols == NULL) ncols = N;
+    for (int64_t i = 0; i < (rows ? nrows : 0); ++i)
+        if (rows[i] < 0 || rows[i] >= M) return -1;
+    for (int64_t i = 0; i < (cols ? ncols : 0); ++i)
+        if (cols[i] < 0 || cols[i] >= N) return -1;
+
+    const int64_t row_bytes = (fmt == MXREF_FMT_MXFP8) ? K : K / 2;
+    const int64_t nblk = K / 32;
+    int err = 0;
+
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+
+#pragma omp parallel
+    {
+        double *a = (double *)malloc(sizeof(double) * (size_t)K);
+        double *b = (double *)malloc(sizeof(double) * (size_t)K);
+        if (!a || !b) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nrows; ++i) {
+            if (!a || !b) continue;
+            const int64_t m = rows ? rows[i] : i;
+            decode_row(fmt, A + m * row_bytes, K, a);
+            for (int64_t jcol = 0; jcol < ncols; ++jcol) {
+                const int64_t n = cols ? cols[jcol] : jcol;
+                decode_row(fmt, B + n * row_bytes, K, b);
+                double acc = 0.0, acc_abs = 0.0;
+                for (int64_t j = 0; j < nblk; ++j) {
+                    double inner = 0.0, inner_abs = 0.0;
+                    for (int64_t t = 0; t < 32; ++t) {
+                        const double p = a[32 * j + t] * b[32 * j + t];
+                        inner += p;
+                        inner_abs += fabs(p);
+                    }
+                    const double sc = tab_e8m0[SA[m * nblk + j]] * tab_e8m0[SB[n * nblk + j]];
+                    acc += sc * inner;
+                    acc_abs += sc * inner_abs;
+                }
+                C[i * ncols + jcol] = acc;
+                if (S) S[i * ncols + jcol] = acc_abs;
+            }
+        }
+        free(a);
+        free(b);
+    }
+    return err ? -1 : 0;
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int mxref_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

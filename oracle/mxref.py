@@ -1,0 +1,107 @@
+"""ctypes front end of the C oracle in ``oracle/mxref.c``.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  This module marshals
+numpy arrays into the C routine and compiles it with gcc when the shared object
+is missing or older than its source.  No arithmetic of the method lives here.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+FMT_MXFP8 = 1
+FMT_MXFP4 = 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mxref.c")
+_SO = os.path.join(_HERE, "_build", "libmxref.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``mxref.c`` into ``oracle/_build/libmxref.so`` (gcc, OpenMP)."""
+    if (not force and os.path.exists(_SO)
+            and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
+        return _SO
+    os.makedirs(os.path.dirname(_SO), exist_ok=True)
+    tmp = _SO + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC",
+           "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.mxref_gemm.restype = ctypes.c_int
+            lib.mxref_gemm.argtypes = [
+                ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.mxref_decode_table.restype = ctypes.c_int
+            lib.mxref_decode_table.argtypes = [ctypes.c_int, ctypes.c_void_p]
+            lib.mxref_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def decode_table(which: str) -> np.ndarray:
+    """Return the oracle's decode table: 'e4m3' (256), 'e2m1' (16) or 'e8m0' (256)."""
+    idx = {"e4m3": 1, "e2m1": 2, "e8m0": 3}[which]
+    out = np.empty(256, dtype=np.float64)
+    n = _load().mxref_decode_table(idx, out.ctypes.data)
+    return out[:n].copy()
+
+
+def num_threads() -> int:
+    return int(_load().mxref_num_threads())
+
+
+def _u8(x, shape):
+    a = np.ascontiguousarray(x, dtype=np.uint8)
+    if a.shape != shape:
+        raise ValueError(f"expected shape {shape}, got {a.shape}")
+    return a
+
+
+def gemm(fmt: int, A, SA, B, SB, K: int, rows=None, cols=None,
+         with_abs: bool = True, nthreads: int = 0):
+    """Reference C = A * B^T (binary64) and S = sum |a*b| (same scaling).
+
+    ``A``: M x (K or K/2) uint8 codes; ``SA``: M x K/32 uint8 E8M0 scales;
+    likewise ``B``/``SB`` with N rows.  ``rows``/``cols`` select a subset of the
+    output (index arrays); the result then has shape (len(rows), len(cols)).
+    Returns ``(C, S)`` (``S`` is None when ``with_abs`` is False).
+    """
+    rb = K if fmt == FMT_MXFP8 else K // 2
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    M, N = A.shape[0], B.shape[0]
+    A = _u8(A, (M, rb))
+    B = _u8(B, (N, rb))
+    SA = _u8(SA, (M, K // 32))
+    SB = _u8(SB, (N, K // 32))
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else r.size
+    nc = N if c is None else c.size
+    C = np.empty((nr, nc), dtype=np.float64)
+    S = np.empty((nr, nc), dtype=np.float64) if with_abs else None
+    rc = _load().mxref_gemm(
+        fmt, M, N, K, A.ctypes.data, SA.ctypes.data, B.ctypes.data, SB.ctypes.data,
+        None if r is None else r.ctypes.data, nr,
+        None if c is None else c.ctypes.data, nc,
+        C.ctypes.data, None if S is None else S.ctypes.data, nthreads)
+    if rc != 0:
+        raise ValueError("mxref_gemm rejected its arguments")
+    return C, S

@@ -1,0 +1,61 @@
+"""Reader for the hand-worked fixtures in ``tests/golden/`` (input construction only)."""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+
+from mx_block_scaled_gb300.inputs import FMT_MXFP4, FMT_MXFP8, pack_fp4
+
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _runs(spec: str, K: int) -> np.ndarray:
+    codes = []
+    for tok in spec.split():
+        code, count = tok.split("*")
+        codes += [int(code, 16)] * int(count)
+    if len(codes) != K:
+        raise ValueError(f"code runs cover {len(codes)} elements, expected {K}")
+    return np.array(codes, dtype=np.uint8)
+
+
+def _value(text: str) -> Fraction:
+    text = text.strip()
+    if text.startswith("2^"):
+        e = int(text[2:])
+        return Fraction(2) ** e
+    return Fraction(text)
+
+
+def load_handworked(K: int = 128):
+    """Return a list of dicts: name, fmt, A, SA, B, SB (operand arrays), expected (Fraction)."""
+    cases = []
+    cur = None
+    with open(os.path.join(GOLDEN_DIR, "handworked_dot.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, val = line.partition(":")
+            val = val.strip()
+            if key == "case":
+                cur = {"name": val}
+                cases.append(cur)
+            elif key == "fmt":
+                cur["fmt"] = {"mxfp8": FMT_MXFP8, "mxfp4": FMT_MXFP4}[val]
+            elif key in ("a", "b"):
+                cur[key] = _runs(val, K)
+            elif key in ("sa", "sb"):
+                cur[key] = np.array([int(v) for v in val.split()], dtype=np.uint8)
+            elif key == "expected":
+                cur["expected"] = _value(val)
+    out = []
+    for c in cases:
+        a, b = c["a"][None, :], c["b"][None, :]
+        if c["fmt"] == FMT_MXFP4:
+            a, b = pack_fp4(a), pack_fp4(b)
+        out.append(dict(name=c["name"], fmt=c["fmt"], A=a, B=b,
+                        SA=c["sa"][None, :], SB=c["sb"][None, :], expected=c["expected"]))
+    return out
