@@ -1,0 +1,194 @@
+/*
+ * mxgemm.h -- C ABI of libmxgemm.so: the MX block-scaled NT GEMM on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ *   C[M,N] = sum_j 2^(SA[m,j]-127) * 2^(SB[n,j]-127) * sum_{t<32} a[m,32j+t] * b[n,32j+t]
+ *
+ * with A (M x K) and B (N x K) both stored row-major ("NT": K is the contiguous
+ * dimension of both operands), one E8M0 scale per 32 consecutive K values,
+ * FP32 accumulation and FP32 or BF16 output.
+ *
+ * Where the operation is defined:
+ *  - "Accelerating PyTorch on AMD GPUs with FlyDSL" (English digest), section
+ *    "API compatibility is not universal input coverage": the MXFP scaled GEMM
+ *    needs specific row/column layouts, one E8M0 scale per 32 values along K,
+ *    and K divisible by 128; incompatible layouts may add copies.
+ *  - Same page, section "Performance numbers need their baselines": the MXFP8 /
+ *    MXFP4 scaled GEMMs are timed from already-quantised inputs; quantisation,
+ *    compilation and initial tuning are outside the measurement.
+ *  - AI-compiler daily digest of 2026-10-22, item 1 (FlyDSL): the scaled GEMMs
+ *    are "BlockWise1x32, E8M0 scale, FP32 accumulation".
+ *  - Element encodings (not printed on the pages; OCP MX): MXFP8 elements are
+ *    E4M3 (bias 7, max 448, 0x7F/0xFF NaN), MXFP4 elements are E2M1 packed two
+ *    per byte (element 2i in the low nibble), E8M0 is 2^(code-127) with 0xFF NaN.
+ *
+ * Conventions for every call:
+ *  - Pointers named A, B, SA, SB, C, src, dst, workspace are DEVICE pointers
+ *    (cudaMalloc / PyTorch CUDA memory on the current device).  The caller owns
+ *    all device memory; the library never allocates device memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Launching calls are stream-ordered and asynchronous; they return once the
+ *    work is enqueued.
+ *  - Every call returns an int status: MXGEMM_OK (0) or a negative MXGEMM_ERR_*.
+ *    Arguments are validated before anything is launched; on an error nothing
+ *    is launched and no output is touched.  No call aborts or throws.
+ *  - A plan is a host object; it is not thread-safe (one thread per plan).
+ */
+#ifndef MXGEMM_H
+#define MXGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MXGEMM_API __attribute__((visibility("default")))
+#else
+#define MXGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element format of A and B (both operands use the same format). */
+typedef enum {
+    MXGEMM_FMT_MXFP8_E4M3 = 1, /* one E4M3 code per byte: row = K bytes        */
+    MXGEMM_FMT_MXFP4_E2M1 = 2  /* two E2M1 codes per byte: row = K/2 bytes     */
+} mxgemm_format_t;
+
+/* Output element type of C (row-major M x N, leading dimension N). */
+typedef enum {
+    MXGEMM_OUT_F32 = 1,  /* FP32: the accumulator, unrounded                     */
+    MXGEMM_OUT_BF16 = 2  /* BF16: the FP32 accumulator rounded to nearest-even   */
+} mxgemm_out_t;
+
+/* Status codes. */
+#define MXGEMM_OK                   0
+#define MXGEMM_ERR_ARG             -1  /* NULL pointer or unknown enum / flag      */
+#define MXGEMM_ERR_SHAPE           -2  /* M, N <= 0, K <= 0 or K % 128 != 0        */
+#define MXGEMM_ERR_ALIGN           -3  /* a device pointer is not 16-byte aligned  */
+#define MXGEMM_ERR_WORKSPACE       -4  /* workspace NULL or smaller than required  */
+#define MXGEMM_ERR_ARCH            -5  /* current device is not sm_103             */
+#define MXGEMM_ERR_CUDA            -6  /* a CUDA runtime/driver call failed        */
+#define MXGEMM_ERR_DEVICE_TIMEOUT  -7  /* a kernel gave up waiting (see below)     */
+#define MXGEMM_ERR_UNSUPPORTED     -8  /* valid request this build does not serve  */
+
+/* Plan flags (mxgemm_plan_create).  0 = the library's per-shape heuristic. */
+#define MXGEMM_PLAN_FORCE_BN128     (1u << 0)  /* force a 128-wide N tile             */
+#define MXGEMM_PLAN_FORCE_BN256     (1u << 1)  /* force a 256-wide N tile             */
+#define MXGEMM_PLAN_FORCE_NOSWAP    (1u << 2)  /* never compute C^T = B*A^T           */
+#define MXGEMM_PLAN_FORCE_SWAP      (1u << 3)  /* always compute C^T = B*A^T          */
+#define MXGEMM_PLAN_SPLITK_SHIFT    8          /* bits 8..15: forced split-K (0=auto) */
+
+/* Run flags (mxgemm_run). */
+#define MXGEMM_RUN_SA_PRELAYOUT     (1u << 0)  /* SA is already in the tile layout    */
+#define MXGEMM_RUN_SB_PRELAYOUT     (1u << 1)  /* SB is already in the tile layout    */
+
+typedef struct mxgemm_plan *mxgemm_plan_t;
+
+/*
+ * Create a plan for C[M,N] = A[M,K] * B[N,K]^T.
+ *   fmt:   mxgemm_format_t; out: mxgemm_out_t; flags: MXGEMM_PLAN_* (0 = auto).
+ * Validates the shape (M, N >= 1; K >= 128 and K % 128 == 0, per the FlyDSL
+ * page's K constraint), checks that the current device is an sm_103 part,
+ * chooses the tile shape, operand roles (swap-AB) and split-K, and sizes the
+ * workspace.  Host memory only.  On success *plan receives a new plan.
+ */
+MXGEMM_API int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
+                       int fmt, int out, uint32_t flags);
+
+/* Free a plan (NULL is accepted). */
+MXGEMM_API int mxgemm_plan_destroy(mxgemm_plan_t plan);
+
+/*
+ * Bytes of device workspace mxgemm_run needs for this plan (0 for NULL plan):
+ * the tile-layout copies of SA and SB (unless both are passed pre-laid-out)
+ * plus split-K partial sums.  Alignment: 256 bytes.
+ */
+MXGEMM_API size_t mxgemm_workspace_bytes(mxgemm_plan_t plan);
+
+/*
+ * Write a one-line, NUL-terminated description of the plan's choices
+ * (tile, roles, split, grid) into buf (at most len bytes).
+ */
+MXGEMM_API int mxgemm_plan_describe(mxgemm_plan_t plan, char *buf, size_t len);
+
+/*
+ * Bytes of a tile-layout scale tensor for `rows` operand rows and K:
+ *   ceil(rows/128) * 128 * (K/32).  Returns 0 if rows < 1 or K % 128 != 0.
+ */
+MXGEMM_API size_t mxgemm_sf_bytes(int64_t rows, int64_t K);
+
+/*
+ * Scale relayout: row-major E8M0 scales -> the tensor-core tile layout.
+ *   src: rows x (K/32) bytes, row-major (scale of row r, K-block j at r*(K/32)+j).
+ *   dst: mxgemm_sf_bytes(rows, K) bytes.  Layout: 512-byte tiles ordered
+ *        [ceil(rows/128)][K/128]; inside the tile of row block R and K-tile T,
+ *        the scale of row r = 128R + 32q + p (q < 4, p < 32) and K-block
+ *        j = 4T + c (c < 4) sits at byte p*16 + q*4 + c.  Rows past `rows`
+ *        are filled with code 127 (x1.0).
+ * This is the copy the FlyDSL page warns about ("incompatible layouts may
+ * introduce copies"); it is a separate, HBM-bound kernel so its cost can be
+ * timed on its own.  A weight's scales need it once; pass the result to
+ * mxgemm_run with MXGEMM_RUN_SB_PRELAYOUT to skip it afterwards.
+ * Errors: MXGEMM_ERR_ARG (NULL), MXGEMM_ERR_SHAPE, MXGEMM_ERR_ALIGN (src or
+ * dst not 16-byte aligned), MXGEMM_ERR_CUDA (launch failed).
+ */
+MXGEMM_API int mxgemm_relayout_scales(const uint8_t *src, int64_t rows, int64_t K,
+                           uint8_t *dst, void *stream);
+
+/*
+ * Run the GEMM on `stream`.
+ *   A:  M x K codes (fmt-dependent bytes per row, row-major, 16-byte aligned)
+ *   SA: M x K/32 scales, row-major -- or, with MXGEMM_RUN_SA_PRELAYOUT,
+ *       mxgemm_sf_bytes(M,K) bytes in the tile layout of mxgemm_relayout_scales
+ *   B, SB: the same for the N x K operand (MXGEMM_RUN_SB_PRELAYOUT)
+ *   C:  M x N output, row-major, element type per the plan's `out`
+ *   workspace / ws_bytes: at least mxgemm_workspace_bytes(plan) bytes
+ *       (may be NULL/0 if that is 0)
+ * Enqueues (1) the relayout of whichever scales are not pre-laid-out and
+ * (2) the persistent tcgen05 block-scaled GEMM kernel (3) a split-K reduce if
+ * the plan splits K.  Inputs are read-only; C is fully overwritten.
+ * Errors: MXGEMM_ERR_ARG, MXGEMM_ERR_ALIGN, MXGEMM_ERR_WORKSPACE,
+ * MXGEMM_ERR_CUDA.  A device-side wait that exceeds its limit is reported by
+ * mxgemm_device_status(), not here (the call is asynchronous).
+ */
+MXGEMM_API int mxgemm_run(mxgemm_plan_t plan, const void *A, const uint8_t *SA,
+               const void *B, const uint8_t *SB, void *C,
+               void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream);
+
+/*
+ * Synchronise `stream` and return the library's sticky device status on the
+ * current device: MXGEMM_OK, or MXGEMM_ERR_DEVICE_TIMEOUT if any kernel since
+ * the last reset gave up on a barrier wait (every wait in the kernels has a
+ * time limit of about one second; on expiry the kernel records the error,
+ * drains its own in-flight work and exits instead of hanging).  If `reset` is
+ * nonzero the status is cleared after reading.  MXGEMM_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+MXGEMM_API int mxgemm_device_status(void *stream, int reset);
+
+/*
+ * Self-test of the device timeout path: launches the GEMM of `plan` with its
+ * loader switched off, so no data ever arrives and every barrier wait in the
+ * kernel expires after ~20 ms.  The kernel then records
+ * MXGEMM_ERR_DEVICE_TIMEOUT, frees its TMEM and exits; C is left unwritten.
+ * SA and SB are taken as pre-laid-out and are not read.  Returns the launch
+ * status; read the device status with mxgemm_device_status().  Used by the
+ * test suite to show that a stalled kernel returns instead of hanging.
+ */
+MXGEMM_API int mxgemm_selftest_stall(mxgemm_plan_t plan, const void *A, const uint8_t *SA,
+                          const void *B, const uint8_t *SB, void *C,
+                          void *workspace, size_t ws_bytes, void *stream);
+
+/* Static, human-readable name of a status code. */
+MXGEMM_API const char *mxgemm_status_str(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+MXGEMM_API int mxgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXGEMM_H */

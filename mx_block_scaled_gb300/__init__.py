@@ -7,14 +7,12 @@ FP32 or BF16 output.  The compute path is the C-ABI library ``libmxgemm.so``
 :mod:`.inputs` generates seeded synthetic operands.
 """
 
-__all__ = ["binding", "inputs"]
+import importlib
+
+__all__ = ["binding", "inputs", "build"]
 
 
 def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
-    if name == "inputs":
-        from . import inputs
-        return inputs
+    if name in __all__:
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

@@ -1,0 +1,396 @@
+// gemm_kernel.cuh -- the persistent, warp-specialised MX block-scaled GEMM for
+// sm_103a (tcgen05 tensor cores, TMA, TMEM accumulators).
+//
+// Computes D[i, j] = sum_k a_i[k] * b_j[k] with a per-32 E8M0 scale on each
+// operand, i over the rows of the "A role" operand (the MMA M dimension, 128
+// per tile) and j over the rows of the "B role" operand (the MMA N dimension,
+// BN per tile).  Normally the A role is the GEMM's A and the B role its B; for
+// small token counts the host swaps them (C^T = B * A^T) so that the weight
+// fills the 128-row MMA dimension.
+//
+// Operation: the MXFP8 / MXFP4 scaled GEMM of "Accelerating PyTorch on AMD
+// GPUs with FlyDSL" (English digest, section "API compatibility is not
+// universal input coverage": E8M0 scale per 32 values along K, K % 128 == 0),
+// FP32 accumulation (AI-compiler daily 2026-10-22, item 1).  The page's own
+// kernel (half-tile-interleaved LDS pipeline on MI355X, section "Explicit
+// layouts bring optimization close to hardware") is replaced here by a TMA ->
+// shared-memory ring -> tcgen05.mma pipeline with mbarrier hand-off.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: per k-stage, A and B tiles (128-byte swizzle) and
+//               the tile-layout scale chunks (bulk copies) into ring slot s.
+//   warp 1      TMEM owner and MMA issuer: per k-stage, tcgen05.cp of the scale
+//               chunks into TMEM, then BK/32 (MXFP8) or BK/64 (MXFP4)
+//               block-scaled MMAs accumulating in TMEM; commits free the slot.
+//   warps 2..5  epilogue: TMEM -> registers -> (BF16) -> global, masked edges.
+// Every mbarrier wait is bounded in time; on expiry the CTA records
+// MXGEMM_ERR_DEVICE_TIMEOUT in *status, drains its in-flight copies and MMAs,
+// frees its TMEM and exits.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace mxg {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;            // MMA M (rows of the A role per tile)
+constexpr int kRowBytes = 128;      // bytes of one operand row per k-stage
+constexpr int kSfChunk = 512;       // bytes of one scale chunk (128 rows x 4 K-blocks)
+constexpr int kSmemBudget = 232448; // 227 KiB opt-in shared memory per block
+
+enum OutKind : int { OUT_F32 = 0, OUT_BF16 = 1 };
+
+struct GemmParams {
+    int rows_a;               // extent of the A role (MMA M)
+    int rows_b;               // extent of the B role (MMA N)
+    int num_kt;               // K / 128: scale K-tiles
+    int kstages;              // k-stages over the whole K (FP8: K/128, FP4: ceil(K/256))
+    int kstages_per_split;    // k-stages per split (the last split may get fewer)
+    int tiles_m, tiles_n, splits;
+    int group_m;              // raster: tiles of the A role walked together
+    int out_kind;             // OutKind
+    int vec_ok;               // 1: stride_j == 1 and rows are 16-byte aligned
+    int test_stall;           // self-test: the producer issues nothing (waits expire)
+    const uint8_t *sfa;       // tile-layout scales of the A role
+    const uint8_t *sfb;       // tile-layout scales of the B role
+    void *out;                // output base (C, or split-K partial slabs)
+    long long stride_i;       // elements between consecutive A-role rows in out
+    long long stride_j;       // elements between consecutive B-role rows in out
+    long long split_stride;   // elements between split partial slabs (0: no split)
+    unsigned long long timeout_ns;
+    int *status;              // sticky device status word
+};
+
+template <bool FP4, int BN>
+struct Cfg {
+    static constexpr int kKtPerStage = FP4 ? 2 : 1;           // scale K-tiles per k-stage
+    static constexpr int kSubPerKt = FP4 ? 2 : 4;             // MMAs per scale K-tile
+    static constexpr int kChunksB = BN >= 128 ? BN / 128 : 1; // 128-row scale chunks of B per K-tile
+    static constexpr int kABytes = kBM * kRowBytes;
+    static constexpr int kBBytes = BN * kRowBytes;
+    static constexpr int kSfaBytes = kKtPerStage * kSfChunk;
+    static constexpr int kSfbBytes = kChunksB * kKtPerStage * kSfChunk;
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+    static constexpr int kStagesRaw = (kSmemBudget - 1024 - 256) / kStageBytes;
+    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    static constexpr int kSfaCols = 4 * kKtPerStage;
+    static constexpr int kSfbCols = 4 * kKtPerStage * kChunksB;
+    static constexpr int kAccStages = (2 * BN + kSfaCols + kSfbCols <= 512) ? 2 : 1;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kSfaCol = kAccStages * BN;
+    static constexpr int kSfbCol = kSfaCol + kSfaCols;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+    static constexpr uint32_t kIdesc = idesc_block_scaled(FP4 ? 1u : 0u, kBM, BN);
+    static_assert(kStages >= 2, "shared memory too small for two stages");
+    static_assert(kSfbCol + kSfbCols <= kTmemCols, "TMEM overflow");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be 32..256, multiple of 32");
+};
+
+__device__ __forceinline__ void tile_coords(const GemmParams &p, int unit, int &tm, int &tn, int &split)
+{
+    split = unit % p.splits;
+    const int t = unit / p.splits;
+    const int per_group = p.group_m * p.tiles_n;
+    const int group = t / per_group;
+    const int first_m = group * p.group_m;
+    const int gsz = min(p.tiles_m - first_m, p.group_m);
+    const int local = t - group * per_group;
+    tm = first_m + local % gsz;
+    tn = local / gsz;
+}
+
+__device__ __forceinline__ void record_timeout(const GemmParams &p, volatile int *abort)
+{
+    *abort = 1;
+    atomicExch(p.status, -7 /* MXGEMM_ERR_DEVICE_TIMEOUT */);
+}
+
+// Store 32 consecutive B-role values of one A-role row: out[off .. off+32).
+__device__ __forceinline__ void store_row32_vec(const GemmParams &p, long long off, const uint32_t (&r)[32])
+{
+    if (p.out_kind == OUT_BF16) {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + off);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[v * 8 + 2 * e]),
+                                                         __uint_as_float(r[v * 8 + 2 * e + 1]));
+                w[e] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<float *>(p.out) + off);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+            dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+    }
+}
+
+// Element-wise store of n (<= 32) values at out[base + (j0+e)*stride_j].
+__device__ __forceinline__ void store_row32_masked(const GemmParams &p, long long base, int j0, int n,
+                                                   const uint32_t (&r)[32])
+{
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        if (e < n) {
+            const long long off = base + static_cast<long long>(j0 + e) * p.stride_j;
+            if (p.out_kind == OUT_BF16)
+                static_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(__uint_as_float(r[e]));
+            else
+                static_cast<float *>(p.out)[off] = __uint_as_float(r[e]);
+        }
+    }
+}
+
+template <bool FP4, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_b)
+{
+    using C = Cfg<FP4, BN>;
+    constexpr int S = C::kStages;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_base_holder;
+    __shared__ int abort_flag;
+
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    // Ring layout: [A x S][B x S][SFA x S][SFB x S][barriers]
+    const uint32_t sA = base;
+    const uint32_t sB = sA + S * C::kABytes;
+    const uint32_t sSFA = sB + S * C::kBBytes;
+    const uint32_t sSFB = sSFA + S * C::kSfaBytes;
+    const uint32_t sBar = sSFB + S * C::kSfbBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + (sBar - base));
+    (void)bars;
+    auto full_bar = [&](int s) { return sBar + 8u * s; };
+    auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
+    auto accf_bar = [&](int a) { return sBar + 8u * (2 * S + a); };
+    auto acce_bar = [&](int a) { return sBar + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = sBar + 8u * (2 * S + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    volatile int *abort = &abort_flag;
+    int never_abort = 0;  // drain waits ignore the abort flag (still time-bounded)
+    const volatile int *no_abort = &never_abort;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), 4);
+        }
+        mbar_init(drain_bar, 1);
+        fence_mbar_init();
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&tmem_base_holder), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_holder;
+
+    const int total_units = p.tiles_m * p.tiles_n * p.splits;
+    const uint64_t lim = p.timeout_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0 && !p.test_stall) {
+            const uint64_t pol_a = l2_policy_evict_last();
+            const uint64_t pol_b = l2_policy_evict_last();
+            int st = 0;
+            uint32_t ph = 0;
+            int armed_parity[S];
+#pragma unroll
+            for (int s = 0; s < S; ++s) armed_parity[s] = -1;
+            bool ok = true;
+            const int nrb_b = (p.rows_b + 127) / 128;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+                int tm, tn, sp;
+                tile_coords(p, u, tm, tn, sp);
+                const int ks0 = sp * p.kstages_per_split;
+                const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+                for (int ks = ks0; ks < ks1; ++ks) {
+                    if (!mbar_wait(empty_bar(st), ph ^ 1u, abort, lim)) {
+                        record_timeout(p, abort);
+                        ok = false;
+                        break;
+                    }
+                    const int kt0 = ks * C::kKtPerStage;
+                    const int nkt = min(C::kKtPerStage, p.num_kt - kt0);
+                    // B-role scale chunks present for this tile (row blocks past the end are skipped)
+                    int nchunk_b = 0;
+                    const int rb_b0 = (tn * BN) / 128;
+#pragma unroll
+                    for (int c = 0; c < C::kChunksB; ++c)
+                        if (rb_b0 + c < nrb_b) ++nchunk_b;
+                    const uint32_t bytes = C::kABytes + C::kBBytes + nkt * kSfChunk * (1 + nchunk_b);
+                    mbar_arrive_expect_tx(full_bar(st), bytes);
+                    armed_parity[st] = static_cast<int>(ph);
+                    tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, tm * kBM, pol_a);
+                    tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, tn * BN, pol_b);
+                    bulk_load(sSFA + st * C::kSfaBytes,
+                              p.sfa + (static_cast<size_t>(tm) * p.num_kt + kt0) * kSfChunk,
+                              nkt * kSfChunk, full_bar(st));
+                    for (int c = 0; c < nchunk_b; ++c)
+                        bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
+                                  p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
+                                  nkt * kSfChunk, full_bar(st));
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Drain: let every armed stage finish landing before the CTA exits.
+                for (int s = 0; s < S; ++s)
+                    if (armed_parity[s] >= 0)
+                        mbar_wait(full_bar(s), static_cast<uint32_t>(armed_parity[s]), no_abort, lim);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int st = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool ok = true;
+            bool issued = false;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
+                int tm, tn, sp;
+                tile_coords(p, u, tm, tn, sp);
+                (void)tm;
+                const int acc = it % C::kAccStages;
+                const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
+                if (!mbar_wait(acce_bar(acc), acc_par ^ 1u, abort, lim)) {
+                    record_timeout(p, abort);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * BN;
+                const uint32_t sub_off = static_cast<uint32_t>(((tn * BN) % 128) / 32); // BN < 128 only
+                const int ks0 = sp * p.kstages_per_split;
+                const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+                for (int ks = ks0; ks < ks1; ++ks) {
+                    if (!mbar_wait(full_bar(st), ph, abort, lim)) {
+                        record_timeout(p, abort);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nkt = min(C::kKtPerStage, p.num_kt - ks * C::kKtPerStage);
+                    // Scales: shared memory -> TMEM (in issue order with the MMAs below).
+                    for (int t = 0; t < nkt; ++t) {
+                        tc_cp_32x128b_warpx4(tmem + C::kSfaCol + 4 * t,
+                                             sdesc_sf_chunk(sSFA + st * C::kSfaBytes + t * kSfChunk));
+#pragma unroll
+                        for (int c = 0; c < C::kChunksB; ++c)
+                            tc_cp_32x128b_warpx4(
+                                tmem + C::kSfbCol + 4 * (t * C::kChunksB + c),
+                                sdesc_sf_chunk(sSFB + st * C::kSfbBytes + (c * C::kKtPerStage + t) * kSfChunk));
+                    }
+                    const uint64_t adesc = sdesc_kmajor_sw128(sA + st * C::kABytes);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(sB + st * C::kBBytes);
+                    const int nsub = nkt * C::kSubPerKt;
+                    for (int s = 0; s < nsub; ++s) {
+                        const int t = s / C::kSubPerKt;
+                        const uint32_t sf_id = FP4 ? static_cast<uint32_t>((s % 2) * 2) : static_cast<uint32_t>(s % 4);
+                        const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, sf_id, sf_id);
+                        const uint32_t sfa_t = tmem + C::kSfaCol + 4 * t;
+                        const uint32_t sfb_t = tmem + C::kSfbCol + 4 * t * C::kChunksB + sub_off;
+                        // advance 32 bytes along K per MMA (32 FP8 or 64 FP4 elements)
+                        const uint64_t koff = static_cast<uint64_t>((s * 32) >> 4);
+                        if (FP4)
+                            mma_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t,
+                                     (ks > ks0 || s > 0) ? 1u : 0u);
+                        else
+                            mma_mxf8f6f4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t,
+                                         (ks > ks0 || s > 0) ? 1u : 0u);
+                        issued = true;
+                    }
+                    tc_commit(empty_bar(st));
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(accf_bar(acc));
+            }
+            if (!ok && issued) {
+                // Drain the tensor pipe before TMEM is released.
+                tc_commit(drain_bar);
+                mbar_wait(drain_bar, 0, no_abort, lim);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int it = 0;
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
+            int tm, tn, sp;
+            tile_coords(p, u, tm, tn, sp);
+            const int acc = it % C::kAccStages;
+            const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(accf_bar(acc), acc_par, abort, lim);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                if (lane == 0) record_timeout(p, abort);
+                break;
+            }
+            tc_fence_after();
+            const int i = tm * kBM + q * 32 + lane;  // A-role row owned by this thread
+            const bool row_ok = i < p.rows_a;
+            const long long split_off = static_cast<long long>(sp) * p.split_stride;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0, r);
+                tmem_ld_wait(r);
+                const int j0 = tn * BN + c0;
+                if (row_ok && j0 < p.rows_b) {
+                    const long long base_off = split_off + static_cast<long long>(i) * p.stride_i;
+                    if (p.vec_ok && j0 + 32 <= p.rows_b)
+                        store_row32_vec(p, base_off + j0, r);
+                    else
+                        store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), r);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(acc));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+}  // namespace mxg

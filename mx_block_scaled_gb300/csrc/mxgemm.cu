@@ -1,0 +1,510 @@
+// mxgemm.cu -- host side of libmxgemm.so: argument validation, the per-shape
+// plan (tile width, operand roles, split-K), TMA descriptor encoding, the scale
+// relayout and split-K reduce kernels, and the C ABI of include/mxgemm.h.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "mxgemm.h"
+
+namespace {
+
+using mxg::GemmParams;
+
+// Sticky device status word, written by kernels that give up on a wait.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool is_sm103 = false;
+    int num_sms = 0;
+    int *status_ptr = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+int device_info(DeviceInfo **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return MXGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+            return MXGEMM_ERR_CUDA;
+        d.is_sm103 = (prop.major == 10 && prop.minor == 3);
+        d.num_sms = prop.multiProcessorCount;
+        if (d.is_sm103) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess)
+                return MXGEMM_ERR_CUDA;
+            d.status_ptr = static_cast<int *>(p);
+        }
+        if (!g_encode_tiled) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return MXGEMM_ERR_CUDA;
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return d.is_sm103 ? MXGEMM_OK : MXGEMM_ERR_ARCH;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ----------------------------------------------------------- scale relayout --
+// One block per (128-row block, up to 32 K-tiles): the 128 x (32 x 4) scale
+// bytes are staged in shared memory as 32-bit words (4 K-blocks each), then
+// written as 512-byte tiles.  Inside a tile, row r = 32q + p and K-block c of
+// the tile go to byte p*16 + q*4 + c: the layout the tensor cores read scale
+// factors from when a 32-row x 16-byte chunk is copied into TMEM.
+struct RelayoutJob {
+    const uint8_t *src;
+    uint8_t *dst;
+    int rows;
+    int num_kt;   // K / 128
+    int blocks_x; // ceil(num_kt / 32)
+    int blocks;   // ceil(rows / 128) * blocks_x
+};
+
+__global__ void __launch_bounds__(256) relayout_scales_kernel(RelayoutJob j0, RelayoutJob j1)
+{
+    __shared__ uint32_t tile[128][33];
+    int b = blockIdx.x;
+    const RelayoutJob &j = (b < j0.blocks) ? j0 : j1;
+    if (b >= j0.blocks)
+        b -= j0.blocks;
+    const int rb = b / j.blocks_x;
+    const int kt0 = (b % j.blocks_x) * 32;
+    const int kb_words = j.num_kt;  // 32-bit words per source row (K/32 bytes / 4)
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(j.src);
+    for (int idx = threadIdx.x; idx < 128 * 32; idx += 256) {
+        const int r = idx >> 5, w = idx & 31;
+        const int row = rb * 128 + r, kt = kt0 + w;
+        uint32_t v = 0x7F7F7F7Fu;  // padding rows: scale code 127 (x1.0)
+        if (row < j.rows && kt < j.num_kt)
+            v = __ldg(src + static_cast<size_t>(row) * kb_words + kt);
+        tile[r][w] = v;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < 32 * 32; idx += 256) {
+        const int w = idx >> 5, p = idx & 31;
+        const int kt = kt0 + w;
+        if (kt >= j.num_kt)
+            continue;
+        uint4 v = make_uint4(tile[p][w], tile[32 + p][w], tile[64 + p][w], tile[96 + p][w]);
+        uint4 *dst = reinterpret_cast<uint4 *>(j.dst + (static_cast<size_t>(rb) * j.num_kt + kt) * 512);
+        dst[p] = v;
+    }
+}
+
+RelayoutJob make_job(const uint8_t *src, int64_t rows, int64_t K, uint8_t *dst)
+{
+    RelayoutJob j;
+    j.src = src;
+    j.dst = dst;
+    j.rows = static_cast<int>(rows);
+    j.num_kt = static_cast<int>(K / 128);
+    j.blocks_x = static_cast<int>(ceil_div(j.num_kt, 32));
+    j.blocks = static_cast<int>(ceil_div(rows, 128)) * j.blocks_x;
+    return j;
+}
+
+cudaError_t launch_relayout(const RelayoutJob &a, const RelayoutJob *b, cudaStream_t s)
+{
+    RelayoutJob none{};
+    none.blocks = 0;
+    const RelayoutJob &j1 = b ? *b : none;
+    const int blocks = a.blocks + j1.blocks;
+    relayout_scales_kernel<<<blocks, 256, 0, s>>>(a, j1);
+    return cudaGetLastError();
+}
+
+// -------------------------------------------------------- split-K reduce --
+// C[e] = sum_s part[s][e], summed in split order (deterministic), then stored
+// as FP32 or rounded to BF16.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ part, int splits,
+                                                             long long n, long long slab, void *out,
+                                                             int out_kind)
+{
+    const long long n4 = n / 4;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    for (long long i = tid; i < n4; i += stride) {
+        float4 acc = __ldg(reinterpret_cast<const float4 *>(part) + i);
+        for (int s = 1; s < splits; ++s) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(part + s * slab) + i);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        if (out_kind == mxg::OUT_BF16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 w = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+            reinterpret_cast<uint2 *>(out)[i] = w;
+        } else {
+            reinterpret_cast<float4 *>(out)[i] = acc;
+        }
+    }
+    if (tid < n - n4 * 4) {  // the last n % 4 elements
+        const long long t = n4 * 4 + tid;
+        float acc = part[t];
+        for (int s = 1; s < splits; ++s)
+            acc += part[s * slab + t];
+        if (out_kind == mxg::OUT_BF16)
+            static_cast<__nv_bfloat16 *>(out)[t] = __float2bfloat16_rn(acc);
+        else
+            static_cast<float *>(out)[t] = acc;
+    }
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------- plan --
+struct mxgemm_plan {
+    int64_t M, N, K;
+    int fmt, out;
+    int swap;          // 1: compute C^T = B * A^T (B fills the MMA M dimension)
+    int bn;            // MMA N tile
+    int splits;        // split-K factor
+    int tiles_m, tiles_n;
+    int kstages, kstages_per_split;
+    int grid;
+    int group_m;
+    int num_sms;
+    size_t off_sfa, off_sfb, off_part, ws_bytes;
+    // TMA descriptor cache (re-encoded when an operand pointer changes)
+    const void *map_ptr_a = nullptr;
+    const void *map_ptr_b = nullptr;
+    CUtensorMap map_a, map_b;
+};
+
+namespace {
+
+int encode_operand_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t row_bytes, int box_rows)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
+}
+
+int pick_bn(int64_t rows_b)
+{
+    if (rows_b <= 32) return 32;
+    if (rows_b <= 64) return 64;
+    if (rows_b <= 128) return 128;
+    return 256;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxgemm_version(void) { return 100; }
+
+const char *mxgemm_status_str(int status)
+{
+    switch (status) {
+    case MXGEMM_OK: return "ok";
+    case MXGEMM_ERR_ARG: return "invalid argument (NULL pointer or unknown enum/flag)";
+    case MXGEMM_ERR_SHAPE: return "invalid shape (need M,N >= 1 and K a positive multiple of 128)";
+    case MXGEMM_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case MXGEMM_ERR_WORKSPACE: return "workspace missing or too small";
+    case MXGEMM_ERR_ARCH: return "current device is not an sm_103 GPU";
+    case MXGEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case MXGEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on a barrier (device timeout)";
+    case MXGEMM_ERR_UNSUPPORTED: return "request not supported by this build";
+    default: return "unknown status";
+    }
+}
+
+size_t mxgemm_sf_bytes(int64_t rows, int64_t K)
+{
+    if (rows < 1 || K < 128 || K % 128 != 0)
+        return 0;
+    return static_cast<size_t>(ceil_div(rows, 128) * 128) * static_cast<size_t>(K / 32);
+}
+
+int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int fmt, int out, uint32_t flags)
+{
+    if (!plan)
+        return MXGEMM_ERR_ARG;
+    *plan = nullptr;
+    if ((fmt != MXGEMM_FMT_MXFP8_E4M3 && fmt != MXGEMM_FMT_MXFP4_E2M1) ||
+        (out != MXGEMM_OUT_F32 && out != MXGEMM_OUT_BF16))
+        return MXGEMM_ERR_ARG;
+    const uint32_t known = MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_NOSWAP |
+                           MXGEMM_PLAN_FORCE_SWAP | (0xFFu << MXGEMM_PLAN_SPLITK_SHIFT);
+    if ((flags & ~known) != 0 || ((flags & MXGEMM_PLAN_FORCE_SWAP) && (flags & MXGEMM_PLAN_FORCE_NOSWAP)) ||
+        ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)))
+        return MXGEMM_ERR_ARG;
+    if (M < 1 || N < 1 || K < 128 || K % 128 != 0)
+        return MXGEMM_ERR_SHAPE;
+    // 32-bit tile and row indices inside the kernels
+    if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30))
+        return MXGEMM_ERR_UNSUPPORTED;
+
+    DeviceInfo *dev = nullptr;
+    int st = device_info(&dev);
+    if (st != MXGEMM_OK)
+        return st;
+
+    mxgemm_plan *p = new (std::nothrow) mxgemm_plan();
+    if (!p)
+        return MXGEMM_ERR_UNSUPPORTED;
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->fmt = fmt;
+    p->out = out;
+    p->num_sms = dev->num_sms;
+
+    // Operand roles: small token counts put the weight (B) in the 128-row MMA dimension.
+    int swap = (M <= 64 && N >= 128) ? 1 : 0;
+    if (flags & MXGEMM_PLAN_FORCE_SWAP) swap = 1;
+    if (flags & MXGEMM_PLAN_FORCE_NOSWAP) swap = 0;
+    p->swap = swap;
+    const int64_t rows_a = swap ? N : M;
+    const int64_t rows_b = swap ? M : N;
+    int bn = pick_bn(rows_b);
+    if (flags & MXGEMM_PLAN_FORCE_BN128) bn = 128;
+    if (flags & MXGEMM_PLAN_FORCE_BN256) bn = 256;
+    p->bn = bn;
+    p->tiles_m = static_cast<int>(ceil_div(rows_a, 128));
+    p->tiles_n = static_cast<int>(ceil_div(rows_b, bn));
+    p->kstages = static_cast<int>(fmt == MXGEMM_FMT_MXFP4_E2M1 ? ceil_div(K, 256) : K / 128);
+
+    // Split-K when the output tiles alone cannot fill the GPU.
+    const int64_t tiles = static_cast<int64_t>(p->tiles_m) * p->tiles_n;
+    int splits = static_cast<int>((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu);
+    if (splits == 0) {
+        splits = 1;
+        if (tiles * 2 <= p->num_sms) {
+            const int64_t by_sms = p->num_sms / tiles;
+            const int64_t by_k = std::max<int64_t>(1, p->kstages / 4);
+            splits = static_cast<int>(std::min<int64_t>(std::min(by_sms, by_k), 32));
+        }
+    }
+    splits = std::max(1, std::min(splits, p->kstages));
+    p->kstages_per_split = static_cast<int>(ceil_div(p->kstages, splits));
+    p->splits = static_cast<int>(ceil_div(p->kstages, p->kstages_per_split));
+    p->group_m = 8;
+    const int64_t units = tiles * p->splits;
+    p->grid = static_cast<int>(std::min<int64_t>(units, p->num_sms));
+
+    size_t off = 0;
+    p->off_sfa = off;
+    off = align256(off + mxgemm_sf_bytes(M, K));
+    p->off_sfb = off;
+    off = align256(off + mxgemm_sf_bytes(N, K));
+    p->off_part = off;
+    if (p->splits > 1)
+        off = align256(off + static_cast<size_t>(p->splits) * ((M * N + 3) & ~3ll) * sizeof(float));
+    p->ws_bytes = off;
+    *plan = p;
+    return MXGEMM_OK;
+}
+
+int mxgemm_plan_destroy(mxgemm_plan_t plan)
+{
+    delete plan;
+    return MXGEMM_OK;
+}
+
+size_t mxgemm_workspace_bytes(mxgemm_plan_t plan) { return plan ? plan->ws_bytes : 0; }
+
+int mxgemm_plan_describe(mxgemm_plan_t plan, char *buf, size_t len)
+{
+    if (!plan || !buf || len == 0)
+        return MXGEMM_ERR_ARG;
+    const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
+    mxg::KernelInfo ki = fp4 ? mxg::gemm_info_fp4(plan->bn) : mxg::gemm_info_fp8(plan->bn);
+    snprintf(buf, len,
+             "fmt=%s out=%s tile=128x%d swap_ab=%d split_k=%d tiles=%dx%d kstages=%d grid=%d stages=%d "
+             "acc_stages=%d smem=%d",
+             fp4 ? "mxfp4" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32", plan->bn, plan->swap,
+             plan->splits, plan->tiles_m, plan->tiles_n, plan->kstages, plan->grid, ki.stages, ki.acc_stages,
+             ki.smem_bytes);
+    return MXGEMM_OK;
+}
+
+int mxgemm_relayout_scales(const uint8_t *src, int64_t rows, int64_t K, uint8_t *dst, void *stream)
+{
+    if (!src || !dst)
+        return MXGEMM_ERR_ARG;
+    if (rows < 1 || K < 128 || K % 128 != 0 || rows > (1ll << 30))
+        return MXGEMM_ERR_SHAPE;
+    if (!aligned16(src) || !aligned16(dst))
+        return MXGEMM_ERR_ALIGN;
+    RelayoutJob j = make_job(src, rows, K, dst);
+    return launch_relayout(j, nullptr, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXGEMM_OK
+                                                                                          : MXGEMM_ERR_CUDA;
+}
+
+static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB, void *C,
+                    void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream, int test_stall,
+                    unsigned long long timeout_ns)
+{
+    if (!plan || !A || !SA || !B || !SB || !C)
+        return MXGEMM_ERR_ARG;
+    if (run_flags & ~(MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT))
+        return MXGEMM_ERR_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(SA) || !aligned16(SB))
+        return MXGEMM_ERR_ALIGN;
+    if (plan->ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan->ws_bytes))
+        return MXGEMM_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace))
+        return MXGEMM_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    int st = device_info(&dev);
+    if (st != MXGEMM_OK)
+        return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int64_t M = plan->M, N = plan->N, K = plan->K;
+    const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
+    const int64_t row_bytes = fp4 ? K / 2 : K;
+
+    // (1) scale relayout for whichever operand is not pre-laid-out (one launch)
+    const uint8_t *sfa = SA, *sfb = SB;
+    RelayoutJob jobs[2];
+    int njobs = 0;
+    if (!(run_flags & MXGEMM_RUN_SA_PRELAYOUT)) {
+        jobs[njobs++] = make_job(SA, M, K, ws + plan->off_sfa);
+        sfa = ws + plan->off_sfa;
+    }
+    if (!(run_flags & MXGEMM_RUN_SB_PRELAYOUT)) {
+        jobs[njobs++] = make_job(SB, N, K, ws + plan->off_sfb);
+        sfb = ws + plan->off_sfb;
+    }
+    if (njobs > 0 && launch_relayout(jobs[0], njobs > 1 ? &jobs[1] : nullptr, s) != cudaSuccess)
+        return MXGEMM_ERR_CUDA;
+
+    // (2) the GEMM, with operand roles per the plan
+    const void *pa = plan->swap ? B : A;
+    const void *pb = plan->swap ? A : B;
+    const int64_t rows_a = plan->swap ? N : M;
+    const int64_t rows_b = plan->swap ? M : N;
+    if (plan->map_ptr_a != pa) {
+        if (encode_operand_map(&plan->map_a, pa, rows_a, row_bytes, 128) != MXGEMM_OK)
+            return MXGEMM_ERR_CUDA;
+        plan->map_ptr_a = pa;
+    }
+    if (plan->map_ptr_b != pb) {
+        if (encode_operand_map(&plan->map_b, pb, rows_b, row_bytes, plan->bn) != MXGEMM_OK)
+            return MXGEMM_ERR_CUDA;
+        plan->map_ptr_b = pb;
+    }
+
+    GemmParams p;
+    memset(&p, 0, sizeof p);
+    p.rows_a = static_cast<int>(rows_a);
+    p.rows_b = static_cast<int>(rows_b);
+    p.num_kt = static_cast<int>(K / 128);
+    p.kstages = plan->kstages;
+    p.kstages_per_split = plan->kstages_per_split;
+    p.tiles_m = plan->tiles_m;
+    p.tiles_n = plan->tiles_n;
+    p.splits = plan->splits;
+    p.group_m = plan->group_m;
+    p.test_stall = test_stall;
+    p.sfa = plan->swap ? sfb : sfa;
+    p.sfb = plan->swap ? sfa : sfb;
+    p.stride_i = plan->swap ? 1 : N;
+    p.stride_j = plan->swap ? N : 1;
+    p.timeout_ns = timeout_ns;
+    p.status = dev->status_ptr;
+    const bool split = plan->splits > 1;
+    const int osize = split ? 4 : (plan->out == MXGEMM_OUT_BF16 ? 2 : 4);
+    if (split) {
+        p.out = ws + plan->off_part;
+        p.out_kind = mxg::OUT_F32;
+        p.split_stride = (M * N + 3) & ~3ll;  // keeps every slab 16-byte aligned
+    } else {
+        p.out = C;
+        p.out_kind = plan->out == MXGEMM_OUT_BF16 ? mxg::OUT_BF16 : mxg::OUT_F32;
+        p.split_stride = 0;
+    }
+    p.vec_ok = (!plan->swap && (N * osize) % 16 == 0 && aligned16(p.out)) ? 1 : 0;
+
+    cudaError_t e = fp4 ? mxg::launch_gemm_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
+                        : mxg::launch_gemm_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
+    if (e != cudaSuccess)
+        return MXGEMM_ERR_CUDA;
+
+    // (3) split-K reduce
+    if (split) {
+        const long long n = M * N;
+        const long long n4 = n / 4;
+        int blocks = static_cast<int>(std::min<long long>(std::max<long long>(1, (n4 + 255) / 256),
+                                                          static_cast<long long>(plan->num_sms) * 8));
+        splitk_reduce_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float *>(ws + plan->off_part),
+                                                    plan->splits, n, (n + 3) & ~3ll, C,
+                                                    plan->out == MXGEMM_OUT_BF16 ? mxg::OUT_BF16 : mxg::OUT_F32);
+        if (cudaGetLastError() != cudaSuccess)
+            return MXGEMM_ERR_CUDA;
+    }
+    return MXGEMM_OK;
+}
+
+int mxgemm_run(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB, void *C,
+               void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream)
+{
+    return run_impl(plan, A, SA, B, SB, C, workspace, ws_bytes, run_flags, stream, 0, 2000000000ull);
+}
+
+int mxgemm_selftest_stall(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB,
+                          void *C, void *workspace, size_t ws_bytes, void *stream)
+{
+    return run_impl(plan, A, SA, B, SB, C, workspace, ws_bytes, MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT,
+                    stream, 1, 20000000ull);
+}
+
+int mxgemm_device_status(void *stream, int reset)
+{
+    DeviceInfo *dev = nullptr;
+    int st = device_info(&dev);
+    if (st != MXGEMM_OK)
+        return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MXGEMM_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess)
+        return MXGEMM_ERR_CUDA;
+    if (reset) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess)
+            return MXGEMM_ERR_CUDA;
+    }
+    return v;
+}
+
+}  // extern "C"

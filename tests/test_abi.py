@@ -1,0 +1,94 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry
+point, and validates arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mx_block_scaled_gb300 import build
+    build.build()
+    from mx_block_scaled_gb300 import binding
+    return binding
+
+
+def declared_entry_points():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MXGEMM_API\s+[\w\s\*]*?\b(mxgemm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_entry_points()
+    for required in ("mxgemm_plan_create", "mxgemm_run", "mxgemm_relayout_scales",
+                     "mxgemm_plan_destroy", "mxgemm_workspace_bytes", "mxgemm_sf_bytes",
+                     "mxgemm_device_status", "mxgemm_status_str"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared_entry_points():
+        assert hasattr(so, name), f"{name} declared in mxgemm.h but not exported"
+    bound = {n for n, _, _ in lib.SIGNATURES}
+    assert set(declared_entry_points()) == bound
+
+
+def test_sf_bytes(lib):
+    assert lib.mxgemm_sf_bytes(1, 128) == 128 * 4
+    assert lib.mxgemm_sf_bytes(129, 256) == 256 * 8
+    assert lib.mxgemm_sf_bytes(57344, 8192) == 57344 * 256
+    assert lib.mxgemm_sf_bytes(0, 128) == 0
+    assert lib.mxgemm_sf_bytes(8, 96) == 0
+
+
+def test_status_strings(lib):
+    for st in range(-8, 1):
+        assert lib.mxgemm_status_str(st) not in ("", "unknown status")
+    assert lib.mxgemm_status_str(5) == "unknown status"
+    assert lib.mxgemm_version() >= 100
+
+
+@pytest.mark.parametrize("M,N,K,fmt,out,flags,expect", [
+    (16, 16, 100, 1, 2, 0, -2),   # K % 128 != 0 (the FlyDSL page's K constraint)
+    (16, 16, 0, 1, 2, 0, -2),
+    (0, 16, 128, 1, 2, 0, -2),
+    (16, -1, 128, 2, 1, 0, -2),
+    (16, 16, 128, 3, 2, 0, -1),   # unknown format
+    (16, 16, 128, 1, 9, 0, -1),   # unknown output type
+    (16, 16, 128, 1, 2, 1 << 20, -1),  # unknown flag
+    (16, 16, 128, 1, 2, (1 << 2) | (1 << 3), -1),  # contradictory flags
+])
+def test_plan_create_validates_before_touching_the_device(lib, M, N, K, fmt, out, flags, expect):
+    st, h = lib.mxgemm_plan_create(M, N, K, fmt, out, flags)
+    assert st == expect and not h.value
+
+
+def test_null_arguments_are_rejected(lib):
+    assert lib._lib.mxgemm_plan_create(None, 16, 16, 128, 1, 2, 0) == lib.MXGEMM_ERR_ARG
+    assert lib.mxgemm_relayout_scales(0, 16, 128, 0, 0) == lib.MXGEMM_ERR_ARG
+    assert lib.mxgemm_relayout_scales(16, 16, 100, 32, 0) == lib.MXGEMM_ERR_SHAPE
+    assert lib.mxgemm_relayout_scales(17, 16, 128, 32, 0) == lib.MXGEMM_ERR_ALIGN
+    assert lib.mxgemm_run(None, 16, 16, 16, 16, 16, 0, 0, 0, 0) == lib.MXGEMM_ERR_ARG
+    assert lib.mxgemm_plan_destroy(None) == lib.MXGEMM_OK
+    assert lib.mxgemm_workspace_bytes(None) == 0
+
+
+def test_valid_plan_needs_an_sm103_device(lib):
+    import torch
+    st, h = lib.mxgemm_plan_create(256, 256, 256, 1, 2, 0)
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the gpu tests")
+    assert st in (lib.MXGEMM_ERR_CUDA, lib.MXGEMM_ERR_ARCH) and not h.value
+
+
+def test_oracle_builds_and_is_separate(oracle_mod):
+    # The oracle is its own shared object, built from oracle/mxref.c only.
+    from oracle import mxref
+    assert os.path.exists(mxref.build())
+    assert "mx_block_scaled_gb300" not in open(os.path.join(ROOT, "oracle", "mxref.c")).read()

@@ -1,0 +1,287 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Exact equality wherever every partial sum is representable in FP32 (then any
+FP32 accumulation order gives the same bits); elsewhere the bound
+|C - C_ref| <= 1e-5 * sum|a*b| (+ 2^-8 |C_ref| for BF16 output).
+"""
+import numpy as np
+import pytest
+
+from golden_io import load_handworked
+from gpu_util import (OUT_BF16, OUT_F32, assert_within, gpu_gemm, lib, sample_indices, to_dev)
+from mx_block_scaled_gb300.inputs import (FMT_MXFP4, FMT_MXFP8, finite_uniform_codes, make_operand,
+                                          pack_fp4, workload_cases)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    cap = torch.cuda.get_device_capability()
+    assert cap == (10, 3), f"expected an sm_103 GPU, got {cap}"
+    lib()
+
+
+# ---- scale relayout: byte-exact against the documented index formula --------
+
+def relayout_reference(S, rows, K):
+    kb = K // 32
+    nrb, nkt = (rows + 127) // 128, K // 128
+    out = np.full((nrb, nkt, 512), 127, np.uint8)
+    for r in range(rows):
+        R, rr = divmod(r, 128)
+        q, p = divmod(rr, 32)
+        for j in range(kb):
+            T, c = divmod(j, 4)
+            out[R, T, p * 16 + q * 4 + c] = S[r, j]
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("rows", [1, 8, 127, 128, 129, 300])
+@pytest.mark.parametrize("K", [128, 256, 28672])
+def test_relayout_matches_index_formula(rows, K):
+    import torch
+    b = lib()
+    rng = np.random.default_rng(rows * 7 + K)
+    S = rng.integers(0, 256, size=(rows, K // 32), dtype=np.uint8)
+    out = b.relayout_scales(to_dev(S), rows, K)
+    torch.cuda.synchronize()
+    ref = relayout_reference(S, rows, K) if rows * K <= 300 * 256 else None
+    got = out.cpu().numpy()
+    assert got.size == b.mxgemm_sf_bytes(rows, K)
+    if ref is not None:
+        assert (got == ref).all()
+    else:  # vectorised form of the same formula for the large K
+        kb = K // 32
+        r = np.arange(rows)[:, None]
+        j = np.arange(kb)[None, :]
+        pos = ((r // 128) * (K // 128) + j // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + j % 4
+        assert (got[pos] == S).all()
+
+
+# ---- element formats and descriptors: all code pairs ---------------------------
+
+@pytest.mark.parametrize("k_pos", [0, 45, 127])
+def test_all_fp8_code_pairs(oracle_mod, k_pos):
+    K = 128
+    A = np.zeros((256, K), np.uint8)
+    A[:, k_pos] = np.arange(256)
+    S = np.full((256, K // 32), 127, np.uint8)
+    C = gpu_gemm(FMT_MXFP8, A, S, A, S, K, OUT_F32)
+    ref, _ = oracle_mod.gemm(FMT_MXFP8, A, S, A, S, K)
+    assert (np.isnan(C) == np.isnan(ref)).all()
+    ok = ~np.isnan(ref)
+    assert (C[ok] == ref[ok]).all()
+
+
+@pytest.mark.parametrize("k_pos", [0, 1, 70, 127])
+def test_all_fp4_code_pairs(oracle_mod, k_pos):
+    K = 128
+    codes = np.zeros((16, K), np.uint8)
+    codes[:, k_pos] = np.arange(16)
+    A = pack_fp4(codes)
+    S = np.full((16, K // 32), 127, np.uint8)
+    C = gpu_gemm(FMT_MXFP4, A, S, A, S, K, OUT_F32)
+    ref, _ = oracle_mod.gemm(FMT_MXFP4, A, S, A, S, K)
+    assert (C == ref).all()
+
+
+@pytest.mark.parametrize("case", load_handworked(), ids=lambda c: c["name"])
+def test_handworked_dot_products(case):
+    C = gpu_gemm(case["fmt"], case["A"], case["SA"], case["B"], case["SB"], 128, OUT_F32)
+    assert C[0, 0] == float(case["expected"])
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+def test_identity_b_returns_dequantised_a(oracle_mod, fmt):
+    K = 256
+    rng = np.random.default_rng(21)
+    A, SA = finite_uniform_codes(rng, 200, K, fmt, 120, 134)
+    one = 0x38 if fmt == FMT_MXFP8 else 0x2
+    eye = np.where(np.eye(K, dtype=bool), one, 0).astype(np.uint8)
+    B = eye if fmt == FMT_MXFP8 else pack_fp4(eye)
+    SB = np.full((K, K // 32), 127, np.uint8)
+    C = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32)
+    ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
+    assert (C == ref).all()
+
+
+def small_int_codes(rng, rows, K, fmt):
+    """Codes of values in {0, +-0.5, +-1, +-2} with scales in [125, 129]: every partial
+    sum of a K <= 2048 product is exact in FP32, so the GPU must match bit for bit."""
+    vals = np.array([0x00, 0x30, 0x38, 0x40, 0xB0, 0xB8, 0xC0], np.uint8) if fmt == FMT_MXFP8 else \
+        np.array([0x0, 0x1, 0x2, 0x4, 0x9, 0xA, 0xC], np.uint8)
+    codes = vals[rng.integers(0, len(vals), size=(rows, K))]
+    if fmt == FMT_MXFP4:
+        codes = pack_fp4(codes)
+    scales = rng.integers(125, 130, size=(rows, K // 32), dtype=np.uint8)
+    return codes, scales
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+def test_per_block_scale_sweep(oracle_mod, fmt):
+    """Each A row has exactly one nonzero 32-block; rows cycle over all blocks, and
+    every (row, block) and (column, block) has its own scale: pins the scale
+    addressing (TMEM scale columns, scale ids, relayout) element by element."""
+    K, M, N = 1024, 300, 272
+    rng = np.random.default_rng(22)
+    A, SA = small_int_codes(rng, M, K, fmt)
+    B, SB = small_int_codes(rng, N, K, fmt)
+    w = 32 if fmt == FMT_MXFP8 else 16  # bytes of one 32-block in a row
+    Ab = A.copy()
+    for m in range(M):
+        j = m % (K // 32)
+        keep = np.zeros(Ab.shape[1], bool)
+        keep[j * w:(j + 1) * w] = True
+        Ab[m, ~keep] = 0
+    C = gpu_gemm(fmt, Ab, SA, B, SB, K, OUT_F32)
+    ref, _ = oracle_mod.gemm(fmt, Ab, SA, B, SB, K)
+    assert (C == ref).all()
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (8, 129, 256), (127, 255, 384), (129, 8, 128),
+                                   (255, 127, 384), (130, 300, 640), (64, 512, 1024)])
+def test_edge_shapes_exact(oracle_mod, fmt, M, N, K):
+    rng = np.random.default_rng(M * 1000 + N + K)
+    A, SA = small_int_codes(rng, M, K, fmt)
+    B, SB = small_int_codes(rng, N, K, fmt)
+    ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
+    for out in (OUT_F32, OUT_BF16):
+        C = gpu_gemm(fmt, A, SA, B, SB, K, out)
+        if out == OUT_F32:
+            assert (C == ref).all(), f"M={M} N={N} K={K}"
+        else:
+            import torch
+            expect = torch.from_numpy(ref.astype(np.float32)).bfloat16().double().numpy()
+            assert (C == expect).all(), f"M={M} N={N} K={K} bf16"
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+@pytest.mark.parametrize("flags", [0, 1 << 2, 1 << 3, (1 << 2) | 1, (1 << 2) | 2, (3 << 8), (1 << 3) | (5 << 8)])
+def test_plan_variants_agree_with_oracle(oracle_mod, fmt, flags):
+    """Forced tile width / swap-AB / split-K variants all reproduce the oracle."""
+    M, N, K = 200, 384, 2048
+    rng = np.random.default_rng(23)
+    A, SA = small_int_codes(rng, M, K, fmt)
+    B, SB = small_int_codes(rng, N, K, fmt)
+    ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
+    C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, flags=flags, return_plan=True)
+    assert (C == ref).all(), desc
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+def test_prelayout_scales_give_the_same_result(fmt):
+    import torch
+    b = lib()
+    M, N, K = 160, 320, 512
+    rng = np.random.default_rng(24)
+    A, SA = finite_uniform_codes(rng, M, K, fmt, 110, 140)
+    B, SB = finite_uniform_codes(rng, N, K, fmt, 110, 140)
+    plan = b.Plan(M, N, K, fmt, OUT_F32)
+    dA, dB, dSA, dSB = to_dev(A), to_dev(B), to_dev(SA), to_dev(SB)
+    C1 = plan.run(dA, dSA, dB, dSB)
+    tSA, tSB = b.relayout_scales(dSA, M, K), b.relayout_scales(dSB, N, K)
+    C2 = plan.run(dA, tSA, dB, tSB, run_flags=b.MXGEMM_RUN_SA_PRELAYOUT | b.MXGEMM_RUN_SB_PRELAYOUT)
+    C3 = plan.run(dA, dSA, dB, tSB, run_flags=b.MXGEMM_RUN_SB_PRELAYOUT)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2) and torch.equal(C1, C3)
+
+
+# ---- invariants at full workload size (GPU vs GPU, no oracle cost) ------------
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+def test_incrementing_every_a_scale_doubles_c_exactly(fmt):
+    import torch
+    b = lib()
+    M, N, K = 4096, 4096, 4096
+    A, SA = make_operand("mxfp8_square_4096", "A", 0, M, K, fmt)
+    B, SB = make_operand("mxfp8_square_4096", "B", 0, N, K, fmt)
+    assert SA.max() < 254
+    for out in (OUT_F32, OUT_BF16):
+        plan = b.Plan(M, N, K, fmt, out)
+        dA, dB, dSB = to_dev(A), to_dev(B), to_dev(SB)
+        C1 = plan.run(dA, to_dev(SA), dB, dSB)
+        C2 = plan.run(dA, to_dev(SA + 1), dB, dSB)
+        torch.cuda.synchronize()
+        assert torch.equal(C2.float(), 2 * C1.float())
+
+
+# ---- the workloads ---------------------------------------------------------------
+
+def test_mxfp4_uniform_256_is_bit_exact(oracle_mod):
+    M = N = K = 256
+    A, SA = make_operand("mxfp4_uniform_256", "A", 0, M, K, FMT_MXFP4)
+    B, SB = make_operand("mxfp4_uniform_256", "B", 0, N, K, FMT_MXFP4)
+    ref, _ = oracle_mod.gemm(FMT_MXFP4, A, SA, B, SB, K)
+    C = gpu_gemm(FMT_MXFP4, A, SA, B, SB, K, OUT_F32)
+    assert (C == ref).all()
+
+
+def test_mxfp8_square_4096_full(oracle_mod):
+    M = N = K = 4096
+    A, SA = make_operand("mxfp8_square_4096", "A", 0, M, K, FMT_MXFP8)
+    B, SB = make_operand("mxfp8_square_4096", "B", 0, N, K, FMT_MXFP8)
+    C = gpu_gemm(FMT_MXFP8, A, SA, B, SB, K, OUT_BF16)
+    ref, S = oracle_mod.gemm(FMT_MXFP8, A, SA, B, SB, K)
+    assert_within(C, ref, S, OUT_BF16, "mxfp8 4096^3")
+
+
+WORKLOAD_SAMPLES = [
+    ("llama31_8b", "mxfp4", 2048, 28672, 4096),
+    ("llama31_8b", "mxfp4", 256, 4096, 14336),
+    ("llama33_70b", "mxfp8", 8, 8192, 28672),
+    ("llama33_70b", "mxfp4", 64, 10240, 8192),
+    ("qwen3_32b", "mxfp8", 128, 5120, 25600),
+    ("qwen3_32b", "mxfp4", 4096, 10240, 5120),
+]
+
+
+def find_case(name, fmt, M, N, K):
+    for f, si, nki, m, n, k in workload_cases(name):
+        if (f, m, n, k) == (fmt, M, N, K):
+            return si, nki
+    raise KeyError((name, fmt, M, N, K))
+
+
+@pytest.mark.parametrize("name,fmt,M,N,K", WORKLOAD_SAMPLES,
+                         ids=[f"{w[0]}-{w[1]}-M{w[2]}-N{w[3]}-K{w[4]}" for w in WORKLOAD_SAMPLES])
+def test_workload_sampled(oracle_mod, name, fmt, M, N, K):
+    f = FMT_MXFP8 if fmt == "mxfp8" else FMT_MXFP4
+    si, nki = find_case(name, fmt, M, N, K)
+    A, SA = make_operand(name, "A", si, M, K, f)
+    B, SB = make_operand(name, "B", nki, N, K, f)
+    C = gpu_gemm(f, A, SA, B, SB, K, OUT_BF16)
+    rows = sample_indices(M, 1) if M > 64 else np.arange(M)
+    cols = sample_indices(N, 2)
+    ref_r, S_r = oracle_mod.gemm(f, A, SA, B, SB, K, rows=rows)
+    assert_within(C[rows], ref_r, S_r, OUT_BF16, f"{name} rows")
+    ref_c, S_c = oracle_mod.gemm(f, A, SA, B, SB, K, cols=cols)
+    assert_within(C[:, cols], ref_c, S_c, OUT_BF16, f"{name} cols")
+
+
+# ---- failure path: a stalled kernel returns an error instead of hanging --------
+
+def test_stalled_kernel_times_out_and_context_survives():
+    import torch
+    b = lib()
+    M = N = K = 256
+    plan = b.Plan(M, N, K, FMT_MXFP8, OUT_F32)
+    A = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    S = torch.full((b.mxgemm_sf_bytes(M, K),), 127, dtype=torch.uint8, device="cuda")
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert b.mxgemm_device_status(stream, True) == b.MXGEMM_OK
+    st = b.mxgemm_selftest_stall(plan.handle, A.data_ptr(), S.data_ptr(), A.data_ptr(), S.data_ptr(),
+                                 C.data_ptr(), plan.workspace.data_ptr(), plan.ws_bytes, stream)
+    assert st == b.MXGEMM_OK
+    assert b.mxgemm_device_status(stream, True) == b.MXGEMM_ERR_DEVICE_TIMEOUT
+    assert b.mxgemm_device_status(stream, True) == b.MXGEMM_OK
+    # the context is still usable: a normal run afterwards is correct
+    A1 = torch.full((M, K), 0x38, dtype=torch.uint8, device="cuda")
+    Srow = torch.full((M, K // 32), 127, dtype=torch.uint8, device="cuda")
+    out = plan.run(A1, Srow, A1, Srow)
+    b.check_device_status()
+    assert torch.all(out == float(K))
