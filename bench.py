@@ -1,0 +1,493 @@
+#!/usr/bin/env python
+"""Benchmark of the MX block-scaled NT GEMM on GB300.
+
+Default line: the 4096^3 MXFP8 workload (E4M3 codes from N(0,1), E8M0 scale per
+32 along K, BF16 out).  One step = the whole hot path on one batch:
+  relayout(SA) + relayout(SB)  -> tile-layout scales   (mxgemm_relayout_scales x2)
+  GEMM                         -> C                    (mxgemm_run, scales pre-laid-out)
+Inputs are resident in HBM when the timed region starts; the step rotates over
+enough input/output sets that their total exceeds twice the L2, so no step
+reads another step's data from L2.  `e2e` repeats the step through mxgemm_run
+from pinned HOST buffers, with the copies in the timed region.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--sweep]
+
+With --gpus N under torchrun every rank runs an independent replica (the GEMM
+has no exchange step); value = all ranks' FLOPs / the slowest rank's time.
+--impl reference times the CPU oracle (the only other program computing the
+same result here) on a bounded sample of the same workload.
+--sweep prints one line per shape of the model workloads (not the headline).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4/MXFP8 NT GEMM TFLOP/s on 1 GB300; % of dense MX tensor (or HBM) roofline"
+WORKLOAD = "mxfp8_square_4096"
+NOMINAL_PF = {"bf16": 2.25, "mxfp8": 4.5, "mxfp4": 13.5}
+KERNEL_SOURCES = ["mx_block_scaled_gb300/csrc/gemm_kernel.cuh", "mx_block_scaled_gb300/csrc/ptx.cuh",
+                  "mx_block_scaled_gb300/csrc/gemm_fp8.cu", "mx_block_scaled_gb300/csrc/gemm_fp4.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+# ----------------------------------------------------------------- helpers --
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def mx_peak_tflops(fmt_name: str, bf16_tflops: float) -> float:
+    return bf16_tflops * NOMINAL_PF[fmt_name] / NOMINAL_PF["bf16"]
+
+
+def algorithmic_bytes(M, N, K, fmt_name, out_bytes):
+    e = 1.0 if fmt_name == "mxfp8" else 0.5
+    return (M + N) * K * e + (M + N) * K / 32 + M * N * out_bytes
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons (200 ms)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "samples_under_load": len(loaded), "power_w_max": max(power)}
+
+
+def read_traffic(fmt_name, M, N, K):
+    """DRAM bytes per GEMM launch from a committed ncu capture, if the kernel sources still match."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None, None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    ent = d.get(f"{fmt_name}_{M}x{N}x{K}")
+    if not ent or ent.get("kernel_source_sha") != kernel_source_sha():
+        return None, None
+    return ent.get("dram_bytes_per_launch"), ent.get("note")
+
+
+# ----------------------------------------------------------- reference arm --
+
+def oracle_sample_time(A, SA, B, SB, K, fmt, target_s: float, rows_cap: int):
+    """Time the CPU oracle on the first r rows of C, r grown until one call takes
+    about target_s.  Returns (rows, seconds, threads)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    rows = 8
+    while True:
+        idx = np.arange(rows, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.gemm(fmt, A, SA, B, SB, K, rows=idx, with_abs=False)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or rows >= rows_cap:
+            return rows, dt, oracle.num_threads()
+        grow = max(2.0, min(16.0, target_s / max(dt, 1e-3)))
+        rows = min(rows_cap, int(rows * grow))
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    from mx_block_scaled_gb300.inputs import FMT_MXFP8, make_operand
+    M = N = K = 4096
+    A, SA = make_operand(WORKLOAD, "A", 0, M, K, FMT_MXFP8)
+    B, SB = make_operand(WORKLOAD, "B", 0, N, K, FMT_MXFP8)
+    # size one step so that warmup + steps finish within a few minutes
+    budget_s = 150.0 / max(1, args.steps + args.warmup)
+    rows, _, threads = oracle_sample_time(A, SA, B, SB, K, 1, min(10.0, budget_s), M)
+    import oracle
+    idx = np.arange(rows, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle.gemm(1, A, SA, B, SB, K, rows=idx, with_abs=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm(1, A, SA, B, SB, K, rows=idx, with_abs=False)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * rows * N * K / dt / 1e12
+    sample = f"rows 0..{rows - 1} of C ({rows}x{N}x{K} of the {M}x{N}x{K} product) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "mxfp8 NT GEMM M=N=K=4096, E4M3 from N(0,1), E8M0/32, BF16 out",
+                   "M": M, "N": N, "K": K, "format": "mxfp8", "out": "bf16"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- our arm --
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    from mx_block_scaled_gb300 import binding as mx
+    from mx_block_scaled_gb300.inputs import FMT_MXFP8, make_operand
+
+    fmt_name, fmt = "mxfp8", FMT_MXFP8
+    M = N = K = 4096
+    out_bytes = 2
+    A, SA = make_operand(WORKLOAD, "A", 0, M, K, fmt)
+    B, SB = make_operand(WORKLOAD, "B", 0, N, K, fmt)
+
+    plan = mx.Plan(M, N, K, fmt, mx.MXGEMM_OUT_BF16, device=dev)
+    desc = plan.describe()
+    split = int(desc.split("split_k=")[1].split()[0])
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = A.nbytes + B.nbytes + SA.nbytes + SB.nbytes + M * N * out_bytes + 2 * mx.mxgemm_sf_bytes(M, K)
+    nsets = max(3, math.ceil(2 * l2 / set_bytes) + 1)
+    sets = []
+    for _ in range(nsets):
+        sets.append({
+            "A": torch.from_numpy(A).to(dev), "B": torch.from_numpy(B).to(dev),
+            "SA": torch.from_numpy(SA).to(dev), "SB": torch.from_numpy(SB).to(dev),
+            "tSA": torch.empty(mx.mxgemm_sf_bytes(M, K), dtype=torch.uint8, device=dev),
+            "tSB": torch.empty(mx.mxgemm_sf_bytes(N, K), dtype=torch.uint8, device=dev),
+            "C": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+        })
+    pre = mx.MXGEMM_RUN_SA_PRELAYOUT | mx.MXGEMM_RUN_SB_PRELAYOUT
+
+    def step(i, ev=None):
+        s = sets[i % nsets]
+        if ev is not None:
+            ev[0].record(stream)
+        assert mx.mxgemm_relayout_scales(s["SA"].data_ptr(), M, K, s["tSA"].data_ptr(), sh) == 0
+        assert mx.mxgemm_relayout_scales(s["SB"].data_ptr(), N, K, s["tSB"].data_ptr(), sh) == 0
+        if ev is not None:
+            ev[1].record(stream)
+        st = mx.mxgemm_run(plan.handle, s["A"].data_ptr(), s["tSA"].data_ptr(), s["B"].data_ptr(),
+                           s["tSB"].data_ptr(), s["C"].data_ptr(), plan.workspace.data_ptr(), plan.ws_bytes,
+                           pre, sh)
+        assert st == 0, mx.mxgemm_status_str(st)
+        if ev is not None:
+            ev[2].record(stream)
+
+    launches_per_step = 3 + (1 if split > 1 else 0)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    # clock soak: the same steps, untimed, long enough for nvidia-smi to see the load
+    t_soak = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_soak < args.soak_s:
+        for _ in range(20):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for k in range(args.steps):
+        step(k, evs[k])
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    wall_s = time.perf_counter() - w0
+    clocks = sampler.stop()
+    mx.check_device_status()
+
+    total_ms = evs[0][0].elapsed_time(evs[-1][2])
+    gemm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    relayout_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    ms_per_step = total_ms / args.steps
+    if ws > 1:
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    flops = 2.0 * M * N * K
+    value = flops * ws / (ms_per_step / 1e3) / 1e12
+
+    # ---- e2e: pinned host inputs -> device -> mxgemm_run (relayout + GEMM) -> host C
+    e2e = None
+    if not args.no_e2e:
+        hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
+        hSA, hSB = torch.from_numpy(SA).pin_memory(), torch.from_numpy(SB).pin_memory()
+        hC = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+        d = sets[0]
+
+        def e2e_step():
+            d["A"].copy_(hA, non_blocking=True)
+            d["SA"].copy_(hSA, non_blocking=True)
+            d["B"].copy_(hB, non_blocking=True)
+            d["SB"].copy_(hSB, non_blocking=True)
+            st = mx.mxgemm_run(plan.handle, d["A"].data_ptr(), d["SA"].data_ptr(), d["B"].data_ptr(),
+                               d["SB"].data_ptr(), d["C"].data_ptr(), plan.workspace.data_ptr(), plan.ws_bytes,
+                               0, sh)
+            assert st == 0
+            hC.copy_(d["C"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(5, min(args.steps, 20))
+        if ws > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if ws > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        mx.check_device_status()
+        e2e = {"value": flops * ws / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(A.nbytes + B.nbytes + SA.nbytes + SB.nbytes),
+               "d2h_bytes_per_step": int(M * N * out_bytes), "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    hbm_gbs, bf16_tf, _, peak_src = load_peaks()
+    peak = mx_peak_tflops(fmt_name, bf16_tf)
+    gemm_avg_s = statistics.mean(gemm_ms) / 1e3
+    achieved = flops / gemm_avg_s / 1e12
+    bytes_alg = algorithmic_bytes(M, N, K, fmt_name, out_bytes)
+    traffic, traffic_note = read_traffic(fmt_name, M, N, K)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8(e4m3 x e8m0/32) -> f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": "mxfp8 NT GEMM M=N=K=4096, E4M3 from N(0,1), E8M0/32, BF16 out",
+                   "M": M, "N": N, "K": K, "format": "mxfp8", "out": "bf16",
+                   "l2": f"rotating {nsets} input/output sets ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2 "
+                         f"{l2 / 2**20:.0f} MiB)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "plan": desc},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "mx_gemm_kernel (persistent tcgen05 block-scaled GEMM)",
+                     "peak_source": f"{peak_src} bf16 burst {bf16_tf} TFLOP/s x nominal mxfp8/bf16 ratio "
+                                    f"{NOMINAL_PF[fmt_name] / NOMINAL_PF['bf16']:g}",
+                     "hbm_view": {"algorithmic_bytes": bytes_alg, "achieved_gbs": bytes_alg / gemm_avg_s / 1e9,
+                                  "peak_gbs": hbm_gbs, "frac": bytes_alg / gemm_avg_s / 1e9 / hbm_gbs},
+                     "traffic_note": traffic_note},
+        "gemm_us": statistics.mean(gemm_ms) * 1e3, "relayout_us": statistics.mean(relayout_ms) * 1e3,
+        "wall_ms_per_step": wall_s * 1e3 / args.steps,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        rows, dt, threads = oracle_sample_time(A, SA, B, SB, K, fmt, args.cpu_target_s, M)
+        line["cpu_baseline"] = {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"rows 0..{rows - 1} of C ({rows}x{N}x{K}), {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+# ------------------------------------------------------------------- sweep --
+
+def run_sweep(args):
+    """Per-shape GEMM time for the model workloads (device-side random codes)."""
+    import torch
+    from mx_block_scaled_gb300 import binding as mx
+    from mx_block_scaled_gb300.inputs import FMT_BY_NAME, WORKLOADS, workload_cases
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    hbm_gbs, bf16_tf, _, peak_src = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    names = args.sweep_workloads.split(",") if args.sweep_workloads else list(WORKLOADS)
+    for name in names:
+        seen = set()
+        for fmt_name, si, nki, M, N, K in workload_cases(name):
+            if (fmt_name, M, N, K) in seen:
+                continue
+            seen.add((fmt_name, M, N, K))
+            fmt = FMT_BY_NAME[fmt_name]
+            rb = K if fmt_name == "mxfp8" else K // 2
+            out = mx.MXGEMM_OUT_BF16 if WORKLOADS[name]["out"] == "bf16" else mx.MXGEMM_OUT_F32
+            ob = 2 if out == mx.MXGEMM_OUT_BF16 else 4
+            g = torch.Generator(device=dev)
+            g.manual_seed(si * 7919 + nki)
+
+            def codes(rows):
+                c = torch.randint(0, 256, (rows, rb), dtype=torch.uint8, device=dev, generator=g)
+                if fmt_name == "mxfp8":
+                    c = torch.where((c & 0x7F) == 0x7F, c & 0xFE, c)
+                return c
+
+            set_bytes = (M + N) * rb + (M + N) * K // 32 + M * N * ob
+            nsets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+            nsets = min(nsets, max(2, int(40e9 // set_bytes)))
+            plan = mx.Plan(M, N, K, fmt, out, device=dev)
+            sets = []
+            for _ in range(nsets):
+                SA = torch.randint(120, 135, (M, K // 32), dtype=torch.uint8, device=dev, generator=g)
+                SB = torch.randint(120, 135, (N, K // 32), dtype=torch.uint8, device=dev, generator=g)
+                sets.append((codes(M), mx.relayout_scales(SA, M, K), codes(N), mx.relayout_scales(SB, N, K),
+                             torch.empty((M, N), dtype=torch.bfloat16 if ob == 2 else torch.float32, device=dev)))
+            pre = mx.MXGEMM_RUN_SA_PRELAYOUT | mx.MXGEMM_RUN_SB_PRELAYOUT
+
+            def one(i):
+                a, sa, b, sb, c = sets[i % nsets]
+                st = mx.mxgemm_run(plan.handle, a.data_ptr(), sa.data_ptr(), b.data_ptr(), sb.data_ptr(),
+                                   c.data_ptr(), plan.workspace.data_ptr(), plan.ws_bytes, pre, sh)
+                assert st == 0
+
+            for i in range(3):
+                one(i)
+            torch.cuda.synchronize()
+            reps = args.sweep_reps
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+            for i in range(reps):
+                e[i].record(stream)
+                one(i)
+            e[reps].record(stream)
+            torch.cuda.synchronize()
+            mx.check_device_status()
+            ts = sorted(e[i].elapsed_time(e[i + 1]) for i in range(reps))
+            t = statistics.median(ts) / 1e3
+            flops = 2.0 * M * N * K
+            byts = algorithmic_bytes(M, N, K, fmt_name, ob)
+            peak = mx_peak_tflops(fmt_name, bf16_tf)
+            t_roof = max(flops / (peak * 1e12), byts / (hbm_gbs * 1e9))
+            print(json.dumps({
+                "workload": name, "format": fmt_name, "M": M, "N": N, "K": K, "us": t * 1e6,
+                "tflops": flops / t / 1e12, "gbs": byts / t / 1e9,
+                "frac_tensor": flops / t / 1e12 / peak, "frac_hbm": byts / t / 1e9 / hbm_gbs,
+                "frac_roofline": t_roof / t, "bound": "tensor" if flops / (peak * 1e12) > byts / (hbm_gbs * 1e9)
+                else "hbm", "plan": plan.describe(), "nsets": nsets}), flush=True)
+            del sets, plan
+            torch.cuda.empty_cache()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--soak-s", type=float, default=2.0, help="untimed load before the timed region (clocks)")
+    ap.add_argument("--cpu-target-s", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-workloads", default="")
+    ap.add_argument("--sweep-reps", type=int, default=20)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
