@@ -181,6 +181,38 @@ MXGEMM_API int mxgemm_selftest_stall(mxgemm_plan_t plan, const void *A, const ui
                           const void *B, const uint8_t *SB, void *C,
                           void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * mxgemm_run without a workspace argument, for callers that cannot allocate
+ * device memory.  (The FlyDSL pages have no counterpart: this is an interface
+ * convenience of this library, not part of the method.)
+ *
+ * Who needs it: callers that own only their inputs and outputs and may not
+ * call cudaMalloc (or any allocating routine) around a GEMM -- e.g. a serving
+ * loop whose device memory was planned once at start-up, where a cudaMalloc
+ * would synchronise the device and can fail once memory is fragmented, or a
+ * plain C host program with no allocator of its own to hand a workspace over.
+ *
+ * The scratch it uses instead (tile-layout scales, split-K partial sums) is
+ * one static device array of MXGEMM_NOALLOC_SCRATCH_BYTES inside the library.
+ * Every GPU that loads the library holds that array until the process exits.
+ *   - Plans whose mxgemm_workspace_bytes() exceeds MXGEMM_NOALLOC_SCRATCH_BYTES
+ *     are rejected with MXGEMM_ERR_WORKSPACE before anything is launched.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents.  Calls that overlap on the GPU (different streams without
+ *     ordering between them, or several host threads) race on it: order them.
+ *     Nothing in the array needs to start at zero -- each call rewrites every
+ *     byte it later reads.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ * Arguments, results and errors are otherwise those of mxgemm_run.  No
+ * cudaMalloc, cudaFree or other allocating call is made.
+ */
+#define MXGEMM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+MXGEMM_API int mxgemm_run_noalloc(mxgemm_plan_t plan, const void *A, const uint8_t *SA,
+                                  const void *B, const uint8_t *SB, void *C,
+                                  uint32_t run_flags, void *stream);
+
 /* Static, human-readable name of a status code. */
 MXGEMM_API const char *mxgemm_status_str(int status);
 

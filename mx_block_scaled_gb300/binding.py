@@ -48,6 +48,7 @@ SIGNATURES = [
     ("mxgemm_sf_bytes", ctypes.c_size_t, [_I64, _I64]),
     ("mxgemm_relayout_scales", ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     ("mxgemm_run", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
+    ("mxgemm_run_noalloc", ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_uint32, _P]),
     ("mxgemm_device_status", ctypes.c_int, [_P, ctypes.c_int]),
     ("mxgemm_selftest_stall", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     ("mxgemm_status_str", ctypes.c_char_p, [ctypes.c_int]),
@@ -117,6 +118,14 @@ def mxgemm_relayout_scales(src_ptr: int, rows: int, K: int, dst_ptr: int, stream
 def mxgemm_run(plan, A_ptr: int, SA_ptr: int, B_ptr: int, SB_ptr: int, C_ptr: int,
                ws_ptr: int, ws_bytes: int, run_flags: int, stream: int) -> int:
     return _lib.mxgemm_run(plan, A_ptr, SA_ptr, B_ptr, SB_ptr, C_ptr, ws_ptr, ws_bytes, run_flags, stream)
+
+
+def mxgemm_run_noalloc(plan, A_ptr: int, SA_ptr: int, B_ptr: int, SB_ptr: int, C_ptr: int,
+                       run_flags: int, stream: int) -> int:
+    return _lib.mxgemm_run_noalloc(plan, A_ptr, SA_ptr, B_ptr, SB_ptr, C_ptr, run_flags, stream)
+
+
+MXGEMM_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def mxgemm_device_status(stream: int, reset: bool = True) -> int:

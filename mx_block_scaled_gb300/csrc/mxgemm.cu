@@ -488,6 +488,44 @@ int mxgemm_selftest_stall(mxgemm_plan_t plan, const void *A, const uint8_t *SA, 
                     stream, 1, 20000000ull);
 }
 
+// ------------------------------------------------------------- no-alloc --
+// Scratch for mxgemm_run_noalloc: a fixed, file-scope device array, so callers
+// that cannot allocate device memory still get the relayout and split-K space
+// mxgemm_run takes from its workspace argument.  Host code never dereferences
+// the symbol itself; it passes the device address found by
+// cudaGetSymbolAddress (looked up once per device, with that device current).
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MXGEMM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void *g_noalloc_addr[kMaxDevices];
+std::mutex g_noalloc_mutex;
+}  // namespace
+
+int mxgemm_run_noalloc(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB,
+                       void *C, uint32_t run_flags, void *stream)
+{
+    if (!plan)
+        return MXGEMM_ERR_ARG;
+    if (plan->ws_bytes > MXGEMM_NOALLOC_SCRATCH_BYTES)
+        return MXGEMM_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return MXGEMM_ERR_CUDA;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (g_noalloc_addr[dev] == nullptr) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+                return MXGEMM_ERR_CUDA;
+            g_noalloc_addr[dev] = p;
+        }
+        scratch = g_noalloc_addr[dev];
+    }
+    return run_impl(plan, A, SA, B, SB, C, scratch, MXGEMM_NOALLOC_SCRATCH_BYTES, run_flags, stream, 0,
+                    2000000000ull);
+}
+
 int mxgemm_device_status(void *stream, int reset)
 {
     DeviceInfo *dev = nullptr;
