@@ -16,13 +16,17 @@
 // layouts bring optimization close to hardware") is replaced here by a TMA ->
 // shared-memory ring -> tcgen05.mma pipeline with mbarrier hand-off.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer: per k-stage, A and B tiles (128-byte swizzle) and
 //               the tile-layout scale chunks (bulk copies) into ring slot s.
 //   warp 1      TMEM owner and MMA issuer: per k-stage, tcgen05.cp of the scale
 //               chunks into TMEM, then BK/32 (MXFP8) or BK/64 (MXFP4)
 //               block-scaled MMAs accumulating in TMEM; commits free the slot.
-//   warps 2..5  epilogue: TMEM -> registers -> (BF16) -> global, masked edges.
+//   warps 2..9  epilogue: warp w owns TMEM lane quarter w%4 and one half of the
+//               tile's columns; it loads its whole share of the accumulator into
+//               registers, releases the TMEM stage to the MMA warp at once, and
+//               only then converts (BF16) and stores to global (masked edges), so
+//               the stores overlap the next tile's MMAs.
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // MXGEMM_ERR_DEVICE_TIMEOUT in *status, drains its in-flight copies and MMAs,
 // frees its TMEM and exits.
@@ -36,7 +40,8 @@
 
 namespace mxg {
 
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                 // epilogue warps (two per TMEM lane quarter)
+constexpr int kThreads = 64 + 32 * kEpiWarps; // producer warp + MMA warp + epilogue
 constexpr int kBM = 128;            // MMA M (rows of the A role per tile)
 constexpr int kRowBytes = 128;      // bytes of one operand row per k-stage
 constexpr int kSfChunk = 512;       // bytes of one scale chunk (128 rows x 4 K-blocks)
@@ -81,12 +86,14 @@ struct Cfg {
     static constexpr int kSfbCols = 4 * kKtPerStage * kChunksB;
     static constexpr int kAccStages = (2 * BN + kSfaCols + kSfbCols <= 512) ? 2 : 1;
     static constexpr int kTmemCols = 512;
-    static constexpr int kSfaCol = kAccStages * BN;
-    static constexpr int kSfbCol = kSfaCol + kSfaCols;
+    // Scale columns: one (SFA, SFB) region per ring slot, so the tcgen05.cp of the
+    // next stage never overwrites scales that MMAs of the previous stage still read.
+    static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
+    static constexpr int kSfCol0 = kAccStages * BN;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
     static constexpr uint32_t kIdesc = idesc_block_scaled(FP4 ? 1u : 0u, kBM, BN);
     static_assert(kStages >= 2, "shared memory too small for two stages");
-    static_assert(kSfbCol + kSfbCols <= kTmemCols, "TMEM overflow");
+    static_assert(kSfCol0 + kStages * kSfSlotCols <= kTmemCols, "TMEM overflow");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be 32..256, multiple of 32");
 };
 
@@ -192,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
-            mbar_init(acce_bar(a), 4);
+            mbar_init(acce_bar(a), kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         fence_mbar_init();
@@ -213,14 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0 && !p.test_stall) {
+        // The whole warp runs the loop (so loop state stays warp-uniform); one
+        // elected lane issues the barrier arm and the copies.
+        if (!p.test_stall) {
             const uint64_t pol_a = l2_policy_evict_last();
             const uint64_t pol_b = l2_policy_evict_last();
             int st = 0;
             uint32_t ph = 0;
-            int armed_parity[S];
-#pragma unroll
-            for (int s = 0; s < S; ++s) armed_parity[s] = -1;
+            uint32_t armed = 0;      // bit s: slot s armed at least once
+            uint32_t armed_ph = 0;   // bit s: parity of slot s's last arm
             bool ok = true;
             const int nrb_b = (p.rows_b + 127) / 128;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
@@ -228,32 +236,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_coords(p, u, tm, tn, sp);
                 const int ks0 = sp * p.kstages_per_split;
                 const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+                // B-role scale chunks present for this tile (row blocks past the end are skipped)
+                const int rb_b0 = (tn * BN) / 128;
+                const int nchunk_b = min(C::kChunksB, nrb_b - rb_b0);
                 for (int ks = ks0; ks < ks1; ++ks) {
-                    if (!mbar_wait(empty_bar(st), ph ^ 1u, abort, lim)) {
-                        record_timeout(p, abort);
+                    if (!warp_wait(empty_bar(st), ph ^ 1u, abort, lim)) {
+                        if (lane == 0) record_timeout(p, abort);
                         ok = false;
                         break;
                     }
                     const int kt0 = ks * C::kKtPerStage;
                     const int nkt = min(C::kKtPerStage, p.num_kt - kt0);
-                    // B-role scale chunks present for this tile (row blocks past the end are skipped)
-                    int nchunk_b = 0;
-                    const int rb_b0 = (tn * BN) / 128;
-#pragma unroll
-                    for (int c = 0; c < C::kChunksB; ++c)
-                        if (rb_b0 + c < nrb_b) ++nchunk_b;
                     const uint32_t bytes = C::kABytes + C::kBBytes + nkt * kSfChunk * (1 + nchunk_b);
-                    mbar_arrive_expect_tx(full_bar(st), bytes);
-                    armed_parity[st] = static_cast<int>(ph);
-                    tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, tm * kBM, pol_a);
-                    tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, tn * BN, pol_b);
-                    bulk_load(sSFA + st * C::kSfaBytes,
-                              p.sfa + (static_cast<size_t>(tm) * p.num_kt + kt0) * kSfChunk,
-                              nkt * kSfChunk, full_bar(st));
-                    for (int c = 0; c < nchunk_b; ++c)
-                        bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
-                                  p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(full_bar(st), bytes);
+                        tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, tm * kBM, pol_a);
+                        tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, tn * BN, pol_b);
+                        bulk_load(sSFA + st * C::kSfaBytes,
+                                  p.sfa + (static_cast<size_t>(tm) * p.num_kt + kt0) * kSfChunk,
                                   nkt * kSfChunk, full_bar(st));
+                        for (int c = 0; c < nchunk_b; ++c)
+                            bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
+                                      p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
+                                      nkt * kSfChunk, full_bar(st));
+                    }
+                    __syncwarp();
+                    armed |= 1u << st;
+                    armed_ph = (armed_ph & ~(1u << st)) | (ph << st);
                     if (++st == S) {
                         st = 0;
                         ph ^= 1u;
@@ -262,91 +271,114 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 // Drain: let every armed stage finish landing before the CTA exits.
-                for (int s = 0; s < S; ++s)
-                    if (armed_parity[s] >= 0)
-                        mbar_wait(full_bar(s), static_cast<uint32_t>(armed_parity[s]), no_abort, lim);
+                for (int s2 = 0; s2 < S; ++s2)
+                    if (armed & (1u << s2))
+                        warp_wait(full_bar(s2), (armed_ph >> s2) & 1u, no_abort, lim);
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            int st = 0;
-            uint32_t ph = 0;
-            int it = 0;
-            bool ok = true;
-            bool issued = false;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
-                int tm, tn, sp;
-                tile_coords(p, u, tm, tn, sp);
-                (void)tm;
-                const int acc = it % C::kAccStages;
-                const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
-                if (!mbar_wait(acce_bar(acc), acc_par ^ 1u, abort, lim)) {
-                    record_timeout(p, abort);
+        // Warp-uniform loop; every tcgen05 instruction is issued by the same
+        // elected lane (tcgen05.commit tracks that lane's earlier operations).
+        int st = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        bool ok = true;
+        bool issued = false;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
+            int tm, tn, sp;
+            tile_coords(p, u, tm, tn, sp);
+            (void)tm;
+            const int acc = it % C::kAccStages;
+            const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
+            if (!warp_wait(acce_bar(acc), acc_par ^ 1u, abort, lim)) {
+                if (lane == 0) record_timeout(p, abort);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + acc * BN;
+            const uint32_t sub_off = static_cast<uint32_t>(((tn * BN) % 128) / 32);  // BN < 128 only
+            const int ks0 = sp * p.kstages_per_split;
+            const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+            for (int ks = ks0; ks < ks1; ++ks) {
+                if (!warp_wait(full_bar(st), ph, abort, lim)) {
+                    if (lane == 0) record_timeout(p, abort);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + acc * BN;
-                const uint32_t sub_off = static_cast<uint32_t>(((tn * BN) % 128) / 32); // BN < 128 only
-                const int ks0 = sp * p.kstages_per_split;
-                const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
-                for (int ks = ks0; ks < ks1; ++ks) {
-                    if (!mbar_wait(full_bar(st), ph, abort, lim)) {
-                        record_timeout(p, abort);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const int nkt = min(C::kKtPerStage, p.num_kt - ks * C::kKtPerStage);
-                    // Scales: shared memory -> TMEM (in issue order with the MMAs below).
-                    for (int t = 0; t < nkt; ++t) {
-                        tc_cp_32x128b_warpx4(tmem + C::kSfaCol + 4 * t,
-                                             sdesc_sf_chunk(sSFA + st * C::kSfaBytes + t * kSfChunk));
+                const int nkt = min(C::kKtPerStage, p.num_kt - ks * C::kKtPerStage);
+                // Scales: shared memory -> this slot's TMEM scale region (in issue order
+                // with the MMAs below).
+                const uint32_t sfa_col = tmem + C::kSfCol0 + st * C::kSfSlotCols;
+                const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                const uint32_t sfa_src = sSFA + st * C::kSfaBytes;
+                const uint32_t sfb_src = sSFB + st * C::kSfbBytes;
 #pragma unroll
-                        for (int c = 0; c < C::kChunksB; ++c)
-                            tc_cp_32x128b_warpx4(
-                                tmem + C::kSfbCol + 4 * (t * C::kChunksB + c),
-                                sdesc_sf_chunk(sSFB + st * C::kSfbBytes + (c * C::kKtPerStage + t) * kSfChunk));
-                    }
-                    const uint64_t adesc = sdesc_kmajor_sw128(sA + st * C::kABytes);
-                    const uint64_t bdesc = sdesc_kmajor_sw128(sB + st * C::kBBytes);
-                    const int nsub = nkt * C::kSubPerKt;
-                    for (int s = 0; s < nsub; ++s) {
-                        const int t = s / C::kSubPerKt;
-                        const uint32_t sf_id = FP4 ? static_cast<uint32_t>((s % 2) * 2) : static_cast<uint32_t>(s % 4);
-                        const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, sf_id, sf_id);
-                        const uint32_t sfa_t = tmem + C::kSfaCol + 4 * t;
-                        const uint32_t sfb_t = tmem + C::kSfbCol + 4 * t * C::kChunksB + sub_off;
-                        // advance 32 bytes along K per MMA (32 FP8 or 64 FP4 elements)
-                        const uint64_t koff = static_cast<uint64_t>((s * 32) >> 4);
-                        if (FP4)
-                            mma_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t,
-                                     (ks > ks0 || s > 0) ? 1u : 0u);
-                        else
-                            mma_mxf8f6f4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t,
-                                         (ks > ks0 || s > 0) ? 1u : 0u);
-                        issued = true;
-                    }
-                    tc_commit(empty_bar(st));
-                    if (++st == S) {
-                        st = 0;
-                        ph ^= 1u;
+                for (int t = 0; t < C::kKtPerStage; ++t) {
+                    if (t < nkt) {
+                        if (elect_one())
+                            tc_cp_32x128b_warpx4(sfa_col + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
+#pragma unroll
+                        for (int c = 0; c < C::kChunksB; ++c) {
+                            const uint64_t d = sdesc_sf_chunk(sfb_src + (c * C::kKtPerStage + t) * kSfChunk);
+                            if (elect_one())
+                                tc_cp_32x128b_warpx4(sfb_col + 4 * (t * C::kChunksB + c), d);
+                        }
                     }
                 }
-                if (!ok) break;
+                const uint64_t adesc = sdesc_kmajor_sw128(sA + st * C::kABytes);
+                const uint64_t bdesc = sdesc_kmajor_sw128(sB + st * C::kBBytes);
+                const uint32_t acc0 = (ks > ks0) ? 1u : 0u;
+#pragma unroll
+                for (int s = 0; s < C::kKtPerStage * C::kSubPerKt; ++s) {
+                    constexpr int kSub = C::kSubPerKt;
+                    const int t = s / kSub;
+                    if (t < nkt) {
+                        const uint32_t sf_id = FP4 ? static_cast<uint32_t>((s % 2) * 2) : static_cast<uint32_t>(s % 4);
+                        const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, sf_id, sf_id);
+                        const uint32_t sfa_t = sfa_col + 4 * t;
+                        const uint32_t sfb_t = sfb_col + 4 * t * C::kChunksB + sub_off;
+                        // advance 32 bytes along K per MMA (32 FP8 or 64 FP4 elements)
+                        const uint64_t koff = static_cast<uint64_t>((s * 32) >> 4);
+                        const uint32_t accum = (s > 0) ? 1u : acc0;
+                        if (elect_one()) {
+                            if (FP4)
+                                mma_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
+                            else
+                                mma_mxf8f6f4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
+                        }
+                    }
+                }
+                issued = true;
+                if (elect_one())
+                    tc_commit(empty_bar(st));
+                __syncwarp();
+                if (++st == S) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (elect_one())
                 tc_commit(accf_bar(acc));
-            }
-            if (!ok && issued) {
-                // Drain the tensor pipe before TMEM is released.
-                tc_commit(drain_bar);
-                mbar_wait(drain_bar, 0, no_abort, lim);
-            }
+            __syncwarp();
         }
-        __syncwarp();
+        if (!ok && issued) {
+            // Drain the tensor pipe before TMEM is released.
+            if (elect_one())
+                tc_commit(drain_bar);
+            __syncwarp();
+            warp_wait(drain_bar, 0, no_abort, lim);
+        }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int q = warp & 3;         // TMEM lane quarter this warp may access
+        const int h = (warp - 2) >> 2;  // column half
+        constexpr int kCols = BN / 2 >= 32 ? BN / 2 : 32;
+        constexpr int kChunks = kCols / 32;
+        const bool has_cols = h * kCols < BN;
         int it = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
             int tm, tn, sp;
@@ -361,27 +393,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const int i = tm * kBM + q * 32 + lane;  // A-role row owned by this thread
-            const bool row_ok = i < p.rows_a;
-            const long long split_off = static_cast<long long>(sp) * p.split_stride;
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t r[32];
-                __syncwarp();
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0, r);
-                tmem_ld_wait(r);
-                const int j0 = tn * BN + c0;
-                if (row_ok && j0 < p.rows_b) {
-                    const long long base_off = split_off + static_cast<long long>(i) * p.stride_i;
-                    if (p.vec_ok && j0 + 32 <= p.rows_b)
-                        store_row32_vec(p, base_off + j0, r);
-                    else
-                        store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), r);
-                }
+            uint32_t r[kChunks][32];
+            if (has_cols) {
+                const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + h * kCols;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    reg_fence(r[c]);
             }
+            // The accumulator stage is in registers now: hand it back to the MMA warp.
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));
+
+            const int i = tm * kBM + q * 32 + lane;  // A-role row owned by this thread
+            if (has_cols && i < p.rows_a) {
+                const long long base_off =
+                    static_cast<long long>(sp) * p.split_stride + static_cast<long long>(i) * p.stride_i;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    const int j0 = tn * BN + h * kCols + c * 32;
+                    if (j0 >= p.rows_b) break;
+                    if (p.vec_ok && j0 + 32 <= p.rows_b)
+                        store_row32_vec(p, base_off + j0, r[c]);
+                    else
+                        store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), r[c]);
+                }
+            }
         }
     }
 

@@ -73,48 +73,54 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ----------------------------------------------------------- scale relayout --
-// One block per (128-row block, up to 32 K-tiles): the 128 x (32 x 4) scale
-// bytes are staged in shared memory as 32-bit words (4 K-blocks each), then
-// written as 512-byte tiles.  Inside a tile, row r = 32q + p and K-block c of
-// the tile go to byte p*16 + q*4 + c: the layout the tensor cores read scale
-// factors from when a 32-row x 16-byte chunk is copied into TMEM.
+// One block per (128-row block, up to 8 K-tiles): the 128 x (8 x 4) scale bytes
+// are staged in shared memory as 32-bit words (4 K-blocks each; all four loads
+// of a thread in flight at once), then written as 512-byte tiles, one 16-byte
+// store per thread.  Inside a tile, row r = 32q + p and K-block c of the tile go
+// to byte p*16 + q*4 + c: the layout the tensor cores read scale factors from
+// when a 32-row x 16-byte chunk is copied into TMEM.
+constexpr int kRelayoutKt = 8;  // K-tiles (of 4 K-blocks) per block
+
 struct RelayoutJob {
     const uint8_t *src;
     uint8_t *dst;
     int rows;
     int num_kt;   // K / 128
-    int blocks_x; // ceil(num_kt / 32)
+    int blocks_x; // ceil(num_kt / kRelayoutKt)
     int blocks;   // ceil(rows / 128) * blocks_x
 };
 
 __global__ void __launch_bounds__(256) relayout_scales_kernel(RelayoutJob j0, RelayoutJob j1)
 {
-    __shared__ uint32_t tile[128][33];
+    __shared__ uint32_t tile[128][kRelayoutKt + 1];
     int b = blockIdx.x;
     const RelayoutJob &j = (b < j0.blocks) ? j0 : j1;
     if (b >= j0.blocks)
         b -= j0.blocks;
     const int rb = b / j.blocks_x;
-    const int kt0 = (b % j.blocks_x) * 32;
-    const int kb_words = j.num_kt;  // 32-bit words per source row (K/32 bytes / 4)
-    const uint32_t *src = reinterpret_cast<const uint32_t *>(j.src);
-    for (int idx = threadIdx.x; idx < 128 * 32; idx += 256) {
-        const int r = idx >> 5, w = idx & 31;
+    const int kt0 = (b % j.blocks_x) * kRelayoutKt;
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(j.src);  // num_kt words per row
+    uint32_t v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = threadIdx.x + 256 * i;
+        const int r = idx / kRelayoutKt, w = idx % kRelayoutKt;
         const int row = rb * 128 + r, kt = kt0 + w;
-        uint32_t v = 0x7F7F7F7Fu;  // padding rows: scale code 127 (x1.0)
+        v[i] = 0x7F7F7F7Fu;  // padding rows: scale code 127 (x1.0)
         if (row < j.rows && kt < j.num_kt)
-            v = __ldg(src + static_cast<size_t>(row) * kb_words + kt);
-        tile[r][w] = v;
+            v[i] = __ldg(src + static_cast<size_t>(row) * j.num_kt + kt);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = threadIdx.x + 256 * i;
+        tile[idx / kRelayoutKt][idx % kRelayoutKt] = v[i];
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < 32 * 32; idx += 256) {
-        const int w = idx >> 5, p = idx & 31;
-        const int kt = kt0 + w;
-        if (kt >= j.num_kt)
-            continue;
-        uint4 v = make_uint4(tile[p][w], tile[32 + p][w], tile[64 + p][w], tile[96 + p][w]);
-        uint4 *dst = reinterpret_cast<uint4 *>(j.dst + (static_cast<size_t>(rb) * j.num_kt + kt) * 512);
-        dst[p] = v;
+    const int w = threadIdx.x >> 5, p = threadIdx.x & 31;
+    const int kt = kt0 + w;
+    if (kt < j.num_kt) {
+        uint4 o = make_uint4(tile[p][w], tile[32 + p][w], tile[64 + p][w], tile[96 + p][w]);
+        reinterpret_cast<uint4 *>(j.dst + (static_cast<size_t>(rb) * j.num_kt + kt) * 512)[p] = o;
     }
 }
 
@@ -125,7 +131,7 @@ RelayoutJob make_job(const uint8_t *src, int64_t rows, int64_t K, uint8_t *dst)
     j.dst = dst;
     j.rows = static_cast<int>(rows);
     j.num_kt = static_cast<int>(K / 128);
-    j.blocks_x = static_cast<int>(ceil_div(j.num_kt, 32));
+    j.blocks_x = static_cast<int>(ceil_div(j.num_kt, kRelayoutKt));
     j.blocks = static_cast<int>(ceil_div(rows, 128)) * j.blocks_x;
     return j;
 }

@@ -20,7 +20,18 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
-__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
+// One lane of the (fully active) warp gets true: the same lane every time.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\t"
+        "elect.sync rx|px, %1;\n\t"
+        "@px mov.s32 %0, 1;\n\t}"
+        : "+r"(pred)
+        : "r"(0xffffffffu));
+    return pred != 0;
+}
 
 // ---------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
@@ -76,6 +87,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
         if (global_timer_ns() - t0 > limit_ns)
             return false;
     }
+}
+
+// Warp-wide bounded wait: every lane polls, the result is the same in all lanes.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                          uint64_t limit_ns)
+{
+    const bool ok = mbar_wait(bar, parity, abort, limit_ns);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // ------------------------------------------------------------ TMA / bulk --
@@ -193,11 +212,12 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
-// Wait for this thread's outstanding tcgen05.ld, then pin the registers after
-// the wait so no use of them can be scheduled before it.
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
+// Wait for all of this thread's outstanding tcgen05.ld.
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Pin registers after a wait so that no use of them is scheduled before it.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32])
 {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i)
         asm volatile("" : "+r"(r[i])::"memory");
