@@ -397,7 +397,6 @@ def run_sweep(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
-    sh = stream.cuda_stream
     hbm_gbs, bf16_tf, _, peak_src = load_peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     names = args.sweep_workloads.split(",") if args.sweep_workloads else list(WORKLOADS)
@@ -423,7 +422,7 @@ def run_sweep(args):
             set_bytes = (M + N) * rb + (M + N) * K // 32 + M * N * ob
             nsets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
             nsets = min(nsets, max(2, int(40e9 // set_bytes)))
-            plan = mx.Plan(M, N, K, fmt, out, device=dev)
+            plan = mx.Plan(M, N, K, fmt, out, flags=args.sweep_flags, device=dev)
             sets = []
             for _ in range(nsets):
                 SA = torch.randint(120, 135, (M, K // 32), dtype=torch.uint8, device=dev, generator=g)
@@ -435,21 +434,32 @@ def run_sweep(args):
             def one(i):
                 a, sa, b, sb, c = sets[i % nsets]
                 st = mx.mxgemm_run(plan.handle, a.data_ptr(), sa.data_ptr(), b.data_ptr(), sb.data_ptr(),
-                                   c.data_ptr(), plan.workspace.data_ptr(), plan.ws_bytes, pre, sh)
+                                   c.data_ptr(), plan.workspace.data_ptr(), plan.ws_bytes, pre,
+                                   torch.cuda.current_stream().cuda_stream)
                 assert st == 0
 
             for i in range(3):
                 one(i)
             torch.cuda.synchronize()
             reps = args.sweep_reps
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-            for i in range(reps):
-                e[i].record(stream)
-                one(i)
-            e[reps].record(stream)
+            # Replay `reps` calls from a CUDA graph so that host-side launch cost does not
+            # show up in the device time of short GEMMs.
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(reps):
+                    one(i)
+            graph.replay()
             torch.cuda.synchronize()
+            ts = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) / reps)
             mx.check_device_status()
-            ts = sorted(e[i].elapsed_time(e[i + 1]) for i in range(reps))
+            del graph
             t = statistics.median(ts) / 1e3
             flops = 2.0 * M * N * K
             byts = algorithmic_bytes(M, N, K, fmt_name, ob)
@@ -479,6 +489,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-workloads", default="")
     ap.add_argument("--sweep-reps", type=int, default=20)
+    ap.add_argument("--sweep-flags", type=int, default=0, help="mxgemm_plan_create flags for --sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

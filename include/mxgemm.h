@@ -78,6 +78,10 @@ typedef enum {
 #define MXGEMM_PLAN_FORCE_BN256     (1u << 1)  /* force a 256-wide N tile             */
 #define MXGEMM_PLAN_FORCE_NOSWAP    (1u << 2)  /* never compute C^T = B*A^T           */
 #define MXGEMM_PLAN_FORCE_SWAP      (1u << 3)  /* always compute C^T = B*A^T          */
+#define MXGEMM_PLAN_FORCE_PAIR      (1u << 4)  /* 256-row tiles on CTA pairs          */
+#define MXGEMM_PLAN_FORCE_SINGLE    (1u << 5)  /* 128-row tiles, one CTA per tile     */
+#define MXGEMM_PLAN_FORCE_MC        (1u << 6)  /* 128-row tiles, CTA pairs share B    */
+#define MXGEMM_PLAN_STREAMK         (1u << 7)  /* spread the last wave's k-stages     */
 #define MXGEMM_PLAN_SPLITK_SHIFT    8          /* bits 8..15: forced split-K (0=auto) */
 
 /* Run flags (mxgemm_run). */
@@ -149,6 +153,8 @@ MXGEMM_API int mxgemm_relayout_scales(const uint8_t *src, int64_t rows, int64_t 
  * Enqueues (1) the relayout of whichever scales are not pre-laid-out and
  * (2) the persistent tcgen05 block-scaled GEMM kernel (3) a split-K reduce if
  * the plan splits K.  Inputs are read-only; C is fully overwritten.
+ * A plan belongs to the device that was current when it was created; running
+ * it with another device current returns MXGEMM_ERR_ARG.
  * Errors: MXGEMM_ERR_ARG, MXGEMM_ERR_ALIGN, MXGEMM_ERR_WORKSPACE,
  * MXGEMM_ERR_CUDA.  A device-side wait that exceeds its limit is reported by
  * mxgemm_device_status(), not here (the call is asynchronous).

@@ -31,6 +31,10 @@ MXGEMM_PLAN_FORCE_BN128 = 1 << 0
 MXGEMM_PLAN_FORCE_BN256 = 1 << 1
 MXGEMM_PLAN_FORCE_NOSWAP = 1 << 2
 MXGEMM_PLAN_FORCE_SWAP = 1 << 3
+MXGEMM_PLAN_FORCE_PAIR = 1 << 4
+MXGEMM_PLAN_FORCE_SINGLE = 1 << 5
+MXGEMM_PLAN_FORCE_MC = 1 << 6
+MXGEMM_PLAN_STREAMK = 1 << 7
 MXGEMM_PLAN_SPLITK_SHIFT = 8
 
 MXGEMM_RUN_SA_PRELAYOUT = 1 << 0

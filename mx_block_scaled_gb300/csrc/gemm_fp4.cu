@@ -1,5 +1,6 @@
 // gemm_fp4.cu -- MXFP4 (E2M1 packed, kind::mxf4, scale_vec::2X) instantiations of
 // the persistent block-scaled GEMM kernel.
+#include "gemm_kernel_pair.cuh"
 #include "launch.h"
 
 namespace mxg {
@@ -9,12 +10,80 @@ template <int BN>
 cudaError_t launch(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid, cudaStream_t s)
 {
     using C = Cfg<true, BN>;
-    auto kern = mx_gemm_kernel<true, BN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess)
-        return e;
-    kern<<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
+    mx_gemm_kernel<true, BN><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
     return cudaGetLastError();
+}
+
+cudaLaunchConfig_t cluster2_config(int clusters, int smem, cudaStream_t s, cudaLaunchAttribute *attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int BN>
+cudaError_t launch_pair(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int clusters,
+                        cudaStream_t s)
+{
+    auto kern = mx_gemm_pair_kernel<true, BN>;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<true, BN>::kSmemBytes, s, attr);
+    return cudaLaunchKernelEx(&cfg, kern, p, ma, mb);
+}
+
+template <int BN>
+int pair_max_clusters()
+{
+    auto kern = mx_gemm_pair_kernel<true, BN>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgPair<true, BN>::kSmemBytes) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster2_config(1, CfgPair<true, BN>::kSmemBytes, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+template <int BN>
+cudaError_t launch_mc(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int clusters, cudaStream_t s)
+{
+    auto kern = mx_gemm_kernel<true, BN, true>;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster2_config(clusters, Cfg<true, BN>::kSmemBytes, s, attr);
+    return cudaLaunchKernelEx(&cfg, kern, p, ma, mb);
+}
+
+template <int BN>
+int mc_max_clusters()
+{
+    auto kern = mx_gemm_kernel<true, BN, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true, BN>::kSmemBytes) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster2_config(1, Cfg<true, BN>::kSmemBytes, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+template <int BN>
+KernelInfo pair_info()
+{
+    using C = CfgPair<true, BN>;
+    return KernelInfo{C::kStages, C::kAccStages, C::kSmemBytes};
 }
 
 template <int BN>
@@ -24,6 +93,31 @@ KernelInfo info()
     return KernelInfo{C::kStages, C::kAccStages, C::kSmemBytes};
 }
 }  // namespace
+
+// Opt every instantiation into its shared-memory size (once per device; called
+// when a plan is created, never on the launch path).
+cudaError_t prepare_gemm_fp4()
+{
+    const void *single[4] = {(const void *)mx_gemm_kernel<true, 32>, (const void *)mx_gemm_kernel<true, 64>,
+                             (const void *)mx_gemm_kernel<true, 128>, (const void *)mx_gemm_kernel<true, 256>};
+    const int single_smem[4] = {Cfg<true, 32>::kSmemBytes, Cfg<true, 64>::kSmemBytes, Cfg<true, 128>::kSmemBytes,
+                                Cfg<true, 256>::kSmemBytes};
+    for (int i = 0; i < 4; ++i) {
+        cudaError_t e = cudaFuncSetAttribute(single[i], cudaFuncAttributeMaxDynamicSharedMemorySize, single_smem[i]);
+        if (e != cudaSuccess)
+            return e;
+    }
+    const void *cl[4] = {(const void *)mx_gemm_kernel<true, 128, true>, (const void *)mx_gemm_kernel<true, 256, true>,
+                         (const void *)mx_gemm_pair_kernel<true, 128>, (const void *)mx_gemm_pair_kernel<true, 256>};
+    const int cl_smem[4] = {Cfg<true, 128>::kSmemBytes, Cfg<true, 256>::kSmemBytes, CfgPair<true, 128>::kSmemBytes,
+                            CfgPair<true, 256>::kSmemBytes};
+    for (int i = 0; i < 4; ++i) {
+        cudaError_t e = cudaFuncSetAttribute(cl[i], cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem[i]);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
 
 cudaError_t launch_gemm_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid,
                             cudaStream_t s)
@@ -36,6 +130,32 @@ cudaError_t launch_gemm_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, 
     default: return cudaErrorInvalidValue;
     }
 }
+
+cudaError_t launch_gemm_pair_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
+                                 int clusters, cudaStream_t s)
+{
+    switch (bn) {
+    case 128: return launch_pair<128>(p, ma, mb, clusters, s);
+    case 256: return launch_pair<256>(p, ma, mb, clusters, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gemm_mc_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
+                               int clusters, cudaStream_t s)
+{
+    switch (bn) {
+    case 128: return launch_mc<128>(p, ma, mb, clusters, s);
+    case 256: return launch_mc<256>(p, ma, mb, clusters, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int gemm_mc_max_clusters_fp4(int bn) { return bn == 128 ? mc_max_clusters<128>() : mc_max_clusters<256>(); }
+
+int gemm_pair_max_clusters_fp4(int bn) { return bn == 128 ? pair_max_clusters<128>() : pair_max_clusters<256>(); }
+
+KernelInfo gemm_pair_info_fp4(int bn) { return bn == 128 ? pair_info<128>() : pair_info<256>(); }
 
 KernelInfo gemm_info_fp4(int bn)
 {

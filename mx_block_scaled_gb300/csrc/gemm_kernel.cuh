@@ -68,6 +68,16 @@ struct GemmParams {
     long long split_stride;   // elements between split partial slabs (0: no split)
     unsigned long long timeout_ns;
     int *status;              // sticky device status word
+    // Stream-K (single-CTA kernel): the first dp_tiles tiles in raster order are
+    // computed whole, round-robin over the grid; the k-stages of the remaining
+    // tiles are divided evenly over CTAs 0..sk_ctas-1.  A tile cut between CTAs is
+    // finished by the last of them to arrive, which adds the others' FP32 partial
+    // sums in k order (deterministic).  sk_ctas == 0: no stream-K phase.
+    int dp_tiles;
+    int sk_ctas;
+    long long sk_stages;      // (tiles - dp_tiles) * kstages
+    int *sk_counters;         // one arrival counter per stream-K tile, zero at launch
+    float *sk_partials;       // two 128 x BN FP32 slots per stream-K CTA
 };
 
 template <bool FP4, int BN>
@@ -109,6 +119,82 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int unit, int &
     tm = first_m + local % gsz;
     tn = local / gsz;
 }
+
+// Raster position of tile t (grouped along the A role for L2 reuse).
+__device__ __forceinline__ void tile_xy(const GemmParams &p, int t, int &tm, int &tn)
+{
+    const int per_group = p.group_m * p.tiles_n;
+    const int group = t / per_group;
+    const int first_m = group * p.group_m;
+    const int gsz = min(p.tiles_m - first_m, p.group_m);
+    const int local = t - group * per_group;
+    tm = first_m + local % gsz;
+    tn = local / gsz;
+}
+
+// One piece of work: k-stages [ks0, ks1) of tile (tm, tn).
+struct Work {
+    int tile, tm, tn, ks0, ks1;
+    int kind;   // 0: the whole K of the tile; 1: stream-K segment; 2: split-K slab
+    int slot;   // kind 1: partial-sum slot (0: first segment of this CTA, 1: last)
+                // kind 2: split index
+};
+
+// The sequence of Work of one CTA; producer, MMA and epilogue warps each walk
+// an identical copy.
+struct WorkIter {
+    int u, step, units, spl;
+    long long pos, end, begin;
+
+    __device__ void init(const GemmParams &p, int cta, int ctas)
+    {
+        u = cta;
+        step = ctas;
+        spl = p.sk_ctas > 0 ? 1 : p.splits;
+        units = p.sk_ctas > 0 ? p.dp_tiles : p.tiles_m * p.tiles_n * p.splits;
+        pos = end = 0;
+        if (p.sk_ctas > 0 && cta < p.sk_ctas) {
+            pos = p.sk_stages * cta / p.sk_ctas;
+            end = p.sk_stages * (cta + 1) / p.sk_ctas;
+        }
+        begin = pos;
+    }
+
+    // Stream-K segments come first, so that the fixup of a cut tile (run by the
+    // epilogue warps of its last CTA) overlaps the whole tiles computed after it.
+    __device__ bool next(const GemmParams &p, Work &w)
+    {
+        if (pos < end) {
+            w.tile = p.dp_tiles + static_cast<int>(pos / p.kstages);
+            w.ks0 = static_cast<int>(pos % p.kstages);
+            w.ks1 = static_cast<int>(min(static_cast<long long>(p.kstages), w.ks0 + (end - pos)));
+            w.kind = (w.ks0 == 0 && w.ks1 == p.kstages) ? 0 : 1;
+            w.slot = pos == begin ? 0 : 1;
+            tile_xy(p, w.tile, w.tm, w.tn);
+            pos += w.ks1 - w.ks0;
+            return true;
+        }
+        if (u < units) {
+            w.tile = u / spl;
+            w.slot = u % spl;
+            w.ks0 = w.slot * p.kstages_per_split;
+            w.ks1 = min(p.kstages, w.ks0 + p.kstages_per_split);
+            w.kind = spl > 1 ? 2 : 0;
+            tile_xy(p, w.tile, w.tm, w.tn);
+            u += step;
+            return true;
+        }
+        return false;
+    }
+};
+
+// The stream-K CTA whose stage range contains stream-K stage x.
+__device__ __forceinline__ int sk_cta_of(const GemmParams &p, long long x)
+{
+    return static_cast<int>(((x + 1) * p.sk_ctas + p.sk_stages - 1) / p.sk_stages - 1);
+}
+
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
 
 __device__ __forceinline__ void record_timeout(const GemmParams &p, volatile int *abort)
 {
@@ -156,7 +242,12 @@ __device__ __forceinline__ void store_row32_masked(const GemmParams &p, long lon
     }
 }
 
-template <bool FP4, int BN>
+// MC = true: the kernel runs in clusters of two CTAs on vertically adjacent tiles
+// (same B-role tile); each CTA loads half of the B-role tile and multicasts it
+// to both, so the pair reads that tile from L2 once.  Slot reuse then needs
+// both CTAs' MMAs done: `empty` counts two commits (each MMA thread commits to
+// both CTAs' barriers).
+template <bool FP4, int BN, bool MC = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b)
@@ -195,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         abort_flag = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), MC ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
@@ -212,10 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (MC)
+        cluster_sync();  // the peer's barriers exist before the first multicast lands
     tc_fence_after();
     const uint32_t tmem = tmem_base_holder;
 
-    const int total_units = p.tiles_m * p.tiles_n * p.splits;
+    // Work: output tiles (x splits, or stream-K segments); with MC, vertical tile
+    // pairs, CTA r of the cluster taking A-role tile 2*tm + r.
+    const int mc_rank = MC ? static_cast<int>(cluster_ctarank()) : 0;
+    const int first_unit = MC ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int unit_step = MC ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
     const uint64_t lim = p.timeout_ns;
 
     if (warp == 0) {
@@ -231,30 +328,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t armed_ph = 0;   // bit s: parity of slot s's last arm
             bool ok = true;
             const int nrb_b = (p.rows_b + 127) / 128;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-                int tm, tn, sp;
-                tile_coords(p, u, tm, tn, sp);
-                const int ks0 = sp * p.kstages_per_split;
-                const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+            WorkIter wi;
+            wi.init(p, first_unit, unit_step);
+            Work w;
+            while (ok && wi.next(p, w)) {
+                int tm = w.tm;
+                const int tn = w.tn;
+                if (MC) tm = 2 * tm + mc_rank;
+                const bool has_sfa = tm < (p.rows_a + 127) / 128;  // false for an MC CTA past the last row
+                const int ks0 = w.ks0;
+                const int ks1 = w.ks1;
                 // B-role scale chunks present for this tile (row blocks past the end are skipped)
                 const int rb_b0 = (tn * BN) / 128;
                 const int nchunk_b = min(C::kChunksB, nrb_b - rb_b0);
                 for (int ks = ks0; ks < ks1; ++ks) {
-                    if (!warp_wait(empty_bar(st), ph ^ 1u, abort, lim)) {
+                    const bool freed = MC ? warp_wait_cluster(empty_bar(st), ph ^ 1u, abort, lim)
+                                          : warp_wait(empty_bar(st), ph ^ 1u, abort, lim);
+                    if (!freed) {
                         if (lane == 0) record_timeout(p, abort);
                         ok = false;
                         break;
                     }
                     const int kt0 = ks * C::kKtPerStage;
                     const int nkt = min(C::kKtPerStage, p.num_kt - kt0);
-                    const uint32_t bytes = C::kABytes + C::kBBytes + nkt * kSfChunk * (1 + nchunk_b);
+                    const uint32_t bytes =
+                        C::kABytes + C::kBBytes + nkt * kSfChunk * ((has_sfa ? 1 : 0) + nchunk_b);
                     if (elect_one()) {
                         mbar_arrive_expect_tx(full_bar(st), bytes);
                         tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, tm * kBM, pol_a);
-                        tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, tn * BN, pol_b);
-                        bulk_load(sSFA + st * C::kSfaBytes,
-                                  p.sfa + (static_cast<size_t>(tm) * p.num_kt + kt0) * kSfChunk,
-                                  nkt * kSfChunk, full_bar(st));
+                        if (MC)  // own half of the B-role tile, to both CTAs
+                            tma_load_2d_multicast(sB + st * C::kBBytes + mc_rank * (C::kBBytes / 2), &map_b,
+                                                  full_bar(st), ks * kRowBytes, tn * BN + mc_rank * (BN / 2), 0x3);
+                        else
+                            tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, tn * BN, pol_b);
+                        if (has_sfa)
+                            bulk_load(sSFA + st * C::kSfaBytes,
+                                      p.sfa + (static_cast<size_t>(tm) * p.num_kt + kt0) * kSfChunk,
+                                      nkt * kSfChunk, full_bar(st));
                         for (int c = 0; c < nchunk_b; ++c)
                             bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
                                       p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
@@ -285,10 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         bool ok = true;
         bool issued = false;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
-            int tm, tn, sp;
-            tile_coords(p, u, tm, tn, sp);
-            (void)tm;
+        WorkIter wi;
+        wi.init(p, first_unit, unit_step);
+        Work w;
+        for (; ok && wi.next(p, w); ++it) {
+            const int tn = w.tn;
             const int acc = it % C::kAccStages;
             const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
             if (!warp_wait(acce_bar(acc), acc_par ^ 1u, abort, lim)) {
@@ -299,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem + acc * BN;
             const uint32_t sub_off = static_cast<uint32_t>(((tn * BN) % 128) / 32);  // BN < 128 only
-            const int ks0 = sp * p.kstages_per_split;
-            const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+            const int ks0 = w.ks0;
+            const int ks1 = w.ks1;
             for (int ks = ks0; ks < ks1; ++ks) {
                 if (!warp_wait(full_bar(st), ph, abort, lim)) {
                     if (lane == 0) record_timeout(p, abort);
@@ -352,8 +463,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 issued = true;
-                if (elect_one())
-                    tc_commit(empty_bar(st));
+                if (elect_one()) {
+                    if (MC)
+                        tc_commit_multicast(empty_bar(st), 0x3);
+                    else
+                        tc_commit(empty_bar(st));
+                }
                 __syncwarp();
                 if (++st == S) {
                     st = 0;
@@ -379,10 +494,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kCols = BN / 2 >= 32 ? BN / 2 : 32;
         constexpr int kChunks = kCols / 32;
         const bool has_cols = h * kCols < BN;
+        __shared__ int sk_last;
+        const int row_local = q * 32 + lane;
         int it = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
-            int tm, tn, sp;
-            tile_coords(p, u, tm, tn, sp);
+        WorkIter wi;
+        wi.init(p, first_unit, unit_step);
+        Work w;
+        for (; wi.next(p, w); ++it) {
+            int tm = w.tm;
+            const int tn = w.tn;
+            if (MC) tm = 2 * tm + mc_rank;
             const int acc = it % C::kAccStages;
             const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
             bool ok = true;
@@ -409,10 +530,102 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));
 
-            const int i = tm * kBM + q * 32 + lane;  // A-role row owned by this thread
+            if (w.kind == 1) {
+                // ---- stream-K segment: publish the partial sum; the last CTA to
+                // arrive at this tile adds all segments in k order and stores C.
+                const int cta = first_unit;
+                // Slot layout [h][chunk][4-column group][row]: each warp access is
+                // 32 consecutive 16-byte vectors (rows of one lane quarter).
+                uint4 *const mine =
+                    reinterpret_cast<uint4 *>(p.sk_partials + static_cast<size_t>(2 * cta + w.slot) * kBM * BN);
+                if (has_cols) {
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            mine[((h * kChunks + c) * 8 + v) * kBM + row_local] =
+                                make_uint4(r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2], r[c][4 * v + 3]);
+                    }
+                }
+                __threadfence();
+                epi_bar_sync();
+                const long long t0 = static_cast<long long>(w.tile - p.dp_tiles) * p.kstages;
+                const int c_first = sk_cta_of(p, t0);
+                const int c_last = sk_cta_of(p, t0 + p.kstages - 1);
+                if (threadIdx.x == 64) {
+                    const int old = atomicAdd(p.sk_counters + (w.tile - p.dp_tiles), 1);
+                    const int last = old == c_last - c_first;
+                    if (last)
+                        p.sk_counters[w.tile - p.dp_tiles] = 0;  // ready for the next launch
+                    sk_last = last;
+                }
+                epi_bar_sync();
+                const bool last = sk_last != 0;
+                epi_bar_sync();  // sk_last is read before the next segment may rewrite it
+                if (!last)
+                    continue;
+                __threadfence();
+                // Sum every segment's partial (this CTA's own included, re-read from
+                // its slot) in k order, one 32-column chunk at a time.
+                const int i = tm * kBM + row_local;
+                if (has_cols && i < p.rows_a) {
+                    const long long base_off = static_cast<long long>(i) * p.stride_i;
+#pragma unroll 1
+                    for (int c = 0; c < kChunks; ++c) {
+                        const int j0 = tn * BN + h * kCols + c * 32;
+                        if (j0 >= p.rows_b) break;
+                        float sum[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            sum[e] = 0.0f;
+                        // k order; the loads of two segments are in flight together
+                        for (int cc0 = c_first; cc0 <= c_last; cc0 += 2) {
+                            float4 x[2][8];
+#pragma unroll
+                            for (int g = 0; g < 2; ++g) {
+                                const int cc = cc0 + g;
+                                if (cc <= c_last) {
+                                    const long long beg = p.sk_stages * cc / p.sk_ctas;
+                                    const int slot = (beg / p.kstages == w.tile - p.dp_tiles) ? 0 : 1;
+                                    const float4 *src =
+                                        reinterpret_cast<const float4 *>(
+                                            p.sk_partials + static_cast<size_t>(2 * cc + slot) * kBM * BN) +
+                                        (h * kChunks + c) * 8 * kBM + row_local;
+#pragma unroll
+                                    for (int v = 0; v < 8; ++v)
+                                        x[g][v] = __ldcg(src + v * kBM);
+                                }
+                            }
+#pragma unroll
+                            for (int g = 0; g < 2; ++g) {
+                                if (cc0 + g <= c_last) {
+#pragma unroll
+                                    for (int v = 0; v < 8; ++v) {
+                                        sum[4 * v] += x[g][v].x;
+                                        sum[4 * v + 1] += x[g][v].y;
+                                        sum[4 * v + 2] += x[g][v].z;
+                                        sum[4 * v + 3] += x[g][v].w;
+                                    }
+                                }
+                            }
+                        }
+                        uint32_t bits[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            bits[e] = __float_as_uint(sum[e]);
+                        if (p.vec_ok && j0 + 32 <= p.rows_b)
+                            store_row32_vec(p, base_off + j0, bits);
+                        else
+                            store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), bits);
+                    }
+                }
+                continue;
+            }
+
+            const int i = tm * kBM + row_local;  // A-role row owned by this thread
             if (has_cols && i < p.rows_a) {
-                const long long base_off =
-                    static_cast<long long>(sp) * p.split_stride + static_cast<long long>(i) * p.stride_i;
+                const long long base_off = (w.kind == 2 ? static_cast<long long>(w.slot) * p.split_stride : 0ll) +
+                                           static_cast<long long>(i) * p.stride_i;
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
                     const int j0 = tn * BN + h * kCols + c * 32;
@@ -428,6 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (MC)
+        cluster_sync();  // the peer may still multicast into, or commit to, this CTA until here
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);

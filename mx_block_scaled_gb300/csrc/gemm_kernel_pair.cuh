@@ -1,0 +1,351 @@
+// gemm_kernel_pair.cuh -- the MX block-scaled GEMM on CTA pairs (tcgen05
+// cta_group::2): a cluster of two CTAs on two SMs computes one 256 x BN output
+// tile with M = 256 MMAs issued by the even CTA.
+//
+// Same operation and pipeline as mx_gemm_kernel (gemm_kernel.cuh); what changes:
+//   * CTA r of the pair loads A-role rows [256*tm + 128*r, +128) and the r-th
+//     half of the B-role tile (BN/2 rows) into its own shared memory; an MMA of
+//     the pair reads A from each CTA's own half and B from both halves, so each
+//     SM fetches 1/3 fewer operand bytes per FLOP than a 128 x BN tile, and one
+//     MMA instruction covers twice the work.
+//   * both CTAs hold the full B-role scales (they are needed for every output
+//     column) and the scales of their own 128 A-role rows; the even CTA's
+//     tcgen05.cp (cta_group::2) moves each CTA's scale chunks into its own TMEM.
+//   * each CTA's loads complete on its own `full` barrier; the odd CTA's warp 1
+//     forwards that completion to the even CTA (a cluster-scope arrive on
+//     `peer_full`), so the even CTA issues a stage's MMAs only when both halves
+//     are resident.  The even CTA's commits arrive on `empty` / `acc_full` in
+//     both CTAs (multicast); both CTAs' epilogue warps arrive on the even CTA's
+//     `acc_empty`.
+//   * every CTA holds its 128 rows x BN FP32 accumulator in its own TMEM, and its
+//     epilogue stores those rows.
+// All waits are bounded as in the single-CTA kernel; the CTAs meet at a cluster
+// barrier before TMEM is released.
+#pragma once
+
+#include "gemm_kernel.cuh"
+
+namespace mxg {
+
+template <bool FP4, int BN>
+struct CfgPair {
+    static constexpr int kKtPerStage = FP4 ? 2 : 1;
+    static constexpr int kSubPerKt = FP4 ? 2 : 4;
+    static constexpr int kChunksB = BN / 128;                 // B-role scale chunks per K-tile (all BN rows)
+    static constexpr int kABytes = kBM * kRowBytes;           // own 128 A-role rows
+    static constexpr int kBBytes = (BN / 2) * kRowBytes;      // own half of the B-role tile
+    static constexpr int kSfaBytes = kKtPerStage * kSfChunk;
+    static constexpr int kSfbBytes = kChunksB * kKtPerStage * kSfChunk;
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+    static constexpr int kStagesRaw = (kSmemBudget - 1024 - 512) / kStageBytes;
+    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    static constexpr int kSfaCols = 4 * kKtPerStage;
+    static constexpr int kSfbCols = 4 * kKtPerStage * kChunksB;
+    static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
+    static constexpr int kAccStages = (2 * BN + kStages * kSfSlotCols <= 512) ? 2 : 1;
+    static constexpr int kSfCol0 = kAccStages * BN;
+    static constexpr int kColsUsed = kSfCol0 + kStages * kSfSlotCols;
+    static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128
+                                   : kColsUsed <= 256 ? 256 : 512;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
+    static constexpr uint32_t kIdesc = idesc_block_scaled(FP4 ? 1u : 0u, 2 * kBM, BN);
+    static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
+    static_assert(kStages >= 2, "shared memory too small for two stages");
+    static_assert(kColsUsed <= 512, "TMEM overflow");
+};
+
+template <bool FP4, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
+                        const __grid_constant__ CUtensorMap map_b)
+{
+    using C = CfgPair<FP4, BN>;
+    constexpr int S = C::kStages;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_base_holder;
+    __shared__ int abort_flag;
+
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t sA = base;
+    const uint32_t sB = sA + S * C::kABytes;
+    const uint32_t sSFA = sB + S * C::kBBytes;
+    const uint32_t sSFB = sSFA + S * C::kSfaBytes;
+    const uint32_t sBar = sSFB + S * C::kSfbBytes;
+    auto full_bar = [&](int s) { return sBar + 8u * s; };
+    auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
+    auto pfull_bar = [&](int s) { return sBar + 8u * (2 * S + s); };  // used in the even CTA
+    auto accf_bar = [&](int a) { return sBar + 8u * (3 * S + a); };
+    auto acce_bar = [&](int a) { return sBar + 8u * (3 * S + 2 + a); };  // used in the even CTA
+    const uint32_t drain_bar = sBar + 8u * (3 * S + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    volatile int *abort = &abort_flag;
+    int never_abort = 0;
+    const volatile int *no_abort = &never_abort;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+            mbar_init(pfull_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), 2 * kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        fence_mbar_init();
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(&tmem_base_holder), C::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // barriers of both CTAs initialised before any cross-CTA arrive
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_holder;
+
+    const int total_units = p.tiles_m * p.tiles_n * p.splits;  // tiles_m counts 256-row pair tiles
+    const int first_unit = static_cast<int>(cluster_id_x());
+    const int unit_step = static_cast<int>(cluster_count_x());
+    const uint64_t lim = p.timeout_ns;
+    const int nrb_a = (p.rows_a + 127) / 128;
+    const int nrb_b = (p.rows_b + 127) / 128;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (!p.test_stall) {
+            const uint64_t pol = l2_policy_evict_last();
+            int st = 0;
+            uint32_t ph = 0;
+            uint32_t armed = 0, armed_ph = 0;
+            bool ok = true;
+            for (int u = first_unit; u < total_units && ok; u += unit_step) {
+                int tm, tn, sp;
+                tile_coords(p, u, tm, tn, sp);
+                const int ks0 = sp * p.kstages_per_split;
+                const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+                const int rb_a = 2 * tm + static_cast<int>(rank);      // own 128-row block of the A role
+                const bool has_sfa = rb_a < nrb_a;
+                const int rb_b0 = (tn * BN) / 128;
+                const int nchunk_b = min(C::kChunksB, nrb_b - rb_b0);
+                for (int ks = ks0; ks < ks1; ++ks) {
+                    if (!warp_wait_cluster(empty_bar(st), ph ^ 1u, abort, lim)) {
+                        if (lane == 0) record_timeout(p, abort);
+                        ok = false;
+                        break;
+                    }
+                    const int kt0 = ks * C::kKtPerStage;
+                    const int nkt = min(C::kKtPerStage, p.num_kt - kt0);
+                    const uint32_t bytes =
+                        C::kABytes + C::kBBytes + nkt * kSfChunk * ((has_sfa ? 1 : 0) + nchunk_b);
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(full_bar(st), bytes);
+                        tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, rb_a * kBM, pol);
+                        tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes,
+                                    tn * BN + static_cast<int>(rank) * (BN / 2), pol);
+                        if (has_sfa)
+                            bulk_load(sSFA + st * C::kSfaBytes,
+                                      p.sfa + (static_cast<size_t>(rb_a) * p.num_kt + kt0) * kSfChunk,
+                                      nkt * kSfChunk, full_bar(st));
+                        for (int c = 0; c < nchunk_b; ++c)
+                            bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
+                                      p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
+                                      nkt * kSfChunk, full_bar(st));
+                    }
+                    __syncwarp();
+                    armed |= 1u << st;
+                    armed_ph = (armed_ph & ~(1u << st)) | (ph << st);
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s2 = 0; s2 < S; ++s2)
+                    if (armed & (1u << s2))
+                        warp_wait(full_bar(s2), (armed_ph >> s2) & 1u, no_abort, lim);
+            }
+        }
+    } else if (warp == 1 && !leader) {
+        // ------------------------------------- odd CTA: forward load completion
+        int st = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int u = first_unit; u < total_units && ok; u += unit_step) {
+            int tm, tn, sp;
+            tile_coords(p, u, tm, tn, sp);
+            const int ks0 = sp * p.kstages_per_split;
+            const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+            for (int ks = ks0; ks < ks1; ++ks) {
+                if (!warp_wait(full_bar(st), ph, abort, lim)) {
+                    if (lane == 0) record_timeout(p, abort);
+                    ok = false;
+                    break;
+                }
+                if (elect_one())
+                    mbar_arrive_cluster(map_to_cta(pfull_bar(st), 0));
+                __syncwarp();
+                if (++st == S) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // -------------------------------------- even CTA: MMA issuer for the pair
+        int st = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        bool ok = true;
+        bool issued = false;
+        for (int u = first_unit; u < total_units && ok; u += unit_step, ++it) {
+            int tm, tn, sp;
+            tile_coords(p, u, tm, tn, sp);
+            (void)tm;
+            (void)tn;
+            const int acc = it % C::kAccStages;
+            const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
+            if (!warp_wait_cluster(acce_bar(acc), acc_par ^ 1u, abort, lim)) {
+                if (lane == 0) record_timeout(p, abort);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + acc * BN;
+            const int ks0 = sp * p.kstages_per_split;
+            const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+            for (int ks = ks0; ks < ks1; ++ks) {
+                if (!warp_wait(full_bar(st), ph, abort, lim) || !warp_wait_cluster(pfull_bar(st), ph, abort, lim)) {
+                    if (lane == 0) record_timeout(p, abort);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int nkt = min(C::kKtPerStage, p.num_kt - ks * C::kKtPerStage);
+                const uint32_t sfa_col = tmem + C::kSfCol0 + st * C::kSfSlotCols;
+                const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                const uint32_t sfa_src = sSFA + st * C::kSfaBytes;
+                const uint32_t sfb_src = sSFB + st * C::kSfbBytes;
+#pragma unroll
+                for (int t = 0; t < C::kKtPerStage; ++t) {
+                    if (t < nkt) {
+                        if (elect_one())
+                            tc_cp_pair_32x128b_warpx4(sfa_col + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
+#pragma unroll
+                        for (int c = 0; c < C::kChunksB; ++c) {
+                            const uint64_t d = sdesc_sf_chunk(sfb_src + (c * C::kKtPerStage + t) * kSfChunk);
+                            if (elect_one())
+                                tc_cp_pair_32x128b_warpx4(sfb_col + 4 * (t * C::kChunksB + c), d);
+                        }
+                    }
+                }
+                const uint64_t adesc = sdesc_kmajor_sw128(sA + st * C::kABytes);
+                const uint64_t bdesc = sdesc_kmajor_sw128(sB + st * C::kBBytes);
+                const uint32_t acc0 = (ks > ks0) ? 1u : 0u;
+#pragma unroll
+                for (int s = 0; s < C::kKtPerStage * C::kSubPerKt; ++s) {
+                    const int t = s / C::kSubPerKt;
+                    if (t < nkt) {
+                        const uint32_t sf_id = FP4 ? static_cast<uint32_t>((s % 2) * 2) : static_cast<uint32_t>(s % 4);
+                        const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, sf_id, sf_id);
+                        const uint32_t sfa_t = sfa_col + 4 * t;
+                        const uint32_t sfb_t = sfb_col + 4 * t * C::kChunksB;
+                        const uint64_t koff = static_cast<uint64_t>((s * 32) >> 4);
+                        const uint32_t accum = (s > 0) ? 1u : acc0;
+                        if (elect_one()) {
+                            if (FP4)
+                                mma_pair_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
+                            else
+                                mma_pair_mxf8f6f4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
+                        }
+                    }
+                }
+                issued = true;
+                if (elect_one())
+                    tc_commit_pair(empty_bar(st), 0x3);
+                __syncwarp();
+                if (++st == S) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (elect_one())
+                tc_commit_pair(accf_bar(acc), 0x3);
+            __syncwarp();
+        }
+        if (!ok && issued) {
+            if (elect_one())
+                tc_commit_pair(drain_bar, 0x1);
+            __syncwarp();
+            warp_wait(drain_bar, 0, no_abort, lim);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        constexpr int kCols = BN / 2;
+        constexpr int kChunks = kCols / 32;
+        int it = 0;
+        for (int u = first_unit; u < total_units; u += unit_step, ++it) {
+            int tm, tn, sp;
+            tile_coords(p, u, tm, tn, sp);
+            const int acc = it % C::kAccStages;
+            const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
+            if (!warp_wait_cluster(accf_bar(acc), acc_par, abort, lim)) {
+                if (lane == 0) record_timeout(p, abort);
+                break;
+            }
+            tc_fence_after();
+            uint32_t r[kChunks][32];
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + h * kCols;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+                tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+                reg_fence(r[c]);
+            // Hand the accumulator stage back to the even CTA's MMA warp.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_cta(acce_bar(acc), 0));
+
+            const int i = tm * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
+            if (i < p.rows_a) {
+                const long long base_off =
+                    static_cast<long long>(sp) * p.split_stride + static_cast<long long>(i) * p.stride_i;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    const int j0 = tn * BN + h * kCols + c * 32;
+                    if (j0 >= p.rows_b) break;
+                    if (p.vec_ok && j0 + 32 <= p.rows_b)
+                        store_row32_vec(p, base_off + j0, r[c]);
+                    else
+                        store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), r[c]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still touch its memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, C::kTmemCols);
+    }
+}
+
+}  // namespace mxg

@@ -9,12 +9,35 @@
 
 namespace mxg {
 
+// Set the shared-memory opt-in of every GEMM instantiation on the current
+// device.  Must run (once per device) before any launch below.
+cudaError_t prepare_gemm_fp8();
+cudaError_t prepare_gemm_fp4();
+
 // Launch the persistent GEMM kernel for tile width `bn` (32, 64, 128, 256) on
 // `grid` CTAs.  Returns cudaErrorInvalidValue for an unsupported bn.
 cudaError_t launch_gemm_fp8(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
                             int grid, cudaStream_t stream);
 cudaError_t launch_gemm_fp4(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
                             int grid, cudaStream_t stream);
+
+// CTA-pair kernel (cluster of 2, cta_group::2), pair tile 256 x bn (bn = 128 or
+// 256), on `clusters` clusters; and the largest co-resident cluster count.
+cudaError_t launch_gemm_pair_fp8(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                 int clusters, cudaStream_t stream);
+cudaError_t launch_gemm_pair_fp4(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                 int clusters, cudaStream_t stream);
+int gemm_pair_max_clusters_fp8(int bn);
+int gemm_pair_max_clusters_fp4(int bn);
+
+// Single-CTA MMAs in clusters of two CTAs that share (multicast) the B-role
+// tile; bn = 128 or 256; `clusters` clusters.
+cudaError_t launch_gemm_mc_fp8(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                               int clusters, cudaStream_t stream);
+cudaError_t launch_gemm_mc_fp4(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                               int clusters, cudaStream_t stream);
+int gemm_mc_max_clusters_fp8(int bn);
+int gemm_mc_max_clusters_fp4(int bn);
 
 // Pipeline facts of one instantiation, for plan descriptions.
 struct KernelInfo {
@@ -24,5 +47,7 @@ struct KernelInfo {
 };
 KernelInfo gemm_info_fp8(int bn);
 KernelInfo gemm_info_fp4(int bn);
+KernelInfo gemm_pair_info_fp8(int bn);
+KernelInfo gemm_pair_info_fp4(int bn);
 
 }  // namespace mxg

@@ -25,6 +25,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     bool ready = false;
+    bool kernels_prepared = false;
     bool is_sm103 = false;
     int num_sms = 0;
     int *status_ptr = nullptr;
@@ -61,6 +62,11 @@ int device_info(DeviceInfo **out)
                 q != cudaDriverEntryPointSuccess || fn == nullptr)
                 return MXGEMM_ERR_CUDA;
             g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        if (d.is_sm103) {
+            if (mxg::prepare_gemm_fp8() != cudaSuccess || mxg::prepare_gemm_fp4() != cudaSuccess)
+                return MXGEMM_ERR_CUDA;
+            d.kernels_prepared = true;
         }
         d.ready = true;
     }
@@ -193,6 +199,9 @@ struct mxgemm_plan {
     int64_t M, N, K;
     int fmt, out;
     int swap;          // 1: compute C^T = B * A^T (B fills the MMA M dimension)
+    int mode;          // 0: one CTA per 128-row tile; 1: clusters of 2 CTAs on vertically adjacent
+                       // 128-row tiles sharing the B-role tile (TMA multicast); 2: 256-row tiles on
+                       // CTA pairs with M = 256 MMAs (cta_group::2)
     int bn;            // MMA N tile
     int splits;        // split-K factor
     int tiles_m, tiles_n;
@@ -200,7 +209,11 @@ struct mxgemm_plan {
     int grid;
     int group_m;
     int num_sms;
-    size_t off_sfa, off_sfb, off_part, ws_bytes;
+    int dp_tiles;      // stream-K: tiles computed whole (first in raster order)
+    int sk_tiles;      // stream-K: tiles whose k-stages are spread over sk_ctas CTAs
+    int sk_ctas;       // 0: no stream-K
+    int device;        // the device current when the plan was created; runs must use it
+    size_t off_sfa, off_sfb, off_part, off_cnt, off_skp, ws_bytes;
     // TMA descriptor cache (re-encoded when an operand pointer changes)
     const void *map_ptr_a = nullptr;
     const void *map_ptr_b = nullptr;
@@ -267,9 +280,11 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         (out != MXGEMM_OUT_F32 && out != MXGEMM_OUT_BF16))
         return MXGEMM_ERR_ARG;
     const uint32_t known = MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_NOSWAP |
-                           MXGEMM_PLAN_FORCE_SWAP | (0xFFu << MXGEMM_PLAN_SPLITK_SHIFT);
+                           MXGEMM_PLAN_FORCE_SWAP | MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE |
+                           MXGEMM_PLAN_FORCE_MC | MXGEMM_PLAN_STREAMK | (0xFFu << MXGEMM_PLAN_SPLITK_SHIFT);
     if ((flags & ~known) != 0 || ((flags & MXGEMM_PLAN_FORCE_SWAP) && (flags & MXGEMM_PLAN_FORCE_NOSWAP)) ||
-        ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)))
+        ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)) ||
+        __builtin_popcount(flags & (MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE | MXGEMM_PLAN_FORCE_MC)) > 1)
         return MXGEMM_ERR_ARG;
     if (M < 1 || N < 1 || K < 128 || K % 128 != 0)
         return MXGEMM_ERR_SHAPE;
@@ -291,6 +306,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     p->fmt = fmt;
     p->out = out;
     p->num_sms = dev->num_sms;
+    cudaGetDevice(&p->device);
 
     // Operand roles: small token counts put the weight (B) in the 128-row MMA dimension.
     int swap = (M <= 64 && N >= 128) ? 1 : 0;
@@ -302,18 +318,49 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     int bn = pick_bn(rows_b);
     if (flags & MXGEMM_PLAN_FORCE_BN128) bn = 128;
     if (flags & MXGEMM_PLAN_FORCE_BN256) bn = 256;
+    // Cluster modes (MC, pair) need 128- or 256-wide N tiles.
+    int mode = 0;
+    if (flags & MXGEMM_PLAN_FORCE_MC) mode = 1;
+    if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 2;
+    if (flags & MXGEMM_PLAN_FORCE_SINGLE) mode = 0;
+    if (mode != 0 && bn < 128) bn = 128;
+    p->mode = mode;
     p->bn = bn;
-    p->tiles_m = static_cast<int>(ceil_div(rows_a, 128));
+    // tiles_m counts the work units along the A role: 128-row tiles (single),
+    // pairs of 128-row tiles (MC), 256-row tiles (pair).
+    p->tiles_m = static_cast<int>(mode == 0 ? ceil_div(rows_a, 128) : ceil_div(rows_a, 256));
     p->tiles_n = static_cast<int>(ceil_div(rows_b, bn));
     p->kstages = static_cast<int>(fmt == MXGEMM_FMT_MXFP4_E2M1 ? ceil_div(K, 256) : K / 128);
 
-    // Split-K when the output tiles alone cannot fill the GPU.
+    // Work decomposition.  Default: whole tiles, plus uniform split-K with a
+    // separate reduce when the tiles alone cannot fill half the GPU.  With
+    // MXGEMM_PLAN_STREAMK (single-CTA tiles only): whole tiles in full waves over
+    // the SMs, and -- when the last wave would leave SMs idle -- the k-stages of
+    // the remaining tiles spread evenly over all SMs, fixed up in the kernel.
     const int64_t tiles = static_cast<int64_t>(p->tiles_m) * p->tiles_n;
     int splits = static_cast<int>((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu);
+    p->dp_tiles = static_cast<int>(tiles);
+    p->sk_tiles = 0;
+    p->sk_ctas = 0;
+    if (mode == 0 && splits == 0 && (flags & MXGEMM_PLAN_STREAMK)) {
+        const int64_t G = p->num_sms;
+        const int64_t waves = ceil_div(tiles, G);
+        const double dp_eff = static_cast<double>(tiles) / static_cast<double>(waves * G);
+        if (dp_eff < 0.95) {
+            const int64_t dp = (tiles / G) * G;
+            const int64_t sk_stages = (tiles - dp) * p->kstages;
+            const int64_t min_seg = 4;  // k-stages per stream-K CTA, at least
+            p->dp_tiles = static_cast<int>(dp);
+            p->sk_tiles = static_cast<int>(tiles - dp);
+            p->sk_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(G, sk_stages / min_seg)));
+        }
+        splits = 1;
+    }
     if (splits == 0) {
         splits = 1;
-        if (tiles * 2 <= p->num_sms) {
-            const int64_t by_sms = p->num_sms / tiles;
+        const int64_t slots = mode != 0 ? p->num_sms / 2 : p->num_sms;  // concurrent work units
+        if (tiles * 2 <= slots) {
+            const int64_t by_sms = slots / tiles;
             const int64_t by_k = std::max<int64_t>(1, p->kstages / 4);
             splits = static_cast<int>(std::min<int64_t>(std::min(by_sms, by_k), 32));
         }
@@ -322,8 +369,24 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     p->kstages_per_split = static_cast<int>(ceil_div(p->kstages, splits));
     p->splits = static_cast<int>(ceil_div(p->kstages, p->kstages_per_split));
     p->group_m = 8;
-    const int64_t units = tiles * p->splits;
-    p->grid = static_cast<int>(std::min<int64_t>(units, p->num_sms));
+    const int64_t units = p->sk_ctas > 0 ? std::max<int64_t>(p->dp_tiles > 0 ? p->num_sms : 0, p->sk_ctas)
+                                         : tiles * p->splits;
+    if (mode != 0) {
+        int max_clusters = 0;
+        if (mode == 1)
+            max_clusters = fmt == MXGEMM_FMT_MXFP4_E2M1 ? mxg::gemm_mc_max_clusters_fp4(bn)
+                                                        : mxg::gemm_mc_max_clusters_fp8(bn);
+        else
+            max_clusters = fmt == MXGEMM_FMT_MXFP4_E2M1 ? mxg::gemm_pair_max_clusters_fp4(bn)
+                                                        : mxg::gemm_pair_max_clusters_fp8(bn);
+        if (max_clusters < 1) {
+            delete p;
+            return MXGEMM_ERR_CUDA;
+        }
+        p->grid = static_cast<int>(std::min<int64_t>(units, max_clusters));  // clusters of 2 CTAs
+    } else {
+        p->grid = static_cast<int>(std::min<int64_t>(units, p->num_sms));
+    }
 
     size_t off = 0;
     p->off_sfa = off;
@@ -333,6 +396,13 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     p->off_part = off;
     if (p->splits > 1)
         off = align256(off + static_cast<size_t>(p->splits) * ((M * N + 3) & ~3ll) * sizeof(float));
+    p->off_cnt = off;
+    p->off_skp = off;
+    if (p->sk_ctas > 0) {
+        off = align256(off + static_cast<size_t>(p->sk_tiles) * sizeof(int));
+        p->off_skp = off;
+        off = align256(off + static_cast<size_t>(2) * p->sk_ctas * 128 * bn * sizeof(float));
+    }
     p->ws_bytes = off;
     *plan = p;
     return MXGEMM_OK;
@@ -351,12 +421,15 @@ int mxgemm_plan_describe(mxgemm_plan_t plan, char *buf, size_t len)
     if (!plan || !buf || len == 0)
         return MXGEMM_ERR_ARG;
     const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
-    mxg::KernelInfo ki = fp4 ? mxg::gemm_info_fp4(plan->bn) : mxg::gemm_info_fp8(plan->bn);
+    static const char *const kModes[3] = {"single", "mc", "pair"};
+    mxg::KernelInfo ki = plan->mode == 2 ? (fp4 ? mxg::gemm_pair_info_fp4(plan->bn) : mxg::gemm_pair_info_fp8(plan->bn))
+                                         : (fp4 ? mxg::gemm_info_fp4(plan->bn) : mxg::gemm_info_fp8(plan->bn));
     snprintf(buf, len,
-             "fmt=%s out=%s tile=128x%d swap_ab=%d split_k=%d tiles=%dx%d kstages=%d grid=%d stages=%d "
-             "acc_stages=%d smem=%d",
-             fp4 ? "mxfp4" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32", plan->bn, plan->swap,
-             plan->splits, plan->tiles_m, plan->tiles_n, plan->kstages, plan->grid, ki.stages, ki.acc_stages,
+             "fmt=%s out=%s tile=%dx%d mode=%s swap_ab=%d split_k=%d streamk=%d+%d/%d units=%dx%d kstages=%d grid=%d%s "
+             "stages=%d acc_stages=%d smem=%d",
+             fp4 ? "mxfp4" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32", plan->mode == 2 ? 256 : 128,
+             plan->bn, kModes[plan->mode], plan->swap, plan->splits, plan->dp_tiles, plan->sk_tiles, plan->sk_ctas,
+             plan->tiles_m, plan->tiles_n, plan->kstages, plan->grid, plan->mode ? "x2" : "", ki.stages, ki.acc_stages,
              ki.smem_bytes);
     return MXGEMM_OK;
 }
@@ -392,6 +465,9 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     int st = device_info(&dev);
     if (st != MXGEMM_OK)
         return st;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device)
+        return MXGEMM_ERR_ARG;  // a plan runs on the device it was created on
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -425,7 +501,8 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
         plan->map_ptr_a = pa;
     }
     if (plan->map_ptr_b != pb) {
-        if (encode_operand_map(&plan->map_b, pb, rows_b, row_bytes, plan->bn) != MXGEMM_OK)
+        if (encode_operand_map(&plan->map_b, pb, rows_b, row_bytes, plan->mode ? plan->bn / 2 : plan->bn) !=
+            MXGEMM_OK)
             return MXGEMM_ERR_CUDA;
         plan->map_ptr_b = pb;
     }
@@ -448,6 +525,14 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     p.stride_j = plan->swap ? N : 1;
     p.timeout_ns = timeout_ns;
     p.status = dev->status_ptr;
+    p.dp_tiles = plan->dp_tiles;
+    p.sk_ctas = plan->sk_ctas;
+    p.sk_stages = static_cast<long long>(plan->sk_tiles) * plan->kstages;
+    p.sk_counters = reinterpret_cast<int *>(ws + plan->off_cnt);
+    p.sk_partials = reinterpret_cast<float *>(ws + plan->off_skp);
+    if (plan->sk_ctas > 0 &&
+        cudaMemsetAsync(ws + plan->off_cnt, 0, static_cast<size_t>(plan->sk_tiles) * sizeof(int), s) != cudaSuccess)
+        return MXGEMM_ERR_CUDA;
     const bool split = plan->splits > 1;
     const int osize = split ? 4 : (plan->out == MXGEMM_OUT_BF16 ? 2 : 4);
     if (split) {
@@ -461,8 +546,16 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     }
     p.vec_ok = (!plan->swap && (N * osize) % 16 == 0 && aligned16(p.out)) ? 1 : 0;
 
-    cudaError_t e = fp4 ? mxg::launch_gemm_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
-                        : mxg::launch_gemm_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
+    cudaError_t e;
+    if (plan->mode == 2)
+        e = fp4 ? mxg::launch_gemm_pair_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
+                : mxg::launch_gemm_pair_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
+    else if (plan->mode == 1)
+        e = fp4 ? mxg::launch_gemm_mc_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
+                : mxg::launch_gemm_mc_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
+    else
+        e = fp4 ? mxg::launch_gemm_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
+                : mxg::launch_gemm_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
     if (e != cudaSuccess)
         return MXGEMM_ERR_CUDA;
 

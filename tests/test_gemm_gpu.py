@@ -14,6 +14,9 @@ from mx_block_scaled_gb300.inputs import (FMT_MXFP4, FMT_MXFP8, finite_uniform_c
 
 pytestmark = pytest.mark.gpu
 
+# plan flags: 256-row tiles on CTA pairs / 128-row tiles on single CTAs / CTA pairs sharing B (multicast)
+PAIR, SINGLE, MC = 1 << 4, 1 << 5, 1 << 6
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _cuda():
@@ -142,15 +145,18 @@ def test_per_block_scale_sweep(oracle_mod, fmt):
 
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+@pytest.mark.parametrize("flags", [0, SINGLE, PAIR, MC])
 @pytest.mark.parametrize("M,N,K", [(1, 1, 128), (8, 129, 256), (127, 255, 384), (129, 8, 128),
-                                   (255, 127, 384), (130, 300, 640), (64, 512, 1024)])
-def test_edge_shapes_exact(oracle_mod, fmt, M, N, K):
+                                   (255, 127, 384), (130, 300, 640), (64, 512, 1024), (385, 264, 384)])
+def test_edge_shapes_exact(oracle_mod, fmt, flags, M, N, K):
+    if flags in (PAIR, MC) and (M < 128 or N < 128):
+        pytest.skip("cluster modes are for shapes with at least 128 rows on each side")
     rng = np.random.default_rng(M * 1000 + N + K)
     A, SA = small_int_codes(rng, M, K, fmt)
     B, SB = small_int_codes(rng, N, K, fmt)
     ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
     for out in (OUT_F32, OUT_BF16):
-        C = gpu_gemm(fmt, A, SA, B, SB, K, out)
+        C = gpu_gemm(fmt, A, SA, B, SB, K, out, flags=flags)
         if out == OUT_F32:
             assert (C == ref).all(), f"M={M} N={N} K={K}"
         else:
@@ -160,7 +166,9 @@ def test_edge_shapes_exact(oracle_mod, fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
-@pytest.mark.parametrize("flags", [0, 1 << 2, 1 << 3, (1 << 2) | 1, (1 << 2) | 2, (3 << 8), (1 << 3) | (5 << 8)])
+@pytest.mark.parametrize("flags", [0, 1 << 2, 1 << 3, (1 << 2) | 1, (1 << 2) | 2, (3 << 8), (1 << 3) | (5 << 8),
+                                   SINGLE, SINGLE | 2, PAIR | 1, PAIR | 2, PAIR | 1 | (3 << 8), PAIR | 2 | (2 << 8),
+                                   MC | 1, MC | 2, MC | 2 | (3 << 8)])
 def test_plan_variants_agree_with_oracle(oracle_mod, fmt, flags):
     """Forced tile width / swap-AB / split-K variants all reproduce the oracle."""
     M, N, K = 200, 384, 2048
@@ -170,6 +178,29 @@ def test_plan_variants_agree_with_oracle(oracle_mod, fmt, flags):
     ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
     C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, flags=flags, return_plan=True)
     assert (C == ref).all(), desc
+
+
+SK = 1 << 7  # stream-K plan flag
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+@pytest.mark.parametrize("M,N,K", [(1024, 1536, 4096), (2560, 2304, 1024), (300, 520, 1152), (8, 8192, 2048)])
+def test_stream_k_exact(oracle_mod, fmt, M, N, K):
+    """Tiles whose k-stages are spread over several CTAs (stream-K, fixed up in the
+    kernel) give the exact result, as does the default decomposition."""
+    rng = np.random.default_rng(M + 7 * N + K)
+    A, SA = small_int_codes(rng, M, K, fmt)
+    B, SB = small_int_codes(rng, N, K, fmt)
+    ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
+    C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, flags=SK, return_plan=True)
+    assert "streamk=" in desc and "/0 " not in desc.split("streamk=")[1][:12], desc
+    assert (C == ref).all(), desc
+    C2, desc2 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16, return_plan=True)
+    import torch
+    expect = torch.from_numpy(ref.astype(np.float32)).bfloat16().double().numpy()
+    assert (C2 == expect).all(), desc2
+    C3 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16, flags=SK)  # stream-K, BF16 out
+    assert (C3 == expect).all(), desc
 
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])

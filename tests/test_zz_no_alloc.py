@@ -15,11 +15,12 @@ from mx_block_scaled_gb300.inputs import FMT_MXFP4, FMT_MXFP8, make_operand
 
 pytestmark = pytest.mark.gpu
 
-# (workload, fmt, M, N, K, A shape index, B (N,K) index, out): a split-K decode shape
-# (scratch holds both tile-layout scales and the partial sums) and an unsplit one.
+# (workload, fmt, M, N, K, A shape index, B (N,K) index, out): a decode shape whose
+# k-stages are spread over all SMs (scratch holds the tile-layout scales, the
+# stream-K partial sums and counters) and a whole-tile prefill shape.
 CASES = [
     ("llama33_70b", FMT_MXFP8, 8, 8192, 8192, 1, 1, OUT_BF16),
-    ("llama31_8b", FMT_MXFP4, 2048, 4096, 4096, 5, 1, OUT_F32),
+    ("llama31_8b", FMT_MXFP4, 8192, 4096, 4096, 9, 1, OUT_F32),
 ]
 
 
