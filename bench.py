@@ -38,7 +38,8 @@ METRIC = "MXFP4/MXFP8 NT GEMM TFLOP/s on 1 GB300; % of dense MX tensor (or HBM) 
 WORKLOAD = "mxfp8_square_4096"
 NOMINAL_PF = {"bf16": 2.25, "mxfp8": 4.5, "mxfp4": 13.5}
 KERNEL_SOURCES = ["mx_block_scaled_gb300/csrc/gemm_kernel.cuh", "mx_block_scaled_gb300/csrc/ptx.cuh",
-                  "mx_block_scaled_gb300/csrc/gemm_fp8.cu", "mx_block_scaled_gb300/csrc/gemm_fp4.cu"]
+                  "mx_block_scaled_gb300/csrc/gemm_fp8.cu", "mx_block_scaled_gb300/csrc/gemm_fp4.cu",
+                  "mx_block_scaled_gb300/csrc/gemm_kernel_pair.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
 
@@ -364,7 +365,8 @@ def run_ours(args):
                    "plan": desc},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "mx_gemm_kernel (persistent tcgen05 block-scaled GEMM)",
+                     "kernel": ("mx_gemm_pair_kernel (CTA-pair tcgen05 block-scaled GEMM)" if "mode=pair" in desc
+                                else "mx_gemm_kernel (persistent tcgen05 block-scaled GEMM)"),
                      "peak_source": f"{peak_src} bf16 burst {bf16_tf} TFLOP/s x nominal mxfp8/bf16 ratio "
                                     f"{NOMINAL_PF[fmt_name] / NOMINAL_PF['bf16']:g}",
                      "hbm_view": {"algorithmic_bytes": bytes_alg, "achieved_gbs": bytes_alg / gemm_avg_s / 1e9,

@@ -31,13 +31,13 @@ cudaLaunchConfig_t cluster2_config(int clusters, int smem, cudaStream_t s, cudaL
 }
 
 template <int BN>
-cudaError_t launch_pair(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int clusters,
-                        cudaStream_t s)
+cudaError_t launch_pair(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &msa,
+                        const CUtensorMap &msb, int clusters, cudaStream_t s)
 {
     auto kern = mx_gemm_pair_kernel<true, BN>;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<true, BN>::kSmemBytes, s, attr);
-    return cudaLaunchKernelEx(&cfg, kern, p, ma, mb);
+    return cudaLaunchKernelEx(&cfg, kern, p, ma, mb, msa, msb);
 }
 
 template <int BN>
@@ -132,11 +132,11 @@ cudaError_t launch_gemm_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, 
 }
 
 cudaError_t launch_gemm_pair_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
-                                 int clusters, cudaStream_t s)
+                                 const CUtensorMap &msa, const CUtensorMap &msb, int clusters, cudaStream_t s)
 {
     switch (bn) {
-    case 128: return launch_pair<128>(p, ma, mb, clusters, s);
-    case 256: return launch_pair<256>(p, ma, mb, clusters, s);
+    case 128: return launch_pair<128>(p, ma, mb, msa, msb, clusters, s);
+    case 256: return launch_pair<256>(p, ma, mb, msa, msb, clusters, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -11,12 +11,12 @@
 //   * both CTAs hold the full B-role scales (they are needed for every output
 //     column) and the scales of their own 128 A-role rows; the even CTA's
 //     tcgen05.cp (cta_group::2) moves each CTA's scale chunks into its own TMEM.
-//   * each CTA's loads complete on its own `full` barrier; the odd CTA's warp 1
-//     forwards that completion to the even CTA (a cluster-scope arrive on
-//     `peer_full`), so the even CTA issues a stage's MMAs only when both halves
-//     are resident.  The even CTA's commits arrive on `empty` / `acc_full` in
-//     both CTAs (multicast); both CTAs' epilogue warps arrive on the even CTA's
-//     `acc_empty`.
+//   * the loads of both CTAs (operand tiles and scale chunks, all TMA tensor
+//     copies) complete on the even CTA's `full` barrier, which the even CTA arms
+//     with the pair's total bytes; so a stage's MMAs are issued as soon as both
+//     halves are resident.  The even CTA's commits arrive on `empty` / `acc_full`
+//     in both CTAs (multicast); both CTAs' epilogue warps arrive on the even
+//     CTA's `acc_empty`.
 //   * every CTA holds its 128 rows x BN FP32 accumulator in its own TMEM, and its
 //     epilogue stores those rows.
 // All waits are bounded as in the single-CTA kernel; the CTAs meet at a cluster
@@ -57,7 +57,8 @@ struct CfgPair {
 template <bool FP4, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
-                        const __grid_constant__ CUtensorMap map_b)
+                        const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
+                        const __grid_constant__ CUtensorMap map_sfb)
 {
     using C = CfgPair<FP4, BN>;
     constexpr int S = C::kStages;
@@ -75,7 +76,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sBar = sSFB + S * C::kSfbBytes;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
-    auto pfull_bar = [&](int s) { return sBar + 8u * (2 * S + s); };  // used in the even CTA
     auto accf_bar = [&](int a) { return sBar + 8u * (3 * S + a); };
     auto acce_bar = [&](int a) { return sBar + 8u * (3 * S + 2 + a); };  // used in the even CTA
     const uint32_t drain_bar = sBar + 8u * (3 * S + 4);
@@ -93,7 +93,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
-            mbar_init(pfull_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
@@ -103,6 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b);
+        tma_prefetch_map(&map_sfa);
+        tma_prefetch_map(&map_sfb);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_addr(&tmem_base_holder), C::kTmemCols);
@@ -123,8 +124,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
+        // Both CTAs load their own halves; every copy completes on the even CTA's
+        // `full` barrier, which only the even CTA arms (with both CTAs' bytes).
         if (!p.test_stall) {
-            const uint64_t pol = l2_policy_evict_last();
             int st = 0;
             uint32_t ph = 0;
             uint32_t armed = 0, armed_ph = 0;
@@ -136,8 +138,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
                 const int rb_a = 2 * tm + static_cast<int>(rank);      // own 128-row block of the A role
                 const bool has_sfa = rb_a < nrb_a;
+                const bool peer_has_sfa = 2 * tm + 1 < nrb_a;
                 const int rb_b0 = (tn * BN) / 128;
                 const int nchunk_b = min(C::kChunksB, nrb_b - rb_b0);
+                // bytes of one CTA's copies, as counted by TMA (whole boxes)
+                const uint32_t common = C::kABytes + C::kBBytes + nchunk_b * C::kSfaBytes;
+                const uint32_t pair_bytes =
+                    2 * common + ((has_sfa ? 1 : 0) + (peer_has_sfa ? 1 : 0)) * C::kSfaBytes;
                 for (int ks = ks0; ks < ks1; ++ks) {
                     if (!warp_wait_cluster(empty_bar(st), ph ^ 1u, abort, lim)) {
                         if (lane == 0) record_timeout(p, abort);
@@ -145,22 +152,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const int kt0 = ks * C::kKtPerStage;
-                    const int nkt = min(C::kKtPerStage, p.num_kt - kt0);
-                    const uint32_t bytes =
-                        C::kABytes + C::kBBytes + nkt * kSfChunk * ((has_sfa ? 1 : 0) + nchunk_b);
                     if (elect_one()) {
-                        mbar_arrive_expect_tx(full_bar(st), bytes);
-                        tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, rb_a * kBM, pol);
-                        tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes,
-                                    tn * BN + static_cast<int>(rank) * (BN / 2), pol);
+                        const uint32_t bar = map_to_cta(full_bar(st), 0);
+                        if (leader)
+                            mbar_arrive_expect_tx(full_bar(st), pair_bytes);
+                        tma_load_2d_pair(sA + st * C::kABytes, &map_a, bar, ks * kRowBytes, rb_a * kBM);
+                        tma_load_2d_pair(sB + st * C::kBBytes, &map_b, bar, ks * kRowBytes,
+                                         tn * BN + static_cast<int>(rank) * (BN / 2));
+                        // scale chunks: rows of 256 bytes, two per 512-byte chunk
                         if (has_sfa)
-                            bulk_load(sSFA + st * C::kSfaBytes,
-                                      p.sfa + (static_cast<size_t>(rb_a) * p.num_kt + kt0) * kSfChunk,
-                                      nkt * kSfChunk, full_bar(st));
+                            tma_load_2d_pair(sSFA + st * C::kSfaBytes, &map_sfa, bar, 0, (rb_a * p.num_kt + kt0) * 2);
                         for (int c = 0; c < nchunk_b; ++c)
-                            bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
-                                      p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
-                                      nkt * kSfChunk, full_bar(st));
+                            tma_load_2d_pair(sSFB + st * C::kSfbBytes + c * C::kSfaBytes, &map_sfb, bar, 0,
+                                             ((rb_b0 + c) * p.num_kt + kt0) * 2);
                     }
                     __syncwarp();
                     armed |= 1u << st;
@@ -171,38 +175,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 for (int s2 = 0; s2 < S; ++s2)
                     if (armed & (1u << s2))
                         warp_wait(full_bar(s2), (armed_ph >> s2) & 1u, no_abort, lim);
             }
         }
-    } else if (warp == 1 && !leader) {
-        // ------------------------------------- odd CTA: forward load completion
-        int st = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int u = first_unit; u < total_units && ok; u += unit_step) {
-            int tm, tn, sp;
-            tile_coords(p, u, tm, tn, sp);
-            const int ks0 = sp * p.kstages_per_split;
-            const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
-            for (int ks = ks0; ks < ks1; ++ks) {
-                if (!warp_wait(full_bar(st), ph, abort, lim)) {
-                    if (lane == 0) record_timeout(p, abort);
-                    ok = false;
-                    break;
-                }
-                if (elect_one())
-                    mbar_arrive_cluster(map_to_cta(pfull_bar(st), 0));
-                __syncwarp();
-                if (++st == S) {
-                    st = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
-    } else if (warp == 1) {
+    } else if (warp == 1 && leader) {
         // -------------------------------------- even CTA: MMA issuer for the pair
         int st = 0;
         uint32_t ph = 0;
@@ -226,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ks0 = sp * p.kstages_per_split;
             const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
             for (int ks = ks0; ks < ks1; ++ks) {
-                if (!warp_wait(full_bar(st), ph, abort, lim) || !warp_wait_cluster(pfull_bar(st), ph, abort, lim)) {
+                if (!warp_wait_cluster(full_bar(st), ph, abort, lim)) {
                     if (lane == 0) record_timeout(p, abort);
                     ok = false;
                     break;
@@ -291,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             warp_wait(drain_bar, 0, no_abort, lim);
         }
-    } else {
+    } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;

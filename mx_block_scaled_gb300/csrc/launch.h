@@ -22,11 +22,14 @@ cudaError_t launch_gemm_fp4(int bn, const GemmParams &p, const CUtensorMap &map_
                             int grid, cudaStream_t stream);
 
 // CTA-pair kernel (cluster of 2, cta_group::2), pair tile 256 x bn (bn = 128 or
-// 256), on `clusters` clusters; and the largest co-resident cluster count.
+// 256), on `clusters` clusters; it also takes 2-D maps of the two tile-layout
+// scale tensors (rows of 256 bytes).  And the largest co-resident cluster count.
 cudaError_t launch_gemm_pair_fp8(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                 int clusters, cudaStream_t stream);
+                                 const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, int clusters,
+                                 cudaStream_t stream);
 cudaError_t launch_gemm_pair_fp4(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                 int clusters, cudaStream_t stream);
+                                 const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, int clusters,
+                                 cudaStream_t stream);
 int gemm_pair_max_clusters_fp8(int bn);
 int gemm_pair_max_clusters_fp4(int bn);
 

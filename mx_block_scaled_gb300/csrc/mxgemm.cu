@@ -217,7 +217,9 @@ struct mxgemm_plan {
     // TMA descriptor cache (re-encoded when an operand pointer changes)
     const void *map_ptr_a = nullptr;
     const void *map_ptr_b = nullptr;
-    CUtensorMap map_a, map_b;
+    const void *map_ptr_sfa = nullptr;
+    const void *map_ptr_sfb = nullptr;
+    CUtensorMap map_a, map_b, map_sfa, map_sfb;
 };
 
 namespace {
@@ -230,6 +232,20 @@ int encode_operand_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t 
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
+}
+
+// Tile-layout scales viewed as rows of 256 bytes (a 512-byte chunk is two
+// rows); box = one ring slot's chunks of one 128-row block.
+int encode_sf_map(CUtensorMap *map, const void *ptr, size_t bytes, int kt_per_stage)
+{
+    cuuint64_t dims[2] = {256u, static_cast<cuuint64_t>(bytes / 256)};
+    cuuint64_t strides[1] = {256u};
+    cuuint32_t box[2] = {256u, static_cast<cuuint32_t>(2 * kt_per_stage)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
 }
@@ -318,8 +334,14 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     int bn = pick_bn(rows_b);
     if (flags & MXGEMM_PLAN_FORCE_BN128) bn = 128;
     if (flags & MXGEMM_PLAN_FORCE_BN256) bn = 256;
-    // Cluster modes (MC, pair) need 128- or 256-wide N tiles.
+    // Cluster modes (MC, pair) need 128- or 256-wide N tiles.  Default: MXFP8
+    // with at least 128 rows on each side runs 256 x 256 pair tiles (measured
+    // faster from 128 tokens up); MXFP4, whose MMAs are issue-bound in both
+    // modes, and swapped decode shapes stay on single-CTA tiles.
     int mode = 0;
+    if (fmt == MXGEMM_FMT_MXFP8_E4M3 && !swap && rows_a >= 128 && rows_b >= 256 &&
+        !(flags & (MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_STREAMK)) && ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0)
+        mode = 2;
     if (flags & MXGEMM_PLAN_FORCE_MC) mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 2;
     if (flags & MXGEMM_PLAN_FORCE_SINGLE) mode = 0;
@@ -547,9 +569,23 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     p.vec_ok = (!plan->swap && (N * osize) % 16 == 0 && aligned16(p.out)) ? 1 : 0;
 
     cudaError_t e;
-    if (plan->mode == 2)
-        e = fp4 ? mxg::launch_gemm_pair_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
-                : mxg::launch_gemm_pair_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
+    if (plan->mode == 2) {
+        const int ktps = fp4 ? 2 : 1;
+        if (plan->map_ptr_sfa != p.sfa) {
+            if (encode_sf_map(&plan->map_sfa, p.sfa, mxgemm_sf_bytes(rows_a, K), ktps) != MXGEMM_OK)
+                return MXGEMM_ERR_CUDA;
+            plan->map_ptr_sfa = p.sfa;
+        }
+        if (plan->map_ptr_sfb != p.sfb) {
+            if (encode_sf_map(&plan->map_sfb, p.sfb, mxgemm_sf_bytes(rows_b, K), ktps) != MXGEMM_OK)
+                return MXGEMM_ERR_CUDA;
+            plan->map_ptr_sfb = p.sfb;
+        }
+        e = fp4 ? mxg::launch_gemm_pair_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->map_sfa, plan->map_sfb,
+                                            plan->grid, s)
+                : mxg::launch_gemm_pair_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->map_sfa, plan->map_sfb,
+                                            plan->grid, s);
+    }
     else if (plan->mode == 1)
         e = fp4 ? mxg::launch_gemm_mc_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
                 : mxg::launch_gemm_mc_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);

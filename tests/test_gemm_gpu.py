@@ -221,6 +221,23 @@ def test_prelayout_scales_give_the_same_result(fmt):
     assert torch.equal(C1, C2) and torch.equal(C1, C3)
 
 
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+def test_nan_scale_makes_its_rows_nan(oracle_mod, fmt):
+    """E8M0 code 0xFF is NaN: every output fed by such a block is NaN, the rest is exact."""
+    M, N, K = 160, 288, 256
+    rng = np.random.default_rng(31)
+    A, SA = small_int_codes(rng, M, K, fmt)
+    B, SB = small_int_codes(rng, N, K, fmt)
+    SA[5, 2] = 0xFF
+    SB[200, 7] = 0xFF
+    ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
+    assert np.isnan(ref[5]).all() and np.isnan(ref[:, 200]).all()
+    C = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32)
+    assert (np.isnan(C) == np.isnan(ref)).all()
+    ok = ~np.isnan(ref)
+    assert (C[ok] == ref[ok]).all()
+
+
 # ---- invariants at full workload size (GPU vs GPU, no oracle cost) ------------
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
