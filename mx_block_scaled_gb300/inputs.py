@@ -24,6 +24,8 @@ floor(log2 amax) comes from frexp, never from a floating-point log2.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 FMT_MXFP8 = 1
@@ -33,7 +35,7 @@ OUT_F32 = 1
 OUT_BF16 = 2
 OUT_BY_NAME = {"f32": OUT_F32, "bf16": OUT_BF16}
 
-_CHUNK = 1 << 22  # elements per quantisation chunk (bounds host memory)
+_CHUNK = 1 << 20  # elements per quantisation chunk (bounds host memory per thread)
 
 # E2M1 magnitude (x2) -> 3-bit code: 0,.5,1,1.5,2,3,4,6 -> 0..7
 _E2M1_CODE_OF_TWICE = np.full(13, 255, dtype=np.uint8)
@@ -86,31 +88,42 @@ def _encode_e2m1(r: np.ndarray) -> np.ndarray:
     return code | (np.signbit(r).astype(np.uint8) << 3)
 
 
+def _quantize_rows(x, fmt, codes, scales, r0, r1):
+    K = x.shape[1]
+    e_max, min_exp, mbits, vmax = ((8, -6, 3, 448.0) if fmt == FMT_MXFP8 else (2, 0, 1, 6.0))
+    xb = x[r0:r1].astype(np.float64).reshape(r1 - r0, K // 32, 32)
+    amax = np.abs(xb).max(axis=2)
+    _, e = np.frexp(amax)
+    s = np.where(amax > 0, e - 1 - e_max, 0)
+    s = np.clip(s, -127, 127)
+    scales[r0:r1] = (s + 127).astype(np.uint8)
+    v = np.ldexp(xb, -s[:, :, None])
+    r = _round_to_grid(v, min_exp, mbits, vmax).reshape(r1 - r0, K)
+    codes[r0:r1] = _encode_e4m3(r) if fmt == FMT_MXFP8 else _encode_e2m1(r)
+
+
 def quantize_mx(x: np.ndarray, fmt: int):
     """Quantise float data [rows, K] to MX codes and E8M0 scales.
 
     Returns ``(codes, scales)``: codes are [rows, K] uint8 for MXFP8 or packed
-    [rows, K/2] for MXFP4; scales are [rows, K/32] uint8.
+    [rows, K/2] for MXFP4; scales are [rows, K/32] uint8.  Row chunks are
+    quantised on a thread pool (each chunk independently, so the result does not
+    depend on the thread count).
     """
     rows, K = x.shape
     if K % 32:
         raise ValueError("K must be a multiple of 32")
-    e_max, min_exp, mbits, vmax = ((8, -6, 3, 448.0) if fmt == FMT_MXFP8
-                                   else (2, 0, 1, 6.0))
     codes = np.empty((rows, K), dtype=np.uint8)
     scales = np.empty((rows, K // 32), dtype=np.uint8)
     step = max(1, _CHUNK // K)
-    for r0 in range(0, rows, step):
-        r1 = min(rows, r0 + step)
-        xb = x[r0:r1].astype(np.float64).reshape(r1 - r0, K // 32, 32)
-        amax = np.abs(xb).max(axis=2)
-        _, e = np.frexp(amax)
-        s = np.where(amax > 0, e - 1 - e_max, 0)
-        s = np.clip(s, -127, 127)
-        scales[r0:r1] = (s + 127).astype(np.uint8)
-        v = np.ldexp(xb, -s[:, :, None])
-        r = _round_to_grid(v, min_exp, mbits, vmax).reshape(r1 - r0, K)
-        codes[r0:r1] = _encode_e4m3(r) if fmt == FMT_MXFP8 else _encode_e2m1(r)
+    spans = [(r0, min(rows, r0 + step)) for r0 in range(0, rows, step)]
+    if len(spans) == 1:
+        _quantize_rows(x, fmt, codes, scales, *spans[0])
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        workers = min(len(spans), os.cpu_count() or 1, 32)
+        with ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(lambda sp: _quantize_rows(x, fmt, codes, scales, *sp), spans))
     if fmt == FMT_MXFP4:
         codes = pack_fp4(codes)
     return codes, scales

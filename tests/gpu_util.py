@@ -21,6 +21,18 @@ def to_dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
 
+def gpu_gemm_device(fmt, A, SA, B, SB, K, out=OUT_F32, flags=0):
+    """Run C = A * B^T through mxgemm_run; return C as a CUDA tensor (no host copy)."""
+    import torch
+    b = lib()
+    M, N = A.shape[0], B.shape[0]
+    plan = b.Plan(M, N, K, fmt, out, flags)
+    C = plan.run(to_dev(A), to_dev(SA), to_dev(B), to_dev(SB))
+    b.check_device_status()
+    torch.cuda.synchronize()
+    return C
+
+
 def gpu_gemm(fmt, A, SA, B, SB, K, out=OUT_F32, flags=0, run_flags=0, return_plan=False):
     """Run C = A * B^T through mxgemm_run; returns C as float64 numpy (and the plan text)."""
     import torch

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 from golden_io import load_handworked
-from gpu_util import (OUT_BF16, OUT_F32, assert_within, gpu_gemm, lib, sample_indices, to_dev)
+from gpu_util import (OUT_BF16, OUT_F32, assert_within, gpu_gemm, gpu_gemm_device, lib, sample_indices, to_dev)
 from mx_block_scaled_gb300.inputs import (FMT_MXFP4, FMT_MXFP8, finite_uniform_codes, make_operand,
                                           pack_fp4, workload_cases)
 
@@ -277,37 +277,50 @@ def test_mxfp8_square_4096_full(oracle_mod):
     assert_within(C, ref, S, OUT_BF16, "mxfp8 4096^3")
 
 
-WORKLOAD_SAMPLES = [
-    ("llama31_8b", "mxfp4", 2048, 28672, 4096),
-    ("llama31_8b", "mxfp4", 256, 4096, 14336),
-    ("llama33_70b", "mxfp8", 8, 8192, 28672),
-    ("llama33_70b", "mxfp4", 64, 10240, 8192),
-    ("qwen3_32b", "mxfp8", 128, 5120, 25600),
-    ("qwen3_32b", "mxfp4", 4096, 10240, 5120),
-]
+def _all_workload_cases():
+    """Every shape of the model workloads, grouped so that consecutive cases share
+    the weight operand B: (workload, fmt, shape index, (N,K) index, M, N, K)."""
+    from mx_block_scaled_gb300.inputs import WORKLOADS
+    out = []
+    for name in ("llama31_8b", "llama33_70b", "qwen3_32b"):
+        cases = list(workload_cases(name))
+        cases.sort(key=lambda c: (c[0], c[2], c[3]))
+        out += [(name, c[0], c[1], c[2], c[3], c[4], c[5]) for c in cases]
+    assert len(out) == sum(len(w["fmts"]) * len(w["ms"]) * len(w["nks"])
+                           for n, w in WORKLOADS.items() if n in ("llama31_8b", "llama33_70b", "qwen3_32b"))
+    return out
 
 
-def find_case(name, fmt, M, N, K):
-    for f, si, nki, m, n, k in workload_cases(name):
-        if (f, m, n, k) == (fmt, M, N, K):
-            return si, nki
-    raise KeyError((name, fmt, M, N, K))
+_WEIGHTS = {}
 
 
-@pytest.mark.parametrize("name,fmt,M,N,K", WORKLOAD_SAMPLES,
-                         ids=[f"{w[0]}-{w[1]}-M{w[2]}-N{w[3]}-K{w[4]}" for w in WORKLOAD_SAMPLES])
-def test_workload_sampled(oracle_mod, name, fmt, M, N, K):
+def _weights(name, fmt, nki, N, K):
+    key = (name, fmt, nki)
+    if key not in _WEIGHTS:
+        _WEIGHTS.clear()  # one weight resident at a time: cases are grouped by weight
+        _WEIGHTS[key] = make_operand(name, "B", nki, N, K, fmt)
+    return _WEIGHTS[key]
+
+
+@pytest.mark.parametrize("name,fmt,si,nki,M,N,K", _all_workload_cases(),
+                         ids=[f"{c[0]}-{c[1]}-M{c[4]}-N{c[5]}-K{c[6]}" for c in _all_workload_cases()])
+def test_workload_full_size_sampled(oracle_mod, name, fmt, si, nki, M, N, K):
+    """Full-size model shapes in the default launch configuration: every output of
+    sampled rows (all columns) and of sampled columns (all rows) within the bound."""
     f = FMT_MXFP8 if fmt == "mxfp8" else FMT_MXFP4
-    si, nki = find_case(name, fmt, M, N, K)
     A, SA = make_operand(name, "A", si, M, K, f)
-    B, SB = make_operand(name, "B", nki, N, K, f)
-    C = gpu_gemm(f, A, SA, B, SB, K, OUT_BF16)
-    rows = sample_indices(M, 1) if M > 64 else np.arange(M)
-    cols = sample_indices(N, 2)
+    B, SB = _weights(name, f, nki, N, K)
+    import torch
+    C = gpu_gemm_device(f, A, SA, B, SB, K, OUT_BF16)
+    rows = sample_indices(M, si, count=12) if M > 64 else np.arange(M)
+    cols = sample_indices(N, nki + 100, count=12)
+    C_rows = C[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    C_cols = C[:, torch.from_numpy(cols).cuda()].double().cpu().numpy()
+    del C
     ref_r, S_r = oracle_mod.gemm(f, A, SA, B, SB, K, rows=rows)
-    assert_within(C[rows], ref_r, S_r, OUT_BF16, f"{name} rows")
+    assert_within(C_rows, ref_r, S_r, OUT_BF16, f"{name} rows")
     ref_c, S_c = oracle_mod.gemm(f, A, SA, B, SB, K, cols=cols)
-    assert_within(C[:, cols], ref_c, S_c, OUT_BF16, f"{name} cols")
+    assert_within(C_cols, ref_c, S_c, OUT_BF16, f"{name} cols")
 
 
 # ---- failure path: a stalled kernel returns an error instead of hanging --------
