@@ -402,15 +402,20 @@ def run_sweep(args):
     hbm_gbs, bf16_tf, _, peak_src = load_peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     names = args.sweep_workloads.split(",") if args.sweep_workloads else list(WORKLOADS)
-    for name in names:
+    if args.shape:
+        M0, N0, K0 = (int(v) for v in args.shape.split(","))
+        cases = [("shape", [(args.fmt, 0, 0, M0, N0, K0)])]
+    else:
+        cases = [(name, list(workload_cases(name))) for name in names]
+    for name, wcases in cases:
         seen = set()
-        for fmt_name, si, nki, M, N, K in workload_cases(name):
+        for fmt_name, si, nki, M, N, K in wcases:
             if (fmt_name, M, N, K) in seen:
                 continue
             seen.add((fmt_name, M, N, K))
             fmt = FMT_BY_NAME[fmt_name]
             rb = K if fmt_name == "mxfp8" else K // 2
-            out = mx.MXGEMM_OUT_BF16 if WORKLOADS[name]["out"] == "bf16" else mx.MXGEMM_OUT_F32
+            out = mx.MXGEMM_OUT_BF16 if name == "shape" or WORKLOADS[name]["out"] == "bf16" else mx.MXGEMM_OUT_F32
             ob = 2 if out == mx.MXGEMM_OUT_BF16 else 4
             g = torch.Generator(device=dev)
             g.manual_seed(si * 7919 + nki)
@@ -492,12 +497,14 @@ def main():
     ap.add_argument("--sweep-workloads", default="")
     ap.add_argument("--sweep-reps", type=int, default=20)
     ap.add_argument("--sweep-flags", type=int, default=0, help="mxgemm_plan_create flags for --sweep")
+    ap.add_argument("--shape", default="", help="M,N,K: sweep this one shape (BF16 out)")
+    ap.add_argument("--fmt", default="mxfp8", choices=["mxfp8", "mxfp4"], help="format for --shape")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
-    if args.sweep:
+    if args.sweep or args.shape:
         return run_sweep(args)
     return run_ours(args)
 
