@@ -11,4 +11,7 @@ from .mxref import (  # noqa: F401
     decode_table,
     gemm,
     num_threads,
+    quantize,
+    IN_F32,
+    IN_BF16,
 )

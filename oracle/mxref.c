@@ -222,3 +222,149 @@ int mxref_num_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------- */
+/* Reference MX quantiser (the step before the GEMM).                         */
+/*                                                                            */
+/* The FlyDSL page (English digest, "Performance numbers need their           */
+/* baselines") times the scaled GEMMs from already-quantised inputs and       */
+/* prints no quantisation formula; the recipe below is this repository's      */
+/* reading.  Per row and 32-value block along K:                              */
+/*   amax = max |x| over the block;                                           */
+/*   E = floor(log2 amax), taken exactly from the binary exponent (frexp);    */
+/*   s = max(E - e_max, -127), e_max = 8 (E4M3: 448 = 1.75 * 2^8) or          */
+/*       2 (E2M1: 6 = 1.5 * 2^2); s cannot exceed 125 for finite input;       */
+/*   an all-zero block takes s = 0;                                           */
+/*   scale code = s + 127;                                                    */
+/*   element = x / 2^s rounded to the nearest value of the element grid,      */
+/*   ties to even, magnitudes past the largest finite value saturate (448 or  */
+/*   6); the sign of a zero result is the sign of x.                          */
+/*   A block holding a NaN or an infinity gets scale code 0xFF (NaN) and all  */
+/*   element codes 0: in MX a NaN scale makes the whole block NaN, and E2M1   */
+/*   has no NaN of its own, so this is the one encoding both formats share.   */
+/* Arithmetic in binary64: x / 2^s is exact, so rounding happens once.        */
+/* ------------------------------------------------------------------------- */
+
+/* Round v (exact binary64) to the nearest value of the grid with `mbits`
+ * fraction bits and smallest normal exponent `emin`, ties to even, then
+ * saturate to vmax. */
+static double grid_round(double v, int emin, int mbits, double vmax)
+{
+    double mag = fabs(v);
+    if (mag == 0.0)
+        return v;
+    int e;
+    frexp(mag, &e); /* mag = f * 2^e, f in [0.5, 1): floor(log2 mag) = e - 1 */
+    int q = (e - 1 > emin ? e - 1 : emin) - mbits;  /* grid spacing 2^q */
+    double t = ldexp(mag, -q);                      /* exact */
+    double fl = floor(t);
+    double fr = t - fl;
+    double r;
+    if (fr > 0.5)
+        r = fl + 1.0;
+    else if (fr < 0.5)
+        r = fl;
+    else
+        r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+    r = ldexp(r, q);
+    if (r > vmax)
+        r = vmax;
+    return v < 0 ? -r : r;  /* a negative v that rounds to zero gives -0 */
+}
+
+/* Code of an E4M3 grid value (|r| <= 448, never NaN here). */
+static uint8_t encode_e4m3(double r)
+{
+    uint8_t sign = signbit(r) ? 0x80 : 0;
+    double mag = fabs(r);
+    if (mag == 0.0)
+        return sign;
+    if (mag < ldexp(1.0, -6))                    /* subnormal: m * 2^-9 */
+        return sign | (uint8_t)(mag * 512.0);
+    int e;
+    double f = frexp(mag, &e);                   /* mag = f * 2^e */
+    int ef = e + 6;                              /* biased exponent (bias 7) */
+    int mf = (int)((2.0 * f - 1.0) * 8.0 + 0.5); /* exact: r is on the grid */
+    return sign | (uint8_t)(ef << 3) | (uint8_t)mf;
+}
+
+/* Code of an E2M1 grid value (|r| <= 6). */
+static uint8_t encode_e2m1(double r)
+{
+    static const double mag_of[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    uint8_t sign = signbit(r) ? 8 : 0;
+    double mag = fabs(r);
+    for (uint8_t c = 0; c < 8; ++c)
+        if (mag_of[c] == mag)
+            return sign | c;
+    return 0; /* unreachable after grid_round */
+}
+
+/*
+ * in_dtype: 1 = FP32, 2 = BF16 (raw 16-bit patterns).  x: rows x K, row-major.
+ * codes: rows x K bytes (MXFP8) or rows x K/2 bytes (MXFP4, element 2i in the
+ * low nibble); scales: rows x K/32 bytes, row-major.  Returns 0, or -1 for
+ * bad arguments (unknown fmt or in_dtype, K not a positive multiple of 32).
+ */
+int mxref_quantize(int fmt, int in_dtype, int64_t rows, int64_t K, const void *x,
+                   uint8_t *codes, uint8_t *scales)
+{
+    if ((fmt != MXREF_FMT_MXFP8 && fmt != MXREF_FMT_MXFP4) || (in_dtype != 1 && in_dtype != 2) ||
+        rows < 0 || K <= 0 || K % 32 != 0)
+        return -1;
+    const int e_max = fmt == MXREF_FMT_MXFP8 ? 8 : 2;
+    const int emin = fmt == MXREF_FMT_MXFP8 ? -6 : 0;
+    const int mbits = fmt == MXREF_FMT_MXFP8 ? 3 : 1;
+    const double vmax = fmt == MXREF_FMT_MXFP8 ? 448.0 : 6.0;
+    const int64_t row_bytes = fmt == MXREF_FMT_MXFP8 ? K : K / 2;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        uint8_t *code_row = codes + r * row_bytes;
+        for (int64_t j = 0; j < K / 32; ++j) {
+            double v[32];
+            double amax = 0.0;
+            int nonfinite = 0;
+            for (int t = 0; t < 32; ++t) {
+                const int64_t k = 32 * j + t;
+                if (in_dtype == 1) {
+                    v[t] = (double)((const float *)x)[r * K + k];
+                } else {
+                    uint32_t bits = (uint32_t)((const uint16_t *)x)[r * K + k] << 16;
+                    float f;
+                    memcpy(&f, &bits, sizeof f);
+                    v[t] = (double)f;
+                }
+                if (!isfinite(v[t]))
+                    nonfinite = 1;
+                else if (fabs(v[t]) > amax)
+                    amax = fabs(v[t]);
+            }
+            if (nonfinite) {
+                scales[r * (K / 32) + j] = 0xFF;
+                memset(code_row + j * (row_bytes / (K / 32)), 0, (size_t)(row_bytes / (K / 32)));
+                continue;
+            }
+            int s = 0;
+            if (amax > 0.0) {
+                int e;
+                frexp(amax, &e);
+                s = (e - 1) - e_max;
+                if (s < -127)
+                    s = -127;
+            }
+            scales[r * (K / 32) + j] = (uint8_t)(s + 127);
+            for (int t = 0; t < 32; ++t) {
+                const int64_t k = 32 * j + t;
+                const double q = grid_round(ldexp(v[t], -s), emin, mbits, vmax);
+                if (fmt == MXREF_FMT_MXFP8) {
+                    code_row[k] = encode_e4m3(q);
+                } else {
+                    const uint8_t c = encode_e2m1(q);
+                    uint8_t *b = &code_row[k / 2];
+                    *b = (k & 1) ? (uint8_t)((*b & 0x0F) | (c << 4)) : (uint8_t)((*b & 0xF0) | c);
+                }
+            }
+        }
+    }
+    return 0;
+}

@@ -51,6 +51,9 @@ def _load():
             lib.mxref_decode_table.restype = ctypes.c_int
             lib.mxref_decode_table.argtypes = [ctypes.c_int, ctypes.c_void_p]
             lib.mxref_num_threads.restype = ctypes.c_int
+            lib.mxref_quantize.restype = ctypes.c_int
+            lib.mxref_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -105,3 +108,20 @@ def gemm(fmt: int, A, SA, B, SB, K: int, rows=None, cols=None,
     if rc != 0:
         raise ValueError("mxref_gemm rejected its arguments")
     return C, S
+
+
+IN_F32 = 1
+IN_BF16 = 2
+
+
+def quantize(fmt: int, x, in_dtype: int = IN_F32):
+    """Reference MX quantiser: x [rows, K] (float32, or uint16 BF16 bit patterns when
+    in_dtype == IN_BF16) -> (codes, row-major scales)."""
+    x = np.ascontiguousarray(x, dtype=np.float32 if in_dtype == IN_F32 else np.uint16)
+    rows, K = x.shape
+    codes = np.zeros((rows, K if fmt == FMT_MXFP8 else K // 2), dtype=np.uint8)
+    scales = np.empty((rows, K // 32), dtype=np.uint8)
+    rc = _load().mxref_quantize(fmt, in_dtype, rows, K, x.ctypes.data, codes.ctypes.data, scales.ctypes.data)
+    if rc != 0:
+        raise ValueError("mxref_quantize rejected its arguments")
+    return codes, scales

@@ -59,3 +59,51 @@ def load_handworked(K: int = 128):
         out.append(dict(name=c["name"], fmt=c["fmt"], A=a, B=b,
                         SA=c["sa"][None, :], SB=c["sb"][None, :], expected=c["expected"]))
     return out
+
+
+def _qvalue(tok: str) -> float:
+    t = tok.lower()
+    if t in ("nan", "inf", "-inf"):
+        return float(t)
+    if "x" in t:
+        m, e = t.split("x")
+        return float(Fraction(m) * Fraction(2) ** int(e))
+    return float(Fraction(t)) if t.lstrip("-") != "0" else (-0.0 if t.startswith("-") else 0.0)
+
+
+def _qruns(spec: str, conv) -> list:
+    out = []
+    for tok in spec.split():
+        val, count = tok.rsplit("*", 1)
+        out += [conv(val)] * int(count)
+    return out
+
+
+def load_quantize_handworked():
+    """Hand-worked quantisation blocks: list of dicts name, fmt, x (float32 [1, 32]),
+    scale (int), codes (uint8 [32], one per element), bf16 (bool)."""
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN_DIR, "quantize_handworked.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, val = line.partition(":")
+            val = val.strip()
+            if key == "case":
+                cur = {"name": val, "bf16": False}
+                cases.append(cur)
+            elif key == "fmt":
+                cur["fmt"] = {"mxfp8": FMT_MXFP8, "mxfp4": FMT_MXFP4}[val]
+            elif key == "x":
+                cur["x"] = np.array(_qruns(val, _qvalue), dtype=np.float32)[None, :]
+            elif key == "scale":
+                cur["scale"] = int(val)
+            elif key == "codes":
+                cur["codes"] = np.array(_qruns(val, lambda v: int(v, 16)), dtype=np.uint8)
+            elif key == "bf16":
+                cur["bf16"] = val == "yes"
+    for c in cases:
+        if c["x"].shape != (1, 32) or c["codes"].shape != (32,):
+            raise ValueError(f"case {c['name']}: expected 32 inputs and 32 codes")
+    return cases
