@@ -60,6 +60,7 @@ struct GemmParams {
     int out_kind;             // OutKind
     int vec_ok;               // 1: stride_j == 1 and rows are 16-byte aligned
     int test_stall;           // self-test: the producer issues nothing (waits expire)
+    int stream_a, stream_b;   // 1: that operand is read by at most two tiles (load it evict-first)
     const uint8_t *sfa;       // tile-layout scales of the A role
     const uint8_t *sfb;       // tile-layout scales of the B role
     void *out;                // output base (C, or split-K partial slabs)
@@ -320,8 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The whole warp runs the loop (so loop state stays warp-uniform); one
         // elected lane issues the barrier arm and the copies.
         if (!p.test_stall) {
-            const uint64_t pol_a = l2_policy_evict_last();
-            const uint64_t pol_b = l2_policy_evict_last();
+            // Operands re-read by many tiles stay in L2 (evict-last); a streamed operand
+            // (the weight of a decode GEMM) is loaded evict-first so it does not push
+            // the re-used one out.
+            const uint64_t pol_a = p.stream_a ? l2_policy_evict_first() : l2_policy_evict_last();
+            const uint64_t pol_b = p.stream_b ? l2_policy_evict_first() : l2_policy_evict_last();
             int st = 0;
             uint32_t ph = 0;
             uint32_t armed = 0;      // bit s: slot s armed at least once

@@ -541,6 +541,10 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     p.splits = plan->splits;
     p.group_m = plan->group_m;
     p.test_stall = test_stall;
+    // An A-role tile is read once per B-role tile column and vice versa (in pair
+    // and MC modes one load of a B-role tile serves the pair).
+    p.stream_a = plan->tiles_n <= 2 ? 1 : 0;
+    p.stream_b = plan->tiles_m <= 2 ? 1 : 0;
     p.sfa = plan->swap ? sfb : sfa;
     p.sfb = plan->swap ? sfa : sfb;
     p.stride_i = plan->swap ? 1 : N;
