@@ -16,7 +16,8 @@ With --gpus N under torchrun every rank runs an independent replica (the GEMM
 has no exchange step); value = all ranks' FLOPs / the slowest rank's time.
 --impl reference times the CPU oracle (the only other program computing the
 same result here) on a bounded sample of the same workload.
---sweep prints one line per shape of the model workloads (not the headline).
+--sweep prints one line per shape of the model workloads (not the headline);
+--quant-sweep one line per activation shape for the MX quantiser.
 """
 from __future__ import annotations
 
@@ -483,6 +484,71 @@ def run_sweep(args):
     return 0
 
 
+def run_quant_sweep(args):
+    """Per-shape time of the MX quantiser (BF16 activations -> codes + tile-layout
+    scales) over the activation shapes [M, K] of the model workloads."""
+    import torch
+    from mx_block_scaled_gb300 import binding as mx
+    from mx_block_scaled_gb300.inputs import FMT_BY_NAME, WORKLOADS, workload_cases
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    hbm_gbs, _, _, _ = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    names = args.sweep_workloads.split(",") if args.sweep_workloads else list(WORKLOADS)
+    shapes = []
+    for name in names:
+        for fmt_name, _, _, M, _, K in workload_cases(name):
+            if (fmt_name, M, K) not in [(f, m, k) for _, f, m, k in shapes]:
+                shapes.append((name, fmt_name, M, K))
+    for name, fmt_name, M, K in shapes:
+        fmt = FMT_BY_NAME[fmt_name]
+        rb = K if fmt_name == "mxfp8" else K // 2
+        sf = mx.mxgemm_sf_bytes(M, K)
+        byts = M * K * 2 + M * rb + sf
+        nsets = max(2, math.ceil(2 * l2 / byts) + 1)
+        nsets = min(nsets, max(2, int(20e9 // byts)))
+        g = torch.Generator(device=dev)
+        g.manual_seed(M * 131 + K)
+        sets = [(torch.randn((M, K), dtype=torch.float32, device=dev, generator=g).to(torch.bfloat16),
+                 torch.empty((M, rb), dtype=torch.uint8, device=dev),
+                 torch.empty(sf, dtype=torch.uint8, device=dev)) for _ in range(nsets)]
+
+        def one(i):
+            x, c, t = sets[i % nsets]
+            st = mx.mxgemm_quantize(fmt, mx.MXGEMM_IN_BF16, x.data_ptr(), M, K, c.data_ptr(), t.data_ptr(),
+                                    mx.MXGEMM_QUANT_SF_TILED, torch.cuda.current_stream().cuda_stream)
+            assert st == 0
+
+        for i in range(3):
+            one(i)
+        torch.cuda.synchronize()
+        reps = args.sweep_reps
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(reps):
+                one(i)
+        graph.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / reps)
+        mx.check_device_status()
+        del graph
+        t = statistics.median(ts) / 1e3
+        print(json.dumps({"kernel": "mx_quantize_kernel", "workload": name, "format": fmt_name, "input": "bf16",
+                          "M": M, "K": K, "us": t * 1e6, "bytes": byts, "gbs": byts / t / 1e9,
+                          "frac_hbm": byts / t / 1e9 / hbm_gbs, "nsets": nsets}), flush=True)
+        del sets
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -499,11 +565,15 @@ def main():
     ap.add_argument("--sweep-flags", type=int, default=0, help="mxgemm_plan_create flags for --sweep")
     ap.add_argument("--shape", default="", help="M,N,K: sweep this one shape (BF16 out)")
     ap.add_argument("--fmt", default="mxfp8", choices=["mxfp8", "mxfp4"], help="format for --shape")
+    ap.add_argument("--quant-sweep", action="store_true",
+                    help="time the MX quantiser over the workloads' activation shapes")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.quant_sweep:
+        return run_quant_sweep(args)
     if args.sweep or args.shape:
         return run_sweep(args)
     return run_ours(args)

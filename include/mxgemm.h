@@ -141,6 +141,46 @@ MXGEMM_API size_t mxgemm_sf_bytes(int64_t rows, int64_t K);
 MXGEMM_API int mxgemm_relayout_scales(const uint8_t *src, int64_t rows, int64_t K,
                            uint8_t *dst, void *stream);
 
+/* Input element type of mxgemm_quantize. */
+#define MXGEMM_IN_F32               1          /* FP32, 4 bytes per value             */
+#define MXGEMM_IN_BF16              2          /* BF16, 2 bytes per value             */
+
+/* Quantise flags (mxgemm_quantize). */
+#define MXGEMM_QUANT_SF_TILED       (1u << 0)  /* write scales in the tile layout     */
+
+/*
+ * MX quantiser: x [rows, K] (FP32 or BF16, row-major) -> element codes in the
+ * operand format mxgemm_run reads, plus one E8M0 scale per 32 values along K.
+ * The step that precedes the GEMM: the FlyDSL page (English digest, section
+ * "Performance numbers need their baselines") times the scaled GEMMs from
+ * already-quantised inputs and prints no quantisation formula.  The recipe
+ * used here, per row and 32-value block (the same reading as the oracle):
+ *     s = max(floor(log2 amax) - e_max, -127)   e_max = 8 (E4M3), 2 (E2M1);
+ *     an all-zero block takes s = 0; scale code = s + 127;
+ *     code = x / 2^s rounded to the nearest E4M3 / E2M1 value, ties to even,
+ *            saturating at +-448 / +-6 (a zero keeps the sign of x);
+ *     a block holding a NaN or an infinity: scale code 0xFF, all codes 0.
+ *   fmt:      mxgemm_format_t of the codes.
+ *   in_dtype: MXGEMM_IN_F32 or MXGEMM_IN_BF16.
+ *   x:        device, rows x K values, 32-byte aligned, read-only.
+ *   codes:    device, rows x K bytes (MXFP8) or rows x K/2 bytes (MXFP4,
+ *             element 2i in the low nibble), 16-byte aligned; overwritten.
+ *   scales:   device, 16-byte aligned; overwritten.  Without flags:
+ *             rows x K/32 bytes row-major (the SA/SB input of mxgemm_run).
+ *             With MXGEMM_QUANT_SF_TILED: mxgemm_sf_bytes(rows, K) bytes in
+ *             the tile layout of mxgemm_relayout_scales (padding rows = 127),
+ *             ready for mxgemm_run with MXGEMM_RUN_SA_PRELAYOUT (or _SB_) --
+ *             this skips the relayout copy the FlyDSL page ("API
+ *             compatibility is not universal input coverage") warns about.
+ *   K:        multiple of 32; a multiple of 128 with MXGEMM_QUANT_SF_TILED.
+ * One stream-ordered kernel launch, no allocation.
+ * Errors: MXGEMM_ERR_ARG (NULL pointer, unknown fmt / in_dtype / flag),
+ * MXGEMM_ERR_SHAPE (rows < 1, K not as above), MXGEMM_ERR_ALIGN,
+ * MXGEMM_ERR_ARCH, MXGEMM_ERR_CUDA (launch failed).
+ */
+MXGEMM_API int mxgemm_quantize(int fmt, int in_dtype, const void *x, int64_t rows, int64_t K,
+                               void *codes, uint8_t *scales, uint32_t flags, void *stream);
+
 /*
  * Run the GEMM on `stream`.
  *   A:  M x K codes (fmt-dependent bytes per row, row-major, 16-byte aligned)

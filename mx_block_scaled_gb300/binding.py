@@ -40,6 +40,10 @@ MXGEMM_PLAN_SPLITK_SHIFT = 8
 MXGEMM_RUN_SA_PRELAYOUT = 1 << 0
 MXGEMM_RUN_SB_PRELAYOUT = 1 << 1
 
+MXGEMM_IN_F32 = 1
+MXGEMM_IN_BF16 = 2
+MXGEMM_QUANT_SF_TILED = 1 << 0
+
 # (name, restype, argtypes) for every entry point declared in include/mxgemm.h
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -51,6 +55,8 @@ SIGNATURES = [
     ("mxgemm_plan_describe", ctypes.c_int, [_P, ctypes.c_char_p, ctypes.c_size_t]),
     ("mxgemm_sf_bytes", ctypes.c_size_t, [_I64, _I64]),
     ("mxgemm_relayout_scales", ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+    ("mxgemm_quantize", ctypes.c_int,
+     [ctypes.c_int, ctypes.c_int, _P, _I64, _I64, _P, _P, ctypes.c_uint32, _P]),
     ("mxgemm_run", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     ("mxgemm_run_noalloc", ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_uint32, _P]),
     ("mxgemm_device_status", ctypes.c_int, [_P, ctypes.c_int]),
@@ -117,6 +123,11 @@ def mxgemm_sf_bytes(rows: int, K: int) -> int:
 
 def mxgemm_relayout_scales(src_ptr: int, rows: int, K: int, dst_ptr: int, stream: int) -> int:
     return _lib.mxgemm_relayout_scales(src_ptr, rows, K, dst_ptr, stream)
+
+
+def mxgemm_quantize(fmt: int, in_dtype: int, x_ptr: int, rows: int, K: int, codes_ptr: int,
+                    scales_ptr: int, flags: int, stream: int) -> int:
+    return _lib.mxgemm_quantize(fmt, in_dtype, x_ptr, rows, K, codes_ptr, scales_ptr, flags, stream)
 
 
 def mxgemm_run(plan, A_ptr: int, SA_ptr: int, B_ptr: int, SB_ptr: int, C_ptr: int,
@@ -201,6 +212,33 @@ def relayout_scales(S, rows: int, K: int, out=None, stream=None):
     _check(mxgemm_relayout_scales(S.data_ptr(), rows, K, out.data_ptr(), _stream_handle(stream)),
            "mxgemm_relayout_scales")
     return out
+
+
+def quantize(x, fmt: int, tiled: bool = False, codes=None, scales=None, stream=None):
+    """MX-quantise a CUDA tensor x [rows, K] (float32 or bfloat16, contiguous).
+
+    Returns ``(codes, scales)`` as CUDA uint8 tensors: codes [rows, K] (MXFP8)
+    or [rows, K/2] (MXFP4); scales [rows, K/32] row-major, or, with
+    ``tiled=True``, mxgemm_sf_bytes(rows, K) bytes in the tile layout.
+    """
+    import torch
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D tensor")
+    in_dtype = {torch.float32: MXGEMM_IN_F32, torch.bfloat16: MXGEMM_IN_BF16}.get(x.dtype)
+    if in_dtype is None:
+        raise ValueError(f"unsupported input dtype {x.dtype}")
+    rows, K = x.shape
+    if codes is None:
+        codes = torch.empty((rows, K if fmt == MXGEMM_FMT_MXFP8_E4M3 else K // 2), dtype=torch.uint8,
+                            device=x.device)
+    if scales is None:
+        n = mxgemm_sf_bytes(rows, K) if tiled else rows * (K // 32)
+        scales = torch.empty(max(n, 1), dtype=torch.uint8, device=x.device)
+        if not tiled:
+            scales = scales[: rows * (K // 32)].view(rows, K // 32) if n else scales
+    _check(mxgemm_quantize(fmt, in_dtype, x.data_ptr(), rows, K, codes.data_ptr(), scales.data_ptr(),
+                           MXGEMM_QUANT_SF_TILED if tiled else 0, _stream_handle(stream)), "mxgemm_quantize")
+    return codes, scales
 
 
 def check_device_status(stream=None) -> None:

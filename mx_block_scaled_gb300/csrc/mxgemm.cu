@@ -13,6 +13,7 @@
 
 #include "launch.h"
 #include "mxgemm.h"
+#include "quantize.h"
 
 namespace {
 
@@ -467,6 +468,37 @@ int mxgemm_relayout_scales(const uint8_t *src, int64_t rows, int64_t K, uint8_t 
     RelayoutJob j = make_job(src, rows, K, dst);
     return launch_relayout(j, nullptr, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXGEMM_OK
                                                                                           : MXGEMM_ERR_CUDA;
+}
+
+int mxgemm_quantize(int fmt, int in_dtype, const void *x, int64_t rows, int64_t K, void *codes, uint8_t *scales,
+                    uint32_t flags, void *stream)
+{
+    if (!x || !codes || !scales)
+        return MXGEMM_ERR_ARG;
+    if ((fmt != MXGEMM_FMT_MXFP8_E4M3 && fmt != MXGEMM_FMT_MXFP4_E2M1) ||
+        (in_dtype != MXGEMM_IN_F32 && in_dtype != MXGEMM_IN_BF16) || (flags & ~MXGEMM_QUANT_SF_TILED) != 0)
+        return MXGEMM_ERR_ARG;
+    const bool tiled = (flags & MXGEMM_QUANT_SF_TILED) != 0;
+    if (rows < 1 || rows > (1ll << 31) || K < 32 || K % 32 != 0 || K > (1ll << 31) || (tiled && K % 128 != 0))
+        return MXGEMM_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(x) & 31u) != 0 || !aligned16(codes) || !aligned16(scales))
+        return MXGEMM_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    const int st = device_info(&dev);
+    if (st != MXGEMM_OK)
+        return st;
+    mxg::QuantParams p;
+    p.x = x;
+    p.codes = codes;
+    p.scales = scales;
+    p.rows = rows;
+    p.K = K;
+    p.fmt = fmt == MXGEMM_FMT_MXFP8_E4M3 ? mxg::kQuantFmtMxfp8 : mxg::kQuantFmtMxfp4;
+    p.in_dtype = in_dtype == MXGEMM_IN_BF16 ? mxg::kQuantInBf16 : mxg::kQuantInF32;
+    p.tiled = tiled ? 1 : 0;
+    p.sf_words = K % 128 == 0 ? 1 : 0;
+    return mxg::launch_quantize(p, dev->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXGEMM_OK
+                                                                                                   : MXGEMM_ERR_CUDA;
 }
 
 static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB, void *C,

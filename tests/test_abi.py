@@ -92,3 +92,22 @@ def test_oracle_builds_and_is_separate(oracle_mod):
     from oracle import mxref
     assert os.path.exists(mxref.build())
     assert "mx_block_scaled_gb300" not in open(os.path.join(ROOT, "oracle", "mxref.c")).read()
+
+
+@pytest.mark.parametrize("fmt,in_dtype,x,rows,K,codes,scales,flags,expect", [
+    (1, 2, 0, 4, 128, 64, 64, 0, -1),          # NULL x
+    (1, 2, 64, 4, 128, 0, 64, 0, -1),          # NULL codes
+    (1, 2, 64, 4, 128, 64, 0, 0, -1),          # NULL scales
+    (3, 2, 64, 4, 128, 64, 64, 0, -1),         # unknown format
+    (1, 7, 64, 4, 128, 64, 64, 0, -1),         # unknown input type
+    (1, 2, 64, 4, 128, 64, 64, 1 << 5, -1),    # unknown flag
+    (1, 2, 64, 0, 128, 64, 64, 0, -2),         # rows < 1
+    (1, 2, 64, 4, 48, 64, 64, 0, -2),          # K % 32 != 0
+    (2, 1, 64, 4, 96, 64, 64, 1, -2),          # tile layout needs K % 128 == 0
+    (1, 2, 48, 4, 128, 64, 64, 0, -3),         # x only 16-byte aligned (needs 32)
+    (1, 2, 64, 4, 128, 72, 64, 0, -3),         # codes misaligned
+    (1, 2, 64, 4, 128, 64, 65, 0, -3),         # scales misaligned
+])
+def test_quantize_validates_before_touching_the_device(lib, fmt, in_dtype, x, rows, K, codes, scales, flags,
+                                                        expect):
+    assert lib.mxgemm_quantize(fmt, in_dtype, x, rows, K, codes, scales, flags, 0) == expect
