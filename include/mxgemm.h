@@ -83,6 +83,7 @@ typedef enum {
 #define MXGEMM_PLAN_FORCE_MC        (1u << 6)  /* 128-row tiles, CTA pairs share B    */
 #define MXGEMM_PLAN_STREAMK         (1u << 7)  /* spread the last wave's k-stages     */
 #define MXGEMM_PLAN_SPLITK_SHIFT    8          /* bits 8..15: forced split-K (0=auto) */
+#define MXGEMM_PLAN_NO_STREAMK      (1u << 16) /* whole tiles only (no stream-K)      */
 
 /* Run flags (mxgemm_run). */
 #define MXGEMM_RUN_SA_PRELAYOUT     (1u << 0)  /* SA is already in the tile layout    */

@@ -69,16 +69,16 @@ struct GemmParams {
     long long split_stride;   // elements between split partial slabs (0: no split)
     unsigned long long timeout_ns;
     int *status;              // sticky device status word
-    // Stream-K (single-CTA kernel): the first dp_tiles tiles in raster order are
-    // computed whole, round-robin over the grid; the k-stages of the remaining
-    // tiles are divided evenly over CTAs 0..sk_ctas-1.  A tile cut between CTAs is
+    // Stream-K: the first dp_tiles tiles in raster order are computed whole,
+    // round-robin over the grid; the k-stages of the remaining tiles are divided
+    // evenly over CTAs (CTA pairs, in the pair kernel) 0..sk_ctas-1.  A tile cut between CTAs is
     // finished by the last of them to arrive, which adds the others' FP32 partial
     // sums in k order (deterministic).  sk_ctas == 0: no stream-K phase.
     int dp_tiles;
     int sk_ctas;
     long long sk_stages;      // (tiles - dp_tiles) * kstages
-    int *sk_counters;         // one arrival counter per stream-K tile, zero at launch
-    float *sk_partials;       // two 128 x BN FP32 slots per stream-K CTA
+    int *sk_counters;         // one arrival counter per stream-K tile and 128-row share, zero at launch
+    float *sk_partials;       // two 128 x BN FP32 slots per stream-K CTA (per CTA of a pair)
 };
 
 template <bool FP4, int BN>
@@ -243,6 +243,105 @@ __device__ __forceinline__ void store_row32_masked(const GemmParams &p, long lon
     }
 }
 
+// Stream-K epilogue of one CTA's 128-row share of a tile cut between CTAs (or
+// CTA pairs): publish this segment's FP32 partial sum; if it is the last
+// segment of the tile to arrive, add every segment's partial in k order
+// (deterministic, this CTA's own re-read from its slot) and store C.
+//   unit:   the CTA's (or pair's) stream-K index; slots are numbered
+//           ((2 * unit + w.slot) * halves + half) -- `halves` 128-row shares
+//           per tile (1: single CTA, 2: CTA pair), `half` this CTA's share;
+//   row0:   first A-role row of this CTA's share.
+// Slot layout [h][chunk][4-column group][row]: each warp access is 32
+// consecutive 16-byte vectors (the rows of one TMEM lane quarter).
+template <int BN, int kCols, int kChunks>
+__device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, const uint32_t (&r)[kChunks][32],
+                                            int unit, int halves, int half, int row0, int h, int row_local,
+                                            bool has_cols, int *sk_last)
+{
+    constexpr size_t kSlot = static_cast<size_t>(kBM) * BN;
+    uint4 *const mine =
+        reinterpret_cast<uint4 *>(p.sk_partials + static_cast<size_t>((2 * unit + w.slot) * halves + half) * kSlot);
+    if (has_cols) {
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                mine[((h * kChunks + c) * 8 + v) * kBM + row_local] =
+                    make_uint4(r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2], r[c][4 * v + 3]);
+        }
+    }
+    __threadfence();
+    epi_bar_sync();
+    const long long t0 = static_cast<long long>(w.tile - p.dp_tiles) * p.kstages;
+    const int c_first = sk_cta_of(p, t0);
+    const int c_last = sk_cta_of(p, t0 + p.kstages - 1);
+    int *const counter = p.sk_counters + (w.tile - p.dp_tiles) * halves + half;
+    if (threadIdx.x == 64) {
+        const int old = atomicAdd(counter, 1);
+        const int last = old == c_last - c_first;
+        if (last)
+            *counter = 0;  // ready for the next launch
+        *sk_last = last;
+    }
+    epi_bar_sync();
+    const bool last = *sk_last != 0;
+    epi_bar_sync();  // sk_last is read before the next segment may rewrite it
+    if (!last)
+        return;
+    __threadfence();
+    const int i = row0 + row_local;
+    if (!has_cols || i >= p.rows_a)
+        return;
+    const long long base_off = static_cast<long long>(i) * p.stride_i;
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c) {
+        const int j0 = w.tn * BN + h * kCols + c * 32;
+        if (j0 >= p.rows_b) break;
+        float sum[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            sum[e] = 0.0f;
+        // k order; the 32 columns of three segments are loaded at once (the sum
+        // is L2-latency bound: keep many loads in flight).  Past the last
+        // segment the loads repeat it and the adds are skipped.
+#pragma unroll 1
+        for (int cc0 = c_first; cc0 <= c_last; cc0 += 3) {
+            float4 x[3][8];
+#pragma unroll
+            for (int g = 0; g < 3; ++g) {
+                const int cc = min(cc0 + g, c_last);
+                const long long beg = p.sk_stages * cc / p.sk_ctas;
+                const int slot = (beg / p.kstages == w.tile - p.dp_tiles) ? 0 : 1;
+                const float4 *src = reinterpret_cast<const float4 *>(
+                                        p.sk_partials + static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
+                                    (h * kChunks + c) * 8 * kBM + row_local;
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    x[g][v] = __ldcg(src + v * kBM);
+            }
+#pragma unroll
+            for (int g = 0; g < 3; ++g) {
+                const bool keep = cc0 + g <= c_last;  // a select, not a product: partials may hold NaN
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    sum[4 * v] += keep ? x[g][v].x : 0.0f;
+                    sum[4 * v + 1] += keep ? x[g][v].y : 0.0f;
+                    sum[4 * v + 2] += keep ? x[g][v].z : 0.0f;
+                    sum[4 * v + 3] += keep ? x[g][v].w : 0.0f;
+                }
+            }
+        }
+        uint32_t bits[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            bits[e] = __float_as_uint(sum[e]);
+        if (p.vec_ok && j0 + 32 <= p.rows_b)
+            store_row32_vec(p, base_off + j0, bits);
+        else
+            store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), bits);
+    }
+}
+
 // MC = true: the kernel runs in clusters of two CTAs on vertically adjacent tiles
 // (same B-role tile); each CTA loads half of the B-role tile and multicasts it
 // to both, so the pair reads that tile from L2 once.  Slot reuse then needs
@@ -399,6 +498,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         bool ok = true;
         bool issued = false;
+        // Stage (slot s_, k-stage k_) in: wait until the slot has landed, then
+        // tcgen05.cp its scale chunks into the slot's own TMEM scale region.
+        auto stage_in = [&](int s_, uint32_t ph_, int k_) -> bool {
+            if (!warp_wait(full_bar(s_), ph_, abort, lim))
+                return false;
+            tc_fence_after();
+            const int nkt_ = min(C::kKtPerStage, p.num_kt - k_ * C::kKtPerStage);
+            const uint32_t sfa_col_ = tmem + C::kSfCol0 + s_ * C::kSfSlotCols;
+            const uint32_t sfb_col_ = sfa_col_ + C::kSfaCols;
+            const uint32_t sfa_src = sSFA + s_ * C::kSfaBytes;
+            const uint32_t sfb_src = sSFB + s_ * C::kSfbBytes;
+#pragma unroll
+            for (int t = 0; t < C::kKtPerStage; ++t) {
+                if (t < nkt_) {
+                    if (elect_one())
+                        tc_cp_32x128b_warpx4(sfa_col_ + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
+#pragma unroll
+                    for (int c = 0; c < C::kChunksB; ++c) {
+                        const uint64_t d = sdesc_sf_chunk(sfb_src + (c * C::kKtPerStage + t) * kSfChunk);
+                        if (elect_one())
+                            tc_cp_32x128b_warpx4(sfb_col_ + 4 * (t * C::kChunksB + c), d);
+                    }
+                }
+            }
+            issued = true;
+            return true;
+        };
         WorkIter wi;
         wi.init(p, first_unit, unit_step);
         Work w;
@@ -417,32 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ks0 = w.ks0;
             const int ks1 = w.ks1;
             for (int ks = ks0; ks < ks1; ++ks) {
-                if (!warp_wait(full_bar(st), ph, abort, lim)) {
+                if (!stage_in(st, ph, ks)) {
                     if (lane == 0) record_timeout(p, abort);
                     ok = false;
                     break;
                 }
-                tc_fence_after();
                 const int nkt = min(C::kKtPerStage, p.num_kt - ks * C::kKtPerStage);
-                // Scales: shared memory -> this slot's TMEM scale region (in issue order
-                // with the MMAs below).
                 const uint32_t sfa_col = tmem + C::kSfCol0 + st * C::kSfSlotCols;
                 const uint32_t sfb_col = sfa_col + C::kSfaCols;
-                const uint32_t sfa_src = sSFA + st * C::kSfaBytes;
-                const uint32_t sfb_src = sSFB + st * C::kSfbBytes;
-#pragma unroll
-                for (int t = 0; t < C::kKtPerStage; ++t) {
-                    if (t < nkt) {
-                        if (elect_one())
-                            tc_cp_32x128b_warpx4(sfa_col + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
-#pragma unroll
-                        for (int c = 0; c < C::kChunksB; ++c) {
-                            const uint64_t d = sdesc_sf_chunk(sfb_src + (c * C::kKtPerStage + t) * kSfChunk);
-                            if (elect_one())
-                                tc_cp_32x128b_warpx4(sfb_col + 4 * (t * C::kChunksB + c), d);
-                        }
-                    }
-                }
                 const uint64_t adesc = sdesc_kmajor_sw128(sA + st * C::kABytes);
                 const uint64_t bdesc = sdesc_kmajor_sw128(sB + st * C::kBBytes);
                 const uint32_t acc0 = (ks > ks0) ? 1u : 0u;
@@ -466,7 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                issued = true;
                 if (elect_one()) {
                     if (MC)
                         tc_commit_multicast(empty_bar(st), 0x3);
@@ -521,9 +628,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[kChunks][32];
             if (has_cols) {
                 const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + h * kCols;
+                if constexpr (kChunks % 2 == 0) {
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
+                    for (int c = 0; c < kChunks; c += 2)
+                        tmem_ld_32x32b_x64(tbase + c * 32, r[c], r[c + 1]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c)
+                        tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
+                }
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
@@ -535,94 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(acce_bar(acc));
 
             if (w.kind == 1) {
-                // ---- stream-K segment: publish the partial sum; the last CTA to
-                // arrive at this tile adds all segments in k order and stores C.
-                const int cta = first_unit;
-                // Slot layout [h][chunk][4-column group][row]: each warp access is
-                // 32 consecutive 16-byte vectors (rows of one lane quarter).
-                uint4 *const mine =
-                    reinterpret_cast<uint4 *>(p.sk_partials + static_cast<size_t>(2 * cta + w.slot) * kBM * BN);
-                if (has_cols) {
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            mine[((h * kChunks + c) * 8 + v) * kBM + row_local] =
-                                make_uint4(r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2], r[c][4 * v + 3]);
-                    }
-                }
-                __threadfence();
-                epi_bar_sync();
-                const long long t0 = static_cast<long long>(w.tile - p.dp_tiles) * p.kstages;
-                const int c_first = sk_cta_of(p, t0);
-                const int c_last = sk_cta_of(p, t0 + p.kstages - 1);
-                if (threadIdx.x == 64) {
-                    const int old = atomicAdd(p.sk_counters + (w.tile - p.dp_tiles), 1);
-                    const int last = old == c_last - c_first;
-                    if (last)
-                        p.sk_counters[w.tile - p.dp_tiles] = 0;  // ready for the next launch
-                    sk_last = last;
-                }
-                epi_bar_sync();
-                const bool last = sk_last != 0;
-                epi_bar_sync();  // sk_last is read before the next segment may rewrite it
-                if (!last)
-                    continue;
-                __threadfence();
-                // Sum every segment's partial (this CTA's own included, re-read from
-                // its slot) in k order, one 32-column chunk at a time.
-                const int i = tm * kBM + row_local;
-                if (has_cols && i < p.rows_a) {
-                    const long long base_off = static_cast<long long>(i) * p.stride_i;
-#pragma unroll 1
-                    for (int c = 0; c < kChunks; ++c) {
-                        const int j0 = tn * BN + h * kCols + c * 32;
-                        if (j0 >= p.rows_b) break;
-                        float sum[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            sum[e] = 0.0f;
-                        // k order; the loads of two segments are in flight together
-                        for (int cc0 = c_first; cc0 <= c_last; cc0 += 2) {
-                            float4 x[2][8];
-#pragma unroll
-                            for (int g = 0; g < 2; ++g) {
-                                const int cc = cc0 + g;
-                                if (cc <= c_last) {
-                                    const long long beg = p.sk_stages * cc / p.sk_ctas;
-                                    const int slot = (beg / p.kstages == w.tile - p.dp_tiles) ? 0 : 1;
-                                    const float4 *src =
-                                        reinterpret_cast<const float4 *>(
-                                            p.sk_partials + static_cast<size_t>(2 * cc + slot) * kBM * BN) +
-                                        (h * kChunks + c) * 8 * kBM + row_local;
-#pragma unroll
-                                    for (int v = 0; v < 8; ++v)
-                                        x[g][v] = __ldcg(src + v * kBM);
-                                }
-                            }
-#pragma unroll
-                            for (int g = 0; g < 2; ++g) {
-                                if (cc0 + g <= c_last) {
-#pragma unroll
-                                    for (int v = 0; v < 8; ++v) {
-                                        sum[4 * v] += x[g][v].x;
-                                        sum[4 * v + 1] += x[g][v].y;
-                                        sum[4 * v + 2] += x[g][v].z;
-                                        sum[4 * v + 3] += x[g][v].w;
-                                    }
-                                }
-                            }
-                        }
-                        uint32_t bits[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            bits[e] = __float_as_uint(sum[e]);
-                        if (p.vec_ok && j0 + 32 <= p.rows_b)
-                            store_row32_vec(p, base_off + j0, bits);
-                        else
-                            store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), bits);
-                    }
-                }
+                // stream-K segment: publish, and finish the tile if this CTA is last
+                sk_epilogue<BN, kCols, kChunks>(p, w, r, first_unit, 1, 0, tm * kBM, h, row_local, has_cols,
+                                                &sk_last);
                 continue;
             }
 

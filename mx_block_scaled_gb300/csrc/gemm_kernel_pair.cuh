@@ -19,6 +19,9 @@
 //     CTA's `acc_empty`.
 //   * every CTA holds its 128 rows x BN FP32 accumulator in its own TMEM, and its
 //     epilogue stores those rows.
+//   * with stream-K, a pair's segment of a cut tile is published per CTA (each
+//     its 128 rows, its own arrival counter), and the last pair to arrive adds
+//     the segments in k order, each CTA for its own rows.
 // All waits are bounded as in the single-CTA kernel; the CTAs meet at a cluster
 // barrier before TMEM is released.
 #pragma once
@@ -115,7 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_holder;
 
-    const int total_units = p.tiles_m * p.tiles_n * p.splits;  // tiles_m counts 256-row pair tiles
+    // Work of this pair (tiles_m counts 256-row pair tiles): stream-K segments,
+    // then whole tiles (or split-K slabs) round-robin over the clusters.
     const int first_unit = static_cast<int>(cluster_id_x());
     const int unit_step = static_cast<int>(cluster_count_x());
     const uint64_t lim = p.timeout_ns;
@@ -131,11 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t armed = 0, armed_ph = 0;
             bool ok = true;
-            for (int u = first_unit; u < total_units && ok; u += unit_step) {
-                int tm, tn, sp;
-                tile_coords(p, u, tm, tn, sp);
-                const int ks0 = sp * p.kstages_per_split;
-                const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+            WorkIter wi;
+            wi.init(p, first_unit, unit_step);
+            Work w;
+            while (ok && wi.next(p, w)) {
+                const int tm = w.tm, tn = w.tn;
+                const int ks0 = w.ks0, ks1 = w.ks1;
                 const int rb_a = 2 * tm + static_cast<int>(rank);      // own 128-row block of the A role
                 const bool has_sfa = rb_a < nrb_a;
                 const bool peer_has_sfa = 2 * tm + 1 < nrb_a;
@@ -188,11 +193,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         bool ok = true;
         bool issued = false;
-        for (int u = first_unit; u < total_units && ok; u += unit_step, ++it) {
-            int tm, tn, sp;
-            tile_coords(p, u, tm, tn, sp);
-            (void)tm;
-            (void)tn;
+        // Stage (slot s_, k-stage k_) in: wait until both CTAs' halves have
+        // landed, then copy each CTA's scale chunks into its own TMEM.
+        auto stage_in = [&](int s_, uint32_t ph_, int k_) -> bool {
+            if (!warp_wait_cluster(full_bar(s_), ph_, abort, lim))
+                return false;
+            tc_fence_after();
+            const int nkt_ = min(C::kKtPerStage, p.num_kt - k_ * C::kKtPerStage);
+            const uint32_t sfa_col_ = tmem + C::kSfCol0 + s_ * C::kSfSlotCols;
+            const uint32_t sfb_col_ = sfa_col_ + C::kSfaCols;
+            const uint32_t sfa_src = sSFA + s_ * C::kSfaBytes;
+            const uint32_t sfb_src = sSFB + s_ * C::kSfbBytes;
+#pragma unroll
+            for (int t = 0; t < C::kKtPerStage; ++t) {
+                if (t < nkt_) {
+                    if (elect_one())
+                        tc_cp_pair_32x128b_warpx4(sfa_col_ + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
+#pragma unroll
+                    for (int c = 0; c < C::kChunksB; ++c) {
+                        const uint64_t d = sdesc_sf_chunk(sfb_src + (c * C::kKtPerStage + t) * kSfChunk);
+                        if (elect_one())
+                            tc_cp_pair_32x128b_warpx4(sfb_col_ + 4 * (t * C::kChunksB + c), d);
+                    }
+                }
+            }
+            issued = true;
+            return true;
+        };
+        WorkIter wi;
+        wi.init(p, first_unit, unit_step);
+        Work w;
+        for (; ok && wi.next(p, w); ++it) {
             const int acc = it % C::kAccStages;
             const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
             if (!warp_wait_cluster(acce_bar(acc), acc_par ^ 1u, abort, lim)) {
@@ -202,33 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem + acc * BN;
-            const int ks0 = sp * p.kstages_per_split;
-            const int ks1 = min(p.kstages, ks0 + p.kstages_per_split);
+            const int ks0 = w.ks0, ks1 = w.ks1;
             for (int ks = ks0; ks < ks1; ++ks) {
-                if (!warp_wait_cluster(full_bar(st), ph, abort, lim)) {
+                if (!stage_in(st, ph, ks)) {
                     if (lane == 0) record_timeout(p, abort);
                     ok = false;
                     break;
                 }
-                tc_fence_after();
                 const int nkt = min(C::kKtPerStage, p.num_kt - ks * C::kKtPerStage);
                 const uint32_t sfa_col = tmem + C::kSfCol0 + st * C::kSfSlotCols;
                 const uint32_t sfb_col = sfa_col + C::kSfaCols;
-                const uint32_t sfa_src = sSFA + st * C::kSfaBytes;
-                const uint32_t sfb_src = sSFB + st * C::kSfbBytes;
-#pragma unroll
-                for (int t = 0; t < C::kKtPerStage; ++t) {
-                    if (t < nkt) {
-                        if (elect_one())
-                            tc_cp_pair_32x128b_warpx4(sfa_col + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
-#pragma unroll
-                        for (int c = 0; c < C::kChunksB; ++c) {
-                            const uint64_t d = sdesc_sf_chunk(sfb_src + (c * C::kKtPerStage + t) * kSfChunk);
-                            if (elect_one())
-                                tc_cp_pair_32x128b_warpx4(sfb_col + 4 * (t * C::kChunksB + c), d);
-                        }
-                    }
-                }
                 const uint64_t adesc = sdesc_kmajor_sw128(sA + st * C::kABytes);
                 const uint64_t bdesc = sdesc_kmajor_sw128(sB + st * C::kBBytes);
                 const uint32_t acc0 = (ks > ks0) ? 1u : 0u;
@@ -250,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                issued = true;
                 if (elect_one())
                     tc_commit_pair(empty_bar(st), 0x3);
                 __syncwarp();
@@ -276,10 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = (warp - 2) >> 2;
         constexpr int kCols = BN / 2;
         constexpr int kChunks = kCols / 32;
+        __shared__ int sk_last;
         int it = 0;
-        for (int u = first_unit; u < total_units; u += unit_step, ++it) {
-            int tm, tn, sp;
-            tile_coords(p, u, tm, tn, sp);
+        WorkIter wi;
+        wi.init(p, first_unit, unit_step);
+        Work w;
+        for (; wi.next(p, w); ++it) {
+            const int tm = w.tm, tn = w.tn;
             const int acc = it % C::kAccStages;
             const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
             if (!warp_wait_cluster(accf_bar(acc), acc_par, abort, lim)) {
@@ -289,9 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             uint32_t r[kChunks][32];
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + h * kCols;
+            if constexpr (kChunks % 2 == 0) {
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-                tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
+                for (int c = 0; c < kChunks; c += 2)
+                    tmem_ld_32x32b_x64(tbase + c * 32, r[c], r[c + 1]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
+            }
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
@@ -301,10 +323,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(map_to_cta(acce_bar(acc), 0));
 
-            const int i = tm * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
+            const int row0 = (2 * tm + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
+            if (w.kind == 1) {
+                // stream-K segment: publish, and finish the tile if this pair is last
+                sk_epilogue<BN, kCols, kChunks>(p, w, r, first_unit, 2, static_cast<int>(rank), row0, h,
+                                                q * 32 + lane, true, &sk_last);
+                continue;
+            }
+            const int i = row0 + q * 32 + lane;
             if (i < p.rows_a) {
-                const long long base_off =
-                    static_cast<long long>(sp) * p.split_stride + static_cast<long long>(i) * p.stride_i;
+                const long long base_off = (w.kind == 2 ? static_cast<long long>(w.slot) * p.split_stride : 0ll) +
+                                           static_cast<long long>(i) * p.stride_i;
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
                     const int j0 = tn * BN + h * kCols + c * 32;

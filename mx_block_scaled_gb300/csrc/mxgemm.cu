@@ -212,7 +212,8 @@ struct mxgemm_plan {
     int num_sms;
     int dp_tiles;      // stream-K: tiles computed whole (first in raster order)
     int sk_tiles;      // stream-K: tiles whose k-stages are spread over sk_ctas CTAs
-    int sk_ctas;       // 0: no stream-K
+    int sk_ctas;       // 0: no stream-K (counts clusters in pair mode)
+    int sk_halves;     // 128-row shares per tile (2 in pair mode): counters and slots per tile / unit
     int device;        // the device current when the plan was created; runs must use it
     size_t off_sfa, off_sfb, off_part, off_cnt, off_skp, ws_bytes;
     // TMA descriptor cache (re-encoded when an operand pointer changes)
@@ -298,8 +299,10 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         return MXGEMM_ERR_ARG;
     const uint32_t known = MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_NOSWAP |
                            MXGEMM_PLAN_FORCE_SWAP | MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE |
-                           MXGEMM_PLAN_FORCE_MC | MXGEMM_PLAN_STREAMK | (0xFFu << MXGEMM_PLAN_SPLITK_SHIFT);
+                           MXGEMM_PLAN_FORCE_MC | MXGEMM_PLAN_STREAMK | MXGEMM_PLAN_NO_STREAMK |
+                           (0xFFu << MXGEMM_PLAN_SPLITK_SHIFT);
     if ((flags & ~known) != 0 || ((flags & MXGEMM_PLAN_FORCE_SWAP) && (flags & MXGEMM_PLAN_FORCE_NOSWAP)) ||
+        ((flags & MXGEMM_PLAN_STREAMK) && (flags & MXGEMM_PLAN_NO_STREAMK)) ||
         ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)) ||
         __builtin_popcount(flags & (MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE | MXGEMM_PLAN_FORCE_MC)) > 1)
         return MXGEMM_ERR_ARG;
@@ -341,7 +344,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     // modes, and swapped decode shapes stay on single-CTA tiles.
     int mode = 0;
     if (fmt == MXGEMM_FMT_MXFP8_E4M3 && !swap && rows_a >= 128 && rows_b >= 256 &&
-        !(flags & (MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_STREAMK)) && ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0)
+        !(flags & MXGEMM_PLAN_FORCE_BN128) && ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0)
         mode = 2;
     if (flags & MXGEMM_PLAN_FORCE_MC) mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 2;
@@ -355,45 +358,8 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     p->tiles_n = static_cast<int>(ceil_div(rows_b, bn));
     p->kstages = static_cast<int>(fmt == MXGEMM_FMT_MXFP4_E2M1 ? ceil_div(K, 256) : K / 128);
 
-    // Work decomposition.  Default: whole tiles, plus uniform split-K with a
-    // separate reduce when the tiles alone cannot fill half the GPU.  With
-    // MXGEMM_PLAN_STREAMK (single-CTA tiles only): whole tiles in full waves over
-    // the SMs, and -- when the last wave would leave SMs idle -- the k-stages of
-    // the remaining tiles spread evenly over all SMs, fixed up in the kernel.
-    const int64_t tiles = static_cast<int64_t>(p->tiles_m) * p->tiles_n;
-    int splits = static_cast<int>((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu);
-    p->dp_tiles = static_cast<int>(tiles);
-    p->sk_tiles = 0;
-    p->sk_ctas = 0;
-    if (mode == 0 && splits == 0 && (flags & MXGEMM_PLAN_STREAMK)) {
-        const int64_t G = p->num_sms;
-        const int64_t waves = ceil_div(tiles, G);
-        const double dp_eff = static_cast<double>(tiles) / static_cast<double>(waves * G);
-        if (dp_eff < 0.95) {
-            const int64_t dp = (tiles / G) * G;
-            const int64_t sk_stages = (tiles - dp) * p->kstages;
-            const int64_t min_seg = 4;  // k-stages per stream-K CTA, at least
-            p->dp_tiles = static_cast<int>(dp);
-            p->sk_tiles = static_cast<int>(tiles - dp);
-            p->sk_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(G, sk_stages / min_seg)));
-        }
-        splits = 1;
-    }
-    if (splits == 0) {
-        splits = 1;
-        const int64_t slots = mode != 0 ? p->num_sms / 2 : p->num_sms;  // concurrent work units
-        if (tiles * 2 <= slots) {
-            const int64_t by_sms = slots / tiles;
-            const int64_t by_k = std::max<int64_t>(1, p->kstages / 4);
-            splits = static_cast<int>(std::min<int64_t>(std::min(by_sms, by_k), 32));
-        }
-    }
-    splits = std::max(1, std::min(splits, p->kstages));
-    p->kstages_per_split = static_cast<int>(ceil_div(p->kstages, splits));
-    p->splits = static_cast<int>(ceil_div(p->kstages, p->kstages_per_split));
-    p->group_m = 8;
-    const int64_t units = p->sk_ctas > 0 ? std::max<int64_t>(p->dp_tiles > 0 ? p->num_sms : 0, p->sk_ctas)
-                                         : tiles * p->splits;
+    // Concurrent work units: SMs, or co-resident clusters of two.
+    int64_t slots = p->num_sms;
     if (mode != 0) {
         int max_clusters = 0;
         if (mode == 1)
@@ -406,10 +372,67 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
             delete p;
             return MXGEMM_ERR_CUDA;
         }
-        p->grid = static_cast<int>(std::min<int64_t>(units, max_clusters));  // clusters of 2 CTAs
-    } else {
-        p->grid = static_cast<int>(std::min<int64_t>(units, p->num_sms));
+        slots = max_clusters;
     }
+
+    // Work decomposition.  Default: whole tiles, plus uniform split-K with a
+    // separate reduce when the tiles alone cannot fill half the GPU.  Stream-K
+    // (single-CTA or pair tiles): whole tiles in full waves over the work slots,
+    // and the k-stages of the remaining tiles spread over the slots, fixed up in
+    // the kernel -- by default for long k-loops with a poor last wave, always
+    // (when the last wave is under 95% full) with MXGEMM_PLAN_STREAMK, never with
+    // MXGEMM_PLAN_NO_STREAMK.
+    const int64_t tiles = static_cast<int64_t>(p->tiles_m) * p->tiles_n;
+    int splits = static_cast<int>((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu);
+    p->dp_tiles = static_cast<int>(tiles);
+    p->sk_tiles = 0;
+    p->sk_ctas = 0;
+    p->sk_halves = mode == 2 ? 2 : 1;
+    if (mode != 1 && splits == 0) {
+        const int64_t G = slots;
+        const int64_t waves = ceil_div(tiles, G);
+        const double dp_eff = static_cast<double>(tiles) / static_cast<double>(waves * G);
+        // Default: only long k-loops (>= 96 k-stages per tile), whose fixup hides
+        // behind a whole tile, and only when the last wave is under 90% full --
+        // measured: +10-18% at K = 25600, a loss at K <= 8192.
+        const bool want = (flags & MXGEMM_PLAN_STREAMK)
+                              ? dp_eff < 0.95
+                              : (!(flags & MXGEMM_PLAN_NO_STREAMK) && tiles * 2 > slots && p->kstages >= 96 &&
+                                 dp_eff < 0.90);
+        if (want) {
+            const int64_t dp = (tiles / G) * G;
+            const int64_t sk_stages = (tiles - dp) * p->kstages;
+            const int64_t min_seg = 4;  // k-stages per stream-K unit, at least
+            // Long k-loops spread the cut tiles' stages over every slot.  Short
+            // ones cut each tile in at most two segments: the last to arrive then
+            // adds two partial sums, which takes less than the whole tile it
+            // overlaps (three or more took longer and stalled the next tile).
+            const int64_t units = p->kstages >= 96 ? std::min<int64_t>(G, sk_stages / min_seg)
+                                                   : std::min<int64_t>(G, 2 * (tiles - dp));
+            p->dp_tiles = static_cast<int>(dp);
+            p->sk_tiles = static_cast<int>(tiles - dp);
+            p->sk_ctas = static_cast<int>(std::max<int64_t>(1, std::min(units, sk_stages / min_seg)));
+        }
+        if (flags & MXGEMM_PLAN_STREAMK)
+            splits = 1;
+    }
+    if (splits == 0 && p->sk_ctas > 0)
+        splits = 1;
+    if (splits == 0) {
+        splits = 1;
+        if (tiles * 2 <= slots) {
+            const int64_t by_sms = slots / tiles;
+            const int64_t by_k = std::max<int64_t>(1, p->kstages / 4);
+            splits = static_cast<int>(std::min<int64_t>(std::min(by_sms, by_k), 32));
+        }
+    }
+    splits = std::max(1, std::min(splits, p->kstages));
+    p->kstages_per_split = static_cast<int>(ceil_div(p->kstages, splits));
+    p->splits = static_cast<int>(ceil_div(p->kstages, p->kstages_per_split));
+    p->group_m = 8;
+    const int64_t units = p->sk_ctas > 0 ? std::max<int64_t>(p->dp_tiles > 0 ? slots : 0, p->sk_ctas)
+                                         : tiles * p->splits;
+    p->grid = static_cast<int>(std::min<int64_t>(units, slots));  // CTAs, or clusters of 2 CTAs
 
     size_t off = 0;
     p->off_sfa = off;
@@ -422,9 +445,9 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     p->off_cnt = off;
     p->off_skp = off;
     if (p->sk_ctas > 0) {
-        off = align256(off + static_cast<size_t>(p->sk_tiles) * sizeof(int));
+        off = align256(off + static_cast<size_t>(p->sk_tiles) * p->sk_halves * sizeof(int));
         p->off_skp = off;
-        off = align256(off + static_cast<size_t>(2) * p->sk_ctas * 128 * bn * sizeof(float));
+        off = align256(off + static_cast<size_t>(2) * p->sk_ctas * p->sk_halves * 128 * bn * sizeof(float));
     }
     p->ws_bytes = off;
     *plan = p;
@@ -589,7 +612,8 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     p.sk_counters = reinterpret_cast<int *>(ws + plan->off_cnt);
     p.sk_partials = reinterpret_cast<float *>(ws + plan->off_skp);
     if (plan->sk_ctas > 0 &&
-        cudaMemsetAsync(ws + plan->off_cnt, 0, static_cast<size_t>(plan->sk_tiles) * sizeof(int), s) != cudaSuccess)
+        cudaMemsetAsync(ws + plan->off_cnt, 0, static_cast<size_t>(plan->sk_tiles) * plan->sk_halves * sizeof(int),
+                        s) != cudaSuccess)
         return MXGEMM_ERR_CUDA;
     const bool split = plan->splits > 1;
     const int osize = split ? 4 : (plan->out == MXGEMM_OUT_BF16 ? 2 : 4);

@@ -63,6 +63,7 @@ def test_status_strings(lib):
     (16, 16, 128, 1, 9, 0, -1),   # unknown output type
     (16, 16, 128, 1, 2, 1 << 20, -1),  # unknown flag
     (16, 16, 128, 1, 2, (1 << 2) | (1 << 3), -1),  # contradictory flags
+    (16, 16, 128, 1, 2, (1 << 7) | (1 << 16), -1),  # stream-K forced on and off
 ])
 def test_plan_create_validates_before_touching_the_device(lib, M, N, K, fmt, out, flags, expect):
     st, h = lib.mxgemm_plan_create(M, N, K, fmt, out, flags)

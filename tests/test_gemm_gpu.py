@@ -184,22 +184,27 @@ SK = 1 << 7  # stream-K plan flag
 
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+@pytest.mark.parametrize("mode", [SINGLE, PAIR])
 @pytest.mark.parametrize("M,N,K", [(1024, 1536, 4096), (2560, 2304, 1024), (300, 520, 1152), (8, 8192, 2048)])
-def test_stream_k_exact(oracle_mod, fmt, M, N, K):
-    """Tiles whose k-stages are spread over several CTAs (stream-K, fixed up in the
-    kernel) give the exact result, as does the default decomposition."""
+def test_stream_k_exact(oracle_mod, fmt, mode, M, N, K):
+    """Tiles whose k-stages are spread over several CTAs or CTA pairs (stream-K,
+    fixed up in the kernel) give the exact result, as does the default
+    decomposition."""
+    if mode == PAIR and min(M, N) < 128:
+        pytest.skip("cluster modes are for shapes with at least 128 rows on each side")
     rng = np.random.default_rng(M + 7 * N + K)
     A, SA = small_int_codes(rng, M, K, fmt)
     B, SB = small_int_codes(rng, N, K, fmt)
     ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
-    C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, flags=SK, return_plan=True)
+    C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, flags=SK | mode, return_plan=True)
+    assert ("mode=pair" in desc) == (mode == PAIR), desc
     assert "streamk=" in desc and "/0 " not in desc.split("streamk=")[1][:12], desc
     assert (C == ref).all(), desc
     C2, desc2 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16, return_plan=True)
     import torch
     expect = torch.from_numpy(ref.astype(np.float32)).bfloat16().double().numpy()
     assert (C2 == expect).all(), desc2
-    C3 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16, flags=SK)  # stream-K, BF16 out
+    C3 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16, flags=SK | mode)  # stream-K, BF16 out
     assert (C3 == expect).all(), desc
 
 
