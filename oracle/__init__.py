@@ -10,6 +10,7 @@ from .mxref import (  # noqa: F401
     build,
     decode_table,
     gemm,
+    grouped_gemm,
     num_threads,
     quantize,
     IN_F32,

@@ -125,3 +125,33 @@ def quantize(fmt: int, x, in_dtype: int = IN_F32):
     if rc != 0:
         raise ValueError("mxref_quantize rejected its arguments")
     return codes, scales
+
+
+def grouped_gemm(fmt: int, offsets, A, SA, B, SB, N: int, K: int, rows=None, with_abs: bool = True,
+                 nthreads: int = 0):
+    """Reference grouped GEMM (mixture-of-experts layout): group e owns rows
+    [offsets[e], offsets[e+1]) of A (and of C) and weight rows [e*N, (e+1)*N) of B;
+    C[r, :] = A[r] * B_e^T for every row r of group e.  Written as one call of the
+    pinned per-group reference :func:`gemm` per group (its plain definition).
+
+    ``offsets``: G+1 non-decreasing row offsets.  ``rows`` (optional): which rows
+    of C to compute.  Returns ``(C, S)`` over those rows (all rows by default);
+    rows outside every group stay 0.
+    """
+    off = [int(v) for v in np.asarray(offsets).reshape(-1)]
+    T = A.shape[0]
+    rsel = np.arange(T, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    C = np.zeros((rsel.size, N), dtype=np.float64)
+    S = np.zeros((rsel.size, N), dtype=np.float64) if with_abs else None
+    for e in range(len(off) - 1):
+        lo, hi = off[e], off[e + 1]
+        pick = np.nonzero((rsel >= lo) & (rsel < hi))[0]
+        if pick.size == 0:
+            continue
+        Be, SBe = B[e * N:(e + 1) * N], SB[e * N:(e + 1) * N]
+        Ce, Se = gemm(fmt, A[lo:hi], SA[lo:hi], Be, SBe, K, rows=rsel[pick] - lo, with_abs=with_abs,
+                      nthreads=nthreads)
+        C[pick] = Ce
+        if with_abs:
+            S[pick] = Se
+    return C, S
