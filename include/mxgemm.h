@@ -260,6 +260,69 @@ MXGEMM_API int mxgemm_run_noalloc(mxgemm_plan_t plan, const void *A, const uint8
                                   const void *B, const uint8_t *SB, void *C,
                                   uint32_t run_flags, void *stream);
 
+/*
+ * Grouped (mixture-of-experts) MX GEMM.  G groups ("experts"); group e owns the
+ * token rows [offsets[e], offsets[e+1]) of A and of C and the weight rows
+ * [e*N, (e+1)*N) of B:
+ *     C[r, n] = sum_j 2^(SA[r,j]-127) * 2^(SB[e*N+n,j]-127) * sum_{t<32} a[r,32j+t] * b[e*N+n,32j+t]
+ * for every row r of group e, i.e. one MX NT GEMM per group.  The FlyDSL page
+ * (English digest, "Performance numbers need their baselines") times grouped
+ * GEMMs with uniform groups, varied projection dimensions and uneven expert
+ * loads; the AI-compiler daily of 2026-10-22 (item 1) names persistent expert
+ * scheduling.  Here one persistent kernel walks the tiles of all groups; each
+ * CTA reads the offsets from device memory, so group sizes may be produced on
+ * the GPU (by a router) without a host round trip.
+ */
+typedef struct mxgemm_grouped_plan *mxgemm_grouped_plan_t;
+
+/*
+ * Plan a grouped GEMM for `groups` groups (1..512), `rows` token rows in total
+ * (the row count of A and C: T), N weight rows per group (a multiple of 128,
+ * so that every group's weight scales start on a 128-row scale tile) and K
+ * (a multiple of 128).  fmt / out as for mxgemm_plan_create; flags: any of
+ * MXGEMM_PLAN_FORCE_{SWAP,NOSWAP,BN128,BN256} (others: MXGEMM_ERR_ARG).  By
+ * default the weights fill the 128-row MMA dimension (swap-AB) when the
+ * expected tokens per group, rows / groups, are at most 64.  Host memory only.
+ * Errors: MXGEMM_ERR_ARG, MXGEMM_ERR_SHAPE, MXGEMM_ERR_UNSUPPORTED (sizes past
+ * the kernel's 32-bit indices), MXGEMM_ERR_ARCH.
+ */
+MXGEMM_API int mxgemm_grouped_plan_create(mxgemm_grouped_plan_t *plan, int64_t groups, int64_t rows, int64_t N,
+                                          int64_t K, int fmt, int out, uint32_t flags);
+
+/* Free a grouped plan (NULL is accepted). */
+MXGEMM_API int mxgemm_grouped_plan_destroy(mxgemm_grouped_plan_t plan);
+
+/* Device workspace bytes of mxgemm_grouped_run (0 for NULL): the tokens'
+ * per-group tile-layout scales and the weights' tile-layout scales. */
+MXGEMM_API size_t mxgemm_grouped_workspace_bytes(mxgemm_grouped_plan_t plan);
+
+/* One-line description of the grouped plan's choices. */
+MXGEMM_API int mxgemm_grouped_plan_describe(mxgemm_grouped_plan_t plan, char *buf, size_t len);
+
+/*
+ * Run the grouped GEMM on `stream`.
+ *   group_offsets: device, G + 1 int64 row offsets, non-decreasing, in
+ *       [0, rows]; 8-byte aligned.  Read on the device by every launch.
+ *       Rows of C outside every group are not written.  Offsets that break
+ *       these rules give unspecified results but no out-of-range access: each
+ *       group's rows are clamped to [0, rows] before use.
+ *   A, SA: rows x K codes (K or K/2 bytes per row) and rows x K/32 row-major
+ *       scales (laid out per group inside the call).
+ *   B, SB: G*N x K codes (group e's weight in rows [e*N, (e+1)*N)) and G*N x
+ *       K/32 row-major scales -- or, with MXGEMM_RUN_SB_PRELAYOUT, the tile
+ *       layout of mxgemm_relayout_scales over all G*N rows (a weight's scales
+ *       need laying out once).
+ *   C: rows x N, row-major, element type per the plan.
+ * All device pointers but group_offsets 16-byte aligned.  Launches: the
+ * per-group token-scale relayout, the weight-scale relayout (unless
+ * pre-laid-out) and the persistent grouped GEMM kernel.
+ * Errors: MXGEMM_ERR_ARG (NULL, unknown run flag, a plan of another device),
+ * MXGEMM_ERR_ALIGN, MXGEMM_ERR_WORKSPACE, MXGEMM_ERR_CUDA.
+ */
+MXGEMM_API int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *group_offsets, const void *A,
+                                  const uint8_t *SA, const void *B, const uint8_t *SB, void *C, void *workspace,
+                                  size_t ws_bytes, uint32_t run_flags, void *stream);
+
 /* Static, human-readable name of a status code. */
 MXGEMM_API const char *mxgemm_status_str(int status);
 

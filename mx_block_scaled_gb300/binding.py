@@ -62,6 +62,12 @@ SIGNATURES = [
     ("mxgemm_run_noalloc", ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_uint32, _P]),
     ("mxgemm_device_status", ctypes.c_int, [_P, ctypes.c_int]),
     ("mxgemm_selftest_stall", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    ("mxgemm_grouped_plan_create", ctypes.c_int,
+     [ctypes.POINTER(ctypes.c_void_p), _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32]),
+    ("mxgemm_grouped_plan_destroy", ctypes.c_int, [_P]),
+    ("mxgemm_grouped_workspace_bytes", ctypes.c_size_t, [_P]),
+    ("mxgemm_grouped_plan_describe", ctypes.c_int, [_P, ctypes.c_char_p, ctypes.c_size_t]),
+    ("mxgemm_grouped_run", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     ("mxgemm_status_str", ctypes.c_char_p, [ctypes.c_int]),
     ("mxgemm_version", ctypes.c_int, []),
 ]
@@ -144,6 +150,33 @@ def mxgemm_run_noalloc(plan, A_ptr: int, SA_ptr: int, B_ptr: int, SB_ptr: int, C
 MXGEMM_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
+def mxgemm_grouped_plan_create(groups: int, rows: int, N: int, K: int, fmt: int, out: int, flags: int = 0):
+    """Return (status, grouped_plan_handle)."""
+    h = ctypes.c_void_p()
+    st = _lib.mxgemm_grouped_plan_create(ctypes.byref(h), groups, rows, N, K, fmt, out, flags)
+    return st, h
+
+
+def mxgemm_grouped_plan_destroy(plan) -> int:
+    return _lib.mxgemm_grouped_plan_destroy(plan)
+
+
+def mxgemm_grouped_workspace_bytes(plan) -> int:
+    return _lib.mxgemm_grouped_workspace_bytes(plan)
+
+
+def mxgemm_grouped_plan_describe(plan) -> str:
+    buf = ctypes.create_string_buffer(512)
+    _check(_lib.mxgemm_grouped_plan_describe(plan, buf, len(buf)), "mxgemm_grouped_plan_describe")
+    return buf.value.decode()
+
+
+def mxgemm_grouped_run(plan, offsets_ptr: int, A_ptr: int, SA_ptr: int, B_ptr: int, SB_ptr: int, C_ptr: int,
+                       ws_ptr: int, ws_bytes: int, run_flags: int, stream: int) -> int:
+    return _lib.mxgemm_grouped_run(plan, offsets_ptr, A_ptr, SA_ptr, B_ptr, SB_ptr, C_ptr, ws_ptr, ws_bytes,
+                                   run_flags, stream)
+
+
 def mxgemm_device_status(stream: int, reset: bool = True) -> int:
     return _lib.mxgemm_device_status(stream, 1 if reset else 0)
 
@@ -202,6 +235,43 @@ class Plan:
         h = getattr(self, "handle", None)
         if h is not None and h.value:
             mxgemm_plan_destroy(h)
+            self.handle = None
+
+
+class GroupedPlan:
+    """Owns a grouped-GEMM plan handle and its device workspace (a torch uint8 tensor)."""
+
+    def __init__(self, groups: int, rows: int, N: int, K: int, fmt: int, out: int, flags: int = 0, device=None):
+        import torch
+        self.groups, self.rows, self.N, self.K, self.fmt, self.out = groups, rows, N, K, fmt, out
+        st, h = mxgemm_grouped_plan_create(groups, rows, N, K, fmt, out, flags)
+        _check(st, "mxgemm_grouped_plan_create")
+        self.handle = h
+        self.ws_bytes = mxgemm_grouped_workspace_bytes(h)
+        self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8,
+                                     device=device or torch.device("cuda"))
+
+    def describe(self) -> str:
+        return mxgemm_grouped_plan_describe(self.handle)
+
+    def run(self, offsets, A, SA, B, SB, C=None, run_flags: int = 0, stream=None):
+        """C = grouped A * B_e^T.  ``offsets``: CUDA int64 tensor of groups + 1 row offsets."""
+        import torch
+        if C is None:
+            C = torch.empty((self.rows, self.N), dtype=torch.bfloat16 if self.out == MXGEMM_OUT_BF16
+                            else torch.float32, device=A.device)
+        if offsets.dtype != torch.int64 or not offsets.is_cuda or offsets.numel() != self.groups + 1:
+            raise ValueError("offsets must be a CUDA int64 tensor of groups + 1 entries")
+        st = mxgemm_grouped_run(self.handle, offsets.data_ptr(), A.data_ptr(), SA.data_ptr(), B.data_ptr(),
+                                SB.data_ptr(), C.data_ptr(), self.workspace.data_ptr(), self.ws_bytes, run_flags,
+                                _stream_handle(stream))
+        _check(st, "mxgemm_grouped_run")
+        return C
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            mxgemm_grouped_plan_destroy(h)
             self.handle = None
 
 

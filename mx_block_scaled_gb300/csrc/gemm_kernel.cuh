@@ -79,7 +79,105 @@ struct GemmParams {
     long long sk_stages;      // (tiles - dp_tiles) * kstages
     int *sk_counters;         // one arrival counter per stream-K tile and 128-row share, zero at launch
     float *sk_partials;       // two 128 x BN FP32 slots per stream-K CTA (per CTA of a pair)
+    // Grouped (mixture-of-experts) GEMM, single-CTA kernel only: group e owns the
+    // token rows [off[e], off[e+1]) of A and C and the weight rows
+    // [e*group_n, (e+1)*group_n) of B.  Offsets are read on the device and
+    // sanitised (clamped to [0, rows_total], end >= start) before use.
+    int grouped;              // 0: plain GEMM
+    int groups;               // G <= kMaxGroups
+    int tok_b;                // 1: the tokens are the B role (swap-AB), 0: the A role
+    int group_n;              // weight rows per group, a multiple of 128
+    int rows_total;           // T: rows of A and C
+    int tok_sf_cap;           // 128-row blocks in the tokens' tile-layout scale region
+    const long long *group_offsets;  // G + 1 row offsets (device)
 };
+
+constexpr int kMaxGroups = 512;
+
+// Per-CTA table of the groups, built once at kernel start from the offsets.
+struct GroupTable {
+    int tile_start[kMaxGroups + 1];  // first global tile of each group (prefix sum)
+    int tok_rb[kMaxGroups + 1];      // first 128-row block of each group's token scales
+    int row0[kMaxGroups];            // sanitised first token row
+    int rows[kMaxGroups];            // sanitised token row count
+};
+
+// One warp scans the groups: sanitise each group's rows from the offsets, count
+// its tiles (token tiles of tok_tile rows x w_tiles weight tiles) and its
+// 128-row scale blocks, and write the exclusive prefix sums; entry G of
+// tile_start / tok_rb holds the totals.  Sanitising: a group starts at its
+// offset clamped to [0, T] but not before the end of any earlier group, and
+// ends at the next offset clamped to [start, T].  For valid (non-decreasing,
+// in-range) offsets this is the identity; for any others the groups stay
+// disjoint inside [0, T], so the totals stay within what the plan validated.
+// The GEMM and the grouped scale relayout both use it, so they agree on where
+// each group's scales live whatever the offsets hold.
+static __device__ __noinline__ void group_scan(const long long *offsets, int G, long long T, int tok_tile,
+                                               int w_tiles, int lane, int *tile_start, int *tok_rb, int *row0,
+                                               int *rows)
+{
+    int carry_t = 0, carry_b = 0;
+    long long carry_end = 0;  // largest end of the groups already scanned
+    for (int base = 0; base < G; base += 32) {
+        const int e = base + lane;
+        long long s = 0, end = 0;
+        if (e < G) {
+            s = min(max(offsets[e], 0ll), T);
+            end = min(max(offsets[e + 1], s), T);
+        }
+        // exclusive prefix max of the ends (within the warp, then the carry)
+        long long prev = end;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long x = __shfl_up_sync(0xFFFFFFFFu, prev, o);
+            if (lane >= o) prev = max(prev, x);
+        }
+        long long before = __shfl_up_sync(0xFFFFFFFFu, prev, 1);
+        if (lane == 0) before = 0;
+        before = max(before, carry_end);
+        carry_end = max(carry_end, __shfl_sync(0xFFFFFFFFu, prev, 31));
+        int tiles = 0, blocks = 0, s0 = 0, m = 0;
+        if (e < G) {
+            const long long s2 = max(s, before);
+            const long long end2 = max(end, s2);
+            s0 = static_cast<int>(s2);
+            m = static_cast<int>(end2 - s2);
+            tiles = ((m + tok_tile - 1) / tok_tile) * w_tiles;
+            blocks = (m + 127) / 128;
+        }
+        int ti = tiles, bi = blocks;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xFFFFFFFFu, ti, o);
+            const int y = __shfl_up_sync(0xFFFFFFFFu, bi, o);
+            if (lane >= o) {
+                ti += x;
+                bi += y;
+            }
+        }
+        if (e < G) {
+            if (tile_start) tile_start[e] = carry_t + ti - tiles;
+            tok_rb[e] = carry_b + bi - blocks;
+            row0[e] = s0;
+            rows[e] = m;
+        }
+        carry_t += __shfl_sync(0xFFFFFFFFu, ti, 31);
+        carry_b += __shfl_sync(0xFFFFFFFFu, bi, 31);
+    }
+    if (lane == 0) {
+        if (tile_start) tile_start[G] = carry_t;
+        tok_rb[G] = carry_b;
+    }
+}
+
+template <int BN>
+__device__ __forceinline__ void build_group_table(const GemmParams &p, GroupTable &g, int lane)
+{
+    const int tok_tile = p.tok_b ? BN : kBM;
+    const int w_tiles = p.tok_b ? p.group_n / kBM : (p.group_n + BN - 1) / BN;
+    group_scan(p.group_offsets, p.groups, p.rows_total, tok_tile, w_tiles, lane, g.tile_start, g.tok_rb, g.row0,
+               g.rows);
+}
 
 template <bool FP4, int BN>
 struct Cfg {
@@ -136,6 +234,7 @@ __device__ __forceinline__ void tile_xy(const GemmParams &p, int t, int &tm, int
 // One piece of work: k-stages [ks0, ks1) of tile (tm, tn).
 struct Work {
     int tile, tm, tn, ks0, ks1;
+    int grp;    // grouped GEMM: the group of the tile (tm, tn are group-local)
     int kind;   // 0: the whole K of the tile; 1: stream-K segment; 2: split-K slab
     int slot;   // kind 1: partial-sum slot (0: first segment of this CTA, 1: last)
                 // kind 2: split index
@@ -144,21 +243,48 @@ struct Work {
 // The sequence of Work of one CTA; producer, MMA and epilogue warps each walk
 // an identical copy.
 struct WorkIter {
-    int u, step, units, spl;
+    int u, step, units, spl, tok_tile;
     long long pos, end, begin;
+    const GroupTable *gt;
 
-    __device__ void init(const GemmParams &p, int cta, int ctas)
+    // gt: the group table (grouped GEMM only); tok_tile: token rows per tile.
+    __device__ void init(const GemmParams &p, int cta, int ctas, const GroupTable *g = nullptr, int tok_tile_ = 0)
     {
         u = cta;
         step = ctas;
+        gt = g;
+        tok_tile = tok_tile_;
         spl = p.sk_ctas > 0 ? 1 : p.splits;
         units = p.sk_ctas > 0 ? p.dp_tiles : p.tiles_m * p.tiles_n * p.splits;
+        if (p.grouped)
+            units = g->tile_start[p.groups];
         pos = end = 0;
         if (p.sk_ctas > 0 && cta < p.sk_ctas) {
             pos = p.sk_stages * cta / p.sk_ctas;
             end = p.sk_stages * (cta + 1) / p.sk_ctas;
         }
         begin = pos;
+    }
+
+    // Grouped: the group holding global tile t (the last group whose first tile
+    // is <= t, so empty groups are skipped), then the tile inside the group --
+    // token tiles fastest, so neighbouring CTAs share a weight tile in L2.
+    __device__ void group_xy(const GemmParams &p, int t, Work &w) const
+    {
+        int lo = 0, hi = p.groups - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gt->tile_start[mid] <= t)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int local = t - gt->tile_start[lo];
+        const int ntok = max(1, (gt->rows[lo] + tok_tile - 1) / tok_tile);
+        const int tok_i = local % ntok, w_i = local / ntok;
+        w.grp = lo;
+        w.tm = p.tok_b ? w_i : tok_i;
+        w.tn = p.tok_b ? tok_i : w_i;
     }
 
     // Stream-K segments come first, so that the fixup of a cut tile (run by the
@@ -171,6 +297,7 @@ struct WorkIter {
             w.ks1 = static_cast<int>(min(static_cast<long long>(p.kstages), w.ks0 + (end - pos)));
             w.kind = (w.ks0 == 0 && w.ks1 == p.kstages) ? 0 : 1;
             w.slot = pos == begin ? 0 : 1;
+            w.grp = 0;
             tile_xy(p, w.tile, w.tm, w.tn);
             pos += w.ks1 - w.ks0;
             return true;
@@ -181,13 +308,77 @@ struct WorkIter {
             w.ks0 = w.slot * p.kstages_per_split;
             w.ks1 = min(p.kstages, w.ks0 + p.kstages_per_split);
             w.kind = spl > 1 ? 2 : 0;
-            tile_xy(p, w.tile, w.tm, w.tn);
+            w.grp = 0;
+            if (p.grouped)
+                group_xy(p, w.tile, w);
+            else
+                tile_xy(p, w.tile, w.tm, w.tn);
             u += step;
             return true;
         }
         return false;
     }
 };
+
+// Where one tile's operands, scales and outputs live.  Epilogue indices: A-role
+// row i = tm*128 + r and B-role row j = tn*BN + c are stored at
+// out_base + i*stride_i + j*stride_j when i < lim_i and j < lim_j.
+struct TileGeom {
+    int a_row, b_row;      // TMA row coordinates of the A- and B-role tiles
+    int sfa_rb, sfb_rb0;   // 128-row block of the A-role scales / first of the B role
+    bool has_sfa;
+    int nchunk_b;          // B-role scale chunks to load
+    int sub_off;           // B-role 32-row group inside its scale chunk (BN < 128)
+    int lim_i, lim_j;
+    long long out_base;
+};
+
+template <int BN, int kChunksB>
+__device__ __forceinline__ void tile_geom(const GemmParams &p, const GroupTable *g, const Work &w, TileGeom &t)
+{
+    // The MMA reads the B-role scales of this tile from TMEM column sub_off of
+    // the chunk (32-row group).  It must be even: an odd column (a BN = 32 tile
+    // starting 32 or 96 rows into its chunk) faulted with a misaligned address,
+    // so plans use BN = 32 only when the whole B role is one tile (sub_off = 0).
+    t.sub_off = ((w.tn * BN) % 128) / 32;
+    if (!p.grouped) {
+        const int nrb_b = (p.rows_b + 127) / 128;
+        t.a_row = w.tm * kBM;
+        t.b_row = w.tn * BN;
+        t.sfa_rb = w.tm;
+        t.has_sfa = w.tm < (p.rows_a + 127) / 128;
+        t.sfb_rb0 = (w.tn * BN) / 128;
+        t.nchunk_b = min(kChunksB, nrb_b - t.sfb_rb0);
+        t.lim_i = p.rows_a;
+        t.lim_j = p.rows_b;
+        t.out_base = 0;
+        return;
+    }
+    const int e = w.grp;
+    const int s0 = g->row0[e], m = g->rows[e];
+    const int wrow = e * p.group_n;             // first weight row of the group
+    const int wblocks = (p.groups * p.group_n) / 128;
+    t.out_base = static_cast<long long>(s0) * p.group_n;
+    if (!p.tok_b) {                              // tokens: A role, 128-row tiles
+        t.a_row = s0 + w.tm * kBM;
+        t.sfa_rb = g->tok_rb[e] + w.tm;
+        t.has_sfa = t.sfa_rb >= 0 && t.sfa_rb < p.tok_sf_cap;
+        t.b_row = wrow + w.tn * BN;
+        t.sfb_rb0 = (wrow + w.tn * BN) / 128;
+        t.nchunk_b = max(0, min(kChunksB, wblocks - t.sfb_rb0));
+        t.lim_i = m;
+        t.lim_j = p.group_n;
+    } else {                                     // tokens: B role, BN-row tiles
+        t.a_row = wrow + w.tm * kBM;
+        t.sfa_rb = wrow / 128 + w.tm;
+        t.has_sfa = t.sfa_rb < wblocks;
+        t.b_row = s0 + w.tn * BN;
+        t.sfb_rb0 = g->tok_rb[e] + (w.tn * BN) / 128;
+        t.nchunk_b = t.sfb_rb0 < 0 ? 0 : max(0, min(kChunksB, p.tok_sf_cap - t.sfb_rb0));
+        t.lim_i = p.group_n;
+        t.lim_j = m;
+    }
+}
 
 // The stream-K CTA whose stage range contains stream-K stage x.
 __device__ __forceinline__ int sk_cta_of(const GemmParams &p, long long x)
@@ -243,6 +434,66 @@ __device__ __forceinline__ void store_row32_masked(const GemmParams &p, long lon
     }
 }
 
+// The sum of a cut tile's segments, run by its last arriving CTA (cold code,
+// kept out of line so that its registers do not count against the hot loops).
+template <int BN, int kCols, int kChunks>
+__device__ __noinline__ void sk_fixup(const GemmParams &p, int tile, int tn, int c_first, int c_last, int halves,
+                                      int half, int row0, int h, int row_local, bool has_cols)
+{
+    constexpr size_t kSlot = static_cast<size_t>(kBM) * BN;
+    const int i = row0 + row_local;
+    if (!has_cols || i >= p.rows_a)
+        return;
+    const long long base_off = static_cast<long long>(i) * p.stride_i;
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c) {
+        const int j0 = tn * BN + h * kCols + c * 32;
+        if (j0 >= p.rows_b) break;
+        float sum[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            sum[e] = 0.0f;
+        // k order; the 32 columns of three segments are loaded at once (the sum
+        // is L2-latency bound: keep many loads in flight).  Past the last
+        // segment the loads repeat it and the adds are skipped.
+#pragma unroll 1
+        for (int cc0 = c_first; cc0 <= c_last; cc0 += 3) {
+            float4 x[3][8];
+#pragma unroll
+            for (int g = 0; g < 3; ++g) {
+                const int cc = min(cc0 + g, c_last);
+                const long long beg = p.sk_stages * cc / p.sk_ctas;
+                const int slot = (beg / p.kstages == tile - p.dp_tiles) ? 0 : 1;
+                const float4 *src = reinterpret_cast<const float4 *>(
+                                        p.sk_partials + static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
+                                    (h * kChunks + c) * 8 * kBM + row_local;
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    x[g][v] = __ldcg(src + v * kBM);
+            }
+#pragma unroll
+            for (int g = 0; g < 3; ++g) {
+                const bool keep = cc0 + g <= c_last;  // a select, not a product: partials may hold NaN
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    sum[4 * v] += keep ? x[g][v].x : 0.0f;
+                    sum[4 * v + 1] += keep ? x[g][v].y : 0.0f;
+                    sum[4 * v + 2] += keep ? x[g][v].z : 0.0f;
+                    sum[4 * v + 3] += keep ? x[g][v].w : 0.0f;
+                }
+            }
+        }
+        uint32_t bits[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            bits[e] = __float_as_uint(sum[e]);
+        if (p.vec_ok && j0 + 32 <= p.rows_b)
+            store_row32_vec(p, base_off + j0, bits);
+        else
+            store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), bits);
+    }
+}
+
 // Stream-K epilogue of one CTA's 128-row share of a tile cut between CTAs (or
 // CTA pairs): publish this segment's FP32 partial sum; if it is the last
 // segment of the tile to arrive, add every segment's partial in k order
@@ -289,57 +540,7 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
     if (!last)
         return;
     __threadfence();
-    const int i = row0 + row_local;
-    if (!has_cols || i >= p.rows_a)
-        return;
-    const long long base_off = static_cast<long long>(i) * p.stride_i;
-#pragma unroll 1
-    for (int c = 0; c < kChunks; ++c) {
-        const int j0 = w.tn * BN + h * kCols + c * 32;
-        if (j0 >= p.rows_b) break;
-        float sum[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-            sum[e] = 0.0f;
-        // k order; the 32 columns of three segments are loaded at once (the sum
-        // is L2-latency bound: keep many loads in flight).  Past the last
-        // segment the loads repeat it and the adds are skipped.
-#pragma unroll 1
-        for (int cc0 = c_first; cc0 <= c_last; cc0 += 3) {
-            float4 x[3][8];
-#pragma unroll
-            for (int g = 0; g < 3; ++g) {
-                const int cc = min(cc0 + g, c_last);
-                const long long beg = p.sk_stages * cc / p.sk_ctas;
-                const int slot = (beg / p.kstages == w.tile - p.dp_tiles) ? 0 : 1;
-                const float4 *src = reinterpret_cast<const float4 *>(
-                                        p.sk_partials + static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
-                                    (h * kChunks + c) * 8 * kBM + row_local;
-#pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    x[g][v] = __ldcg(src + v * kBM);
-            }
-#pragma unroll
-            for (int g = 0; g < 3; ++g) {
-                const bool keep = cc0 + g <= c_last;  // a select, not a product: partials may hold NaN
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    sum[4 * v] += keep ? x[g][v].x : 0.0f;
-                    sum[4 * v + 1] += keep ? x[g][v].y : 0.0f;
-                    sum[4 * v + 2] += keep ? x[g][v].z : 0.0f;
-                    sum[4 * v + 3] += keep ? x[g][v].w : 0.0f;
-                }
-            }
-        }
-        uint32_t bits[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-            bits[e] = __float_as_uint(sum[e]);
-        if (p.vec_ok && j0 + 32 <= p.rows_b)
-            store_row32_vec(p, base_off + j0, bits);
-        else
-            store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), bits);
-    }
+    sk_fixup<BN, kCols, kChunks>(p, w.tile, w.tn, c_first, c_last, halves, half, row0, h, row_local, has_cols);
 }
 
 // MC = true: the kernel runs in clusters of two CTAs on vertically adjacent tiles
@@ -358,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_holder;
     __shared__ int abort_flag;
+    __shared__ GroupTable gtab;  // grouped GEMM only
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -401,6 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_addr(&tmem_base_holder), C::kTmemCols);
         tmem_relinquish();
     }
+    if (p.grouped && warp == 2)
+        build_group_table<BN>(p, gtab, lane);
     tc_fence_before();
     __syncthreads();
     if (MC)
@@ -411,6 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Work: output tiles (x splits, or stream-K segments); with MC, vertical tile
     // pairs, CTA r of the cluster taking A-role tile 2*tm + r.
     const int mc_rank = MC ? static_cast<int>(cluster_ctarank()) : 0;
+    const GroupTable *const gt = p.grouped ? &gtab : nullptr;
+    const int tok_tile = p.tok_b ? BN : kBM;
     const int first_unit = MC ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
     const int unit_step = MC ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
     const uint64_t lim = p.timeout_ns;
@@ -430,20 +636,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t armed = 0;      // bit s: slot s armed at least once
             uint32_t armed_ph = 0;   // bit s: parity of slot s's last arm
             bool ok = true;
-            const int nrb_b = (p.rows_b + 127) / 128;
             WorkIter wi;
-            wi.init(p, first_unit, unit_step);
+            wi.init(p, first_unit, unit_step, gt, tok_tile);
             Work w;
             while (ok && wi.next(p, w)) {
-                int tm = w.tm;
-                const int tn = w.tn;
-                if (MC) tm = 2 * tm + mc_rank;
-                const bool has_sfa = tm < (p.rows_a + 127) / 128;  // false for an MC CTA past the last row
+                if (MC) w.tm = 2 * w.tm + mc_rank;
+                TileGeom g;
+                tile_geom<BN, C::kChunksB>(p, gt, w, g);
+                const bool has_sfa = g.has_sfa;  // false for an MC CTA past the last row
                 const int ks0 = w.ks0;
                 const int ks1 = w.ks1;
                 // B-role scale chunks present for this tile (row blocks past the end are skipped)
-                const int rb_b0 = (tn * BN) / 128;
-                const int nchunk_b = min(C::kChunksB, nrb_b - rb_b0);
+                const int rb_b0 = g.sfb_rb0;
+                const int nchunk_b = g.nchunk_b;
                 for (int ks = ks0; ks < ks1; ++ks) {
                     const bool freed = MC ? warp_wait_cluster(empty_bar(st), ph ^ 1u, abort, lim)
                                           : warp_wait(empty_bar(st), ph ^ 1u, abort, lim);
@@ -458,15 +663,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         C::kABytes + C::kBBytes + nkt * kSfChunk * ((has_sfa ? 1 : 0) + nchunk_b);
                     if (elect_one()) {
                         mbar_arrive_expect_tx(full_bar(st), bytes);
-                        tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, tm * kBM, pol_a);
+                        tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, g.a_row, pol_a);
                         if (MC)  // own half of the B-role tile, to both CTAs
                             tma_load_2d_multicast(sB + st * C::kBBytes + mc_rank * (C::kBBytes / 2), &map_b,
-                                                  full_bar(st), ks * kRowBytes, tn * BN + mc_rank * (BN / 2), 0x3);
+                                                  full_bar(st), ks * kRowBytes, g.b_row + mc_rank * (BN / 2), 0x3);
                         else
-                            tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, tn * BN, pol_b);
+                            tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, g.b_row, pol_b);
                         if (has_sfa)
                             bulk_load(sSFA + st * C::kSfaBytes,
-                                      p.sfa + (static_cast<size_t>(tm) * p.num_kt + kt0) * kSfChunk,
+                                      p.sfa + (static_cast<size_t>(g.sfa_rb) * p.num_kt + kt0) * kSfChunk,
                                       nkt * kSfChunk, full_bar(st));
                         for (int c = 0; c < nchunk_b; ++c)
                             bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
@@ -526,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         WorkIter wi;
-        wi.init(p, first_unit, unit_step);
+        wi.init(p, first_unit, unit_step, gt, tok_tile);
         Work w;
         for (; ok && wi.next(p, w); ++it) {
             const int tn = w.tn;
@@ -609,12 +814,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_local = q * 32 + lane;
         int it = 0;
         WorkIter wi;
-        wi.init(p, first_unit, unit_step);
+        wi.init(p, first_unit, unit_step, gt, tok_tile);
         Work w;
         for (; wi.next(p, w); ++it) {
-            int tm = w.tm;
+            if (MC) w.tm = 2 * w.tm + mc_rank;
+            const int tm = w.tm;
             const int tn = w.tn;
-            if (MC) tm = 2 * tm + mc_rank;
             const int acc = it % C::kAccStages;
             const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
             bool ok = true;
@@ -654,18 +859,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
 
+            // Output limits and origin (computed after the release: fewer live registers)
+            TileGeom g;
+            tile_geom<BN, C::kChunksB>(p, gt, w, g);
             const int i = tm * kBM + row_local;  // A-role row owned by this thread
-            if (has_cols && i < p.rows_a) {
-                const long long base_off = (w.kind == 2 ? static_cast<long long>(w.slot) * p.split_stride : 0ll) +
+            if (has_cols && i < g.lim_i) {
+                const long long base_off = g.out_base +
+                                           (w.kind == 2 ? static_cast<long long>(w.slot) * p.split_stride : 0ll) +
                                            static_cast<long long>(i) * p.stride_i;
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
                     const int j0 = tn * BN + h * kCols + c * 32;
-                    if (j0 >= p.rows_b) break;
-                    if (p.vec_ok && j0 + 32 <= p.rows_b)
+                    if (j0 >= g.lim_j) break;
+                    if (p.vec_ok && j0 + 32 <= g.lim_j)
                         store_row32_vec(p, base_off + j0, r[c]);
                     else
-                        store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), r[c]);
+                        store_row32_masked(p, base_off, j0, min(32, g.lim_j - j0), r[c]);
                 }
             }
         }

@@ -153,6 +153,63 @@ cudaError_t launch_relayout(const RelayoutJob &a, const RelayoutJob *b, cudaStre
     return cudaGetLastError();
 }
 
+// ------------------------------------------------- grouped scale relayout --
+// Token scales of a grouped GEMM: the rows of group e (start and count
+// sanitised exactly as the GEMM does it) go to their own run of 128-row tile
+// blocks starting at block tok_rb[e], the last block padded with code 127, so
+// that every 128-row token tile finds its scales in one 512-byte chunk per
+// K-tile.  One block per (tile block, up to 8 K-tiles); blocks past the used
+// (or available) ones exit at once.
+__global__ void __launch_bounds__(256)
+    grouped_relayout_kernel(const uint8_t *src, const long long *offsets, int groups, int total_rows, int num_kt,
+                            int blocks_x, int cap_blocks, uint8_t *dst)
+{
+    __shared__ int tok_rb[mxg::kMaxGroups + 1];
+    __shared__ int row0[mxg::kMaxGroups];
+    __shared__ int rows[mxg::kMaxGroups];
+    __shared__ uint32_t tile[128][kRelayoutKt + 1];
+    if (threadIdx.x < 32)
+        mxg::group_scan(offsets, groups, total_rows, 128, 1, static_cast<int>(threadIdx.x), nullptr, tok_rb, row0,
+                        rows);
+    __syncthreads();
+    const int rb = static_cast<int>(blockIdx.x) / blocks_x;
+    const int kt0 = (static_cast<int>(blockIdx.x) % blocks_x) * kRelayoutKt;
+    if (rb >= tok_rb[groups] || rb >= cap_blocks)
+        return;  // block-uniform
+    int lo = 0, hi = groups - 1;  // the last group whose first block is <= rb (skips empty groups)
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tok_rb[mid] <= rb)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int lb = rb - tok_rb[lo];
+    const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src);  // num_kt words per row
+    uint32_t v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = threadIdx.x + 256 * i;
+        const int r = idx / kRelayoutKt, w = idx % kRelayoutKt;
+        const int local = lb * 128 + r, kt = kt0 + w;
+        v[i] = 0x7F7F7F7Fu;
+        if (local < rows[lo] && kt < num_kt)
+            v[i] = __ldg(s32 + static_cast<size_t>(row0[lo] + local) * num_kt + kt);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = threadIdx.x + 256 * i;
+        tile[idx / kRelayoutKt][idx % kRelayoutKt] = v[i];
+    }
+    __syncthreads();
+    const int w = threadIdx.x >> 5, pr = threadIdx.x & 31;
+    const int kt = kt0 + w;
+    if (kt < num_kt) {
+        uint4 o = make_uint4(tile[pr][w], tile[32 + pr][w], tile[64 + pr][w], tile[96 + pr][w]);
+        reinterpret_cast<uint4 *>(dst + (static_cast<size_t>(rb) * num_kt + kt) * 512)[pr] = o;
+    }
+}
+
 // -------------------------------------------------------- split-K reduce --
 // C[e] = sum_s part[s][e], summed in split order (deterministic), then stored
 // as FP32 or rounded to BF16.
@@ -224,6 +281,21 @@ struct mxgemm_plan {
     CUtensorMap map_a, map_b, map_sfa, map_sfb;
 };
 
+struct mxgemm_grouped_plan {
+    int64_t G, T, N, K;  // groups, token rows (of A and C), weight rows per group, K
+    int fmt, out;
+    int swap;            // 1: tokens are the MMA N (B) role, weights fill the 128-row M role
+    int bn;              // MMA N tile
+    int kstages;
+    int num_sms;
+    int device;
+    int tok_sf_cap;      // 128-row blocks of the tokens' tile-layout scale region
+    size_t off_tok_sf, off_w_sf, ws_bytes;
+    const void *map_ptr_tok = nullptr;
+    const void *map_ptr_w = nullptr;
+    CUtensorMap map_tok, map_w;
+};
+
 namespace {
 
 int encode_operand_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t row_bytes, int box_rows)
@@ -252,6 +324,9 @@ int encode_sf_map(CUtensorMap *map, const void *ptr, size_t bytes, int kt_per_st
     return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
 }
 
+// N tile for a B role of rows_b rows.  BN = 32 only when the whole B role fits
+// in one tile, so a 32-row tile always starts on its scale chunk's first 32 rows
+// (see tile_geom: the B scale-factor TMEM column must be even).
 int pick_bn(int64_t rows_b)
 {
     if (rows_b <= 32) return 32;
@@ -719,6 +794,185 @@ int mxgemm_run_noalloc(mxgemm_plan_t plan, const void *A, const uint8_t *SA, con
     }
     return run_impl(plan, A, SA, B, SB, C, scratch, MXGEMM_NOALLOC_SCRATCH_BYTES, run_flags, stream, 0,
                     2000000000ull);
+}
+
+// ------------------------------------------------------------ grouped --
+int mxgemm_grouped_plan_create(mxgemm_grouped_plan_t *plan, int64_t groups, int64_t rows, int64_t N, int64_t K,
+                               int fmt, int out, uint32_t flags)
+{
+    if (!plan)
+        return MXGEMM_ERR_ARG;
+    *plan = nullptr;
+    if ((fmt != MXGEMM_FMT_MXFP8_E4M3 && fmt != MXGEMM_FMT_MXFP4_E2M1) ||
+        (out != MXGEMM_OUT_F32 && out != MXGEMM_OUT_BF16))
+        return MXGEMM_ERR_ARG;
+    const uint32_t known =
+        MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_NOSWAP | MXGEMM_PLAN_FORCE_SWAP;
+    if ((flags & ~known) != 0 || ((flags & MXGEMM_PLAN_FORCE_SWAP) && (flags & MXGEMM_PLAN_FORCE_NOSWAP)) ||
+        ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)))
+        return MXGEMM_ERR_ARG;
+    if (groups < 1 || groups > mxg::kMaxGroups || rows < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0)
+        return MXGEMM_ERR_SHAPE;
+    if (rows > (1ll << 30) || groups * N > (1ll << 30) || K > (1ll << 30) ||
+        (ceil_div(rows, 32) + groups) * ceil_div(N, 32) >= (1ll << 31))
+        return MXGEMM_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    const int st = device_info(&dev);
+    if (st != MXGEMM_OK)
+        return st;
+    mxgemm_grouped_plan *p = new (std::nothrow) mxgemm_grouped_plan();
+    if (!p)
+        return MXGEMM_ERR_UNSUPPORTED;
+    p->G = groups;
+    p->T = rows;
+    p->N = N;
+    p->K = K;
+    p->fmt = fmt;
+    p->out = out;
+    p->num_sms = dev->num_sms;
+    cudaGetDevice(&p->device);
+    // Expected tokens per group: few -> the weights fill the 128-row MMA dimension.
+    const int64_t avg = std::max<int64_t>(1, rows / groups);
+    int swap = avg <= 64 ? 1 : 0;
+    if (flags & MXGEMM_PLAN_FORCE_SWAP) swap = 1;
+    if (flags & MXGEMM_PLAN_FORCE_NOSWAP) swap = 0;
+    p->swap = swap;
+    // Token tiles in the B role are at least 64 rows: a B-role tile that starts
+    // 32 rows into its 128-row scale chunk would put the MMA's B scale factors at
+    // an odd TMEM column, which the hardware rejects (misaligned address).
+    int bn = swap ? std::min(std::max(pick_bn(avg), 64), 128) : (N >= 256 ? 256 : 128);
+    if (flags & MXGEMM_PLAN_FORCE_BN128) bn = 128;
+    if (flags & MXGEMM_PLAN_FORCE_BN256) bn = 256;
+    p->bn = bn;
+    p->kstages = static_cast<int>(fmt == MXGEMM_FMT_MXFP4_E2M1 ? ceil_div(K, 256) : K / 128);
+    p->tok_sf_cap = static_cast<int>(ceil_div(rows, 128) + groups);
+    p->off_tok_sf = 0;
+    p->off_w_sf = align256(static_cast<size_t>(p->tok_sf_cap) * 128 * static_cast<size_t>(K / 32));
+    p->ws_bytes = align256(p->off_w_sf + static_cast<size_t>(groups * N) * static_cast<size_t>(K / 32));
+    *plan = p;
+    return MXGEMM_OK;
+}
+
+int mxgemm_grouped_plan_destroy(mxgemm_grouped_plan_t plan)
+{
+    delete plan;
+    return MXGEMM_OK;
+}
+
+size_t mxgemm_grouped_workspace_bytes(mxgemm_grouped_plan_t plan) { return plan ? plan->ws_bytes : 0; }
+
+int mxgemm_grouped_plan_describe(mxgemm_grouped_plan_t plan, char *buf, size_t len)
+{
+    if (!plan || !buf || len == 0)
+        return MXGEMM_ERR_ARG;
+    const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
+    mxg::KernelInfo ki = fp4 ? mxg::gemm_info_fp4(plan->bn) : mxg::gemm_info_fp8(plan->bn);
+    snprintf(buf, len,
+             "grouped fmt=%s out=%s groups=%lld rows=%lld N=%lld K=%lld tile=128x%d swap_ab=%d kstages=%d grid=%d "
+             "stages=%d acc_stages=%d smem=%d",
+             fp4 ? "mxfp4" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32", static_cast<long long>(plan->G),
+             static_cast<long long>(plan->T), static_cast<long long>(plan->N), static_cast<long long>(plan->K),
+             plan->bn, plan->swap, plan->kstages, plan->num_sms, ki.stages, ki.acc_stages, ki.smem_bytes);
+    return MXGEMM_OK;
+}
+
+int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *group_offsets, const void *A, const uint8_t *SA,
+                       const void *B, const uint8_t *SB, void *C, void *workspace, size_t ws_bytes, uint32_t run_flags,
+                       void *stream)
+{
+    if (!plan || !group_offsets || !A || !SA || !B || !SB || !C)
+        return MXGEMM_ERR_ARG;
+    if (run_flags & ~MXGEMM_RUN_SB_PRELAYOUT)
+        return MXGEMM_ERR_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(SA) || !aligned16(SB) ||
+        (reinterpret_cast<uintptr_t>(group_offsets) & 7u) != 0)
+        return MXGEMM_ERR_ALIGN;
+    if (workspace == nullptr || ws_bytes < plan->ws_bytes)
+        return MXGEMM_ERR_WORKSPACE;
+    if (!aligned16(workspace))
+        return MXGEMM_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    int st = device_info(&dev);
+    if (st != MXGEMM_OK)
+        return st;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device)
+        return MXGEMM_ERR_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
+    const int64_t G = plan->G, T = plan->T, N = plan->N, K = plan->K;
+    const int64_t row_bytes = fp4 ? K / 2 : K;
+    const int num_kt = static_cast<int>(K / 128);
+    const long long *offs = reinterpret_cast<const long long *>(group_offsets);
+
+    // (1) token scales -> per-group tile blocks; (2) weight scales -> tile layout
+    uint8_t *tok_sf = ws + plan->off_tok_sf;
+    {
+        const int blocks_x = static_cast<int>(ceil_div(num_kt, kRelayoutKt));
+        grouped_relayout_kernel<<<static_cast<unsigned>(plan->tok_sf_cap) * blocks_x, 256, 0, s>>>(
+            SA, offs, static_cast<int>(G), static_cast<int>(T), num_kt, blocks_x, plan->tok_sf_cap, tok_sf);
+        if (cudaGetLastError() != cudaSuccess)
+            return MXGEMM_ERR_CUDA;
+    }
+    const uint8_t *w_sf = SB;
+    if (!(run_flags & MXGEMM_RUN_SB_PRELAYOUT)) {
+        RelayoutJob j = make_job(SB, G * N, K, ws + plan->off_w_sf);
+        if (launch_relayout(j, nullptr, s) != cudaSuccess)
+            return MXGEMM_ERR_CUDA;
+        w_sf = ws + plan->off_w_sf;
+    }
+
+    // (3) the GEMM: tokens in the A role (128-row tiles) or, swapped, the B role
+    if (plan->map_ptr_tok != A) {
+        if (encode_operand_map(&plan->map_tok, A, T, row_bytes, plan->swap ? plan->bn : 128) != MXGEMM_OK)
+            return MXGEMM_ERR_CUDA;
+        plan->map_ptr_tok = A;
+    }
+    if (plan->map_ptr_w != B) {
+        if (encode_operand_map(&plan->map_w, B, G * N, row_bytes, plan->swap ? 128 : plan->bn) != MXGEMM_OK)
+            return MXGEMM_ERR_CUDA;
+        plan->map_ptr_w = B;
+    }
+    GemmParams p;
+    memset(&p, 0, sizeof p);
+    p.rows_a = static_cast<int>(plan->swap ? G * N : T);
+    p.rows_b = static_cast<int>(plan->swap ? T : G * N);
+    p.num_kt = num_kt;
+    p.kstages = plan->kstages;
+    p.kstages_per_split = plan->kstages;
+    p.tiles_m = 1;
+    p.tiles_n = 1;
+    p.splits = 1;
+    p.group_m = 8;
+    p.out = C;
+    p.out_kind = plan->out == MXGEMM_OUT_BF16 ? mxg::OUT_BF16 : mxg::OUT_F32;
+    const int osize = plan->out == MXGEMM_OUT_BF16 ? 2 : 4;
+    p.stride_i = plan->swap ? 1 : N;
+    p.stride_j = plan->swap ? N : 1;
+    p.vec_ok = (!plan->swap && (N * osize) % 16 == 0 && aligned16(C)) ? 1 : 0;
+    // the weights are streamed when each group has at most two token tiles
+    const int64_t avg = std::max<int64_t>(1, T / G);
+    const bool stream_w = ceil_div(avg, plan->swap ? plan->bn : 128) <= 2;
+    p.stream_a = (plan->swap && stream_w) ? 1 : 0;
+    p.stream_b = (!plan->swap && stream_w) ? 1 : 0;
+    p.sfa = plan->swap ? w_sf : tok_sf;
+    p.sfb = plan->swap ? tok_sf : w_sf;
+    p.timeout_ns = 2000000000ull;
+    p.status = dev->status_ptr;
+    p.grouped = 1;
+    p.groups = static_cast<int>(G);
+    p.tok_b = plan->swap;
+    p.group_n = static_cast<int>(N);
+    p.rows_total = static_cast<int>(T);
+    p.tok_sf_cap = plan->tok_sf_cap;
+    p.group_offsets = offs;
+    const CUtensorMap &ma = plan->swap ? plan->map_w : plan->map_tok;
+    const CUtensorMap &mb = plan->swap ? plan->map_tok : plan->map_w;
+    const cudaError_t e = fp4 ? mxg::launch_gemm_fp4(plan->bn, p, ma, mb, plan->num_sms, s)
+                              : mxg::launch_gemm_fp8(plan->bn, p, ma, mb, plan->num_sms, s);
+    return e == cudaSuccess ? MXGEMM_OK : MXGEMM_ERR_CUDA;
 }
 
 int mxgemm_device_status(void *stream, int reset)

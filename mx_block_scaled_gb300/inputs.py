@@ -224,3 +224,52 @@ def make_operand(name: str, which: str, index: int, rows: int, K: int, fmt: int)
     if w["values"] == "normal_outliers":
         x = with_outlier_blocks(x, rng)
     return quantize_mx(x, fmt)
+
+
+# ---------------------------------------------------------------------------
+# Grouped (mixture-of-experts) workloads.  The FlyDSL page (English digest,
+# "Performance numbers need their baselines") times 24 grouped GEMMs covering
+# uniform groups, projection-dimension changes and uneven expert loads, without
+# listing them; these synthetic cases stand in for those three axes with
+# expert shapes of common MoE layers: 8 experts with (N, K) = (28672, 4096)
+# gate+up and (4096, 14336) down projections, and 64 fine-grained experts with
+# (1536, 2048) / (2048, 768).  Tokens are N(0,1) rows quantised like the dense
+# workloads; group sizes are uniform or drawn from a seeded Zipf-like law.
+# ---------------------------------------------------------------------------
+
+MOE_WORKLOADS = {
+    # name: groups, total token rows, (N, K) per expert, load ("uniform" or "zipf")
+    "moe8_uniform_prefill": dict(groups=8, rows=8192, nks=[(28672, 4096), (4096, 14336)], load="uniform"),
+    "moe64_uneven_prefill": dict(groups=64, rows=8192, nks=[(1536, 2048), (2048, 768)], load="zipf"),
+    "moe64_uneven_decode": dict(groups=64, rows=256, nks=[(1536, 2048), (2048, 768)], load="zipf"),
+    "moe8_uneven_decode": dict(groups=8, rows=64, nks=[(28672, 4096), (4096, 14336)], load="zipf"),
+}
+
+
+def group_sizes(groups: int, rows: int, load: str, seed) -> np.ndarray:
+    """Rows per group summing to `rows`: equal shares, or a Zipf-like draw
+    (weights 1/rank^1.2 over a seeded permutation of the groups; some groups
+    may receive no rows)."""
+    if load == "uniform":
+        base = np.full(groups, rows // groups, dtype=np.int64)
+        base[: rows - base.sum()] += 1
+        return base
+    rng = np.random.default_rng(seed)
+    w = 1.0 / np.arange(1, groups + 1) ** 1.2
+    w = w[rng.permutation(groups)]
+    counts = rng.multinomial(rows, w / w.sum()).astype(np.int64)
+    return counts
+
+
+def group_offsets(sizes) -> np.ndarray:
+    """Offsets [0, s0, s0+s1, ...] (groups + 1 entries, int64)."""
+    return np.concatenate([[0], np.cumsum(np.asarray(sizes, dtype=np.int64))]).astype(np.int64)
+
+
+def moe_cases(name: str):
+    """Yield (fmt_name, nk_index, groups, rows, N, K, sizes) for a grouped workload (both formats)."""
+    w = MOE_WORKLOADS[name]
+    for fmt in ("mxfp8", "mxfp4"):
+        for nki, (n, k) in enumerate(w["nks"]):
+            sizes = group_sizes(w["groups"], w["rows"], w["load"], [len(name), nki, w["groups"]])
+            yield fmt, nki, w["groups"], w["rows"], n, k, sizes

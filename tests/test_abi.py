@@ -112,3 +112,26 @@ def test_oracle_builds_and_is_separate(oracle_mod):
 def test_quantize_validates_before_touching_the_device(lib, fmt, in_dtype, x, rows, K, codes, scales, flags,
                                                         expect):
     assert lib.mxgemm_quantize(fmt, in_dtype, x, rows, K, codes, scales, flags, 0) == expect
+
+
+@pytest.mark.parametrize("groups,rows,N,K,fmt,out,flags,expect", [
+    (0, 64, 128, 128, 1, 2, 0, -2),        # no groups
+    (513, 64, 128, 128, 1, 2, 0, -2),      # more groups than a CTA's table holds
+    (4, 0, 128, 128, 1, 2, 0, -2),         # no rows
+    (4, 64, 100, 128, 1, 2, 0, -2),        # N not a multiple of 128
+    (4, 64, 128, 96, 1, 2, 0, -2),         # K not a multiple of 128
+    (4, 64, 128, 128, 3, 2, 0, -1),        # unknown format
+    (4, 64, 128, 128, 1, 9, 0, -1),        # unknown output type
+    (4, 64, 128, 128, 1, 2, 1 << 4, -1),   # CTA-pair tiles are not offered for grouped GEMMs
+    (4, 64, 128, 128, 1, 2, (1 << 2) | (1 << 3), -1),
+])
+def test_grouped_plan_validates_before_touching_the_device(lib, groups, rows, N, K, fmt, out, flags, expect):
+    st, h = lib.mxgemm_grouped_plan_create(groups, rows, N, K, fmt, out, flags)
+    assert st == expect and not h.value
+
+
+def test_grouped_null_arguments_are_rejected(lib):
+    assert lib._lib.mxgemm_grouped_plan_create(None, 4, 64, 128, 128, 1, 2, 0) == lib.MXGEMM_ERR_ARG
+    assert lib.mxgemm_grouped_run(None, 8, 16, 16, 16, 16, 16, 16, 0, 0, 0) == lib.MXGEMM_ERR_ARG
+    assert lib.mxgemm_grouped_plan_destroy(None) == lib.MXGEMM_OK
+    assert lib.mxgemm_grouped_workspace_bytes(None) == 0
