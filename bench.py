@@ -18,7 +18,8 @@ has no exchange step); value = all ranks' FLOPs / the slowest rank's time.
 --impl reference times the CPU oracle (the only other program computing the
 same result here) on a bounded sample of the same workload.
 --sweep prints one line per shape of the model workloads (not the headline);
---quant-sweep one line per activation shape for the MX quantiser.
+--quant-sweep one line per activation shape for the MX quantiser; --grouped-sweep
+one line per grouped (mixture-of-experts) case.
 """
 from __future__ import annotations
 
@@ -554,6 +555,93 @@ def run_quant_sweep(args):
     return 0
 
 
+def run_grouped_sweep(args):
+    """Per-case time of the grouped (mixture-of-experts) MX GEMM over the grouped
+    workloads: device-side random codes, weight scales laid out once per set,
+    token-scale relayout inside each call; CUDA-graph replay over rotating sets."""
+    import torch
+    from mx_block_scaled_gb300 import binding as mx
+    from mx_block_scaled_gb300.inputs import FMT_BY_NAME, MOE_WORKLOADS, group_offsets, moe_cases
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    hbm_gbs, bf16_tf, _, _ = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    names = args.sweep_workloads.split(",") if args.sweep_workloads else list(MOE_WORKLOADS)
+    for name in names:
+        for fmt_name, nki, G, T, N, K, sizes in moe_cases(name):
+            fmt = FMT_BY_NAME[fmt_name]
+            rb = K if fmt_name == "mxfp8" else K // 2
+            e = 1.0 if fmt_name == "mxfp8" else 0.5
+            active = int((sizes > 0).sum())
+            flops = 2.0 * float(sizes.sum()) * N * K
+            byts = T * K * e + T * K / 32 + active * N * (K * e + K / 32) + T * N * 2
+            set_bytes = T * rb + T * K // 32 + G * N * rb + mx.mxgemm_sf_bytes(G * N, K) + T * N * 2
+            nsets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+            nsets = min(nsets, max(2, int(30e9 // set_bytes)))
+            plan = mx.GroupedPlan(G, T, N, K, fmt, mx.MXGEMM_OUT_BF16, device=dev)
+            g = torch.Generator(device=dev)
+            g.manual_seed(G * 131 + N + K)
+
+            def codes(rows):
+                c = torch.randint(0, 256, (rows, rb), dtype=torch.uint8, device=dev, generator=g)
+                if fmt_name == "mxfp8":
+                    c = torch.where((c & 0x7F) == 0x7F, c & 0xFE, c)
+                return c
+
+            offs = torch.tensor(group_offsets(sizes), dtype=torch.int64, device=dev)
+            sets = []
+            for _ in range(nsets):
+                SB = torch.randint(120, 135, (G * N, K // 32), dtype=torch.uint8, device=dev, generator=g)
+                sets.append((codes(T), torch.randint(120, 135, (T, K // 32), dtype=torch.uint8, device=dev,
+                                                      generator=g),
+                             codes(G * N), mx.relayout_scales(SB, G * N, K),
+                             torch.empty((T, N), dtype=torch.bfloat16, device=dev)))
+                del SB
+
+            def one(i):
+                a, sa, b, sb, c = sets[i % nsets]
+                st = mx.mxgemm_grouped_run(plan.handle, offs.data_ptr(), a.data_ptr(), sa.data_ptr(), b.data_ptr(),
+                                           sb.data_ptr(), c.data_ptr(), plan.workspace.data_ptr(), plan.ws_bytes,
+                                           mx.MXGEMM_RUN_SB_PRELAYOUT, torch.cuda.current_stream().cuda_stream)
+                assert st == 0, mx.mxgemm_status_str(st)
+
+            for i in range(3):
+                one(i)
+            torch.cuda.synchronize()
+            reps = args.sweep_reps
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(reps):
+                    one(i)
+            graph.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) / reps)
+            mx.check_device_status()
+            del graph
+            t = statistics.median(ts) / 1e3
+            peak = mx_peak_tflops(fmt_name, bf16_tf)
+            t_roof = max(flops / (peak * 1e12), byts / (hbm_gbs * 1e9))
+            print(json.dumps({
+                "kernel": "mx_gemm_kernel (grouped)", "workload": name, "format": fmt_name, "groups": G,
+                "rows": T, "N": N, "K": K, "active_groups": active, "max_group": int(sizes.max()),
+                "us": t * 1e6, "tflops": flops / t / 1e12, "gbs": byts / t / 1e9,
+                "frac_tensor": flops / t / 1e12 / peak, "frac_hbm": byts / t / 1e9 / hbm_gbs,
+                "frac_roofline": t_roof / t,
+                "bound": "tensor" if flops / (peak * 1e12) > byts / (hbm_gbs * 1e9) else "hbm",
+                "plan": plan.describe(), "nsets": nsets}), flush=True)
+            del sets, plan
+            torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -572,6 +660,8 @@ def main():
     ap.add_argument("--fmt", default="mxfp8", choices=["mxfp8", "mxfp4"], help="format for --shape")
     ap.add_argument("--quant-sweep", action="store_true",
                     help="time the MX quantiser over the workloads' activation shapes")
+    ap.add_argument("--grouped-sweep", action="store_true",
+                    help="time the grouped (mixture-of-experts) MX GEMM over the grouped workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -579,6 +669,8 @@ def main():
         return run_reference(args)
     if args.quant_sweep:
         return run_quant_sweep(args)
+    if args.grouped_sweep:
+        return run_grouped_sweep(args)
     if args.sweep or args.shape:
         return run_sweep(args)
     return run_ours(args)

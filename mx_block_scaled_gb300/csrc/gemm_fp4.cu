@@ -80,6 +80,14 @@ int mc_max_clusters()
 }
 
 template <int BN>
+cudaError_t launch_grouped(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid, cudaStream_t s)
+{
+    using C = Cfg<true, BN>;
+    mx_gemm_kernel<true, BN, false, true><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
+    return cudaGetLastError();
+}
+
+template <int BN>
 KernelInfo pair_info()
 {
     using C = CfgPair<true, BN>;
@@ -116,6 +124,15 @@ cudaError_t prepare_gemm_fp4()
         if (e != cudaSuccess)
             return e;
     }
+    const void *gr[3] = {(const void *)mx_gemm_kernel<true, 64, false, true>,
+                         (const void *)mx_gemm_kernel<true, 128, false, true>,
+                         (const void *)mx_gemm_kernel<true, 256, false, true>};
+    const int gr_smem[3] = {Cfg<true, 64>::kSmemBytes, Cfg<true, 128>::kSmemBytes, Cfg<true, 256>::kSmemBytes};
+    for (int i = 0; i < 3; ++i) {
+        cudaError_t e = cudaFuncSetAttribute(gr[i], cudaFuncAttributeMaxDynamicSharedMemorySize, gr_smem[i]);
+        if (e != cudaSuccess)
+            return e;
+    }
     return cudaSuccess;
 }
 
@@ -127,6 +144,17 @@ cudaError_t launch_gemm_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, 
     case 64: return launch<64>(p, ma, mb, grid, s);
     case 128: return launch<128>(p, ma, mb, grid, s);
     case 256: return launch<256>(p, ma, mb, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gemm_grouped_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
+                                    int grid, cudaStream_t s)
+{
+    switch (bn) {
+    case 64: return launch_grouped<64>(p, ma, mb, grid, s);
+    case 128: return launch_grouped<128>(p, ma, mb, grid, s);
+    case 256: return launch_grouped<256>(p, ma, mb, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }

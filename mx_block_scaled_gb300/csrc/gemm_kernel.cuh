@@ -256,7 +256,7 @@ struct WorkIter {
         tok_tile = tok_tile_;
         spl = p.sk_ctas > 0 ? 1 : p.splits;
         units = p.sk_ctas > 0 ? p.dp_tiles : p.tiles_m * p.tiles_n * p.splits;
-        if (p.grouped)
+        if (g)
             units = g->tile_start[p.groups];
         pos = end = 0;
         if (p.sk_ctas > 0 && cta < p.sk_ctas) {
@@ -309,7 +309,7 @@ struct WorkIter {
             w.ks1 = min(p.kstages, w.ks0 + p.kstages_per_split);
             w.kind = spl > 1 ? 2 : 0;
             w.grp = 0;
-            if (p.grouped)
+            if (gt)
                 group_xy(p, w.tile, w);
             else
                 tile_xy(p, w.tile, w.tm, w.tn);
@@ -341,7 +341,7 @@ __device__ __forceinline__ void tile_geom(const GemmParams &p, const GroupTable 
     // starting 32 or 96 rows into its chunk) faulted with a misaligned address,
     // so plans use BN = 32 only when the whole B role is one tile (sub_off = 0).
     t.sub_off = ((w.tn * BN) % 128) / 32;
-    if (!p.grouped) {
+    if (g == nullptr) {
         const int nrb_b = (p.rows_b + 127) / 128;
         t.a_row = w.tm * kBM;
         t.b_row = w.tn * BN;
@@ -543,12 +543,15 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
     sk_fixup<BN, kCols, kChunks>(p, w.tile, w.tn, c_first, c_last, halves, half, row0, h, row_local, has_cols);
 }
 
+// GROUPED = true: the grouped (mixture-of-experts) form, tiles of all groups
+// walked through the per-CTA group table (p.grouped must be 1); plain GEMMs
+// use GROUPED = false, so none of its code or shared memory is in them.
 // MC = true: the kernel runs in clusters of two CTAs on vertically adjacent tiles
 // (same B-role tile); each CTA loads half of the B-role tile and multicasts it
 // to both, so the pair reads that tile from L2 once.  Slot reuse then needs
 // both CTAs' MMAs done: `empty` counts two commits (each MMA thread commits to
 // both CTAs' barriers).
-template <bool FP4, int BN, bool MC = false>
+template <bool FP4, int BN, bool MC = false, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b)
@@ -603,8 +606,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_addr(&tmem_base_holder), C::kTmemCols);
         tmem_relinquish();
     }
-    if (p.grouped && warp == 2)
-        build_group_table<BN>(p, gtab, lane);
+    if constexpr (GROUPED) {
+        if (warp == 2)
+            build_group_table<BN>(p, gtab, lane);
+    }
     tc_fence_before();
     __syncthreads();
     if (MC)
@@ -615,7 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Work: output tiles (x splits, or stream-K segments); with MC, vertical tile
     // pairs, CTA r of the cluster taking A-role tile 2*tm + r.
     const int mc_rank = MC ? static_cast<int>(cluster_ctarank()) : 0;
-    const GroupTable *const gt = p.grouped ? &gtab : nullptr;
+    const GroupTable *gt = nullptr;  // grouped kernels only (a constant null pointer otherwise)
+    if constexpr (GROUPED)
+        gt = &gtab;
     const int tok_tile = p.tok_b ? BN : kBM;
     const int first_unit = MC ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
     const int unit_step = MC ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);

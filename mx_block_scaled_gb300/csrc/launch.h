@@ -21,6 +21,13 @@ cudaError_t launch_gemm_fp8(int bn, const GemmParams &p, const CUtensorMap &map_
 cudaError_t launch_gemm_fp4(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
                             int grid, cudaStream_t stream);
 
+// Grouped (mixture-of-experts) form of the single-CTA kernel, bn = 64, 128 or
+// 256 (p.grouped = 1), on `grid` CTAs.
+cudaError_t launch_gemm_grouped_fp8(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                    int grid, cudaStream_t stream);
+cudaError_t launch_gemm_grouped_fp4(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                    int grid, cudaStream_t stream);
+
 // CTA-pair kernel (cluster of 2, cta_group::2), pair tile 256 x bn (bn = 128 or
 // 256), on `clusters` clusters; it also takes 2-D maps of the two tile-layout
 // scale tensors (rows of 256 bytes).  And the largest co-resident cluster count.

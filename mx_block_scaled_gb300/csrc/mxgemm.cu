@@ -970,8 +970,8 @@ int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *group_offsets,
     p.group_offsets = offs;
     const CUtensorMap &ma = plan->swap ? plan->map_w : plan->map_tok;
     const CUtensorMap &mb = plan->swap ? plan->map_tok : plan->map_w;
-    const cudaError_t e = fp4 ? mxg::launch_gemm_fp4(plan->bn, p, ma, mb, plan->num_sms, s)
-                              : mxg::launch_gemm_fp8(plan->bn, p, ma, mb, plan->num_sms, s);
+    const cudaError_t e = fp4 ? mxg::launch_gemm_grouped_fp4(plan->bn, p, ma, mb, plan->num_sms, s)
+                              : mxg::launch_gemm_grouped_fp8(plan->bn, p, ma, mb, plan->num_sms, s);
     return e == cudaSuccess ? MXGEMM_OK : MXGEMM_ERR_CUDA;
 }
 
