@@ -11,6 +11,8 @@ from .mxref import (  # noqa: F401
     decode_table,
     gemm,
     grouped_gemm,
+    bf16_gemm,
+    bf16_to_f64,
     num_threads,
     quantize,
     IN_F32,

@@ -155,3 +155,28 @@ def grouped_gemm(fmt: int, offsets, A, SA, B, SB, N: int, K: int, rows=None, wit
         if with_abs:
             S[pick] = Se
     return C, S
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """BF16 bit patterns (uint16) -> binary64, exactly: a BF16 value is the FP32
+    value whose upper 16 bits are the pattern and whose lower 16 bits are zero."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    with np.errstate(invalid="ignore"):  # NaN patterns widen to NaN
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_gemm(A_bits, B_bits, rows=None, cols=None, with_abs: bool = True):
+    """Reference BF16 NT GEMM: C = A * B^T and S = |A| * |B|^T in binary64 from
+    BF16 operands (the FlyDSL page's BF16 "NT GEMM" set, section "Performance
+    numbers need their baselines").  Every product of two BF16 values is exact
+    in binary64; the sums go through one binary64 matrix product (error far below
+    the FP32-accumulation bound the parity tests allow)."""
+    A = bf16_to_f64(A_bits)
+    B = bf16_to_f64(B_bits)
+    if rows is not None:
+        A = A[np.asarray(rows, dtype=np.int64)]
+    if cols is not None:
+        B = B[np.asarray(cols, dtype=np.int64)]
+    C = A @ B.T
+    S = np.abs(A) @ np.abs(B).T if with_abs else None
+    return C, S
