@@ -642,6 +642,84 @@ def run_grouped_sweep(args):
     return 0
 
 
+def run_bf16_sweep(args):
+    """BF16 NT GEMM (kind::f16 on the same kernels) over the dense workload shapes,
+    with cuBLAS (torch.matmul, BF16 in/out) timed the same way as a comparison."""
+    import torch
+    from mx_block_scaled_gb300 import binding as mx
+    from mx_block_scaled_gb300.inputs import WORKLOADS, workload_cases
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    hbm_gbs, bf16_tf, _, _ = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    names = args.sweep_workloads.split(",") if args.sweep_workloads else list(WORKLOADS)
+    seen = set()
+    shapes = []
+    for name in names:
+        for _, _, _, M, N, K in workload_cases(name):
+            if (M, N, K) not in seen and K % 64 == 0:
+                seen.add((M, N, K))
+                shapes.append((name, M, N, K))
+    for name, M, N, K in shapes:
+        byts = (M + N) * K * 2 + M * N * 2
+        nsets = max(2, math.ceil(2 * l2 / byts) + 1)
+        nsets = min(nsets, max(2, int(30e9 // byts)))
+        g = torch.Generator(device=dev)
+        g.manual_seed(M + N + K)
+        sets = [(torch.randn((M, K), device=dev, generator=g).to(torch.bfloat16),
+                 torch.randn((N, K), device=dev, generator=g).to(torch.bfloat16),
+                 torch.empty((M, N), dtype=torch.bfloat16, device=dev)) for _ in range(nsets)]
+        plan = mx.Plan(M, N, K, mx.MXGEMM_FMT_BF16, mx.MXGEMM_OUT_BF16, device=dev)
+
+        def ours(i):
+            a, b, c = sets[i % nsets]
+            st = mx.mxgemm_run(plan.handle, a.data_ptr(), 0, b.data_ptr(), 0, c.data_ptr(),
+                               plan.workspace.data_ptr(), plan.ws_bytes, 0, torch.cuda.current_stream().cuda_stream)
+            assert st == 0, mx.mxgemm_status_str(st)
+
+        def cublas(i):
+            a, b, c = sets[i % nsets]
+            torch.matmul(a, b.t(), out=c)
+
+        res = {}
+        for tag, fn_ in (("ours", ours), ("cublas", cublas)):
+            for i in range(3):
+                fn_(i)
+            torch.cuda.synchronize()
+            reps = args.sweep_reps
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(reps):
+                    fn_(i)
+            graph.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) / reps)
+            del graph
+            res[tag] = statistics.median(ts) / 1e3
+        mx.check_device_status()
+        flops = 2.0 * M * N * K
+        t_roof = max(flops / (bf16_tf * 1e12), byts / (hbm_gbs * 1e9))
+        print(json.dumps({
+            "kernel": "mx_gemm (bf16)", "workload": name, "M": M, "N": N, "K": K,
+            "us": res["ours"] * 1e6, "tflops": flops / res["ours"] / 1e12,
+            "frac_roofline": t_roof / res["ours"],
+            "cublas_us": res["cublas"] * 1e6, "cublas_tflops": flops / res["cublas"] / 1e12,
+            "cublas_frac_roofline": t_roof / res["cublas"], "speedup_vs_cublas": res["cublas"] / res["ours"],
+            "bound": "tensor" if flops / (bf16_tf * 1e12) > byts / (hbm_gbs * 1e9) else "hbm",
+            "plan": plan.describe(), "nsets": nsets}), flush=True)
+        del sets, plan
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -660,6 +738,8 @@ def main():
     ap.add_argument("--fmt", default="mxfp8", choices=["mxfp8", "mxfp4"], help="format for --shape")
     ap.add_argument("--quant-sweep", action="store_true",
                     help="time the MX quantiser over the workloads' activation shapes")
+    ap.add_argument("--bf16-sweep", action="store_true",
+                    help="time the BF16 NT GEMM (and cuBLAS beside it) over the dense workload shapes")
     ap.add_argument("--grouped-sweep", action="store_true",
                     help="time the grouped (mixture-of-experts) MX GEMM over the grouped workloads")
     args = ap.parse_args()
@@ -671,6 +751,8 @@ def main():
         return run_quant_sweep(args)
     if args.grouped_sweep:
         return run_grouped_sweep(args)
+    if args.bf16_sweep:
+        return run_bf16_sweep(args)
     if args.sweep or args.shape:
         return run_sweep(args)
     return run_ours(args)

@@ -53,7 +53,8 @@ extern "C" {
 /* Element format of A and B (both operands use the same format). */
 typedef enum {
     MXGEMM_FMT_MXFP8_E4M3 = 1, /* one E4M3 code per byte: row = K bytes        */
-    MXGEMM_FMT_MXFP4_E2M1 = 2  /* two E2M1 codes per byte: row = K/2 bytes     */
+    MXGEMM_FMT_MXFP4_E2M1 = 2, /* two E2M1 codes per byte: row = K/2 bytes     */
+    MXGEMM_FMT_BF16 = 3        /* plain BF16, no scales: row = 2K bytes         */
 } mxgemm_format_t;
 
 /* Output element type of C (row-major M x N, leading dimension N). */
@@ -94,6 +95,10 @@ typedef struct mxgemm_plan *mxgemm_plan_t;
 /*
  * Create a plan for C[M,N] = A[M,K] * B[N,K]^T.
  *   fmt:   mxgemm_format_t; out: mxgemm_out_t; flags: MXGEMM_PLAN_* (0 = auto).
+ *   MXGEMM_FMT_BF16 plans the plain BF16 NT GEMM on the same kernels (the
+ *   FlyDSL page's BF16 "NT GEMM" comparison set, section "Performance numbers
+ *   need their baselines"): K a multiple of 64, SA / SB not read (may be NULL),
+ *   no workspace for scales; MXGEMM_PLAN_FORCE_MC -> MXGEMM_ERR_UNSUPPORTED.
  * Validates the shape (M, N >= 1; K >= 128 and K % 128 == 0, per the FlyDSL
  * page's K constraint), checks that the current device is an sm_103 part,
  * chooses the tile shape, operand roles (swap-AB) and split-K, and sizes the

@@ -14,6 +14,7 @@ from .build import LIB_PATH
 
 MXGEMM_FMT_MXFP8_E4M3 = 1
 MXGEMM_FMT_MXFP4_E2M1 = 2
+MXGEMM_FMT_BF16 = 3
 MXGEMM_OUT_F32 = 1
 MXGEMM_OUT_BF16 = 2
 
@@ -226,7 +227,9 @@ class Plan:
         import torch
         if C is None:
             C = torch.empty((self.M, self.N), dtype=self.out_dtype(), device=A.device)
-        st = mxgemm_run(self.handle, A.data_ptr(), SA.data_ptr(), B.data_ptr(), SB.data_ptr(), C.data_ptr(),
+        sa = SA.data_ptr() if SA is not None else 0
+        sb = SB.data_ptr() if SB is not None else 0
+        st = mxgemm_run(self.handle, A.data_ptr(), sa, B.data_ptr(), sb, C.data_ptr(),
                         self.workspace.data_ptr(), self.ws_bytes, run_flags, _stream_handle(stream))
         _check(st, "mxgemm_run")
         return C

@@ -9,8 +9,8 @@ namespace {
 template <int BN>
 cudaError_t launch(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid, cudaStream_t s)
 {
-    using C = Cfg<true, BN>;
-    mx_gemm_kernel<true, BN><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
+    using C = Cfg<K_MXFP4, BN>;
+    mx_gemm_kernel<K_MXFP4, BN><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
     return cudaGetLastError();
 }
 
@@ -34,21 +34,21 @@ template <int BN>
 cudaError_t launch_pair(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &msa,
                         const CUtensorMap &msb, int clusters, cudaStream_t s)
 {
-    auto kern = mx_gemm_pair_kernel<true, BN>;
+    auto kern = mx_gemm_pair_kernel<K_MXFP4, BN>;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<true, BN>::kSmemBytes, s, attr);
+    cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<K_MXFP4, BN>::kSmemBytes, s, attr);
     return cudaLaunchKernelEx(&cfg, kern, p, ma, mb, msa, msb);
 }
 
 template <int BN>
 int pair_max_clusters()
 {
-    auto kern = mx_gemm_pair_kernel<true, BN>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgPair<true, BN>::kSmemBytes) !=
+    auto kern = mx_gemm_pair_kernel<K_MXFP4, BN>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgPair<K_MXFP4, BN>::kSmemBytes) !=
         cudaSuccess)
         return 0;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(1, CfgPair<true, BN>::kSmemBytes, nullptr, attr);
+    cudaLaunchConfig_t cfg = cluster2_config(1, CfgPair<K_MXFP4, BN>::kSmemBytes, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
         return 0;
@@ -58,21 +58,21 @@ int pair_max_clusters()
 template <int BN>
 cudaError_t launch_mc(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int clusters, cudaStream_t s)
 {
-    auto kern = mx_gemm_kernel<true, BN, true>;
+    auto kern = mx_gemm_kernel<K_MXFP4, BN, true>;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(clusters, Cfg<true, BN>::kSmemBytes, s, attr);
+    cudaLaunchConfig_t cfg = cluster2_config(clusters, Cfg<K_MXFP4, BN>::kSmemBytes, s, attr);
     return cudaLaunchKernelEx(&cfg, kern, p, ma, mb);
 }
 
 template <int BN>
 int mc_max_clusters()
 {
-    auto kern = mx_gemm_kernel<true, BN, true>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true, BN>::kSmemBytes) !=
+    auto kern = mx_gemm_kernel<K_MXFP4, BN, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<K_MXFP4, BN>::kSmemBytes) !=
         cudaSuccess)
         return 0;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(1, Cfg<true, BN>::kSmemBytes, nullptr, attr);
+    cudaLaunchConfig_t cfg = cluster2_config(1, Cfg<K_MXFP4, BN>::kSmemBytes, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
         return 0;
@@ -82,22 +82,22 @@ int mc_max_clusters()
 template <int BN>
 cudaError_t launch_grouped(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid, cudaStream_t s)
 {
-    using C = Cfg<true, BN>;
-    mx_gemm_kernel<true, BN, false, true><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
+    using C = Cfg<K_MXFP4, BN>;
+    mx_gemm_kernel<K_MXFP4, BN, false, true><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
     return cudaGetLastError();
 }
 
 template <int BN>
 KernelInfo pair_info()
 {
-    using C = CfgPair<true, BN>;
+    using C = CfgPair<K_MXFP4, BN>;
     return KernelInfo{C::kStages, C::kAccStages, C::kSmemBytes};
 }
 
 template <int BN>
 KernelInfo info()
 {
-    using C = Cfg<true, BN>;
+    using C = Cfg<K_MXFP4, BN>;
     return KernelInfo{C::kStages, C::kAccStages, C::kSmemBytes};
 }
 }  // namespace
@@ -106,28 +106,28 @@ KernelInfo info()
 // when a plan is created, never on the launch path).
 cudaError_t prepare_gemm_fp4()
 {
-    const void *single[4] = {(const void *)mx_gemm_kernel<true, 32>, (const void *)mx_gemm_kernel<true, 64>,
-                             (const void *)mx_gemm_kernel<true, 128>, (const void *)mx_gemm_kernel<true, 256>};
-    const int single_smem[4] = {Cfg<true, 32>::kSmemBytes, Cfg<true, 64>::kSmemBytes, Cfg<true, 128>::kSmemBytes,
-                                Cfg<true, 256>::kSmemBytes};
+    const void *single[4] = {(const void *)mx_gemm_kernel<K_MXFP4, 32>, (const void *)mx_gemm_kernel<K_MXFP4, 64>,
+                             (const void *)mx_gemm_kernel<K_MXFP4, 128>, (const void *)mx_gemm_kernel<K_MXFP4, 256>};
+    const int single_smem[4] = {Cfg<K_MXFP4, 32>::kSmemBytes, Cfg<K_MXFP4, 64>::kSmemBytes, Cfg<K_MXFP4, 128>::kSmemBytes,
+                                Cfg<K_MXFP4, 256>::kSmemBytes};
     for (int i = 0; i < 4; ++i) {
         cudaError_t e = cudaFuncSetAttribute(single[i], cudaFuncAttributeMaxDynamicSharedMemorySize, single_smem[i]);
         if (e != cudaSuccess)
             return e;
     }
-    const void *cl[4] = {(const void *)mx_gemm_kernel<true, 128, true>, (const void *)mx_gemm_kernel<true, 256, true>,
-                         (const void *)mx_gemm_pair_kernel<true, 128>, (const void *)mx_gemm_pair_kernel<true, 256>};
-    const int cl_smem[4] = {Cfg<true, 128>::kSmemBytes, Cfg<true, 256>::kSmemBytes, CfgPair<true, 128>::kSmemBytes,
-                            CfgPair<true, 256>::kSmemBytes};
+    const void *cl[4] = {(const void *)mx_gemm_kernel<K_MXFP4, 128, true>, (const void *)mx_gemm_kernel<K_MXFP4, 256, true>,
+                         (const void *)mx_gemm_pair_kernel<K_MXFP4, 128>, (const void *)mx_gemm_pair_kernel<K_MXFP4, 256>};
+    const int cl_smem[4] = {Cfg<K_MXFP4, 128>::kSmemBytes, Cfg<K_MXFP4, 256>::kSmemBytes, CfgPair<K_MXFP4, 128>::kSmemBytes,
+                            CfgPair<K_MXFP4, 256>::kSmemBytes};
     for (int i = 0; i < 4; ++i) {
         cudaError_t e = cudaFuncSetAttribute(cl[i], cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem[i]);
         if (e != cudaSuccess)
             return e;
     }
-    const void *gr[3] = {(const void *)mx_gemm_kernel<true, 64, false, true>,
-                         (const void *)mx_gemm_kernel<true, 128, false, true>,
-                         (const void *)mx_gemm_kernel<true, 256, false, true>};
-    const int gr_smem[3] = {Cfg<true, 64>::kSmemBytes, Cfg<true, 128>::kSmemBytes, Cfg<true, 256>::kSmemBytes};
+    const void *gr[3] = {(const void *)mx_gemm_kernel<K_MXFP4, 64, false, true>,
+                         (const void *)mx_gemm_kernel<K_MXFP4, 128, false, true>,
+                         (const void *)mx_gemm_kernel<K_MXFP4, 256, false, true>};
+    const int gr_smem[3] = {Cfg<K_MXFP4, 64>::kSmemBytes, Cfg<K_MXFP4, 128>::kSmemBytes, Cfg<K_MXFP4, 256>::kSmemBytes};
     for (int i = 0; i < 3; ++i) {
         cudaError_t e = cudaFuncSetAttribute(gr[i], cudaFuncAttributeMaxDynamicSharedMemorySize, gr_smem[i]);
         if (e != cudaSuccess)

@@ -179,20 +179,26 @@ __device__ __forceinline__ void build_group_table(const GemmParams &p, GroupTabl
                g.rows);
 }
 
-template <bool FP4, int BN>
+// Element kind of the operands: MX block-scaled E4M3 or E2M1, or plain BF16.
+enum ElemKind : int { K_MXFP8 = 0, K_MXFP4 = 1, K_BF16 = 2 };
+
+template <int KIND, int BN>
 struct Cfg {
-    static constexpr int kKtPerStage = FP4 ? 2 : 1;           // scale K-tiles per k-stage
-    static constexpr int kSubPerKt = FP4 ? 2 : 4;             // MMAs per scale K-tile
+    static constexpr bool kFp4 = KIND == K_MXFP4;
+    static constexpr bool kScaled = KIND != K_BF16;           // MX kinds carry E8M0 scales
+    // A k-stage is 128 bytes of K per row: 128 E4M3, 256 E2M1 or 64 BF16 values.
+    static constexpr int kKtPerStage = kFp4 ? 2 : 1;          // scale K-tiles per k-stage
+    static constexpr int kSubPerKt = kFp4 ? 2 : 4;            // MMAs per K-tile (K = 32 B each)
     static constexpr int kChunksB = BN >= 128 ? BN / 128 : 1; // 128-row scale chunks of B per K-tile
     static constexpr int kABytes = kBM * kRowBytes;
     static constexpr int kBBytes = BN * kRowBytes;
-    static constexpr int kSfaBytes = kKtPerStage * kSfChunk;
-    static constexpr int kSfbBytes = kChunksB * kKtPerStage * kSfChunk;
+    static constexpr int kSfaBytes = kScaled ? kKtPerStage * kSfChunk : 0;
+    static constexpr int kSfbBytes = kScaled ? kChunksB * kKtPerStage * kSfChunk : 0;
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     static constexpr int kStagesRaw = (kSmemBudget - 1024 - 256) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-    static constexpr int kSfaCols = 4 * kKtPerStage;
-    static constexpr int kSfbCols = 4 * kKtPerStage * kChunksB;
+    static constexpr int kSfaCols = kScaled ? 4 * kKtPerStage : 0;
+    static constexpr int kSfbCols = kScaled ? 4 * kKtPerStage * kChunksB : 0;
     static constexpr int kAccStages = (2 * BN + kSfaCols + kSfbCols <= 512) ? 2 : 1;
     static constexpr int kTmemCols = 512;
     // Scale columns: one (SFA, SFB) region per ring slot, so the tcgen05.cp of the
@@ -200,7 +206,7 @@ struct Cfg {
     static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
     static constexpr int kSfCol0 = kAccStages * BN;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
-    static constexpr uint32_t kIdesc = idesc_block_scaled(FP4 ? 1u : 0u, kBM, BN);
+    static constexpr uint32_t kIdesc = kScaled ? idesc_block_scaled(kFp4 ? 1u : 0u, kBM, BN) : idesc_bf16(kBM, BN);
     static_assert(kStages >= 2, "shared memory too small for two stages");
     static_assert(kSfCol0 + kStages * kSfSlotCols <= kTmemCols, "TMEM overflow");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be 32..256, multiple of 32");
@@ -551,12 +557,12 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
 // to both, so the pair reads that tile from L2 once.  Slot reuse then needs
 // both CTAs' MMAs done: `empty` counts two commits (each MMA thread commits to
 // both CTAs' barriers).
-template <bool FP4, int BN, bool MC = false, bool GROUPED = false>
+template <int KIND, int BN, bool MC = false, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b)
 {
-    using C = Cfg<FP4, BN>;
+    using C = Cfg<KIND, BN>;
     constexpr int S = C::kStages;
 
     extern __shared__ uint8_t smem_raw[];
@@ -667,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int kt0 = ks * C::kKtPerStage;
                     const int nkt = min(C::kKtPerStage, p.num_kt - kt0);
                     const uint32_t bytes =
-                        C::kABytes + C::kBBytes + nkt * kSfChunk * ((has_sfa ? 1 : 0) + nchunk_b);
+                        C::kABytes + C::kBBytes + (C::kScaled ? nkt * kSfChunk * ((has_sfa ? 1 : 0) + nchunk_b) : 0);
                     if (elect_one()) {
                         mbar_arrive_expect_tx(full_bar(st), bytes);
                         tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, g.a_row, pol_a);
@@ -676,14 +682,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   full_bar(st), ks * kRowBytes, g.b_row + mc_rank * (BN / 2), 0x3);
                         else
                             tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, g.b_row, pol_b);
-                        if (has_sfa)
-                            bulk_load(sSFA + st * C::kSfaBytes,
-                                      p.sfa + (static_cast<size_t>(g.sfa_rb) * p.num_kt + kt0) * kSfChunk,
-                                      nkt * kSfChunk, full_bar(st));
-                        for (int c = 0; c < nchunk_b; ++c)
-                            bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
-                                      p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
-                                      nkt * kSfChunk, full_bar(st));
+                        if constexpr (C::kScaled) {
+                            if (has_sfa)
+                                bulk_load(sSFA + st * C::kSfaBytes,
+                                          p.sfa + (static_cast<size_t>(g.sfa_rb) * p.num_kt + kt0) * kSfChunk,
+                                          nkt * kSfChunk, full_bar(st));
+                            for (int c = 0; c < nchunk_b; ++c)
+                                bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
+                                          p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
+                                          nkt * kSfChunk, full_bar(st));
+                        }
                     }
                     __syncwarp();
                     armed |= 1u << st;
@@ -723,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sfb_src = sSFB + s_ * C::kSfbBytes;
 #pragma unroll
             for (int t = 0; t < C::kKtPerStage; ++t) {
-                if (t < nkt_) {
+                if (C::kScaled && t < nkt_) {
                     if (elect_one())
                         tc_cp_32x128b_warpx4(sfa_col_ + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
 #pragma unroll
@@ -771,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     constexpr int kSub = C::kSubPerKt;
                     const int t = s / kSub;
                     if (t < nkt) {
-                        const uint32_t sf_id = FP4 ? static_cast<uint32_t>((s % 2) * 2) : static_cast<uint32_t>(s % 4);
+                        const uint32_t sf_id = C::kFp4 ? static_cast<uint32_t>((s % 2) * 2) : static_cast<uint32_t>(s % 4);
                         const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, sf_id, sf_id);
                         const uint32_t sfa_t = sfa_col + 4 * t;
                         const uint32_t sfb_t = sfb_col + 4 * t * C::kChunksB + sub_off;
@@ -779,7 +787,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t koff = static_cast<uint64_t>((s * 32) >> 4);
                         const uint32_t accum = (s > 0) ? 1u : acc0;
                         if (elect_one()) {
-                            if (FP4)
+                            if constexpr (KIND == K_BF16)
+                                mma_bf16(d_tmem, adesc + koff, bdesc + koff, C::kIdesc, accum);
+                            else if constexpr (C::kFp4)
                                 mma_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
                             else
                                 mma_mxf8f6f4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);

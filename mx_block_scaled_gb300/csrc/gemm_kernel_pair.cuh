@@ -30,20 +30,22 @@
 
 namespace mxg {
 
-template <bool FP4, int BN>
+template <int KIND, int BN>
 struct CfgPair {
-    static constexpr int kKtPerStage = FP4 ? 2 : 1;
-    static constexpr int kSubPerKt = FP4 ? 2 : 4;
+    static constexpr bool kFp4 = KIND == K_MXFP4;
+    static constexpr bool kScaled = KIND != K_BF16;
+    static constexpr int kKtPerStage = kFp4 ? 2 : 1;
+    static constexpr int kSubPerKt = kFp4 ? 2 : 4;
     static constexpr int kChunksB = BN / 128;                 // B-role scale chunks per K-tile (all BN rows)
     static constexpr int kABytes = kBM * kRowBytes;           // own 128 A-role rows
     static constexpr int kBBytes = (BN / 2) * kRowBytes;      // own half of the B-role tile
-    static constexpr int kSfaBytes = kKtPerStage * kSfChunk;
-    static constexpr int kSfbBytes = kChunksB * kKtPerStage * kSfChunk;
+    static constexpr int kSfaBytes = kScaled ? kKtPerStage * kSfChunk : 0;
+    static constexpr int kSfbBytes = kScaled ? kChunksB * kKtPerStage * kSfChunk : 0;
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     static constexpr int kStagesRaw = (kSmemBudget - 1024 - 512) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-    static constexpr int kSfaCols = 4 * kKtPerStage;
-    static constexpr int kSfbCols = 4 * kKtPerStage * kChunksB;
+    static constexpr int kSfaCols = kScaled ? 4 * kKtPerStage : 0;
+    static constexpr int kSfbCols = kScaled ? 4 * kKtPerStage * kChunksB : 0;
     static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
     static constexpr int kAccStages = (2 * BN + kStages * kSfSlotCols <= 512) ? 2 : 1;
     static constexpr int kSfCol0 = kAccStages * BN;
@@ -51,19 +53,20 @@ struct CfgPair {
     static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128
                                    : kColsUsed <= 256 ? 256 : 512;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
-    static constexpr uint32_t kIdesc = idesc_block_scaled(FP4 ? 1u : 0u, 2 * kBM, BN);
+    static constexpr uint32_t kIdesc =
+        kScaled ? idesc_block_scaled(kFp4 ? 1u : 0u, 2 * kBM, BN) : idesc_bf16(2 * kBM, BN);
     static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
     static_assert(kStages >= 2, "shared memory too small for two stages");
     static_assert(kColsUsed <= 512, "TMEM overflow");
 };
 
-template <bool FP4, int BN>
+template <int KIND, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
                         const __grid_constant__ CUtensorMap map_sfb)
 {
-    using C = CfgPair<FP4, BN>;
+    using C = CfgPair<KIND, BN>;
     constexpr int S = C::kStages;
 
     extern __shared__ uint8_t smem_raw[];
@@ -165,9 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d_pair(sB + st * C::kBBytes, &map_b, bar, ks * kRowBytes,
                                          tn * BN + static_cast<int>(rank) * (BN / 2));
                         // scale chunks: rows of 256 bytes, two per 512-byte chunk
-                        if (has_sfa)
+                        if (C::kScaled && has_sfa)
                             tma_load_2d_pair(sSFA + st * C::kSfaBytes, &map_sfa, bar, 0, (rb_a * p.num_kt + kt0) * 2);
-                        for (int c = 0; c < nchunk_b; ++c)
+                        for (int c = 0; c < (C::kScaled ? nchunk_b : 0); ++c)
                             tma_load_2d_pair(sSFB + st * C::kSfbBytes + c * C::kSfaBytes, &map_sfb, bar, 0,
                                              ((rb_b0 + c) * p.num_kt + kt0) * 2);
                     }
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sfb_src = sSFB + s_ * C::kSfbBytes;
 #pragma unroll
             for (int t = 0; t < C::kKtPerStage; ++t) {
-                if (t < nkt_) {
+                if (C::kScaled && t < nkt_) {
                     if (elect_one())
                         tc_cp_pair_32x128b_warpx4(sfa_col_ + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
 #pragma unroll
@@ -250,14 +253,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int s = 0; s < C::kKtPerStage * C::kSubPerKt; ++s) {
                     const int t = s / C::kSubPerKt;
                     if (t < nkt) {
-                        const uint32_t sf_id = FP4 ? static_cast<uint32_t>((s % 2) * 2) : static_cast<uint32_t>(s % 4);
+                        const uint32_t sf_id = C::kFp4 ? static_cast<uint32_t>((s % 2) * 2) : static_cast<uint32_t>(s % 4);
                         const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, sf_id, sf_id);
                         const uint32_t sfa_t = sfa_col + 4 * t;
                         const uint32_t sfb_t = sfb_col + 4 * t * C::kChunksB;
                         const uint64_t koff = static_cast<uint64_t>((s * 32) >> 4);
                         const uint32_t accum = (s > 0) ? 1u : acc0;
                         if (elect_one()) {
-                            if (FP4)
+                            if constexpr (KIND == K_BF16)
+                                mma_pair_bf16(d_tmem, adesc + koff, bdesc + koff, C::kIdesc, accum);
+                            else if constexpr (C::kFp4)
                                 mma_pair_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
                             else
                                 mma_pair_mxf8f6f4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);

@@ -13,6 +13,7 @@ namespace mxg {
 // device.  Must run (once per device) before any launch below.
 cudaError_t prepare_gemm_fp8();
 cudaError_t prepare_gemm_fp4();
+cudaError_t prepare_gemm_bf16();
 
 // Launch the persistent GEMM kernel for tile width `bn` (32, 64, 128, 256) on
 // `grid` CTAs.  Returns cudaErrorInvalidValue for an unsupported bn.
@@ -49,6 +50,15 @@ cudaError_t launch_gemm_mc_fp4(int bn, const GemmParams &p, const CUtensorMap &m
 int gemm_mc_max_clusters_fp8(int bn);
 int gemm_mc_max_clusters_fp4(int bn);
 
+// BF16 (kind::f16, no scales) GEMM: single-CTA tiles (bn 32..256) and CTA-pair
+// tiles (bn 128, 256; the scale maps are not read).
+cudaError_t launch_gemm_bf16(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                             int grid, cudaStream_t stream);
+cudaError_t launch_gemm_pair_bf16(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                  const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, int clusters,
+                                  cudaStream_t stream);
+int gemm_pair_max_clusters_bf16(int bn);
+
 // Pipeline facts of one instantiation, for plan descriptions.
 struct KernelInfo {
     int stages;
@@ -59,5 +69,7 @@ KernelInfo gemm_info_fp8(int bn);
 KernelInfo gemm_info_fp4(int bn);
 KernelInfo gemm_pair_info_fp8(int bn);
 KernelInfo gemm_pair_info_fp4(int bn);
+KernelInfo gemm_info_bf16(int bn);
+KernelInfo gemm_pair_info_bf16(int bn);
 
 }  // namespace mxg

@@ -65,7 +65,8 @@ int device_info(DeviceInfo **out)
             g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
         if (d.is_sm103) {
-            if (mxg::prepare_gemm_fp8() != cudaSuccess || mxg::prepare_gemm_fp4() != cudaSuccess)
+            if (mxg::prepare_gemm_fp8() != cudaSuccess || mxg::prepare_gemm_fp4() != cudaSuccess ||
+                mxg::prepare_gemm_bf16() != cudaSuccess)
                 return MXGEMM_ERR_CUDA;
             d.kernels_prepared = true;
         }
@@ -369,9 +370,10 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     if (!plan)
         return MXGEMM_ERR_ARG;
     *plan = nullptr;
-    if ((fmt != MXGEMM_FMT_MXFP8_E4M3 && fmt != MXGEMM_FMT_MXFP4_E2M1) ||
+    if ((fmt != MXGEMM_FMT_MXFP8_E4M3 && fmt != MXGEMM_FMT_MXFP4_E2M1 && fmt != MXGEMM_FMT_BF16) ||
         (out != MXGEMM_OUT_F32 && out != MXGEMM_OUT_BF16))
         return MXGEMM_ERR_ARG;
+    const bool bf16 = fmt == MXGEMM_FMT_BF16;
     const uint32_t known = MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_NOSWAP |
                            MXGEMM_PLAN_FORCE_SWAP | MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE |
                            MXGEMM_PLAN_FORCE_MC | MXGEMM_PLAN_STREAMK | MXGEMM_PLAN_NO_STREAMK |
@@ -381,8 +383,12 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)) ||
         __builtin_popcount(flags & (MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE | MXGEMM_PLAN_FORCE_MC)) > 1)
         return MXGEMM_ERR_ARG;
-    if (M < 1 || N < 1 || K < 128 || K % 128 != 0)
+    // MX formats: K a multiple of 128 (the FlyDSL page's constraint); BF16: of 64
+    // (one 128-byte k-stage row).
+    if (M < 1 || N < 1 || K < (bf16 ? 64 : 128) || K % (bf16 ? 64 : 128) != 0)
         return MXGEMM_ERR_SHAPE;
+    if (bf16 && (flags & MXGEMM_PLAN_FORCE_MC))
+        return MXGEMM_ERR_UNSUPPORTED;  // no multicast instantiation for BF16
     // 32-bit tile and row indices inside the kernels
     if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30))
         return MXGEMM_ERR_UNSUPPORTED;
@@ -418,7 +424,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     // faster from 128 tokens up); MXFP4, whose MMAs are issue-bound in both
     // modes, and swapped decode shapes stay on single-CTA tiles.
     int mode = 0;
-    if (fmt == MXGEMM_FMT_MXFP8_E4M3 && !swap && rows_a >= 128 && rows_b >= 256 &&
+    if ((fmt == MXGEMM_FMT_MXFP8_E4M3 || bf16) && !swap && rows_a >= 128 && rows_b >= 256 &&
         !(flags & MXGEMM_PLAN_FORCE_BN128) && ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0)
         mode = 2;
     if (flags & MXGEMM_PLAN_FORCE_MC) mode = 1;
@@ -431,7 +437,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     // pairs of 128-row tiles (MC), 256-row tiles (pair).
     p->tiles_m = static_cast<int>(mode == 0 ? ceil_div(rows_a, 128) : ceil_div(rows_a, 256));
     p->tiles_n = static_cast<int>(ceil_div(rows_b, bn));
-    p->kstages = static_cast<int>(fmt == MXGEMM_FMT_MXFP4_E2M1 ? ceil_div(K, 256) : K / 128);
+    p->kstages = static_cast<int>(fmt == MXGEMM_FMT_MXFP4_E2M1 ? ceil_div(K, 256) : bf16 ? K / 64 : K / 128);
 
     // Concurrent work units: SMs, or co-resident clusters of two.
     int64_t slots = p->num_sms;
@@ -442,7 +448,8 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
                                                         : mxg::gemm_mc_max_clusters_fp8(bn);
         else
             max_clusters = fmt == MXGEMM_FMT_MXFP4_E2M1 ? mxg::gemm_pair_max_clusters_fp4(bn)
-                                                        : mxg::gemm_pair_max_clusters_fp8(bn);
+                           : bf16                           ? mxg::gemm_pair_max_clusters_bf16(bn)
+                                                            : mxg::gemm_pair_max_clusters_fp8(bn);
         if (max_clusters < 1) {
             delete p;
             return MXGEMM_ERR_CUDA;
@@ -511,9 +518,9 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
 
     size_t off = 0;
     p->off_sfa = off;
-    off = align256(off + mxgemm_sf_bytes(M, K));
+    off = align256(off + (bf16 ? 0 : mxgemm_sf_bytes(M, K)));
     p->off_sfb = off;
-    off = align256(off + mxgemm_sf_bytes(N, K));
+    off = align256(off + (bf16 ? 0 : mxgemm_sf_bytes(N, K)));
     p->off_part = off;
     if (p->splits > 1)
         off = align256(off + static_cast<size_t>(p->splits) * ((M * N + 3) & ~3ll) * sizeof(float));
@@ -542,13 +549,18 @@ int mxgemm_plan_describe(mxgemm_plan_t plan, char *buf, size_t len)
     if (!plan || !buf || len == 0)
         return MXGEMM_ERR_ARG;
     const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
+    const bool bf16 = plan->fmt == MXGEMM_FMT_BF16;
     static const char *const kModes[3] = {"single", "mc", "pair"};
-    mxg::KernelInfo ki = plan->mode == 2 ? (fp4 ? mxg::gemm_pair_info_fp4(plan->bn) : mxg::gemm_pair_info_fp8(plan->bn))
-                                         : (fp4 ? mxg::gemm_info_fp4(plan->bn) : mxg::gemm_info_fp8(plan->bn));
+    mxg::KernelInfo ki = plan->mode == 2 ? (fp4 ? mxg::gemm_pair_info_fp4(plan->bn)
+                                                : bf16 ? mxg::gemm_pair_info_bf16(plan->bn)
+                                                       : mxg::gemm_pair_info_fp8(plan->bn))
+                                         : (fp4 ? mxg::gemm_info_fp4(plan->bn)
+                                                : bf16 ? mxg::gemm_info_bf16(plan->bn) : mxg::gemm_info_fp8(plan->bn));
     snprintf(buf, len,
              "fmt=%s out=%s tile=%dx%d mode=%s swap_ab=%d split_k=%d streamk=%d+%d/%d units=%dx%d kstages=%d grid=%d%s "
              "stages=%d acc_stages=%d smem=%d",
-             fp4 ? "mxfp4" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32", plan->mode == 2 ? 256 : 128,
+             fp4 ? "mxfp4" : bf16 ? "bf16" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32",
+             plan->mode == 2 ? 256 : 128,
              plan->bn, kModes[plan->mode], plan->swap, plan->splits, plan->dp_tiles, plan->sk_tiles, plan->sk_ctas,
              plan->tiles_m, plan->tiles_n, plan->kstages, plan->grid, plan->mode ? "x2" : "", ki.stages, ki.acc_stages,
              ki.smem_bytes);
@@ -603,11 +615,14 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
                     void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream, int test_stall,
                     unsigned long long timeout_ns)
 {
-    if (!plan || !A || !SA || !B || !SB || !C)
+    if (!plan || !A || !B || !C)
+        return MXGEMM_ERR_ARG;
+    const bool bf16 = plan->fmt == MXGEMM_FMT_BF16;  // no scales: SA and SB are not read
+    if (!bf16 && (!SA || !SB))
         return MXGEMM_ERR_ARG;
     if (run_flags & ~(MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT))
         return MXGEMM_ERR_ARG;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(SA) || !aligned16(SB))
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (!bf16 && (!aligned16(SA) || !aligned16(SB))))
         return MXGEMM_ERR_ALIGN;
     if (plan->ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan->ws_bytes))
         return MXGEMM_ERR_WORKSPACE;
@@ -625,12 +640,14 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int64_t M = plan->M, N = plan->N, K = plan->K;
     const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
-    const int64_t row_bytes = fp4 ? K / 2 : K;
+    const int64_t row_bytes = fp4 ? K / 2 : bf16 ? 2 * K : K;
 
     // (1) scale relayout for whichever operand is not pre-laid-out (one launch)
     const uint8_t *sfa = SA, *sfb = SB;
     RelayoutJob jobs[2];
     int njobs = 0;
+    if (bf16)
+        run_flags = MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT;  // nothing to lay out
     if (!(run_flags & MXGEMM_RUN_SA_PRELAYOUT)) {
         jobs[njobs++] = make_job(SA, M, K, ws + plan->off_sfa);
         sfa = ws + plan->off_sfa;
@@ -663,7 +680,7 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     memset(&p, 0, sizeof p);
     p.rows_a = static_cast<int>(rows_a);
     p.rows_b = static_cast<int>(rows_b);
-    p.num_kt = static_cast<int>(K / 128);
+    p.num_kt = static_cast<int>(bf16 ? K / 64 : K / 128);  // BF16: one "K-tile" per 64-value stage
     p.kstages = plan->kstages;
     p.kstages_per_split = plan->kstages_per_split;
     p.tiles_m = plan->tiles_m;
@@ -704,7 +721,11 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     p.vec_ok = (!plan->swap && (N * osize) % 16 == 0 && aligned16(p.out)) ? 1 : 0;
 
     cudaError_t e;
-    if (plan->mode == 2) {
+    if (plan->mode == 2 && bf16) {
+        // the kernel reads no scale maps for BF16; pass valid descriptors anyway
+        e = mxg::launch_gemm_pair_bf16(plan->bn, p, plan->map_a, plan->map_b, plan->map_a, plan->map_b, plan->grid,
+                                       s);
+    } else if (plan->mode == 2) {
         const int ktps = fp4 ? 2 : 1;
         if (plan->map_ptr_sfa != p.sfa) {
             if (encode_sf_map(&plan->map_sfa, p.sfa, mxgemm_sf_bytes(rows_a, K), ktps) != MXGEMM_OK)
@@ -724,6 +745,8 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     else if (plan->mode == 1)
         e = fp4 ? mxg::launch_gemm_mc_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
                 : mxg::launch_gemm_mc_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
+    else if (bf16)
+        e = mxg::launch_gemm_bf16(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
     else
         e = fp4 ? mxg::launch_gemm_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
                 : mxg::launch_gemm_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);

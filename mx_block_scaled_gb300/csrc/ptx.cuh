@@ -318,6 +318,18 @@ __device__ __forceinline__ void mma_pair_mxf4(uint32_t d, uint64_t adesc, uint64
         : "memory");
 }
 
+// Pair MMA, BF16 operands (kind::f16), FP32 accumulator; M = 256 over both CTAs.
+__device__ __forceinline__ void mma_pair_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc),
+        "r"(accumulate)
+        : "memory");
+}
+
 // Single-CTA MMA commit that arrives on `bar` (same offset) in every CTA of `mask`.
 __device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t mask)
 {
@@ -353,6 +365,18 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bd
         "setp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T, BF16 operands (kind::f16), FP32 accumulator.
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc),
+        "r"(accumulate)
         : "memory");
 }
 
@@ -430,6 +454,13 @@ __device__ __forceinline__ uint64_t sdesc_sf_chunk(uint32_t saddr)
 __host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t elem_type, uint32_t m, uint32_t n)
 {
     return (elem_type << 7) | (elem_type << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f16 with BF16 A and B (type code 1), FP32 D
+// (bits [4,6) = 1), K-major A and B, dense: N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t m, uint32_t n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 __device__ __forceinline__ uint32_t idesc_with_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id)

@@ -59,7 +59,7 @@ def test_status_strings(lib):
     (16, 16, 0, 1, 2, 0, -2),
     (0, 16, 128, 1, 2, 0, -2),
     (16, -1, 128, 2, 1, 0, -2),
-    (16, 16, 128, 3, 2, 0, -1),   # unknown format
+    (16, 16, 128, 4, 2, 0, -1),   # unknown format
     (16, 16, 128, 1, 9, 0, -1),   # unknown output type
     (16, 16, 128, 1, 2, 1 << 20, -1),  # unknown flag
     (16, 16, 128, 1, 2, (1 << 2) | (1 << 3), -1),  # contradictory flags
@@ -135,3 +135,13 @@ def test_grouped_null_arguments_are_rejected(lib):
     assert lib.mxgemm_grouped_run(None, 8, 16, 16, 16, 16, 16, 16, 0, 0, 0) == lib.MXGEMM_ERR_ARG
     assert lib.mxgemm_grouped_plan_destroy(None) == lib.MXGEMM_OK
     assert lib.mxgemm_grouped_workspace_bytes(None) == 0
+
+
+@pytest.mark.parametrize("M,N,K,flags,expect", [
+    (16, 16, 96, 0, -2),        # BF16 needs K % 64 == 0
+    (16, 16, 0, 0, -2),
+    (16, 16, 64, 1 << 6, -8),   # no multicast instantiation for BF16
+])
+def test_bf16_plan_validation(lib, M, N, K, flags, expect):
+    st, h = lib.mxgemm_plan_create(M, N, K, 3, 2, flags)
+    assert st == expect and not h.value
