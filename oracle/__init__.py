@@ -15,6 +15,9 @@ from .mxref import (  # noqa: F401
     bf16_to_f64,
     num_threads,
     quantize,
+    placement_scan,
+    placement_eval,
+    placement_tuple,
     IN_F32,
     IN_BF16,
 )

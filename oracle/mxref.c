@@ -368,3 +368,121 @@ int mxref_quantize(int fmt, int in_dtype, int64_t rows, int64_t K, const void *x
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Scale placement in MXFP4 dot products (reference checker).                 */
+/*                                                                            */
+/* AI-compiler daily digest of 2026-10-22, item 2 ("Deciding Scale Placement  */
+/* in MXFP4 Dot Products with Integer Arithmetic"): lowering an MXFP4 dot     */
+/* product may apply the shared power-of-two scales before the products       */
+/* ("pre") or after the sum ("post"); in binary32 the two can round           */
+/* differently (overflow, NaN, subnormals), and the study bounds the sum of   */
+/* scale exponents for which they agree under a fixed binary reduction tree.  */
+/* The bound is not printed on the page.  Readings taken here:                */
+/*   k elements a_i, b_i (E2M1), scales sa, sb (E8M0 codes 0..254),           */
+/*   f_a = 2^(sa-127), f_b = 2^(sb-127) as binary32 values (exact, also when  */
+/*   subnormal);                                                              */
+/*   pre  = tree_sum(  (a_i * f_a) * (b_i * f_b) ),                           */
+/*   post = (tree_sum( a_i * b_i ) * f_a) * f_b,                              */
+/*   every operation one binary32 operation rounded to nearest-even, no fused */
+/*   multiply-add; tree_sum over n terms = tree_sum(first ceil(n/2)) +        */
+/*   tree_sum(rest);                                                          */
+/*   exact = sum a_i b_i * 2^(sa+sb-254), and rn_exact its binary32 rounding; */
+/*   two results are "equal" when both are NaN or they are equal values       */
+/*   (+0 == -0: the sign of a zero sum is not a placement question).          */
+/* Tuples are numbered t = sum_i a_i << 4i + sum_i b_i << 4(k+i) over the     */
+/* 4-bit codes, 16^(2k) of them.                                              */
+/* ------------------------------------------------------------------------- */
+
+static float tree_sum_f(const float *v, int n)
+{
+    if (n == 1)
+        return v[0];
+    const int h = (n + 1) / 2;
+    volatile float l = tree_sum_f(v, h);
+    volatile float r = tree_sum_f(v + h, n - h);
+    volatile float s = l + r;
+    return s;
+}
+
+static int same_f(float x, float y)
+{
+    if (isnan(x) || isnan(y))
+        return isnan(x) && isnan(y);
+    return x == y;
+}
+
+/* The three values of tuple t under scales fa = 2^(sa-127), fb = 2^(sb-127). */
+static void placement_eval(int k, int sa, int sb, float fa, float fb, long long t, float *pre, float *post,
+                           float *rn)
+{
+    float prod_pre[4], prod_post[4];
+    double exact_sum = 0.0;
+    for (int i = 0; i < k; ++i) {
+        const double a = tab_e2m1[(t >> (4 * i)) & 15];
+        const double b = tab_e2m1[(t >> (4 * (k + i))) & 15];
+        volatile float as = (float)a * fa;
+        volatile float bs = (float)b * fb;
+        volatile float pp = as * bs;
+        prod_pre[i] = pp;
+        volatile float q = (float)a * (float)b;  /* exact: a multiple of 1/4, |.| <= 36 */
+        prod_post[i] = q;
+        exact_sum += a * b;                         /* exact */
+    }
+    *pre = tree_sum_f(prod_pre, k);
+    volatile float post1 = tree_sum_f(prod_post, k) * fa;
+    volatile float post2 = post1 * fb;
+    *post = post2;
+    *rn = (float)ldexp(exact_sum, sa + sb - 254);  /* one rounding of an exact value */
+}
+
+/* pre, post and rn of one tuple (out[0..2]).  Returns 0, or -1 for bad arguments. */
+int mxref_placement_eval(int k, int sa, int sb, long long t, float *out)
+{
+    mxref_init();
+    if (k < 1 || k > 4 || sa < 0 || sa > 254 || sb < 0 || sb > 254 || t < 0 || t >= (1ll << (8 * k)))
+        return -1;
+    placement_eval(k, sa, sb, (float)ldexp(1.0, sa - 127), (float)ldexp(1.0, sb - 127), t, &out[0], &out[1],
+                   &out[2]);
+    return 0;
+}
+
+/*
+ * For each of the npairs scale pairs (sa[p], sb[p]), enumerate every tuple of a
+ * k-element (1 <= k <= 4) MXFP4 dot product and write
+ *   counts[3p+0] = tuples with pre != post,
+ *   counts[3p+1] = tuples with pre == rn,
+ *   counts[3p+2] = tuples with post == rn,
+ *   first_diff[p] = the smallest tuple number with pre != post, or -1.
+ * Returns 0, or -1 for bad arguments.
+ */
+int mxref_placement_scan(int k, const int *sa, const int *sb, int npairs, long long *counts, long long *first_diff)
+{
+    mxref_init();
+    if (k < 1 || k > 4 || npairs < 0)
+        return -1;
+    for (int p = 0; p < npairs; ++p)
+        if (sa[p] < 0 || sa[p] > 254 || sb[p] < 0 || sb[p] > 254)
+            return -1;
+    const long long ntup = 1ll << (8 * k);
+    for (int p = 0; p < npairs; ++p) {
+        const float fa = (float)ldexp(1.0, sa[p] - 127), fb = (float)ldexp(1.0, sb[p] - 127);
+        long long n_diff = 0, n_pre = 0, n_post = 0, first = ntup;
+#pragma omp parallel for schedule(static) reduction(+ : n_diff, n_pre, n_post) reduction(min : first)
+        for (long long t = 0; t < ntup; ++t) {
+            float pre, post, rn;
+            placement_eval(k, sa[p], sb[p], fa, fb, t, &pre, &post, &rn);
+            const int d = !same_f(pre, post);
+            n_diff += d;
+            n_pre += same_f(pre, rn);
+            n_post += same_f(post, rn);
+            if (d && t < first)
+                first = t;
+        }
+        counts[3 * p] = n_diff;
+        counts[3 * p + 1] = n_pre;
+        counts[3 * p + 2] = n_post;
+        first_diff[p] = n_diff ? first : -1;
+    }
+    return 0;
+}

@@ -51,6 +51,12 @@ def _load():
             lib.mxref_decode_table.restype = ctypes.c_int
             lib.mxref_decode_table.argtypes = [ctypes.c_int, ctypes.c_void_p]
             lib.mxref_num_threads.restype = ctypes.c_int
+            lib.mxref_placement_scan.restype = ctypes.c_int
+            lib.mxref_placement_scan.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                                 ctypes.c_void_p, ctypes.c_void_p]
+            lib.mxref_placement_eval.restype = ctypes.c_int
+            lib.mxref_placement_eval.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                                 ctypes.c_void_p]
             lib.mxref_quantize.restype = ctypes.c_int
             lib.mxref_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
@@ -180,3 +186,35 @@ def bf16_gemm(A_bits, B_bits, rows=None, cols=None, with_abs: bool = True):
     C = A @ B.T
     S = np.abs(A) @ np.abs(B).T if with_abs else None
     return C, S
+
+
+def placement_scan(k: int, sa, sb):
+    """Reference scale-placement checker (see ``mxref_placement_scan``): for each
+    scale pair, counts [pre != post, pre == rn_exact, post == rn_exact] over all
+    16^(2k) E2M1 tuples and the first tuple where pre and post differ (-1: none)."""
+    sa = np.ascontiguousarray(sa, dtype=np.int32)
+    sb = np.ascontiguousarray(sb, dtype=np.int32)
+    n = sa.size
+    counts = np.zeros((n, 3), dtype=np.int64)
+    first = np.zeros(n, dtype=np.int64)
+    if _load().mxref_placement_scan(k, sa.ctypes.data, sb.ctypes.data, n, counts.ctypes.data, first.ctypes.data):
+        raise ValueError("mxref_placement_scan rejected its arguments")
+    return counts, first
+
+
+def placement_tuple(k: int, a_codes, b_codes) -> int:
+    """Tuple number of E2M1 codes (element 0 first): a_i at bits 4i, b_i at 4(k+i)."""
+    t = 0
+    for i, c in enumerate(a_codes):
+        t |= int(c) << (4 * i)
+    for i, c in enumerate(b_codes):
+        t |= int(c) << (4 * (k + i))
+    return t
+
+
+def placement_eval(k: int, sa: int, sb: int, t: int):
+    """(pre, post, rn) of tuple t as binary32 values (see ``mxref_placement_scan``)."""
+    out = np.zeros(3, dtype=np.float32)
+    if _load().mxref_placement_eval(k, sa, sb, t, out.ctypes.data):
+        raise ValueError("mxref_placement_eval rejected its arguments")
+    return tuple(float(v) for v in out)

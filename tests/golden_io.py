@@ -107,3 +107,32 @@ def load_quantize_handworked():
         if c["x"].shape != (1, 32) or c["codes"].shape != (32,):
             raise ValueError(f"case {c['name']}: expected 32 inputs and 32 codes")
     return cases
+
+
+def _pvalue(tok: str) -> float:
+    t = tok.lower()
+    if t in ("nan", "inf", "-inf"):
+        return float(t)
+    if "x" in t:
+        m, e = t.split("x")
+        return float(Fraction(m) * Fraction(2) ** int(e))
+    return float(Fraction(t))
+
+
+def load_placement_handworked():
+    """Hand-worked scale placements: list of dicts k, sa, sb, a (codes), b (codes), pre, post, rn."""
+    out = []
+    with open(os.path.join(GOLDEN_DIR, "placement_handworked.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line.startswith("case:"):
+                continue
+            head, a, b, vals = [x.strip() for x in line[len("case:"):].split("|")]
+            k, sa, sb = (int(v) for v in head.split())
+            ac = [int(v, 16) for v in a.split()]
+            bc = [int(v, 16) for v in b.split()]
+            pre, post, rn = (_pvalue(v) for v in vals.split())
+            if len(ac) != k or len(bc) != k:
+                raise ValueError(f"placement case {line}: expected {k} codes per operand")
+            out.append(dict(k=k, sa=sa, sb=sb, a=ac, b=bc, pre=pre, post=post, rn=rn))
+    return out
