@@ -720,6 +720,55 @@ def run_bf16_sweep(args):
     return 0
 
 
+def run_placement_sweep(args):
+    """Scale-placement checker over every pair of valid scale codes (255 x 255) for
+    k = 1, 2, 3 elements per operand; prints the time, the tuple rate, the oracle's
+    rate on a few pairs, and which pairs agree in both placements."""
+    import numpy as np
+    import torch
+    from mx_block_scaled_gb300 import binding as mx
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    sa, sb = np.meshgrid(np.arange(255, dtype=np.int32), np.arange(255, dtype=np.int32), indexing="ij")
+    sa, sb = sa.reshape(-1), sb.reshape(-1)
+    dsa, dsb = torch.from_numpy(sa).cuda(), torch.from_numpy(sb).cuda()
+    out_dir = os.path.join(ROOT, "gpurun_out")
+    for k in (1, 2, 3):
+        mx.placement_scan(k, dsa[:64], dsb[:64])  # warm-up
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        counts, first = mx.placement_scan(k, dsa, dsb)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        mx.check_device_status()
+        sec = e0.elapsed_time(e1) / 1e3
+        c, f = counts.cpu().numpy(), first.cpu().numpy()
+        ntup = float(1 << (8 * k)) * len(sa)
+        agree = c[:, 0] == 0
+        ea, eb = sa.astype(int) - 127, sb.astype(int) - 127
+        rec = {"kernel": "placement_scan", "k": k, "pairs": int(len(sa)), "tuples": ntup, "s": sec,
+               "tuples_per_s": ntup / sec, "pairs_agreeing": int(agree.sum()),
+               "tuples_differing": int(c[:, 0].sum()), "pre_equals_rn": int(c[:, 1].sum()),
+               "post_equals_rn": int(c[:, 2].sum())}
+        if agree.any():
+            rec["agree_ea_range"] = [int(ea[agree].min()), int(ea[agree].max())]
+            rec["agree_eb_range"] = [int(eb[agree].min()), int(eb[agree].max())]
+            rec["agree_sum_range"] = [int((ea + eb)[agree].min()), int((ea + eb)[agree].max())]
+        if os.path.isdir(out_dir):
+            np.savez_compressed(os.path.join(out_dir, f"placement_k{k}.npz"), sa=sa, sb=sb, counts=c, first=f)
+        if not args.no_cpu_baseline and k == 3:
+            import oracle
+            picks = [(127, 127), (250, 3), (40, 200)]
+            t0 = time.perf_counter()
+            oracle.placement_scan(k, [p[0] for p in picks], [p[1] for p in picks])
+            cpu_s = time.perf_counter() - t0
+            rec["cpu_baseline"] = {"kind": "oracle", "tuples_per_s": float(1 << (8 * k)) * len(picks) / cpu_s,
+                                   "cores": oracle.num_threads(), "sample": f"{len(picks)} scale pairs at k={k}"}
+        print(json.dumps(rec), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -742,6 +791,8 @@ def main():
                     help="time the BF16 NT GEMM (and cuBLAS beside it) over the dense workload shapes")
     ap.add_argument("--grouped-sweep", action="store_true",
                     help="time the grouped (mixture-of-experts) MX GEMM over the grouped workloads")
+    ap.add_argument("--placement-sweep", action="store_true",
+                    help="run the scale-placement checker over every scale pair for k = 1, 2, 3")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -753,6 +804,8 @@ def main():
         return run_grouped_sweep(args)
     if args.bf16_sweep:
         return run_bf16_sweep(args)
+    if args.placement_sweep:
+        return run_placement_sweep(args)
     if args.sweep or args.shape:
         return run_sweep(args)
     return run_ours(args)

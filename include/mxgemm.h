@@ -328,6 +328,29 @@ MXGEMM_API int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *gro
                                   const uint8_t *SA, const void *B, const uint8_t *SB, void *C, void *workspace,
                                   size_t ws_bytes, uint32_t run_flags, void *stream);
 
+/*
+ * Scale-placement checker for MXFP4 dot products ("Deciding Scale Placement in
+ * MXFP4 Dot Products with Integer Arithmetic", AI-compiler daily digest of
+ * 2026-10-22, item 2): for each scale pair (sa[p], sb[p]) (E8M0 codes 0..254)
+ * and every tuple of k (1..4) E2M1 elements per operand -- 16^(2k) tuples,
+ * numbered t = sum a_i << 4i + sum b_i << 4(k+i) over the 4-bit codes --
+ * compare, in binary32 with every operation rounded to nearest even and no
+ * fused multiply-add (f_a = 2^(sa-127), f_b = 2^(sb-127)):
+ *     pre  = tree( (a_i f_a) (b_i f_b) )      scales applied to the elements
+ *     post = (tree( a_i b_i ) f_a) f_b        scales applied to the sum
+ *     rn   = sum a_i b_i * 2^(sa+sb-254) rounded once to binary32
+ * with tree(n) = tree(first ceil(n/2)) + tree(rest); equal = both NaN or equal
+ * values.  Writes counts[3p] = #(pre != post), counts[3p+1] = #(pre == rn),
+ * counts[3p+2] = #(post == rn), first_diff[p] = the smallest t with
+ * pre != post, or -1; a scale code outside 0..254 gives -1 in all four.
+ *   sa, sb: device int32[npairs]; counts: device int64[3*npairs]; first_diff:
+ *   device int64[npairs].  Stream-ordered; k = 4 costs 4.3e9 tuples per pair.
+ * Errors: MXGEMM_ERR_ARG (NULL), MXGEMM_ERR_SHAPE (k, npairs outside 1..4,
+ * 1..2^24), MXGEMM_ERR_ALIGN, MXGEMM_ERR_ARCH, MXGEMM_ERR_CUDA.
+ */
+MXGEMM_API int mxgemm_placement_scan(int k, const int *sa, const int *sb, int npairs, long long *counts,
+                                     long long *first_diff, void *stream);
+
 /* Static, human-readable name of a status code. */
 MXGEMM_API const char *mxgemm_status_str(int status);
 

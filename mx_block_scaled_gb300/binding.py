@@ -69,6 +69,7 @@ SIGNATURES = [
     ("mxgemm_grouped_workspace_bytes", ctypes.c_size_t, [_P]),
     ("mxgemm_grouped_plan_describe", ctypes.c_int, [_P, ctypes.c_char_p, ctypes.c_size_t]),
     ("mxgemm_grouped_run", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
+    ("mxgemm_placement_scan", ctypes.c_int, [ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P]),
     ("mxgemm_status_str", ctypes.c_char_p, [ctypes.c_int]),
     ("mxgemm_version", ctypes.c_int, []),
 ]
@@ -313,6 +314,23 @@ def quantize(x, fmt: int, tiled: bool = False, codes=None, scales=None, stream=N
     _check(mxgemm_quantize(fmt, in_dtype, x.data_ptr(), rows, K, codes.data_ptr(), scales.data_ptr(),
                            MXGEMM_QUANT_SF_TILED if tiled else 0, _stream_handle(stream)), "mxgemm_quantize")
     return codes, scales
+
+
+def mxgemm_placement_scan(k: int, sa_ptr: int, sb_ptr: int, npairs: int, counts_ptr: int, first_ptr: int,
+                          stream: int) -> int:
+    return _lib.mxgemm_placement_scan(k, sa_ptr, sb_ptr, npairs, counts_ptr, first_ptr, stream)
+
+
+def placement_scan(k: int, sa, sb, stream=None):
+    """Scale-placement checker on the GPU: ``sa``, ``sb`` CUDA int32 tensors of scale
+    codes; returns (counts [npairs, 3] int64, first_diff [npairs] int64) CUDA tensors."""
+    import torch
+    n = sa.numel()
+    counts = torch.empty((n, 3), dtype=torch.int64, device=sa.device)
+    first = torch.empty(n, dtype=torch.int64, device=sa.device)
+    _check(mxgemm_placement_scan(k, sa.data_ptr(), sb.data_ptr(), n, counts.data_ptr(), first.data_ptr(),
+                                 _stream_handle(stream)), "mxgemm_placement_scan")
+    return counts, first
 
 
 def check_device_status(stream=None) -> None:

@@ -1,7 +1,8 @@
 """Build libmxgemm.so in-tree with nvcc for sm_103a.
 
-Five translation units (host API + relayout/reduce kernels, MXFP8 GEMM,
-MXFP4 GEMM, BF16 GEMM, MX quantiser) are compiled in parallel and linked into
+Six translation units (host API + relayout/reduce kernels, MXFP8 GEMM,
+MXFP4 GEMM, BF16 GEMM, MX quantiser, scale-placement checker) are compiled in
+parallel and linked into
 ``mx_block_scaled_gb300/lib/libmxgemm.so``.
 """
 from __future__ import annotations
@@ -19,7 +20,7 @@ OBJ_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmxgemm.so")
 
-SOURCES = ["mxgemm.cu", "gemm_fp8.cu", "gemm_fp4.cu", "gemm_bf16.cu", "quantize.cu"]
+SOURCES = ["mxgemm.cu", "gemm_fp8.cu", "gemm_fp4.cu", "gemm_bf16.cu", "quantize.cu", "placement.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I" + INCLUDE, "-I" + CSRC]

@@ -13,6 +13,7 @@
 
 #include "launch.h"
 #include "mxgemm.h"
+#include "placement.h"
 #include "quantize.h"
 
 namespace {
@@ -996,6 +997,26 @@ int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *group_offsets,
     const cudaError_t e = fp4 ? mxg::launch_gemm_grouped_fp4(plan->bn, p, ma, mb, plan->num_sms, s)
                               : mxg::launch_gemm_grouped_fp8(plan->bn, p, ma, mb, plan->num_sms, s);
     return e == cudaSuccess ? MXGEMM_OK : MXGEMM_ERR_CUDA;
+}
+
+int mxgemm_placement_scan(int k, const int *sa, const int *sb, int npairs, long long *counts, long long *first_diff,
+                          void *stream)
+{
+    if (!sa || !sb || !counts || !first_diff)
+        return MXGEMM_ERR_ARG;
+    if (k < 1 || k > 4 || npairs < 1 || npairs > (1 << 24))
+        return MXGEMM_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(sa) & 3u) || (reinterpret_cast<uintptr_t>(sb) & 3u) ||
+        (reinterpret_cast<uintptr_t>(counts) & 7u) || (reinterpret_cast<uintptr_t>(first_diff) & 7u))
+        return MXGEMM_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    const int st = device_info(&dev);
+    if (st != MXGEMM_OK)
+        return st;
+    return mxg::launch_placement_scan(k, sa, sb, npairs, counts, first_diff, dev->num_sms,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MXGEMM_OK
+               : MXGEMM_ERR_CUDA;
 }
 
 int mxgemm_device_status(void *stream, int reset)

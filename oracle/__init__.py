@@ -18,6 +18,7 @@ from .mxref import (  # noqa: F401
     placement_scan,
     placement_eval,
     placement_tuple,
+    placement_values,
     IN_F32,
     IN_BF16,
 )

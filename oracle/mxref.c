@@ -486,3 +486,18 @@ int mxref_placement_scan(int k, const int *sa, const int *sb, int npairs, long l
     }
     return 0;
 }
+
+/* pre, post and rn of every tuple of one scale pair: out[3t+0..2]
+ * (16^(2k) x 3 floats).  Returns 0, or -1 for bad arguments. */
+int mxref_placement_values(int k, int sa, int sb, float *out)
+{
+    mxref_init();
+    if (k < 1 || k > 3 || sa < 0 || sa > 254 || sb < 0 || sb > 254)
+        return -1;
+    const long long ntup = 1ll << (8 * k);
+    const float fa = (float)ldexp(1.0, sa - 127), fb = (float)ldexp(1.0, sb - 127);
+#pragma omp parallel for schedule(static)
+    for (long long t = 0; t < ntup; ++t)
+        placement_eval(k, sa, sb, fa, fb, t, &out[3 * t], &out[3 * t + 1], &out[3 * t + 2]);
+    return 0;
+}

@@ -57,6 +57,8 @@ def _load():
             lib.mxref_placement_eval.restype = ctypes.c_int
             lib.mxref_placement_eval.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                                  ctypes.c_void_p]
+            lib.mxref_placement_values.restype = ctypes.c_int
+            lib.mxref_placement_values.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
             lib.mxref_quantize.restype = ctypes.c_int
             lib.mxref_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
@@ -218,3 +220,11 @@ def placement_eval(k: int, sa: int, sb: int, t: int):
     if _load().mxref_placement_eval(k, sa, sb, t, out.ctypes.data):
         raise ValueError("mxref_placement_eval rejected its arguments")
     return tuple(float(v) for v in out)
+
+
+def placement_values(k: int, sa: int, sb: int) -> np.ndarray:
+    """[16^(2k), 3] float32: pre, post and rn of every tuple of one scale pair (k <= 3)."""
+    out = np.zeros((1 << (8 * k), 3), dtype=np.float32)
+    if _load().mxref_placement_values(k, sa, sb, out.ctypes.data):
+        raise ValueError("mxref_placement_values rejected its arguments")
+    return out

@@ -145,3 +145,15 @@ def test_grouped_null_arguments_are_rejected(lib):
 def test_bf16_plan_validation(lib, M, N, K, flags, expect):
     st, h = lib.mxgemm_plan_create(M, N, K, 3, 2, flags)
     assert st == expect and not h.value
+
+
+@pytest.mark.parametrize("k,npairs,sa,sb,counts,first,expect", [
+    (2, 4, 0, 16, 32, 64, -1),     # NULL sa
+    (0, 4, 16, 16, 32, 64, -2),    # k < 1
+    (5, 4, 16, 16, 32, 64, -2),    # k > 4
+    (2, 0, 16, 16, 32, 64, -2),    # no pairs
+    (2, 4, 18, 16, 32, 64, -3),    # sa not 4-byte aligned
+    (2, 4, 16, 16, 36, 64, -3),    # counts not 8-byte aligned
+])
+def test_placement_scan_validates_before_touching_the_device(lib, k, npairs, sa, sb, counts, first, expect):
+    assert lib.mxgemm_placement_scan(k, sa, sb, npairs, counts, first, 0) == expect

@@ -82,3 +82,64 @@ def test_rejects_bad_arguments(oracle_mod):
         oracle_mod.placement_scan(5, [127], [127])
     with pytest.raises(ValueError):
         oracle_mod.placement_scan(1, [255], [127])
+
+
+def test_vector_values_agree_with_single_evaluations(oracle_mod):
+    v = oracle_mod.placement_values(2, 254, 3)
+    rng = np.random.default_rng(4)
+    for t in rng.integers(0, 1 << 16, size=64):
+        pre, post, rn = oracle_mod.placement_eval(2, 254, 3, int(t))
+        assert _same(pre, v[t, 0]) and _same(post, v[t, 1]) and _same(rn, v[t, 2])
+
+
+def _e2m1(code):
+    mag = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0][code & 7]
+    return -mag if code & 8 else mag
+
+
+def test_rn_is_the_exact_rational_value_rounded_once(oracle_mod):
+    """The exact value sum a_i b_i * 2^(sa+sb-254) is a multiple of 2^(sa+sb-256)
+    with at most 10 significant bits, so Python's exact Fraction -> float is exact
+    and numpy's binary32 conversion rounds it once (to nearest even, subnormals and
+    overflow to infinity included): an independent statement of rn."""
+    from fractions import Fraction
+    rng = np.random.default_rng(17)
+    for _ in range(400):
+        k = int(rng.integers(1, 4))
+        sa, sb = int(rng.integers(0, 255)), int(rng.integers(0, 255))
+        a = [int(x) for x in rng.integers(0, 16, size=k)]
+        b = [int(x) for x in rng.integers(0, 16, size=k)]
+        exact = sum(Fraction(_e2m1(x)) * Fraction(_e2m1(y)) for x, y in zip(a, b)) * Fraction(2) ** (sa + sb - 254)
+        with np.errstate(over="ignore"):
+            want = float(np.float32(float(exact)))
+        _, _, rn = oracle_mod.placement_eval(k, sa, sb, oracle_mod.placement_tuple(k, a, b))
+        assert _same(rn, want), (k, sa, sb, a, b, rn, want)
+
+
+@pytest.mark.parametrize("sa,sb", [(254, 127), (0, 30), (250, 1), (127, 127)])
+def test_counts_are_recounts_of_single_evaluations(oracle_mod, sa, sb):
+    """Brute force: the scan's counts and first counterexample equal a recount of
+    every tuple's individually evaluated values."""
+    v = oracle_mod.placement_values(2, sa, sb)
+    pre, post, rn = v[:, 0], v[:, 1], v[:, 2]
+
+    def same(x, y):
+        return (np.isnan(x) & np.isnan(y)) | (x == y)
+    d = ~same(pre, post)
+    counts, first = oracle_mod.placement_scan(2, [sa], [sb])
+    assert counts[0].tolist() == [int(d.sum()), int(same(pre, rn).sum()), int(same(post, rn).sum())]
+    assert first[0] == (int(np.argmax(d)) if d.any() else -1)
+
+
+@pytest.mark.parametrize("sa,sb", [(254, 3), (0, 200), (126, 129)])
+def test_pre_and_rn_are_symmetric_in_the_operands(oracle_mod, sa, sb):
+    """Swapping the operands (codes and scales) leaves every product (a f_a)(b f_b)
+    and the exact value unchanged, so pre and rn of tuple (a, b) at (sa, sb) equal
+    those of (b, a) at (sb, sa); post is not symmetric (f_a is applied first)."""
+    v1 = oracle_mod.placement_values(2, sa, sb)
+    v2 = oracle_mod.placement_values(2, sb, sa)
+    t = np.arange(1 << 16)
+    swapped = (t >> 8) | ((t & 255) << 8)
+    for col in (0, 2):
+        x, y = v1[:, col], v2[swapped, col]
+        assert ((np.isnan(x) & np.isnan(y)) | (x == y)).all()
