@@ -12,15 +12,22 @@ template <int BN>
 cudaError_t launch(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid, cudaStream_t s)
 {
     using C = Cfg<K_BF16, BN>;
+    if constexpr (BN == 256) {
+        if (p.sk_ctas > 0) {  // stream-K plans: the instantiation with fixup warps
+            mx_gemm_kernel<K_BF16, BN, false, false, true><<<grid, kThreadsSk, C::kSmemBytes, s>>>(p, ma, mb);
+            return cudaGetLastError();
+        }
+    }
     mx_gemm_kernel<K_BF16, BN><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
     return cudaGetLastError();
 }
 
-cudaLaunchConfig_t cluster2_config(int clusters, int smem, cudaStream_t s, cudaLaunchAttribute *attr)
+cudaLaunchConfig_t cluster2_config(int clusters, int smem, cudaStream_t s, cudaLaunchAttribute *attr,
+                                   int threads)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -36,9 +43,16 @@ template <int BN>
 cudaError_t launch_pair(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &msa,
                         const CUtensorMap &msb, int clusters, cudaStream_t s)
 {
-    auto kern = mx_gemm_pair_kernel<K_BF16, BN>;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<K_BF16, BN>::kSmemBytes, s, attr);
+    if constexpr (BN == 256) {
+        if (p.sk_ctas > 0) {  // stream-K plans: the instantiation with fixup warps
+            auto kern = mx_gemm_pair_kernel<K_BF16, BN, true>;
+            cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<K_BF16, BN>::kSmemBytes, s, attr, kThreadsSk);
+            return cudaLaunchKernelEx(&cfg, kern, p, ma, mb, msa, msb);
+        }
+    }
+    auto kern = mx_gemm_pair_kernel<K_BF16, BN>;
+    cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<K_BF16, BN>::kSmemBytes, s, attr, kThreads);
     return cudaLaunchKernelEx(&cfg, kern, p, ma, mb, msa, msb);
 }
 
@@ -50,7 +64,7 @@ int pair_max_clusters()
         cudaSuccess)
         return 0;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(1, CfgPair<K_BF16, BN>::kSmemBytes, nullptr, attr);
+    cudaLaunchConfig_t cfg = cluster2_config(1, CfgPair<K_BF16, BN>::kSmemBytes, nullptr, attr, kThreads);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
         return 0;
@@ -74,13 +88,18 @@ KernelInfo info()
 
 cudaError_t prepare_gemm_bf16()
 {
-    const void *k[6] = {(const void *)mx_gemm_kernel<K_BF16, 32>, (const void *)mx_gemm_kernel<K_BF16, 64>,
-                        (const void *)mx_gemm_kernel<K_BF16, 128>, (const void *)mx_gemm_kernel<K_BF16, 256>,
-                        (const void *)mx_gemm_pair_kernel<K_BF16, 128>, (const void *)mx_gemm_pair_kernel<K_BF16, 256>};
-    const int smem[6] = {Cfg<K_BF16, 32>::kSmemBytes, Cfg<K_BF16, 64>::kSmemBytes, Cfg<K_BF16, 128>::kSmemBytes,
-                         Cfg<K_BF16, 256>::kSmemBytes, CfgPair<K_BF16, 128>::kSmemBytes,
-                         CfgPair<K_BF16, 256>::kSmemBytes};
-    for (int i = 0; i < 6; ++i) {
+    const void *k[8] = {(const void *)mx_gemm_kernel<K_BF16, 32>,
+                        (const void *)mx_gemm_kernel<K_BF16, 64>,
+                        (const void *)mx_gemm_kernel<K_BF16, 128>,
+                        (const void *)mx_gemm_kernel<K_BF16, 256>,
+                        (const void *)mx_gemm_kernel<K_BF16, 256, false, false, true>,
+                        (const void *)mx_gemm_pair_kernel<K_BF16, 128>,
+                        (const void *)mx_gemm_pair_kernel<K_BF16, 256>,
+                        (const void *)mx_gemm_pair_kernel<K_BF16, 256, true>};
+    const int smem[8] = {Cfg<K_BF16, 32>::kSmemBytes,      Cfg<K_BF16, 64>::kSmemBytes,      Cfg<K_BF16, 128>::kSmemBytes,
+                         Cfg<K_BF16, 256>::kSmemBytes,     Cfg<K_BF16, 256>::kSmemBytes,     CfgPair<K_BF16, 128>::kSmemBytes,
+                         CfgPair<K_BF16, 256>::kSmemBytes, CfgPair<K_BF16, 256>::kSmemBytes};
+    for (int i = 0; i < 8; ++i) {
         cudaError_t e = cudaFuncSetAttribute(k[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
         if (e != cudaSuccess)
             return e;

@@ -10,15 +10,22 @@ template <int BN>
 cudaError_t launch(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid, cudaStream_t s)
 {
     using C = Cfg<K_MXFP8, BN>;
+    if constexpr (BN == 256) {
+        if (p.sk_ctas > 0) {  // stream-K plans: the instantiation with fixup warps
+            mx_gemm_kernel<K_MXFP8, BN, false, false, true><<<grid, kThreadsSk, C::kSmemBytes, s>>>(p, ma, mb);
+            return cudaGetLastError();
+        }
+    }
     mx_gemm_kernel<K_MXFP8, BN><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
     return cudaGetLastError();
 }
 
-cudaLaunchConfig_t cluster2_config(int clusters, int smem, cudaStream_t s, cudaLaunchAttribute *attr)
+cudaLaunchConfig_t cluster2_config(int clusters, int smem, cudaStream_t s, cudaLaunchAttribute *attr,
+                                   int threads)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -34,9 +41,16 @@ template <int BN>
 cudaError_t launch_pair(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &msa,
                         const CUtensorMap &msb, int clusters, cudaStream_t s)
 {
-    auto kern = mx_gemm_pair_kernel<K_MXFP8, BN>;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<K_MXFP8, BN>::kSmemBytes, s, attr);
+    if constexpr (BN == 256) {
+        if (p.sk_ctas > 0) {  // stream-K plans: the instantiation with fixup warps
+            auto kern = mx_gemm_pair_kernel<K_MXFP8, BN, true>;
+            cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<K_MXFP8, BN>::kSmemBytes, s, attr, kThreadsSk);
+            return cudaLaunchKernelEx(&cfg, kern, p, ma, mb, msa, msb);
+        }
+    }
+    auto kern = mx_gemm_pair_kernel<K_MXFP8, BN>;
+    cudaLaunchConfig_t cfg = cluster2_config(clusters, CfgPair<K_MXFP8, BN>::kSmemBytes, s, attr, kThreads);
     return cudaLaunchKernelEx(&cfg, kern, p, ma, mb, msa, msb);
 }
 
@@ -48,7 +62,7 @@ int pair_max_clusters()
         cudaSuccess)
         return 0;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(1, CfgPair<K_MXFP8, BN>::kSmemBytes, nullptr, attr);
+    cudaLaunchConfig_t cfg = cluster2_config(1, CfgPair<K_MXFP8, BN>::kSmemBytes, nullptr, attr, kThreads);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
         return 0;
@@ -60,7 +74,7 @@ cudaError_t launch_mc(const GemmParams &p, const CUtensorMap &ma, const CUtensor
 {
     auto kern = mx_gemm_kernel<K_MXFP8, BN, true>;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(clusters, Cfg<K_MXFP8, BN>::kSmemBytes, s, attr);
+    cudaLaunchConfig_t cfg = cluster2_config(clusters, Cfg<K_MXFP8, BN>::kSmemBytes, s, attr, kThreads);
     return cudaLaunchKernelEx(&cfg, kern, p, ma, mb);
 }
 
@@ -72,7 +86,7 @@ int mc_max_clusters()
         cudaSuccess)
         return 0;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(1, Cfg<K_MXFP8, BN>::kSmemBytes, nullptr, attr);
+    cudaLaunchConfig_t cfg = cluster2_config(1, Cfg<K_MXFP8, BN>::kSmemBytes, nullptr, attr, kThreads);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
         return 0;
@@ -106,20 +120,22 @@ KernelInfo info()
 // when a plan is created, never on the launch path).
 cudaError_t prepare_gemm_fp8()
 {
-    const void *single[4] = {(const void *)mx_gemm_kernel<K_MXFP8, 32>, (const void *)mx_gemm_kernel<K_MXFP8, 64>,
-                             (const void *)mx_gemm_kernel<K_MXFP8, 128>, (const void *)mx_gemm_kernel<K_MXFP8, 256>};
-    const int single_smem[4] = {Cfg<K_MXFP8, 32>::kSmemBytes, Cfg<K_MXFP8, 64>::kSmemBytes, Cfg<K_MXFP8, 128>::kSmemBytes,
-                                Cfg<K_MXFP8, 256>::kSmemBytes};
-    for (int i = 0; i < 4; ++i) {
+    const void *single[5] = {(const void *)mx_gemm_kernel<K_MXFP8, 32>, (const void *)mx_gemm_kernel<K_MXFP8, 64>,
+                             (const void *)mx_gemm_kernel<K_MXFP8, 128>, (const void *)mx_gemm_kernel<K_MXFP8, 256>,
+                             (const void *)mx_gemm_kernel<K_MXFP8, 256, false, false, true>};
+    const int single_smem[5] = {Cfg<K_MXFP8, 32>::kSmemBytes, Cfg<K_MXFP8, 64>::kSmemBytes, Cfg<K_MXFP8, 128>::kSmemBytes,
+                                Cfg<K_MXFP8, 256>::kSmemBytes, Cfg<K_MXFP8, 256>::kSmemBytes};
+    for (int i = 0; i < 5; ++i) {
         cudaError_t e = cudaFuncSetAttribute(single[i], cudaFuncAttributeMaxDynamicSharedMemorySize, single_smem[i]);
         if (e != cudaSuccess)
             return e;
     }
-    const void *cl[4] = {(const void *)mx_gemm_kernel<K_MXFP8, 128, true>, (const void *)mx_gemm_kernel<K_MXFP8, 256, true>,
-                         (const void *)mx_gemm_pair_kernel<K_MXFP8, 128>, (const void *)mx_gemm_pair_kernel<K_MXFP8, 256>};
-    const int cl_smem[4] = {Cfg<K_MXFP8, 128>::kSmemBytes, Cfg<K_MXFP8, 256>::kSmemBytes, CfgPair<K_MXFP8, 128>::kSmemBytes,
-                            CfgPair<K_MXFP8, 256>::kSmemBytes};
-    for (int i = 0; i < 4; ++i) {
+    const void *cl[5] = {(const void *)mx_gemm_kernel<K_MXFP8, 128, true>, (const void *)mx_gemm_kernel<K_MXFP8, 256, true>,
+                         (const void *)mx_gemm_pair_kernel<K_MXFP8, 128>, (const void *)mx_gemm_pair_kernel<K_MXFP8, 256>,
+                         (const void *)mx_gemm_pair_kernel<K_MXFP8, 256, true>};
+    const int cl_smem[5] = {Cfg<K_MXFP8, 128>::kSmemBytes, Cfg<K_MXFP8, 256>::kSmemBytes, CfgPair<K_MXFP8, 128>::kSmemBytes,
+                            CfgPair<K_MXFP8, 256>::kSmemBytes, CfgPair<K_MXFP8, 256>::kSmemBytes};
+    for (int i = 0; i < 5; ++i) {
         cudaError_t e = cudaFuncSetAttribute(cl[i], cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem[i]);
         if (e != cudaSuccess)
             return e;

@@ -16,7 +16,7 @@
 // layouts bring optimization close to hardware") is replaced here by a TMA ->
 // shared-memory ring -> tcgen05.mma pipeline with mbarrier hand-off.
 //
-// Warp roles (320 threads):
+// Warp roles (320 threads; 384 with the stream-K fixup warps):
 //   warp 0      TMA producer: per k-stage, A and B tiles (128-byte swizzle) and
 //               the tile-layout scale chunks (bulk copies) into ring slot s.
 //   warp 1      TMEM owner and MMA issuer: per k-stage, tcgen05.cp of the scale
@@ -27,6 +27,9 @@
 //               registers, releases the TMEM stage to the MMA warp at once, and
 //               only then converts (BF16) and stores to global (masked edges), so
 //               the stores overlap the next tile's MMAs.
+//   warps 10,11 stream-K fixup: add the partial sums of a tile cut between CTAs
+//               (posted by the epilogue when this CTA's segment arrived last)
+//               and store it, concurrently with everything else.
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // MXGEMM_ERR_DEVICE_TIMEOUT in *status, drains its in-flight copies and MMAs,
 // frees its TMEM and exits.
@@ -40,8 +43,14 @@
 
 namespace mxg {
 
-constexpr int kEpiWarps = 8;                 // epilogue warps (two per TMEM lane quarter)
-constexpr int kThreads = 64 + 32 * kEpiWarps; // producer warp + MMA warp + epilogue
+constexpr int kEpiWarps = 8;  // epilogue warps (two per TMEM lane quarter)
+constexpr int kFixWarps = 2;  // stream-K fixup warps (one per column half)
+constexpr int kFixWarp0 = 2 + kEpiWarps;
+constexpr int kThreads = 64 + 32 * kEpiWarps;         // producer + MMA + epilogue
+constexpr int kThreadsSk = kThreads + 32 * kFixWarps;  // ... + stream-K fixup warps
+// Both allow 168 registers a thread (10 or 12 warps over the four SM
+// sub-partitions), but the 128 x 256 single-CTA tile only fits without spills in
+// the 10-warp form, so it has a separate stream-K instantiation.
 constexpr int kBM = 128;            // MMA M (rows of the A role per tile)
 constexpr int kRowBytes = 128;      // bytes of one operand row per k-stage
 constexpr int kSfChunk = 512;       // bytes of one scale chunk (128 rows x 4 K-blocks)
@@ -440,59 +449,70 @@ __device__ __forceinline__ void store_row32_masked(const GemmParams &p, long lon
     }
 }
 
-// The sum of a cut tile's segments, run by its last arriving CTA (cold code,
-// kept out of line so that its registers do not count against the hot loops).
+// The fixup of a tile cut between CTAs that this CTA finishes (its segment
+// arrived last), handed from the epilogue to the fixup warps through one
+// shared-memory slot guarded by a full / empty mbarrier pair (the empty one
+// counts one arrival per fixup warp).  tile < 0: stop.
+struct SkFix {
+    int tile, tn, c_first, c_last, row0;
+};
+
+// Post a job (one thread).  Bounded: false if the slot did not free in time.
+__device__ __forceinline__ bool sk_post(SkFix &slot, const SkFix &job, uint32_t bar_full, uint32_t bar_empty,
+                                        uint32_t &posted, const volatile int *abort, uint64_t lim)
+{
+    if (!mbar_wait(bar_empty, (posted & 1u) ^ 1u, abort, lim))
+        return false;
+    slot = job;
+    mbar_arrive(bar_full);  // release: the job's fields are visible to the waiting warps
+    ++posted;
+    return true;
+}
+
+// Chunks c0 and c0 + 1 of a tile cut in exactly two segments, for this
+// thread's row: all 32 loads issued before any add (the fixup warps hold no
+// accumulator, so the registers go to loads in flight).  Same sums as
+// sk_fixup_chunk: (0 + first) + second.
 template <int BN, int kCols, int kChunks>
-__device__ __noinline__ void sk_fixup(const GemmParams &p, int tile, int tn, int c_first, int c_last, int halves,
-                                      int half, int row0, int h, int row_local, bool has_cols)
+__device__ __noinline__ void sk_fixup_two(const GemmParams &p, int tile, int tn, int c_first, int halves, int half,
+                                          int row0, int h, int row_local, int c0)
 {
     constexpr size_t kSlot = static_cast<size_t>(kBM) * BN;
     const int i = row0 + row_local;
-    if (!has_cols || i >= p.rows_a)
+    if (i >= p.rows_a)
         return;
+    const float4 *src[2];
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        const int cc = c_first + g;
+        const long long beg = p.sk_stages * cc / p.sk_ctas;
+        const int slot = (beg / p.kstages == tile - p.dp_tiles) ? 0 : 1;
+        src[g] = reinterpret_cast<const float4 *>(p.sk_partials +
+                                                  static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
+                 row_local;
+    }
+    float4 x[2][2][8];  // [segment][chunk][4-column group]
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                x[g][k][v] = __ldcg(src[g] + ((h * kChunks + c0 + k) * 8 + v) * kBM);
     const long long base_off = static_cast<long long>(i) * p.stride_i;
-#pragma unroll 1
-    for (int c = 0; c < kChunks; ++c) {
-        const int j0 = tn * BN + h * kCols + c * 32;
-        if (j0 >= p.rows_b) break;
-        float sum[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-            sum[e] = 0.0f;
-        // k order; the 32 columns of three segments are loaded at once (the sum
-        // is L2-latency bound: keep many loads in flight).  Past the last
-        // segment the loads repeat it and the adds are skipped.
-#pragma unroll 1
-        for (int cc0 = c_first; cc0 <= c_last; cc0 += 3) {
-            float4 x[3][8];
-#pragma unroll
-            for (int g = 0; g < 3; ++g) {
-                const int cc = min(cc0 + g, c_last);
-                const long long beg = p.sk_stages * cc / p.sk_ctas;
-                const int slot = (beg / p.kstages == tile - p.dp_tiles) ? 0 : 1;
-                const float4 *src = reinterpret_cast<const float4 *>(
-                                        p.sk_partials + static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
-                                    (h * kChunks + c) * 8 * kBM + row_local;
-#pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    x[g][v] = __ldcg(src + v * kBM);
-            }
-#pragma unroll
-            for (int g = 0; g < 3; ++g) {
-                const bool keep = cc0 + g <= c_last;  // a select, not a product: partials may hold NaN
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    sum[4 * v] += keep ? x[g][v].x : 0.0f;
-                    sum[4 * v + 1] += keep ? x[g][v].y : 0.0f;
-                    sum[4 * v + 2] += keep ? x[g][v].z : 0.0f;
-                    sum[4 * v + 3] += keep ? x[g][v].w : 0.0f;
-                }
-            }
-        }
+    for (int k = 0; k < 2; ++k) {
+        const int j0 = tn * BN + h * kCols + (c0 + k) * 32;
+        if (j0 >= p.rows_b)
+            break;
         uint32_t bits[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-            bits[e] = __float_as_uint(sum[e]);
+        for (int v = 0; v < 8; ++v) {
+            bits[4 * v] = __float_as_uint((0.0f + x[0][k][v].x) + x[1][k][v].x);
+            bits[4 * v + 1] = __float_as_uint((0.0f + x[0][k][v].y) + x[1][k][v].y);
+            bits[4 * v + 2] = __float_as_uint((0.0f + x[0][k][v].z) + x[1][k][v].z);
+            bits[4 * v + 3] = __float_as_uint((0.0f + x[0][k][v].w) + x[1][k][v].w);
+        }
         if (p.vec_ok && j0 + 32 <= p.rows_b)
             store_row32_vec(p, base_off + j0, bits);
         else
@@ -500,10 +520,111 @@ __device__ __noinline__ void sk_fixup(const GemmParams &p, int tile, int tn, int
     }
 }
 
+// One 32-column chunk of a cut tile, for this thread's row: the segments'
+// partials added in k order (deterministic), then stored to C.  Cold code,
+// kept out of line so that its registers do not count against the hot loops.
+template <int BN, int kCols, int kChunks>
+__device__ __noinline__ void sk_fixup_chunk(const GemmParams &p, int tile, int tn, int c_first, int c_last,
+                                            int halves, int half, int row0, int h, int row_local, int c)
+{
+    constexpr size_t kSlot = static_cast<size_t>(kBM) * BN;
+    const int i = row0 + row_local;
+    const int j0 = tn * BN + h * kCols + c * 32;
+    if (i >= p.rows_a || j0 >= p.rows_b)
+        return;
+    const long long base_off = static_cast<long long>(i) * p.stride_i;
+    float sum[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        sum[e] = 0.0f;
+    // three segments' 32 columns are loaded at once (many loads in flight)
+#pragma unroll 1
+    for (int cc0 = c_first; cc0 <= c_last; cc0 += 3) {
+        float4 x[3][8];
+#pragma unroll
+        for (int g = 0; g < 3; ++g) {
+            const int cc = min(cc0 + g, c_last);
+            const long long beg = p.sk_stages * cc / p.sk_ctas;
+            const int slot = (beg / p.kstages == tile - p.dp_tiles) ? 0 : 1;
+            const float4 *src = reinterpret_cast<const float4 *>(
+                                    p.sk_partials + static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
+                                (h * kChunks + c) * 8 * kBM + row_local;
+            if (cc0 + g <= c_last) {  // uniform over the CTA: no load past the last segment
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    x[g][v] = __ldcg(src + v * kBM);
+            } else {
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    x[g][v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < 3; ++g) {
+            const bool keep = cc0 + g <= c_last;  // a select, not a product: partials may hold NaN
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                sum[4 * v] += keep ? x[g][v].x : 0.0f;
+                sum[4 * v + 1] += keep ? x[g][v].y : 0.0f;
+                sum[4 * v + 2] += keep ? x[g][v].z : 0.0f;
+                sum[4 * v + 3] += keep ? x[g][v].w : 0.0f;
+            }
+        }
+    }
+    uint32_t bits[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        bits[e] = __float_as_uint(sum[e]);
+    if (p.vec_ok && j0 + 32 <= p.rows_b)
+        store_row32_vec(p, base_off + j0, bits);
+    else
+        store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), bits);
+}
+
+// The fixup warps: take jobs until the stop job (or an abort / time-out).
+// Warp fw adds column half fw of the CTA's 128 rows, four lane quarters.
+template <int BN, int kCols, int kChunks>
+__device__ __noinline__ void sk_fixup_warps(const GemmParams &p, const SkFix &slot, uint32_t bar_full,
+                                               uint32_t bar_empty, int halves, int half, volatile int *abort,
+                                               uint64_t lim)
+{
+    const int fw = static_cast<int>(threadIdx.x >> 5) - kFixWarp0;
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    for (uint32_t j = 0;; ++j) {
+        if (!warp_wait(bar_full, j & 1u, abort, lim)) {
+            if (lane == 0) record_timeout(p, abort);
+            return;
+        }
+        const SkFix job = slot;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar_empty);  // this warp holds the job: the slot may be reused
+        if (job.tile < 0)
+            return;
+        __threadfence();  // the other segments' partials, published before their arrivals
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            const int row_local = q * 32 + lane;
+            if (job.c_last == job.c_first + 1 && kChunks % 2 == 0) {
+#pragma unroll 1
+                for (int c = 0; c < kChunks; c += 2)
+                    sk_fixup_two<BN, kCols, kChunks>(p, job.tile, job.tn, job.c_first, halves, half, job.row0, fw,
+                                                     row_local, c);
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c)
+                    sk_fixup_chunk<BN, kCols, kChunks>(p, job.tile, job.tn, job.c_first, job.c_last, halves, half,
+                                                       job.row0, fw, row_local, c);
+            }
+        }
+    }
+}
+
 // Stream-K epilogue of one CTA's 128-row share of a tile cut between CTAs (or
 // CTA pairs): publish this segment's FP32 partial sum; if it is the last
-// segment of the tile to arrive, add every segment's partial in k order
-// (deterministic, this CTA's own re-read from its slot) and store C.
+// segment of the tile to arrive, post the tile's fixup to the fixup warps
+// (every segment's partial added in k order, this CTA's own re-read from its
+// slot).
 //   unit:   the CTA's (or pair's) stream-K index; slots are numbered
 //           ((2 * unit + w.slot) * halves + half) -- `halves` 128-row shares
 //           per tile (1: single CTA, 2: CTA pair), `half` this CTA's share;
@@ -513,7 +634,8 @@ __device__ __noinline__ void sk_fixup(const GemmParams &p, int tile, int tn, int
 template <int BN, int kCols, int kChunks>
 __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, const uint32_t (&r)[kChunks][32],
                                             int unit, int halves, int half, int row0, int h, int row_local,
-                                            bool has_cols, int *sk_last)
+                                            bool has_cols, int *sk_last, SkFix &fx, uint32_t fix_full,
+                                            uint32_t fix_empty, uint32_t &posted, volatile int *abort, uint64_t lim)
 {
     constexpr size_t kSlot = static_cast<size_t>(kBM) * BN;
     uint4 *const mine =
@@ -545,8 +667,12 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
     epi_bar_sync();  // sk_last is read before the next segment may rewrite it
     if (!last)
         return;
-    __threadfence();
-    sk_fixup<BN, kCols, kChunks>(p, w.tile, w.tn, c_first, c_last, halves, half, row0, h, row_local, has_cols);
+    if (threadIdx.x == 64) {
+        __threadfence();
+        const SkFix job{w.tile, w.tn, c_first, c_last, row0};
+        if (!sk_post(fx, job, fix_full, fix_empty, posted, abort, lim))
+            record_timeout(p, abort);
+    }
 }
 
 // GROUPED = true: the grouped (mixture-of-experts) form, tiles of all groups
@@ -557,8 +683,8 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
 // to both, so the pair reads that tile from L2 once.  Slot reuse then needs
 // both CTAs' MMAs done: `empty` counts two commits (each MMA thread commits to
 // both CTAs' barriers).
-template <int KIND, int BN, bool MC = false, bool GROUPED = false>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KIND, int BN, bool MC = false, bool GROUPED = false, bool SK = false>
+__global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b)
 {
@@ -569,6 +695,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t tmem_base_holder;
     __shared__ int abort_flag;
     __shared__ GroupTable gtab;  // grouped GEMM only
+    __shared__ uint64_t fix_bars[2];  // stream-K fixup hand-off: full, empty
+    __shared__ SkFix sk_fix;
+    constexpr bool kSk = SK;  // this instantiation runs stream-K plans (fixup warps 10, 11)
+    static_assert(!SK || (!MC && !GROUPED && BN == 256), "stream-K: plain 128 x 256 tiles only");
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -604,6 +734,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acce_bar(a), kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(smem_addr(&fix_bars[0]), 1);
+        mbar_init(smem_addr(&fix_bars[1]), kFixWarps);
         fence_mbar_init();
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b);
@@ -820,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             warp_wait(drain_bar, 0, no_abort, lim);
         }
-    } else {
+    } else if (warp >= 2 && warp < kFixWarp0) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;         // TMEM lane quarter this warp may access
         const int h = (warp - 2) >> 2;  // column half
@@ -829,6 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool has_cols = h * kCols < BN;
         __shared__ int sk_last;
         const int row_local = q * 32 + lane;
+        uint32_t sk_posted = 0;  // jobs posted to the fixup warps (thread 64)
         int it = 0;
         WorkIter wi;
         wi.init(p, first_unit, unit_step, gt, tok_tile);
@@ -869,11 +1002,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));
 
-            if (w.kind == 1) {
-                // stream-K segment: publish, and finish the tile if this CTA is last
-                sk_epilogue<BN, kCols, kChunks>(p, w, r, first_unit, 1, 0, tm * kBM, h, row_local, has_cols,
-                                                &sk_last);
-                continue;
+            if constexpr (kSk) {
+                if (w.kind == 1) {
+                    // stream-K segment: publish, and queue the tile's fixup if this CTA is last
+                    sk_epilogue<BN, kCols, kChunks>(p, w, r, first_unit, 1, 0, tm * kBM, h, row_local, has_cols,
+                                                    &sk_last, sk_fix, smem_addr(&fix_bars[0]),
+                                                    smem_addr(&fix_bars[1]), sk_posted, abort, lim);
+                    continue;
+                }
             }
 
             // Output limits and origin (computed after the release: fewer live registers)
@@ -893,6 +1029,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else
                         store_row32_masked(p, base_off, j0, min(32, g.lim_j - j0), r[c]);
                 }
+            }
+        }
+        if constexpr (kSk) {
+            if (p.sk_ctas > 0 && threadIdx.x == 64) {
+                const SkFix stop{-1, 0, 0, 0, 0};
+                if (!sk_post(sk_fix, stop, smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]), sk_posted, abort, lim))
+                    record_timeout(p, abort);
+            }
+        }
+    } else if (warp >= kFixWarp0) {
+        // ------------------------------------------------- stream-K fixup
+        if constexpr (kSk) {
+            if (p.sk_ctas > 0) {
+                constexpr int kCols = BN / 2;
+                sk_fixup_warps<BN, kCols, kCols / 32>(p, sk_fix, smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]),
+                                                      1, 0, abort, lim);
             }
         }
     }

@@ -60,8 +60,10 @@ struct CfgPair {
     static_assert(kColsUsed <= 512, "TMEM overflow");
 };
 
-template <int KIND, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+// SK = true: the instantiation for stream-K plans, with the two fixup warps
+// (384 threads); plans without cut tiles run the 320-thread form.
+template <int KIND, int BN, bool SK = false>
+__global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
                         const __grid_constant__ CUtensorMap map_sfb)
@@ -72,6 +74,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_holder;
     __shared__ int abort_flag;
+    __shared__ uint64_t fix_bars[2];  // stream-K fixup hand-off: full, empty
+    __shared__ SkFix sk_fix;
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -105,6 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acce_bar(a), 2 * kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(smem_addr(&fix_bars[0]), 1);
+        mbar_init(smem_addr(&fix_bars[1]), kFixWarps);
         fence_mbar_init();
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b);
@@ -288,13 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             warp_wait(drain_bar, 0, no_abort, lim);
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < kFixWarp0) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         constexpr int kCols = BN / 2;
         constexpr int kChunks = kCols / 32;
         __shared__ int sk_last;
+        uint32_t sk_posted = 0;  // jobs posted to the fixup warps (thread 64)
         int it = 0;
         WorkIter wi;
         wi.init(p, first_unit, unit_step);
@@ -329,11 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive_cluster(map_to_cta(acce_bar(acc), 0));
 
             const int row0 = (2 * tm + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
-            if (w.kind == 1) {
-                // stream-K segment: publish, and finish the tile if this pair is last
-                sk_epilogue<BN, kCols, kChunks>(p, w, r, first_unit, 2, static_cast<int>(rank), row0, h,
-                                                q * 32 + lane, true, &sk_last);
-                continue;
+            if constexpr (SK) {
+                if (w.kind == 1) {
+                    // stream-K segment: publish, and queue the tile's fixup if this pair is last
+                    sk_epilogue<BN, kCols, kChunks>(p, w, r, first_unit, 2, static_cast<int>(rank), row0, h,
+                                                    q * 32 + lane, true, &sk_last, sk_fix, smem_addr(&fix_bars[0]),
+                                                    smem_addr(&fix_bars[1]), sk_posted, abort, lim);
+                    continue;
+                }
             }
             const int i = row0 + q * 32 + lane;
             if (i < p.rows_a) {
@@ -349,6 +359,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), r[c]);
                 }
             }
+        }
+        if (SK && p.sk_ctas > 0 && threadIdx.x == 64) {
+            const SkFix stop{-1, 0, 0, 0, 0};
+            if (!sk_post(sk_fix, stop, smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]), sk_posted, abort, lim))
+                record_timeout(p, abort);
+        }
+    } else if (warp >= kFixWarp0) {
+        // ------------------------------------------------- stream-K fixup
+        if (SK && p.sk_ctas > 0) {
+            constexpr int kCols = BN / 2;
+            sk_fixup_warps<BN, kCols, kCols / 32>(p, sk_fix, smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]), 2,
+                                                  static_cast<int>(rank), abort, lim);
         }
     }
 

@@ -99,10 +99,16 @@ struct RelayoutJob {
     int blocks;   // ceil(rows / 128) * blocks_x
 };
 
-__global__ void __launch_bounds__(256) relayout_scales_kernel(RelayoutJob j0, RelayoutJob j1)
+// zero / nzero: words the GEMM that follows needs zeroed (its stream-K arrival
+// counters), cleared by block 0 so that no separate memset is launched.
+__global__ void __launch_bounds__(256)
+    relayout_scales_kernel(RelayoutJob j0, RelayoutJob j1, int *zero, int nzero)
 {
     __shared__ uint32_t tile[128][kRelayoutKt + 1];
     int b = blockIdx.x;
+    if (b == 0)
+        for (int i = threadIdx.x; i < nzero; i += 256)
+            zero[i] = 0;
     const RelayoutJob &j = (b < j0.blocks) ? j0 : j1;
     if (b >= j0.blocks)
         b -= j0.blocks;
@@ -145,13 +151,14 @@ RelayoutJob make_job(const uint8_t *src, int64_t rows, int64_t K, uint8_t *dst)
     return j;
 }
 
-cudaError_t launch_relayout(const RelayoutJob &a, const RelayoutJob *b, cudaStream_t s)
+cudaError_t launch_relayout(const RelayoutJob &a, const RelayoutJob *b, cudaStream_t s, int *zero = nullptr,
+                            int nzero = 0)
 {
     RelayoutJob none{};
     none.blocks = 0;
     const RelayoutJob &j1 = b ? *b : none;
     const int blocks = a.blocks + j1.blocks;
-    relayout_scales_kernel<<<blocks, 256, 0, s>>>(a, j1);
+    relayout_scales_kernel<<<blocks, 256, 0, s>>>(a, j1, zero, nzero);
     return cudaGetLastError();
 }
 
@@ -432,6 +439,9 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 2;
     if (flags & MXGEMM_PLAN_FORCE_SINGLE) mode = 0;
     if (mode != 0 && bn < 128) bn = 128;
+    // Stream-K runs on 256-wide tiles only (the instantiations with fixup
+    // warps): a forced stream-K plan takes them.
+    if ((flags & MXGEMM_PLAN_STREAMK) && mode != 1) bn = 256;
     p->mode = mode;
     p->bn = bn;
     // tiles_m counts the work units along the A role: 128-row tiles (single),
@@ -475,21 +485,29 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         const int64_t G = slots;
         const int64_t waves = ceil_div(tiles, G);
         const double dp_eff = static_cast<double>(tiles) / static_cast<double>(waves * G);
-        // Default: only long k-loops (>= 96 k-stages per tile), whose fixup hides
-        // behind a whole tile, and only when the last wave is under 90% full --
-        // measured: +10-18% at K = 25600, a loss at K <= 8192.
+        // Default: when the last wave is under 90% full, and the fixup of a cut
+        // tile (run by the CTA's fixup warps, ~30 us with the operand streams
+        // loading L2) hides behind the whole tiles each slot computes after its
+        // segment: long k-loops (>= 96 k-stages a tile), or >= 64 k-stages of
+        // whole tiles per slot.  Measured: +3-9% from K = 4096 (MXFP8 4096^3,
+        // 2048 x 8192 x 8192, 4096 x 10240 x 5120), +10-18% at K = 25600; a loss
+        // at MXFP4 4096^3 (48 k-stages of whole tiles per slot).
+        // Short k-loops also need every cut tile in exactly two segments (2 x the
+        // tiles of the last wave <= slots): three-way cuts take the slow general
+        // fixup (measured 1.7x slower at 128 x 51200 x 5120).
+        const int64_t dp_stages_per_slot = (tiles / G) * p->kstages;
+        const bool short_ok = dp_stages_per_slot >= 64 && 2 * (tiles % G) <= G;
         const bool want = (flags & MXGEMM_PLAN_STREAMK)
                               ? dp_eff < 0.95
-                              : (!(flags & MXGEMM_PLAN_NO_STREAMK) && tiles * 2 > slots && p->kstages >= 96 &&
-                                 dp_eff < 0.90);
+                              : (!(flags & MXGEMM_PLAN_NO_STREAMK) && p->bn == 256 && tiles * 2 > slots &&
+                                 (p->kstages >= 96 || short_ok) && dp_eff < 0.90);
         if (want) {
             const int64_t dp = (tiles / G) * G;
             const int64_t sk_stages = (tiles - dp) * p->kstages;
             const int64_t min_seg = 4;  // k-stages per stream-K unit, at least
             // Long k-loops spread the cut tiles' stages over every slot.  Short
-            // ones cut each tile in at most two segments: the last to arrive then
-            // adds two partial sums, which takes less than the whole tile it
-            // overlaps (three or more took longer and stalled the next tile).
+            // ones cut each tile in at most two segments, so that the fixup adds
+            // two partial sums (the fixup warps' fast path) and stays short.
             const int64_t units = p->kstages >= 96 ? std::min<int64_t>(G, sk_stages / min_seg)
                                                    : std::min<int64_t>(G, 2 * (tiles - dp));
             p->dp_tiles = static_cast<int>(dp);
@@ -657,8 +675,18 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
         jobs[njobs++] = make_job(SB, N, K, ws + plan->off_sfb);
         sfb = ws + plan->off_sfb;
     }
-    if (njobs > 0 && launch_relayout(jobs[0], njobs > 1 ? &jobs[1] : nullptr, s) != cudaSuccess)
+    // stream-K arrival counters start at zero: cleared by the relayout launch when
+    // there is one, else by a memset (the kernel leaves them zero when it
+    // completes, but the workspace may be fresh or hold an aborted launch's)
+    int *const sk_counters = reinterpret_cast<int *>(ws + plan->off_cnt);
+    const int sk_ncnt = plan->sk_ctas > 0 ? plan->sk_tiles * plan->sk_halves : 0;
+    if (njobs > 0) {
+        if (launch_relayout(jobs[0], njobs > 1 ? &jobs[1] : nullptr, s, sk_counters, sk_ncnt) != cudaSuccess)
+            return MXGEMM_ERR_CUDA;
+    } else if (sk_ncnt > 0 &&
+               cudaMemsetAsync(sk_counters, 0, static_cast<size_t>(sk_ncnt) * sizeof(int), s) != cudaSuccess) {
         return MXGEMM_ERR_CUDA;
+    }
 
     // (2) the GEMM, with operand roles per the plan
     const void *pa = plan->swap ? B : A;
@@ -702,12 +730,8 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     p.dp_tiles = plan->dp_tiles;
     p.sk_ctas = plan->sk_ctas;
     p.sk_stages = static_cast<long long>(plan->sk_tiles) * plan->kstages;
-    p.sk_counters = reinterpret_cast<int *>(ws + plan->off_cnt);
+    p.sk_counters = sk_counters;
     p.sk_partials = reinterpret_cast<float *>(ws + plan->off_skp);
-    if (plan->sk_ctas > 0 &&
-        cudaMemsetAsync(ws + plan->off_cnt, 0, static_cast<size_t>(plan->sk_tiles) * plan->sk_halves * sizeof(int),
-                        s) != cudaSuccess)
-        return MXGEMM_ERR_CUDA;
     const bool split = plan->splits > 1;
     const int osize = split ? 4 : (plan->out == MXGEMM_OUT_BF16 ? 2 : 4);
     if (split) {
