@@ -89,6 +89,7 @@ typedef enum {
 /* Run flags (mxgemm_run). */
 #define MXGEMM_RUN_SA_PRELAYOUT     (1u << 0)  /* SA is already in the tile layout    */
 #define MXGEMM_RUN_SB_PRELAYOUT     (1u << 1)  /* SB is already in the tile layout    */
+#define MXGEMM_RUN_PREPARED         (1u << 2)  /* mxgemm_prepare ran on this workspace */
 
 typedef struct mxgemm_plan *mxgemm_plan_t;
 
@@ -208,6 +209,26 @@ MXGEMM_API int mxgemm_quantize(int fmt, int in_dtype, const void *x, int64_t row
 MXGEMM_API int mxgemm_run(mxgemm_plan_t plan, const void *A, const uint8_t *SA,
                const void *B, const uint8_t *SB, void *C,
                void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream);
+
+/*
+ * Step (1) of mxgemm_run on its own: lays out whichever of SA / SB is not
+ * flagged MXGEMM_RUN_S{A,B}_PRELAYOUT into `workspace` and resets the plan's
+ * stream-K arrival counters there, in one launch on `stream` (a memset when
+ * both scales are pre-laid-out).  A following mxgemm_run on the same
+ * workspace and stream with MXGEMM_RUN_PREPARED (plus the same PRELAYOUT
+ * flags) then enqueues only the GEMM (and its split-K reduce): the scales laid
+ * out here are read from the workspace, so mxgemm_run's SA / SB arguments
+ * without a PRELAYOUT flag are not read and may be NULL.  Lets a caller time
+ * or schedule the two steps separately (the FlyDSL page's "layout copies" are
+ * step (1)).  Nothing else may use the workspace in between.
+ *   SA, SB:  row-major scales as for mxgemm_run (pre-laid-out ones not read;
+ *            all ignored for MXGEMM_FMT_BF16)
+ * Errors: MXGEMM_ERR_ARG (NULL plan, unknown flag, missing scales, another
+ * device current), MXGEMM_ERR_ALIGN, MXGEMM_ERR_WORKSPACE, MXGEMM_ERR_CUDA.
+ * mxgemm_run_noalloc rejects MXGEMM_RUN_PREPARED (its scratch is internal).
+ */
+MXGEMM_API int mxgemm_prepare(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB,
+                   void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream);
 
 /*
  * Synchronise `stream` and return the library's sticky device status on the

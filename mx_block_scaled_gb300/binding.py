@@ -41,6 +41,7 @@ MXGEMM_PLAN_NO_STREAMK = 1 << 16
 
 MXGEMM_RUN_SA_PRELAYOUT = 1 << 0
 MXGEMM_RUN_SB_PRELAYOUT = 1 << 1
+MXGEMM_RUN_PREPARED = 1 << 2
 
 MXGEMM_IN_F32 = 1
 MXGEMM_IN_BF16 = 2
@@ -60,6 +61,7 @@ SIGNATURES = [
     ("mxgemm_quantize", ctypes.c_int,
      [ctypes.c_int, ctypes.c_int, _P, _I64, _I64, _P, _P, ctypes.c_uint32, _P]),
     ("mxgemm_run", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
+    ("mxgemm_prepare", ctypes.c_int, [_P, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     ("mxgemm_run_noalloc", ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_uint32, _P]),
     ("mxgemm_device_status", ctypes.c_int, [_P, ctypes.c_int]),
     ("mxgemm_selftest_stall", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -142,6 +144,10 @@ def mxgemm_quantize(fmt: int, in_dtype: int, x_ptr: int, rows: int, K: int, code
 def mxgemm_run(plan, A_ptr: int, SA_ptr: int, B_ptr: int, SB_ptr: int, C_ptr: int,
                ws_ptr: int, ws_bytes: int, run_flags: int, stream: int) -> int:
     return _lib.mxgemm_run(plan, A_ptr, SA_ptr, B_ptr, SB_ptr, C_ptr, ws_ptr, ws_bytes, run_flags, stream)
+
+
+def mxgemm_prepare(plan, SA_ptr: int, SB_ptr: int, ws_ptr: int, ws_bytes: int, run_flags: int, stream: int) -> int:
+    return _lib.mxgemm_prepare(plan, SA_ptr, SB_ptr, ws_ptr, ws_bytes, run_flags, stream)
 
 
 def mxgemm_run_noalloc(plan, A_ptr: int, SA_ptr: int, B_ptr: int, SB_ptr: int, C_ptr: int,
@@ -234,6 +240,16 @@ class Plan:
                         self.workspace.data_ptr(), self.ws_bytes, run_flags, _stream_handle(stream))
         _check(st, "mxgemm_run")
         return C
+
+    def prepare(self, SA, SB, run_flags: int = 0, stream=None):
+        """Step (1) alone: lay out the scales not flagged pre-laid-out into this
+        plan's workspace and reset its stream-K counters; follow with
+        run(..., run_flags=MXGEMM_RUN_PREPARED | <same flags>)."""
+        sa = SA.data_ptr() if SA is not None else 0
+        sb = SB.data_ptr() if SB is not None else 0
+        st = mxgemm_prepare(self.handle, sa, sb, self.workspace.data_ptr(), self.ws_bytes, run_flags,
+                            _stream_handle(stream))
+        _check(st, "mxgemm_prepare")
 
     def __del__(self):
         h = getattr(self, "handle", None)

@@ -630,6 +630,34 @@ int mxgemm_quantize(int fmt, int in_dtype, const void *x, int64_t rows, int64_t 
                                                                                                    : MXGEMM_ERR_CUDA;
 }
 
+// Phase 1 of a run: the relayout of whichever scales are not pre-laid-out into
+// the workspace, in one launch that also zeroes the stream-K arrival counters
+// (a memset when nothing is laid out).  The kernel leaves the counters zero
+// when it completes, but the workspace may be fresh or hold an aborted
+// launch's.  Arguments checked by the callers.
+static int prepare_impl(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB, uint8_t *ws, uint32_t run_flags,
+                        cudaStream_t s)
+{
+    RelayoutJob jobs[2];
+    int njobs = 0;
+    if (plan->fmt != MXGEMM_FMT_BF16) {
+        if (!(run_flags & MXGEMM_RUN_SA_PRELAYOUT))
+            jobs[njobs++] = make_job(SA, plan->M, plan->K, ws + plan->off_sfa);
+        if (!(run_flags & MXGEMM_RUN_SB_PRELAYOUT))
+            jobs[njobs++] = make_job(SB, plan->N, plan->K, ws + plan->off_sfb);
+    }
+    int *const sk_counters = reinterpret_cast<int *>(ws + plan->off_cnt);
+    const int sk_ncnt = plan->sk_ctas > 0 ? plan->sk_tiles * plan->sk_halves : 0;
+    if (njobs > 0) {
+        if (launch_relayout(jobs[0], njobs > 1 ? &jobs[1] : nullptr, s, sk_counters, sk_ncnt) != cudaSuccess)
+            return MXGEMM_ERR_CUDA;
+    } else if (sk_ncnt > 0 &&
+               cudaMemsetAsync(sk_counters, 0, static_cast<size_t>(sk_ncnt) * sizeof(int), s) != cudaSuccess) {
+        return MXGEMM_ERR_CUDA;
+    }
+    return MXGEMM_OK;
+}
+
 static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB, void *C,
                     void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream, int test_stall,
                     unsigned long long timeout_ns)
@@ -637,11 +665,15 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     if (!plan || !A || !B || !C)
         return MXGEMM_ERR_ARG;
     const bool bf16 = plan->fmt == MXGEMM_FMT_BF16;  // no scales: SA and SB are not read
-    if (!bf16 && (!SA || !SB))
+    if (run_flags & ~(MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT | MXGEMM_RUN_PREPARED))
         return MXGEMM_ERR_ARG;
-    if (run_flags & ~(MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT))
+    // after mxgemm_prepare, scales that were not pre-laid-out are in the workspace
+    const bool prepared = (run_flags & MXGEMM_RUN_PREPARED) != 0;
+    const bool read_sa = !bf16 && (!prepared || (run_flags & MXGEMM_RUN_SA_PRELAYOUT));
+    const bool read_sb = !bf16 && (!prepared || (run_flags & MXGEMM_RUN_SB_PRELAYOUT));
+    if ((read_sa && !SA) || (read_sb && !SB))
         return MXGEMM_ERR_ARG;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (!bf16 && (!aligned16(SA) || !aligned16(SB))))
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (read_sa && !aligned16(SA)) || (read_sb && !aligned16(SB)))
         return MXGEMM_ERR_ALIGN;
     if (plan->ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan->ws_bytes))
         return MXGEMM_ERR_WORKSPACE;
@@ -661,31 +693,17 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
     const int64_t row_bytes = fp4 ? K / 2 : bf16 ? 2 * K : K;
 
-    // (1) scale relayout for whichever operand is not pre-laid-out (one launch)
-    const uint8_t *sfa = SA, *sfb = SB;
-    RelayoutJob jobs[2];
-    int njobs = 0;
+    // (1) scale relayout for whichever operand is not pre-laid-out, and the
+    // stream-K counter reset -- unless mxgemm_prepare did both already
     if (bf16)
-        run_flags = MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT;  // nothing to lay out
-    if (!(run_flags & MXGEMM_RUN_SA_PRELAYOUT)) {
-        jobs[njobs++] = make_job(SA, M, K, ws + plan->off_sfa);
-        sfa = ws + plan->off_sfa;
-    }
-    if (!(run_flags & MXGEMM_RUN_SB_PRELAYOUT)) {
-        jobs[njobs++] = make_job(SB, N, K, ws + plan->off_sfb);
-        sfb = ws + plan->off_sfb;
-    }
-    // stream-K arrival counters start at zero: cleared by the relayout launch when
-    // there is one, else by a memset (the kernel leaves them zero when it
-    // completes, but the workspace may be fresh or hold an aborted launch's)
+        run_flags = (run_flags & MXGEMM_RUN_PREPARED) | MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT;
+    const uint8_t *sfa = (run_flags & MXGEMM_RUN_SA_PRELAYOUT) ? SA : ws + plan->off_sfa;
+    const uint8_t *sfb = (run_flags & MXGEMM_RUN_SB_PRELAYOUT) ? SB : ws + plan->off_sfb;
     int *const sk_counters = reinterpret_cast<int *>(ws + plan->off_cnt);
-    const int sk_ncnt = plan->sk_ctas > 0 ? plan->sk_tiles * plan->sk_halves : 0;
-    if (njobs > 0) {
-        if (launch_relayout(jobs[0], njobs > 1 ? &jobs[1] : nullptr, s, sk_counters, sk_ncnt) != cudaSuccess)
-            return MXGEMM_ERR_CUDA;
-    } else if (sk_ncnt > 0 &&
-               cudaMemsetAsync(sk_counters, 0, static_cast<size_t>(sk_ncnt) * sizeof(int), s) != cudaSuccess) {
-        return MXGEMM_ERR_CUDA;
+    if (!(run_flags & MXGEMM_RUN_PREPARED)) {
+        st = prepare_impl(plan, SA, SB, ws, run_flags, s);
+        if (st != MXGEMM_OK)
+            return st;
     }
 
     // (2) the GEMM, with operand roles per the plan
@@ -793,6 +811,34 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     return MXGEMM_OK;
 }
 
+int mxgemm_prepare(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB, void *workspace, size_t ws_bytes,
+                   uint32_t run_flags, void *stream)
+{
+    if (!plan)
+        return MXGEMM_ERR_ARG;
+    if (run_flags & ~(MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT))
+        return MXGEMM_ERR_ARG;
+    const bool bf16 = plan->fmt == MXGEMM_FMT_BF16;
+    const bool read_sa = !bf16 && !(run_flags & MXGEMM_RUN_SA_PRELAYOUT);
+    const bool read_sb = !bf16 && !(run_flags & MXGEMM_RUN_SB_PRELAYOUT);
+    if ((read_sa && !SA) || (read_sb && !SB))
+        return MXGEMM_ERR_ARG;
+    if ((read_sa && !aligned16(SA)) || (read_sb && !aligned16(SB)))
+        return MXGEMM_ERR_ALIGN;
+    if (plan->ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan->ws_bytes))
+        return MXGEMM_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace))
+        return MXGEMM_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    int st = device_info(&dev);
+    if (st != MXGEMM_OK)
+        return st;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device)
+        return MXGEMM_ERR_ARG;
+    return prepare_impl(plan, SA, SB, static_cast<uint8_t *>(workspace), run_flags, static_cast<cudaStream_t>(stream));
+}
+
 int mxgemm_run(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB, void *C,
                void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream)
 {
@@ -822,7 +868,7 @@ std::mutex g_noalloc_mutex;
 int mxgemm_run_noalloc(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB,
                        void *C, uint32_t run_flags, void *stream)
 {
-    if (!plan)
+    if (!plan || (run_flags & MXGEMM_RUN_PREPARED))  // the scratch is not the caller's to prepare
         return MXGEMM_ERR_ARG;
     if (plan->ws_bytes > MXGEMM_NOALLOC_SCRATCH_BYTES)
         return MXGEMM_ERR_WORKSPACE;

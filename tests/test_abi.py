@@ -157,3 +157,9 @@ def test_bf16_plan_validation(lib, M, N, K, flags, expect):
 ])
 def test_placement_scan_validates_before_touching_the_device(lib, k, npairs, sa, sb, counts, first, expect):
     assert lib.mxgemm_placement_scan(k, sa, sb, npairs, counts, first, 0) == expect
+
+
+def test_prepare_rejects_a_null_plan_on_the_host(lib):
+    """mxgemm_prepare checks its arguments before any CUDA call."""
+    assert lib.mxgemm_prepare(None, 0, 0, 0, 0, 0, None) == lib.MXGEMM_ERR_ARG
+    assert lib.mxgemm_prepare(None, 0, 0, 0, 0, lib.MXGEMM_RUN_PREPARED, None) == lib.MXGEMM_ERR_ARG

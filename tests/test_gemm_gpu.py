@@ -351,3 +351,38 @@ def test_stalled_kernel_times_out_and_context_survives():
     out = plan.run(A1, Srow, A1, Srow)
     b.check_device_status()
     assert torch.all(out == float(K))
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+@pytest.mark.parametrize("plan_flags", [0, SK])
+def test_prepare_then_run_equals_run(oracle_mod, fmt, plan_flags):
+    """mxgemm_prepare (scale relayout into the workspace + stream-K counter reset)
+    followed by mxgemm_run with MXGEMM_RUN_PREPARED gives the same exact result
+    as mxgemm_run alone, for every choice of pre-laid-out operands, and again
+    on a second prepared run over the same workspace."""
+    import torch
+    b = lib()
+    M, N, K = 1024, 1536, 4096
+    rng = np.random.default_rng([fmt, plan_flags, 3])
+    A, SA = small_int_codes(rng, M, K, fmt)
+    B, SB = small_int_codes(rng, N, K, fmt)
+    ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
+    plan = b.Plan(M, N, K, fmt, OUT_F32, plan_flags)
+    if plan_flags & SK:
+        assert "/0 " not in plan.describe().split("streamk=")[1][:12], plan.describe()
+    dA, dB, dSA, dSB = to_dev(A), to_dev(B), to_dev(SA), to_dev(SB)
+    tSA, tSB = b.relayout_scales(dSA, M, K), b.relayout_scales(dSB, N, K)
+    C0 = plan.run(dA, dSA, dB, dSB)
+    torch.cuda.synchronize()
+    assert (C0.double().cpu().numpy() == ref).all()
+    for rf in (0, b.MXGEMM_RUN_SB_PRELAYOUT, b.MXGEMM_RUN_SA_PRELAYOUT,
+               b.MXGEMM_RUN_SA_PRELAYOUT | b.MXGEMM_RUN_SB_PRELAYOUT):
+        sa_pre = rf & b.MXGEMM_RUN_SA_PRELAYOUT
+        sb_pre = rf & b.MXGEMM_RUN_SB_PRELAYOUT
+        for _ in range(2):
+            plan.prepare(None if sa_pre else dSA, None if sb_pre else dSB, rf)
+            C = plan.run(dA, tSA if sa_pre else None, dB, tSB if sb_pre else None,
+                         run_flags=rf | b.MXGEMM_RUN_PREPARED)
+            b.check_device_status()
+            torch.cuda.synchronize()
+            assert (C.double().cpu().numpy() == ref).all(), (rf, plan.describe())

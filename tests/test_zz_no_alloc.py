@@ -74,3 +74,14 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
         assert st == b.MXGEMM_ERR_WORKSPACE
     finally:
         b.mxgemm_plan_destroy(h)
+
+
+def test_noalloc_rejects_a_prepared_run():
+    """mxgemm_run_noalloc's scratch is internal, so MXGEMM_RUN_PREPARED cannot apply."""
+    import torch
+    b = lib()
+    plan = b.Plan(256, 256, 256, FMT_MXFP8, OUT_F32)
+    p = plan.workspace.data_ptr()
+    st = b.mxgemm_run_noalloc(plan.handle, p, p, p, p, p, b.MXGEMM_RUN_PREPARED,
+                              torch.cuda.current_stream().cuda_stream)
+    assert st == b.MXGEMM_ERR_ARG
