@@ -774,6 +774,61 @@ def run_placement_sweep(args):
     return 0
 
 
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def run_oracle_sweep(args):
+    """The CPU oracle (the baseline, not a target) on the host cores: the full
+    product for the 256^3 and 4096^3 cases and every shape with M <= 256, the
+    first rows of C extrapolated linearly for larger M (labelled), and a
+    single-core rate on 4096^3.  Operand values do not change the oracle's
+    speed; seeded finite random codes stand in for the workloads' values."""
+    import numpy as np
+    import oracle
+    from mx_block_scaled_gb300.inputs import FMT_BY_NAME, WORKLOADS, finite_uniform_codes, workload_cases
+    threads = oracle.num_threads()
+    print(json.dumps({"kind": "oracle", "cpu": _cpu_model(), "threads": threads}), flush=True)
+    seen = set()
+    for name in WORKLOADS:
+        for fmt_name, si, nki, M, N, K in workload_cases(name):
+            if (fmt_name, M, N, K) in seen:
+                continue
+            seen.add((fmt_name, M, N, K))
+            fmt = FMT_BY_NAME[fmt_name]
+            rng = np.random.default_rng([M, N, K, fmt])
+            full = M <= 256 or (M, N, K) == (4096, 4096, 4096)
+            rows = M if full else min(M, 64)
+            A, SA = finite_uniform_codes(rng, rows, K, fmt, 120, 134)
+            B, SB = finite_uniform_codes(rng, N, K, fmt, 120, 134)
+            t0 = time.perf_counter()
+            oracle.gemm(fmt, A, SA, B, SB, K, with_abs=False)
+            dt = time.perf_counter() - t0
+            sec = dt * (M / rows)
+            print(json.dumps({"kind": "oracle", "workload": name, "format": fmt_name, "M": M, "N": N, "K": K,
+                              "seconds": sec, "mode": "full" if full else f"extrapolated from {rows} rows",
+                              "threads": threads, "tflops": 2.0 * M * N * K / sec / 1e12}), flush=True)
+    # one core, 4096^3 (first 64 rows, extrapolated)
+    rng = np.random.default_rng(1)
+    A, SA = finite_uniform_codes(rng, 64, 4096, FMT_BY_NAME["mxfp8"], 120, 134)
+    B, SB = finite_uniform_codes(rng, 4096, 4096, FMT_BY_NAME["mxfp8"], 120, 134)
+    t0 = time.perf_counter()
+    oracle.gemm(FMT_BY_NAME["mxfp8"], A, SA, B, SB, 4096, with_abs=False, nthreads=1)
+    dt = time.perf_counter() - t0
+    print(json.dumps({"kind": "oracle", "workload": "mxfp8_square_4096", "format": "mxfp8", "M": 4096, "N": 4096,
+                      "K": 4096, "seconds": dt * 64, "mode": "extrapolated from 64 rows", "threads": 1,
+                      "tflops": 2.0 * 4096 ** 3 / (dt * 64) / 1e12}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -796,6 +851,8 @@ def main():
                     help="time the BF16 NT GEMM (and cuBLAS beside it) over the dense workload shapes")
     ap.add_argument("--grouped-sweep", action="store_true",
                     help="time the grouped (mixture-of-experts) MX GEMM over the grouped workloads")
+    ap.add_argument("--oracle-sweep", action="store_true",
+                    help="time the CPU oracle over the workload shapes (full for M <= 256, else extrapolated)")
     ap.add_argument("--placement-sweep", action="store_true",
                     help="run the scale-placement checker over every scale pair for k = 1, 2, 3")
     args = ap.parse_args()
@@ -811,6 +868,8 @@ def main():
         return run_bf16_sweep(args)
     if args.placement_sweep:
         return run_placement_sweep(args)
+    if args.oracle_sweep:
+        return run_oracle_sweep(args)
     if args.sweep or args.shape:
         return run_sweep(args)
     return run_ours(args)

@@ -485,22 +485,25 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         const int64_t G = slots;
         const int64_t waves = ceil_div(tiles, G);
         const double dp_eff = static_cast<double>(tiles) / static_cast<double>(waves * G);
-        // Default: when the last wave is under 90% full, and the fixup of a cut
-        // tile (run by the CTA's fixup warps, ~30 us with the operand streams
-        // loading L2) hides behind the whole tiles each slot computes after its
-        // segment: long k-loops (>= 96 k-stages a tile), or >= 64 k-stages of
-        // whole tiles per slot.  Measured: +3-9% from K = 4096 (MXFP8 4096^3,
-        // 2048 x 8192 x 8192, 4096 x 10240 x 5120), +10-18% at K = 25600; a loss
-        // at MXFP4 4096^3 (48 k-stages of whole tiles per slot).
-        // Short k-loops also need every cut tile in exactly two segments (2 x the
-        // tiles of the last wave <= slots): three-way cuts take the slow general
-        // fixup (measured 1.7x slower at 128 x 51200 x 5120).
-        const int64_t dp_stages_per_slot = (tiles / G) * p->kstages;
-        const bool short_ok = dp_stages_per_slot >= 64 && 2 * (tiles % G) <= G;
+        // Default (256-wide tiles, last wave under 90% full): the fixup of a cut
+        // tile (run by the CTA's fixup warps, ~30 us with every SM streaming
+        // operands into L2; longer for three or more partials) must hide behind
+        // the whole tiles each slot computes after its segment, so
+        //  - halves: each tile of the last wave cut into two segments (2 x its
+        //    tiles <= slots), when the whole tiles give every slot >= 96
+        //    k-stages (MXFP8 4096^3: +6.5%; MXFP4 4096^3 at 48: a loss);
+        //  - spread: the last wave's k-stages over every slot (cuts of any
+        //    length), for long k-loops (>= 96 k-stages a tile) with >= 3 waves
+        //    of whole tiles (K = 25600: +10%).
+        // With no full wave of whole tiles (every tile cut) the fixups run
+        // back to back after the segments: measured 1.4x slower.
+        const int64_t full_waves = tiles / G;
+        const bool spread = p->kstages >= 96 && full_waves >= 3;
+        const bool halves = full_waves * p->kstages >= 96 && 2 * (tiles % G) <= G;
         const bool want = (flags & MXGEMM_PLAN_STREAMK)
                               ? dp_eff < 0.95
-                              : (!(flags & MXGEMM_PLAN_NO_STREAMK) && p->bn == 256 && tiles * 2 > slots &&
-                                 (p->kstages >= 96 || short_ok) && dp_eff < 0.90);
+                              : (!(flags & MXGEMM_PLAN_NO_STREAMK) && p->bn == 256 && dp_eff < 0.90 &&
+                                 (spread || halves));
         if (want) {
             const int64_t dp = (tiles / G) * G;
             const int64_t sk_stages = (tiles - dp) * p->kstages;
@@ -508,8 +511,9 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
             // Long k-loops spread the cut tiles' stages over every slot.  Short
             // ones cut each tile in at most two segments, so that the fixup adds
             // two partial sums (the fixup warps' fast path) and stays short.
-            const int64_t units = p->kstages >= 96 ? std::min<int64_t>(G, sk_stages / min_seg)
-                                                   : std::min<int64_t>(G, 2 * (tiles - dp));
+            const bool spread_units = (flags & MXGEMM_PLAN_STREAMK) ? p->kstages >= 96 : spread;
+            const int64_t units = spread_units ? std::min<int64_t>(G, sk_stages / min_seg)
+                                               : std::min<int64_t>(G, 2 * (tiles - dp));
             p->dp_tiles = static_cast<int>(dp);
             p->sk_tiles = static_cast<int>(tiles - dp);
             p->sk_ctas = static_cast<int>(std::max<int64_t>(1, std::min(units, sk_stages / min_seg)));
