@@ -57,6 +57,23 @@ def dist_env():
     return ws, rank, local
 
 
+def slowest_rank_ms(ms: float, ws: int, device) -> float:
+    """Replicas: every rank times the same work; the job's time is the slowest
+    rank's (all_reduce MAX over the default process group when ws > 1)."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, ws: int, ms_per_step: float) -> float:
+    """Whole-job throughput: all ranks' FLOPs over the slowest rank's step time."""
+    return flops_per_rank_step * ws / (ms_per_step / 1e3) / 1e12
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -305,13 +322,9 @@ def run_ours(args):
     total_ms = evs[0][0].elapsed_time(evs[-1][2])
     gemm_ms = [e[1].elapsed_time(e[2]) for e in evs]
     relayout_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    ms_per_step = total_ms / args.steps
-    if ws > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = slowest_rank_ms(total_ms / args.steps, ws, dev)
     flops = 2.0 * M * N * K
-    value = flops * ws / (ms_per_step / 1e3) / 1e12
+    value = job_tflops(flops, ws, ms_per_step)
 
     # ---- e2e: pinned host inputs -> device -> mxgemm_run (relayout + GEMM) -> host C
     e2e = None
@@ -344,13 +357,9 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if ws > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = slowest_rank_ms(e0.elapsed_time(e1) / n_e2e, ws, dev)
         mx.check_device_status()
-        e2e = {"value": flops * ws / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_tflops(flops, ws, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(A.nbytes + B.nbytes + SA.nbytes + SB.nbytes),
                "d2h_bytes_per_step": int(M * N * out_bytes), "ms_per_step": e2e_ms}
 
