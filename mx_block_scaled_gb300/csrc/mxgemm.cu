@@ -525,10 +525,29 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         splits = 1;
     if (splits == 0) {
         splits = 1;
+        const int64_t by_k = std::max<int64_t>(1, p->kstages / 4);
         if (tiles * 2 <= slots) {
             const int64_t by_sms = slots / tiles;
-            const int64_t by_k = std::max<int64_t>(1, p->kstages / 4);
             splits = static_cast<int>(std::min<int64_t>(std::min(by_sms, by_k), 32));
+        } else if (tiles < 2 * slots) {
+            // Between half a wave and two waves of tiles: split K so that the
+            // units fill the slots better (time ~ waves(s) / s), as long as the
+            // FP32 partials stay within 10% of the operand bytes -- the
+            // weight-streaming decode shapes (M <= 64), where a wave of 80
+            // tiles on 152 SMs left half the SMs without a weight stream.
+            const double e = fmt == MXGEMM_FMT_MXFP4_E2M1 ? 0.5 : bf16 ? 2.0 : 1.0;
+            const double operand_bytes = static_cast<double>(M + N) * static_cast<double>(K) * e;
+            const double split_bytes = 4.0 * static_cast<double>(M) * static_cast<double>(N);
+            const int64_t by_traffic = static_cast<int64_t>(0.1 * operand_bytes / split_bytes);
+            const int64_t max_s = std::min<int64_t>(std::min(by_k, by_traffic), 32);
+            double best = static_cast<double>(ceil_div(tiles, slots));
+            for (int64_t s2 = 2; s2 <= max_s; ++s2) {
+                const double t = static_cast<double>(ceil_div(tiles * s2, slots)) / static_cast<double>(s2);
+                if (t < 0.95 * best) {
+                    best = t;
+                    splits = static_cast<int>(s2);
+                }
+            }
         }
     }
     splits = std::max(1, std::min(splits, p->kstages));
