@@ -93,7 +93,6 @@ struct QTraits {
     static constexpr int kG = IN == kQuantInBf16 ? 4 : 2;        // chunks per unit
     static constexpr int kLoads = IN == kQuantInBf16 ? 1 : 2;    // 32-B loads per lane per chunk
     static constexpr int kInBytes = IN == kQuantInBf16 ? 2 : 4;
-    static constexpr int kCodeBytesPerLane = FMT == kQuantFmtMxfp8 ? 16 : 8;
 };
 
 template <int FMT, int IN>
