@@ -69,6 +69,26 @@ def slowest_rank_ms(ms: float, ws: int, device) -> float:
     return float(t.item())
 
 
+def versions() -> dict:
+    """Library, CUDA, driver and PyTorch versions of the run (recorded beside the plan)."""
+    import torch
+    out = {"torch": torch.__version__, "cuda_runtime": torch.version.cuda}
+    try:
+        from mx_block_scaled_gb300 import binding as mx
+        out["libmxgemm"] = int(mx.mxgemm_version())
+    except Exception:  # the line is still useful without it
+        pass
+    try:
+        q = subprocess.run(["nvidia-smi", "--query-gpu=driver_version,name", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=10).stdout.strip().splitlines()
+        if q:
+            drv, name = (x.strip() for x in q[0].split(",", 1))
+            out.update(driver=drv, gpu=name)
+    except (OSError, subprocess.SubprocessError, ValueError):
+        pass
+    return out
+
+
 def job_tflops(flops_per_rank_step: float, ws: int, ms_per_step: float) -> float:
     """Whole-job throughput: all ranks' FLOPs over the slowest rank's step time."""
     return flops_per_rank_step * ws / (ms_per_step / 1e3) / 1e12
@@ -428,6 +448,7 @@ def run_ours(args):
                          f"{l2 / 2**20:.0f} MiB)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "plan": desc},
+        "versions": versions(),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": ("mx_gemm_pair_kernel (CTA-pair tcgen05 block-scaled GEMM)" if "mode=pair" in desc
