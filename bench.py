@@ -70,9 +70,12 @@ def slowest_rank_ms(ms: float, ws: int, device) -> float:
 
 
 def versions() -> dict:
-    """Library, CUDA, driver and PyTorch versions of the run (recorded beside the plan)."""
+    """Library, CUDA, driver, PyTorch and numpy versions of the run and the hash of the
+    kernel sources (recorded beside the plan; the GPU machine gets no git history)."""
+    import numpy
     import torch
-    out = {"torch": torch.__version__, "cuda_runtime": torch.version.cuda}
+    out = {"torch": torch.__version__, "numpy": numpy.__version__, "cuda_runtime": torch.version.cuda,
+           "kernel_source_sha": kernel_source_sha()}
     try:
         from mx_block_scaled_gb300 import binding as mx
         out["libmxgemm"] = int(mx.mxgemm_version())
