@@ -98,10 +98,16 @@ def job_tflops(flops_per_rank_step: float, ws: int, ms_per_step: float) -> float
 
 
 def kernel_source_sha() -> str:
+    """Hash of the kernel and planner sources with comments and whitespace removed,
+    so that a comment edit does not orphan a DRAM-traffic capture of the same code."""
+    import re
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                 # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -303,7 +303,7 @@ struct WorkIter {
     }
 
     // Stream-K segments come first, so that the fixup of a cut tile (run by the
-    // epilogue warps of its last CTA) overlaps the whole tiles computed after it.
+    // fixup warps of its last CTA) overlaps the whole tiles computed after it.
     __device__ bool next(const GemmParams &p, Work &w)
     {
         if (pos < end) {
