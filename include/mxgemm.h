@@ -102,8 +102,13 @@ typedef struct mxgemm_plan *mxgemm_plan_t;
  *   no workspace for scales; MXGEMM_PLAN_FORCE_MC -> MXGEMM_ERR_UNSUPPORTED.
  * Validates the shape (M, N >= 1; K >= 128 and K % 128 == 0, per the FlyDSL
  * page's K constraint), checks that the current device is an sm_103 part,
- * chooses the tile shape, operand roles (swap-AB) and split-K, and sizes the
- * workspace.  Host memory only.  On success *plan receives a new plan.
+ * chooses the tile shape, operand roles (swap-AB), split-K and stream-K, and
+ * sizes the workspace.  Host memory only.  On success *plan receives a new plan.
+ * Stream-K (256-wide tiles): when the last wave of tiles would leave more than
+ * 10% of the SMs idle, its tiles are cut along K between CTAs and each cut
+ * tile's partial sums are added in k order inside the kernel (the result does
+ * not depend on the run); MXGEMM_PLAN_STREAMK forces it where the last wave is
+ * under 95% full, MXGEMM_PLAN_NO_STREAMK keeps whole tiles.
  */
 MXGEMM_API int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
                        int fmt, int out, uint32_t flags);
@@ -113,8 +118,10 @@ MXGEMM_API int mxgemm_plan_destroy(mxgemm_plan_t plan);
 
 /*
  * Bytes of device workspace mxgemm_run needs for this plan (0 for NULL plan):
- * the tile-layout copies of SA and SB (unless both are passed pre-laid-out)
- * plus split-K partial sums.  Alignment: 256 bytes.
+ * the tile-layout copies of SA and SB (unless both are passed pre-laid-out),
+ * split-K partial sums, and for stream-K plans the cut tiles' partial sums and
+ * arrival counters (reset by every run, so the workspace holds nothing between
+ * calls).  Alignment: 256 bytes.
  */
 MXGEMM_API size_t mxgemm_workspace_bytes(mxgemm_plan_t plan);
 
