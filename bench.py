@@ -820,7 +820,7 @@ def run_placement_sweep(args):
     sa, sb = np.meshgrid(np.arange(255, dtype=np.int32), np.arange(255, dtype=np.int32), indexing="ij")
     sa, sb = sa.reshape(-1), sb.reshape(-1)
     dsa, dsb = torch.from_numpy(sa).cuda(), torch.from_numpy(sb).cuda()
-    out_dir = os.path.join(ROOT, "gpurun_out")
+    out_dir = args.out_dir  # per-pair counts saved as .npz when given
     for k in (1, 2, 3):
         mx.placement_scan(k, dsa[:64], dsb[:64])  # warm-up
         torch.cuda.synchronize()
@@ -843,7 +843,8 @@ def run_placement_sweep(args):
             rec["agree_ea_range"] = [int(ea[agree].min()), int(ea[agree].max())]
             rec["agree_eb_range"] = [int(eb[agree].min()), int(eb[agree].max())]
             rec["agree_sum_range"] = [int((ea + eb)[agree].min()), int((ea + eb)[agree].max())]
-        if os.path.isdir(out_dir):
+        if out_dir:
+            os.makedirs(out_dir, exist_ok=True)
             np.savez_compressed(os.path.join(out_dir, f"placement_k{k}.npz"), sa=sa, sb=sb, counts=c, first=f)
         if not args.no_cpu_baseline and k == 3:
             import oracle
@@ -936,6 +937,7 @@ def main():
                     help="time the grouped (mixture-of-experts) MX GEMM over the grouped workloads")
     ap.add_argument("--oracle-sweep", action="store_true",
                     help="time the CPU oracle over the workload shapes (full for M <= 256, else extrapolated)")
+    ap.add_argument("--out-dir", default="", help="--placement-sweep: save the per-pair counts here (.npz)")
     ap.add_argument("--placement-sweep", action="store_true",
                     help="run the scale-placement checker over every scale pair for k = 1, 2, 3")
     args = ap.parse_args()
