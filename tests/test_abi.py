@@ -163,3 +163,25 @@ def test_prepare_rejects_a_null_plan_on_the_host(lib):
     """mxgemm_prepare checks its arguments before any CUDA call."""
     assert lib.mxgemm_prepare(None, 0, 0, 0, 0, 0, None) == lib.MXGEMM_ERR_ARG
     assert lib.mxgemm_prepare(None, 0, 0, 0, 0, lib.MXGEMM_RUN_PREPARED, None) == lib.MXGEMM_ERR_ARG
+
+
+def test_binding_constants_match_the_header(lib):
+    """Every MXGEMM_* #define and enum value in mxgemm.h that the binding exposes
+    has the same value there (flags, status codes, formats)."""
+    text = open(HEADER).read()
+    values = {}
+    for name, expr in re.findall(r"#define\s+(MXGEMM_[A-Z0-9_]+)\s+([^\s/]+(?:\s*<<\s*\d+\))?)", text):
+        expr = expr.strip()
+        m = re.fullmatch(r"\(?(\d+)u?\s*<<\s*(\d+)\)?", expr)
+        if m:
+            values[name] = int(m.group(1)) << int(m.group(2))
+        elif re.fullmatch(r"-?\d+", expr):
+            values[name] = int(expr)
+    for name, val in re.findall(r"(MXGEMM_(?:FMT|OUT)_[A-Z0-9_]+)\s*=\s*(\d+)", text):
+        values[name] = int(val)
+    checked = 0
+    for name, val in values.items():
+        if hasattr(lib, name):
+            assert getattr(lib, name) == val, name
+            checked += 1
+    assert checked >= 15
