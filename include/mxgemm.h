@@ -33,6 +33,12 @@
  *    Arguments are validated before anything is launched; on an error nothing
  *    is launched and no output is touched.  No call aborts or throws.
  *  - A plan is a host object; it is not thread-safe (one thread per plan).
+ *  - On its first use on a device the library caches per-device state: the
+ *    kernels' shared-memory opt-in, the device addresses of its own device
+ *    variables (the status word, the mxgemm_run_noalloc scratch) and the
+ *    device's properties.  cudaDeviceReset discards what the cache refers to;
+ *    a process that resets a device must not call this library on that
+ *    device again (the cached addresses would be stale).
  */
 #ifndef MXGEMM_H
 #define MXGEMM_H
@@ -81,7 +87,7 @@ typedef enum {
 #define MXGEMM_PLAN_FORCE_SWAP      (1u << 3)  /* always compute C^T = B*A^T          */
 #define MXGEMM_PLAN_FORCE_PAIR      (1u << 4)  /* 256-row tiles on CTA pairs          */
 #define MXGEMM_PLAN_FORCE_SINGLE    (1u << 5)  /* 128-row tiles, one CTA per tile     */
-#define MXGEMM_PLAN_FORCE_MC        (1u << 6)  /* 128-row tiles, CTA pairs share B    */
+/* (bit 6 is not a flag: passing it gives MXGEMM_ERR_ARG)                     */
 #define MXGEMM_PLAN_STREAMK         (1u << 7)  /* spread the last wave's k-stages     */
 #define MXGEMM_PLAN_SPLITK_SHIFT    8          /* bits 8..15: forced split-K (0=auto) */
 #define MXGEMM_PLAN_NO_STREAMK      (1u << 16) /* whole tiles only (no stream-K)      */
@@ -99,7 +105,7 @@ typedef struct mxgemm_plan *mxgemm_plan_t;
  *   MXGEMM_FMT_BF16 plans the plain BF16 NT GEMM on the same kernels (the
  *   FlyDSL page's BF16 "NT GEMM" comparison set, section "Performance numbers
  *   need their baselines"): K a multiple of 64, SA / SB not read (may be NULL),
- *   no workspace for scales; MXGEMM_PLAN_FORCE_MC -> MXGEMM_ERR_UNSUPPORTED.
+ *   no workspace for scales.
  * Validates the shape (M, N >= 1; K >= 128 and K % 128 == 0, per the FlyDSL
  * page's K constraint), checks that the current device is an sm_103 part,
  * chooses the tile shape, operand roles (swap-AB), split-K and stream-K, and
@@ -237,12 +243,17 @@ MXGEMM_API int mxgemm_run(mxgemm_plan_t plan, const void *A, const uint8_t *SA,
 MXGEMM_API int mxgemm_prepare(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB,
                    void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream);
 
+/* Time limit, in nanoseconds of GPU global time, of every barrier wait inside
+ * the GEMM kernels launched by mxgemm_run, mxgemm_run_noalloc and
+ * mxgemm_grouped_run (mxgemm_selftest_stall uses 20 ms). */
+#define MXGEMM_WAIT_LIMIT_NS 2000000000ull
+
 /*
  * Synchronise `stream` and return the library's sticky device status on the
  * current device: MXGEMM_OK, or MXGEMM_ERR_DEVICE_TIMEOUT if any kernel since
  * the last reset gave up on a barrier wait (every wait in the kernels has a
- * time limit of about one second; on expiry the kernel records the error,
- * drains its own in-flight work and exits instead of hanging).  If `reset` is
+ * time limit of MXGEMM_WAIT_LIMIT_NS, two seconds; on expiry the kernel records
+ * the error, drains its own in-flight work and exits instead of hanging).  If `reset` is
  * nonzero the status is cleared after reading.  MXGEMM_ERR_CUDA if the
  * synchronisation itself fails.
  */
@@ -284,7 +295,9 @@ MXGEMM_API int mxgemm_selftest_stall(mxgemm_plan_t plan, const void *A, const ui
  *     byte it later reads.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: after a cudaDeviceReset of that device it is stale (see the
+ *     conventions at the top of this file).
  * Arguments, results and errors are otherwise those of mxgemm_run.  No
  * cudaMalloc, cudaFree or other allocating call is made.
  */

@@ -34,7 +34,6 @@ MXGEMM_PLAN_FORCE_NOSWAP = 1 << 2
 MXGEMM_PLAN_FORCE_SWAP = 1 << 3
 MXGEMM_PLAN_FORCE_PAIR = 1 << 4
 MXGEMM_PLAN_FORCE_SINGLE = 1 << 5
-MXGEMM_PLAN_FORCE_MC = 1 << 6
 MXGEMM_PLAN_STREAMK = 1 << 7
 MXGEMM_PLAN_SPLITK_SHIFT = 8
 MXGEMM_PLAN_NO_STREAMK = 1 << 16

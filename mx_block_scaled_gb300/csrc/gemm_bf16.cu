@@ -14,7 +14,7 @@ cudaError_t launch(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap
     using C = Cfg<K_BF16, BN>;
     if constexpr (BN == 256) {
         if (p.sk_ctas > 0) {  // stream-K plans: the instantiation with fixup warps
-            mx_gemm_kernel<K_BF16, BN, false, false, true><<<grid, kThreadsSk, C::kSmemBytes, s>>>(p, ma, mb);
+            mx_gemm_kernel<K_BF16, BN, false, true><<<grid, kThreadsSk, C::kSmemBytes, s>>>(p, ma, mb);
             return cudaGetLastError();
         }
     }
@@ -92,7 +92,7 @@ cudaError_t prepare_gemm_bf16()
                         (const void *)mx_gemm_kernel<K_BF16, 64>,
                         (const void *)mx_gemm_kernel<K_BF16, 128>,
                         (const void *)mx_gemm_kernel<K_BF16, 256>,
-                        (const void *)mx_gemm_kernel<K_BF16, 256, false, false, true>,
+                        (const void *)mx_gemm_kernel<K_BF16, 256, false, true>,
                         (const void *)mx_gemm_pair_kernel<K_BF16, 128>,
                         (const void *)mx_gemm_pair_kernel<K_BF16, 256>,
                         (const void *)mx_gemm_pair_kernel<K_BF16, 256, true>};

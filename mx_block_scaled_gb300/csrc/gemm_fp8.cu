@@ -12,7 +12,7 @@ cudaError_t launch(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap
     using C = Cfg<K_MXFP8, BN>;
     if constexpr (BN == 256) {
         if (p.sk_ctas > 0) {  // stream-K plans: the instantiation with fixup warps
-            mx_gemm_kernel<K_MXFP8, BN, false, false, true><<<grid, kThreadsSk, C::kSmemBytes, s>>>(p, ma, mb);
+            mx_gemm_kernel<K_MXFP8, BN, false, true><<<grid, kThreadsSk, C::kSmemBytes, s>>>(p, ma, mb);
             return cudaGetLastError();
         }
     }
@@ -70,34 +70,10 @@ int pair_max_clusters()
 }
 
 template <int BN>
-cudaError_t launch_mc(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int clusters, cudaStream_t s)
-{
-    auto kern = mx_gemm_kernel<K_MXFP8, BN, true>;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(clusters, Cfg<K_MXFP8, BN>::kSmemBytes, s, attr, kThreads);
-    return cudaLaunchKernelEx(&cfg, kern, p, ma, mb);
-}
-
-template <int BN>
-int mc_max_clusters()
-{
-    auto kern = mx_gemm_kernel<K_MXFP8, BN, true>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<K_MXFP8, BN>::kSmemBytes) !=
-        cudaSuccess)
-        return 0;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster2_config(1, Cfg<K_MXFP8, BN>::kSmemBytes, nullptr, attr, kThreads);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
-        return 0;
-    return n;
-}
-
-template <int BN>
 cudaError_t launch_grouped(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid, cudaStream_t s)
 {
     using C = Cfg<K_MXFP8, BN>;
-    mx_gemm_kernel<K_MXFP8, BN, false, true><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
+    mx_gemm_kernel<K_MXFP8, BN, true><<<grid, kThreads, C::kSmemBytes, s>>>(p, ma, mb);
     return cudaGetLastError();
 }
 
@@ -122,7 +98,7 @@ cudaError_t prepare_gemm_fp8()
 {
     const void *single[5] = {(const void *)mx_gemm_kernel<K_MXFP8, 32>, (const void *)mx_gemm_kernel<K_MXFP8, 64>,
                              (const void *)mx_gemm_kernel<K_MXFP8, 128>, (const void *)mx_gemm_kernel<K_MXFP8, 256>,
-                             (const void *)mx_gemm_kernel<K_MXFP8, 256, false, false, true>};
+                             (const void *)mx_gemm_kernel<K_MXFP8, 256, false, true>};
     const int single_smem[5] = {Cfg<K_MXFP8, 32>::kSmemBytes, Cfg<K_MXFP8, 64>::kSmemBytes, Cfg<K_MXFP8, 128>::kSmemBytes,
                                 Cfg<K_MXFP8, 256>::kSmemBytes, Cfg<K_MXFP8, 256>::kSmemBytes};
     for (int i = 0; i < 5; ++i) {
@@ -130,19 +106,18 @@ cudaError_t prepare_gemm_fp8()
         if (e != cudaSuccess)
             return e;
     }
-    const void *cl[5] = {(const void *)mx_gemm_kernel<K_MXFP8, 128, true>, (const void *)mx_gemm_kernel<K_MXFP8, 256, true>,
-                         (const void *)mx_gemm_pair_kernel<K_MXFP8, 128>, (const void *)mx_gemm_pair_kernel<K_MXFP8, 256>,
+    const void *cl[3] = {(const void *)mx_gemm_pair_kernel<K_MXFP8, 128>, (const void *)mx_gemm_pair_kernel<K_MXFP8, 256>,
                          (const void *)mx_gemm_pair_kernel<K_MXFP8, 256, true>};
-    const int cl_smem[5] = {Cfg<K_MXFP8, 128>::kSmemBytes, Cfg<K_MXFP8, 256>::kSmemBytes, CfgPair<K_MXFP8, 128>::kSmemBytes,
-                            CfgPair<K_MXFP8, 256>::kSmemBytes, CfgPair<K_MXFP8, 256>::kSmemBytes};
-    for (int i = 0; i < 5; ++i) {
+    const int cl_smem[3] = {CfgPair<K_MXFP8, 128>::kSmemBytes, CfgPair<K_MXFP8, 256>::kSmemBytes,
+                            CfgPair<K_MXFP8, 256>::kSmemBytes};
+    for (int i = 0; i < 3; ++i) {
         cudaError_t e = cudaFuncSetAttribute(cl[i], cudaFuncAttributeMaxDynamicSharedMemorySize, cl_smem[i]);
         if (e != cudaSuccess)
             return e;
     }
-    const void *gr[3] = {(const void *)mx_gemm_kernel<K_MXFP8, 64, false, true>,
-                         (const void *)mx_gemm_kernel<K_MXFP8, 128, false, true>,
-                         (const void *)mx_gemm_kernel<K_MXFP8, 256, false, true>};
+    const void *gr[3] = {(const void *)mx_gemm_kernel<K_MXFP8, 64, true>,
+                         (const void *)mx_gemm_kernel<K_MXFP8, 128, true>,
+                         (const void *)mx_gemm_kernel<K_MXFP8, 256, true>};
     const int gr_smem[3] = {Cfg<K_MXFP8, 64>::kSmemBytes, Cfg<K_MXFP8, 128>::kSmemBytes, Cfg<K_MXFP8, 256>::kSmemBytes};
     for (int i = 0; i < 3; ++i) {
         cudaError_t e = cudaFuncSetAttribute(gr[i], cudaFuncAttributeMaxDynamicSharedMemorySize, gr_smem[i]);
@@ -184,18 +159,6 @@ cudaError_t launch_gemm_pair_fp8(int bn, const GemmParams &p, const CUtensorMap 
     default: return cudaErrorInvalidValue;
     }
 }
-
-cudaError_t launch_gemm_mc_fp8(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
-                               int clusters, cudaStream_t s)
-{
-    switch (bn) {
-    case 128: return launch_mc<128>(p, ma, mb, clusters, s);
-    case 256: return launch_mc<256>(p, ma, mb, clusters, s);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
-int gemm_mc_max_clusters_fp8(int bn) { return bn == 128 ? mc_max_clusters<128>() : mc_max_clusters<256>(); }
 
 int gemm_pair_max_clusters_fp8(int bn) { return bn == 128 ? pair_max_clusters<128>() : pair_max_clusters<256>(); }
 

@@ -678,12 +678,7 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
 // GROUPED = true: the grouped (mixture-of-experts) form, tiles of all groups
 // walked through the per-CTA group table (p.grouped must be 1); plain GEMMs
 // use GROUPED = false, so none of its code or shared memory is in them.
-// MC = true: the kernel runs in clusters of two CTAs on vertically adjacent tiles
-// (same B-role tile); each CTA loads half of the B-role tile and multicasts it
-// to both, so the pair reads that tile from L2 once.  Slot reuse then needs
-// both CTAs' MMAs done: `empty` counts two commits (each MMA thread commits to
-// both CTAs' barriers).
-template <int KIND, int BN, bool MC = false, bool GROUPED = false, bool SK = false>
+template <int KIND, int BN, bool GROUPED = false, bool SK = false>
 __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b)
@@ -698,7 +693,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     __shared__ uint64_t fix_bars[2];  // stream-K fixup hand-off: full, empty
     __shared__ SkFix sk_fix;
     constexpr bool kSk = SK;  // this instantiation runs stream-K plans (fixup warps 10, 11)
-    static_assert(!SK || (!MC && !GROUPED && BN == 256), "stream-K: plain 128 x 256 tiles only");
+    static_assert(!SK || (!GROUPED && BN == 256), "stream-K: plain 128 x 256 tiles only");
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -727,7 +722,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         abort_flag = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), MC ? 2 : 1);
+            mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
@@ -750,20 +745,16 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (MC)
-        cluster_sync();  // the peer's barriers exist before the first multicast lands
     tc_fence_after();
     const uint32_t tmem = tmem_base_holder;
 
-    // Work: output tiles (x splits, or stream-K segments); with MC, vertical tile
-    // pairs, CTA r of the cluster taking A-role tile 2*tm + r.
-    const int mc_rank = MC ? static_cast<int>(cluster_ctarank()) : 0;
+    // Work: output tiles (x splits, or stream-K segments).
     const GroupTable *gt = nullptr;  // grouped kernels only (a constant null pointer otherwise)
     if constexpr (GROUPED)
         gt = &gtab;
     const int tok_tile = p.tok_b ? BN : kBM;
-    const int first_unit = MC ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-    const int unit_step = MC ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+    const int first_unit = static_cast<int>(blockIdx.x);
+    const int unit_step = static_cast<int>(gridDim.x);
     const uint64_t lim = p.timeout_ns;
 
     if (warp == 0) {
@@ -785,19 +776,16 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             wi.init(p, first_unit, unit_step, gt, tok_tile);
             Work w;
             while (ok && wi.next(p, w)) {
-                if (MC) w.tm = 2 * w.tm + mc_rank;
                 TileGeom g;
                 tile_geom<BN, C::kChunksB>(p, gt, w, g);
-                const bool has_sfa = g.has_sfa;  // false for an MC CTA past the last row
+                const bool has_sfa = g.has_sfa;
                 const int ks0 = w.ks0;
                 const int ks1 = w.ks1;
                 // B-role scale chunks present for this tile (row blocks past the end are skipped)
                 const int rb_b0 = g.sfb_rb0;
                 const int nchunk_b = g.nchunk_b;
                 for (int ks = ks0; ks < ks1; ++ks) {
-                    const bool freed = MC ? warp_wait_cluster(empty_bar(st), ph ^ 1u, abort, lim)
-                                          : warp_wait(empty_bar(st), ph ^ 1u, abort, lim);
-                    if (!freed) {
+                    if (!warp_wait(empty_bar(st), ph ^ 1u, abort, lim)) {
                         if (lane == 0) record_timeout(p, abort);
                         ok = false;
                         break;
@@ -809,11 +797,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                     if (elect_one()) {
                         mbar_arrive_expect_tx(full_bar(st), bytes);
                         tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, g.a_row, pol_a);
-                        if (MC)  // own half of the B-role tile, to both CTAs
-                            tma_load_2d_multicast(sB + st * C::kBBytes + mc_rank * (C::kBBytes / 2), &map_b,
-                                                  full_bar(st), ks * kRowBytes, g.b_row + mc_rank * (BN / 2), 0x3);
-                        else
-                            tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, g.b_row, pol_b);
+                        tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, g.b_row, pol_b);
                         if constexpr (C::kScaled) {
                             if (has_sfa)
                                 bulk_load(sSFA + st * C::kSfaBytes,
@@ -931,10 +915,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                                 mma_mxf8f6f4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
                         }
                     }
-                    if (MC)
-                        tc_commit_multicast(empty_bar(st), 0x3);
-                    else
-                        tc_commit(empty_bar(st));
+                    tc_commit(empty_bar(st));
                 }
                 __syncwarp();
                 if (++st == S) {
@@ -969,7 +950,6 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         wi.init(p, first_unit, unit_step, gt, tok_tile);
         Work w;
         for (; wi.next(p, w); ++it) {
-            if (MC) w.tm = 2 * w.tm + mc_rank;
             const int tm = w.tm;
             const int tn = w.tn;
             const int acc = it % C::kAccStages;
@@ -1053,8 +1033,6 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (MC)
-        cluster_sync();  // the peer may still multicast into, or commit to, this CTA until here
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);

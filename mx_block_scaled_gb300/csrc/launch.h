@@ -41,15 +41,6 @@ cudaError_t launch_gemm_pair_fp4(int bn, const GemmParams &p, const CUtensorMap 
 int gemm_pair_max_clusters_fp8(int bn);
 int gemm_pair_max_clusters_fp4(int bn);
 
-// Single-CTA MMAs in clusters of two CTAs that share (multicast) the B-role
-// tile; bn = 128 or 256; `clusters` clusters.
-cudaError_t launch_gemm_mc_fp8(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                               int clusters, cudaStream_t stream);
-cudaError_t launch_gemm_mc_fp4(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                               int clusters, cudaStream_t stream);
-int gemm_mc_max_clusters_fp8(int bn);
-int gemm_mc_max_clusters_fp4(int bn);
-
 // BF16 (kind::f16, no scales) GEMM: single-CTA tiles (bn 32..256) and CTA-pair
 // tiles (bn 128, 256; the scale maps are not read).
 cudaError_t launch_gemm_bf16(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,

@@ -266,9 +266,8 @@ struct mxgemm_plan {
     int64_t M, N, K;
     int fmt, out;
     int swap;          // 1: compute C^T = B * A^T (B fills the MMA M dimension)
-    int mode;          // 0: one CTA per 128-row tile; 1: clusters of 2 CTAs on vertically adjacent
-                       // 128-row tiles sharing the B-role tile (TMA multicast); 2: 256-row tiles on
-                       // CTA pairs with M = 256 MMAs (cta_group::2)
+    int mode;          // 0: one CTA per 128-row tile; 1: 256-row tiles on CTA pairs with M = 256
+                       // MMAs (cta_group::2)
     int bn;            // MMA N tile
     int splits;        // split-K factor
     int tiles_m, tiles_n;
@@ -384,19 +383,17 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     const bool bf16 = fmt == MXGEMM_FMT_BF16;
     const uint32_t known = MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_NOSWAP |
                            MXGEMM_PLAN_FORCE_SWAP | MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE |
-                           MXGEMM_PLAN_FORCE_MC | MXGEMM_PLAN_STREAMK | MXGEMM_PLAN_NO_STREAMK |
+                           MXGEMM_PLAN_STREAMK | MXGEMM_PLAN_NO_STREAMK |
                            (0xFFu << MXGEMM_PLAN_SPLITK_SHIFT);
     if ((flags & ~known) != 0 || ((flags & MXGEMM_PLAN_FORCE_SWAP) && (flags & MXGEMM_PLAN_FORCE_NOSWAP)) ||
         ((flags & MXGEMM_PLAN_STREAMK) && (flags & MXGEMM_PLAN_NO_STREAMK)) ||
         ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)) ||
-        __builtin_popcount(flags & (MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE | MXGEMM_PLAN_FORCE_MC)) > 1)
+        ((flags & MXGEMM_PLAN_FORCE_PAIR) && (flags & MXGEMM_PLAN_FORCE_SINGLE)))
         return MXGEMM_ERR_ARG;
     // MX formats: K a multiple of 128 (the FlyDSL page's constraint); BF16: of 64
     // (one 128-byte k-stage row).
     if (M < 1 || N < 1 || K < (bf16 ? 64 : 128) || K % (bf16 ? 64 : 128) != 0)
         return MXGEMM_ERR_SHAPE;
-    if (bf16 && (flags & MXGEMM_PLAN_FORCE_MC))
-        return MXGEMM_ERR_UNSUPPORTED;  // no multicast instantiation for BF16
     // 32-bit tile and row indices inside the kernels
     if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30))
         return MXGEMM_ERR_UNSUPPORTED;
@@ -427,25 +424,24 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     int bn = pick_bn(rows_b);
     if (flags & MXGEMM_PLAN_FORCE_BN128) bn = 128;
     if (flags & MXGEMM_PLAN_FORCE_BN256) bn = 256;
-    // Cluster modes (MC, pair) need 128- or 256-wide N tiles.  Default: MXFP8
+    // Pair tiles need 128- or 256-wide N tiles.  Default: MXFP8
     // with at least 128 rows on each side runs 256 x 256 pair tiles (measured
     // faster from 128 tokens up); MXFP4, whose MMAs are issue-bound in both
     // modes, and swapped decode shapes stay on single-CTA tiles.
     int mode = 0;
     if ((fmt == MXGEMM_FMT_MXFP8_E4M3 || bf16) && !swap && rows_a >= 128 && rows_b >= 256 &&
         !(flags & MXGEMM_PLAN_FORCE_BN128) && ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0)
-        mode = 2;
-    if (flags & MXGEMM_PLAN_FORCE_MC) mode = 1;
-    if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 2;
+        mode = 1;
+    if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_SINGLE) mode = 0;
     if (mode != 0 && bn < 128) bn = 128;
     // Stream-K runs on 256-wide tiles only (the instantiations with fixup
     // warps): a forced stream-K plan takes them.
-    if ((flags & MXGEMM_PLAN_STREAMK) && mode != 1) bn = 256;
+    if (flags & MXGEMM_PLAN_STREAMK) bn = 256;
     p->mode = mode;
     p->bn = bn;
     // tiles_m counts the work units along the A role: 128-row tiles (single),
-    // pairs of 128-row tiles (MC), 256-row tiles (pair).
+    // 256-row tiles (pair).
     p->tiles_m = static_cast<int>(mode == 0 ? ceil_div(rows_a, 128) : ceil_div(rows_a, 256));
     p->tiles_n = static_cast<int>(ceil_div(rows_b, bn));
     p->kstages = static_cast<int>(fmt == MXGEMM_FMT_MXFP4_E2M1 ? ceil_div(K, 256) : bf16 ? K / 64 : K / 128);
@@ -453,14 +449,9 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     // Concurrent work units: SMs, or co-resident clusters of two.
     int64_t slots = p->num_sms;
     if (mode != 0) {
-        int max_clusters = 0;
-        if (mode == 1)
-            max_clusters = fmt == MXGEMM_FMT_MXFP4_E2M1 ? mxg::gemm_mc_max_clusters_fp4(bn)
-                                                        : mxg::gemm_mc_max_clusters_fp8(bn);
-        else
-            max_clusters = fmt == MXGEMM_FMT_MXFP4_E2M1 ? mxg::gemm_pair_max_clusters_fp4(bn)
-                           : bf16                           ? mxg::gemm_pair_max_clusters_bf16(bn)
-                                                            : mxg::gemm_pair_max_clusters_fp8(bn);
+        const int max_clusters = fmt == MXGEMM_FMT_MXFP4_E2M1 ? mxg::gemm_pair_max_clusters_fp4(bn)
+                                 : bf16                           ? mxg::gemm_pair_max_clusters_bf16(bn)
+                                                                  : mxg::gemm_pair_max_clusters_fp8(bn);
         if (max_clusters < 1) {
             delete p;
             return MXGEMM_ERR_CUDA;
@@ -480,8 +471,8 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     p->dp_tiles = static_cast<int>(tiles);
     p->sk_tiles = 0;
     p->sk_ctas = 0;
-    p->sk_halves = mode == 2 ? 2 : 1;
-    if (mode != 1 && splits == 0) {
+    p->sk_halves = mode == 1 ? 2 : 1;
+    if (splits == 0) {
         const int64_t G = slots;
         const int64_t waves = ceil_div(tiles, G);
         const double dp_eff = static_cast<double>(tiles) / static_cast<double>(waves * G);
@@ -592,8 +583,8 @@ int mxgemm_plan_describe(mxgemm_plan_t plan, char *buf, size_t len)
         return MXGEMM_ERR_ARG;
     const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
     const bool bf16 = plan->fmt == MXGEMM_FMT_BF16;
-    static const char *const kModes[3] = {"single", "mc", "pair"};
-    mxg::KernelInfo ki = plan->mode == 2 ? (fp4 ? mxg::gemm_pair_info_fp4(plan->bn)
+    static const char *const kModes[2] = {"single", "pair"};
+    mxg::KernelInfo ki = plan->mode == 1 ? (fp4 ? mxg::gemm_pair_info_fp4(plan->bn)
                                                 : bf16 ? mxg::gemm_pair_info_bf16(plan->bn)
                                                        : mxg::gemm_pair_info_fp8(plan->bn))
                                          : (fp4 ? mxg::gemm_info_fp4(plan->bn)
@@ -602,7 +593,7 @@ int mxgemm_plan_describe(mxgemm_plan_t plan, char *buf, size_t len)
              "fmt=%s out=%s tile=%dx%d mode=%s swap_ab=%d split_k=%d streamk=%d+%d/%d units=%dx%d kstages=%d grid=%d%s "
              "stages=%d acc_stages=%d smem=%d",
              fp4 ? "mxfp4" : bf16 ? "bf16" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32",
-             plan->mode == 2 ? 256 : 128,
+             plan->mode == 1 ? 256 : 128,
              plan->bn, kModes[plan->mode], plan->swap, plan->splits, plan->dp_tiles, plan->sk_tiles, plan->sk_ctas,
              plan->tiles_m, plan->tiles_n, plan->kstages, plan->grid, plan->mode ? "x2" : "", ki.stages, ki.acc_stages,
              ki.smem_bytes);
@@ -759,7 +750,7 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     p.group_m = plan->group_m;
     p.test_stall = test_stall;
     // An A-role tile is read once per B-role tile column and vice versa (in pair
-    // and MC modes one load of a B-role tile serves the pair).
+    // mode one load of a B-role tile serves the pair).
     p.stream_a = plan->tiles_n <= 2 ? 1 : 0;
     p.stream_b = plan->tiles_m <= 2 ? 1 : 0;
     p.sfa = plan->swap ? sfb : sfa;
@@ -787,11 +778,11 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     p.vec_ok = (!plan->swap && (N * osize) % 16 == 0 && aligned16(p.out)) ? 1 : 0;
 
     cudaError_t e;
-    if (plan->mode == 2 && bf16) {
+    if (plan->mode == 1 && bf16) {
         // the kernel reads no scale maps for BF16; pass valid descriptors anyway
         e = mxg::launch_gemm_pair_bf16(plan->bn, p, plan->map_a, plan->map_b, plan->map_a, plan->map_b, plan->grid,
                                        s);
-    } else if (plan->mode == 2) {
+    } else if (plan->mode == 1) {
         const int ktps = fp4 ? 2 : 1;
         if (plan->map_ptr_sfa != p.sfa) {
             if (encode_sf_map(&plan->map_sfa, p.sfa, mxgemm_sf_bytes(rows_a, K), ktps) != MXGEMM_OK)
@@ -807,11 +798,7 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
                                             plan->grid, s)
                 : mxg::launch_gemm_pair_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->map_sfa, plan->map_sfb,
                                             plan->grid, s);
-    }
-    else if (plan->mode == 1)
-        e = fp4 ? mxg::launch_gemm_mc_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
-                : mxg::launch_gemm_mc_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
-    else if (bf16)
+    } else if (bf16)
         e = mxg::launch_gemm_bf16(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
     else
         e = fp4 ? mxg::launch_gemm_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
@@ -865,7 +852,7 @@ int mxgemm_prepare(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB, voi
 int mxgemm_run(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB, void *C,
                void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream)
 {
-    return run_impl(plan, A, SA, B, SB, C, workspace, ws_bytes, run_flags, stream, 0, 2000000000ull);
+    return run_impl(plan, A, SA, B, SB, C, workspace, ws_bytes, run_flags, stream, 0, MXGEMM_WAIT_LIMIT_NS);
 }
 
 int mxgemm_selftest_stall(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB,
@@ -910,7 +897,7 @@ int mxgemm_run_noalloc(mxgemm_plan_t plan, const void *A, const uint8_t *SA, con
         scratch = g_noalloc_addr[dev];
     }
     return run_impl(plan, A, SA, B, SB, C, scratch, MXGEMM_NOALLOC_SCRATCH_BYTES, run_flags, stream, 0,
-                    2000000000ull);
+                    MXGEMM_WAIT_LIMIT_NS);
 }
 
 // ------------------------------------------------------------ grouped --
@@ -1076,7 +1063,7 @@ int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *group_offsets,
     p.stream_b = (!plan->swap && stream_w) ? 1 : 0;
     p.sfa = plan->swap ? w_sf : tok_sf;
     p.sfb = plan->swap ? tok_sf : w_sf;
-    p.timeout_ns = 2000000000ull;
+    p.timeout_ns = MXGEMM_WAIT_LIMIT_NS;
     p.status = dev->status_ptr;
     p.grouped = 1;
     p.groups = static_cast<int>(G);

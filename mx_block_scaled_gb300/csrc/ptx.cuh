@@ -201,19 +201,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// 2-D tiled load multicast to the same shared-memory offset in every CTA of
-// `mask` (this cluster); each destination CTA's barrier at `bar`'s offset
-// receives the completed bytes of its copy.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                                      int32_t x, int32_t y, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-        : "memory");
-}
-
 // 2-D tiled load into this CTA's shared memory whose completed bytes are
 // counted on a barrier in either CTA of the pair (`bar`: shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
@@ -342,14 +329,6 @@ __device__ __forceinline__ void mma_pair_bf16(uint32_t d, uint64_t adesc, uint64
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc),
         "r"(accumulate)
         : "memory");
-}
-
-// Single-CTA MMA commit that arrives on `bar` (same offset) in every CTA of `mask`.
-__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-                 "h"(mask)
-                 : "memory");
 }
 
 // Copy 32 rows x 16 bytes from shared memory into TMEM columns [taddr, taddr+4),

@@ -82,4 +82,19 @@ def sample_indices(n, seed, count=32):
     return np.array(sorted(idx), dtype=np.int64)
 
 
+def tile_sample_indices(n, seed, block=128):
+    """One seeded index inside every `block`-wide block of [0, n), plus the first
+    and the last index.  Where the tiles of a plan are 128 or 256 rows (or
+    columns) wide and start on multiples of 128 -- every plan of a shape with
+    more than 256 rows on that side -- sampled rows over all columns (or sampled
+    columns over all rows) touch every tile of the plan, split-K slabs and
+    stream-K cut tiles included."""
+    rng = np.random.default_rng(seed)
+    nb = (n + block - 1) // block
+    starts = np.arange(nb, dtype=np.int64) * block
+    widths = np.minimum(block, n - starts)
+    idx = starts + np.floor(rng.random(nb) * widths).astype(np.int64)
+    return np.unique(np.concatenate([idx, [0, n - 1]])).astype(np.int64)
+
+
 FMTS = {"mxfp8": FMT_MXFP8, "mxfp4": FMT_MXFP4}

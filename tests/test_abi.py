@@ -64,6 +64,8 @@ def test_status_strings(lib):
     (16, 16, 128, 1, 2, 1 << 20, -1),  # unknown flag
     (16, 16, 128, 1, 2, (1 << 2) | (1 << 3), -1),  # contradictory flags
     (16, 16, 128, 1, 2, (1 << 7) | (1 << 16), -1),  # stream-K forced on and off
+    (16, 16, 128, 1, 2, 1 << 6, -1),  # bit 6 is not a plan flag
+    (16, 16, 128, 1, 2, (1 << 4) | (1 << 5), -1),  # pair and single tiles at once
 ])
 def test_plan_create_validates_before_touching_the_device(lib, M, N, K, fmt, out, flags, expect):
     st, h = lib.mxgemm_plan_create(M, N, K, fmt, out, flags)
@@ -140,7 +142,7 @@ def test_grouped_null_arguments_are_rejected(lib):
 @pytest.mark.parametrize("M,N,K,flags,expect", [
     (16, 16, 96, 0, -2),        # BF16 needs K % 64 == 0
     (16, 16, 0, 0, -2),
-    (16, 16, 64, 1 << 6, -8),   # no multicast instantiation for BF16
+    (16, 16, 64, 1 << 6, -1),   # bit 6 is not a plan flag
 ])
 def test_bf16_plan_validation(lib, M, N, K, flags, expect):
     st, h = lib.mxgemm_plan_create(M, N, K, 3, 2, flags)

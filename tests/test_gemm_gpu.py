@@ -8,14 +8,15 @@ import numpy as np
 import pytest
 
 from golden_io import load_handworked
-from gpu_util import (OUT_BF16, OUT_F32, assert_within, gpu_gemm, gpu_gemm_device, lib, sample_indices, to_dev)
+from gpu_util import (OUT_BF16, OUT_F32, assert_within, gpu_gemm, gpu_gemm_device, lib,
+                      tile_sample_indices, to_dev)
 from mx_block_scaled_gb300.inputs import (FMT_MXFP4, FMT_MXFP8, finite_uniform_codes, make_operand,
                                           pack_fp4, workload_cases)
 
 pytestmark = pytest.mark.gpu
 
-# plan flags: 256-row tiles on CTA pairs / 128-row tiles on single CTAs / CTA pairs sharing B (multicast)
-PAIR, SINGLE, MC = 1 << 4, 1 << 5, 1 << 6
+# plan flags: 256-row tiles on CTA pairs / 128-row tiles on single CTAs
+PAIR, SINGLE = 1 << 4, 1 << 5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -145,12 +146,12 @@ def test_per_block_scale_sweep(oracle_mod, fmt):
 
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
-@pytest.mark.parametrize("flags", [0, SINGLE, PAIR, MC])
+@pytest.mark.parametrize("flags", [0, SINGLE, PAIR])
 @pytest.mark.parametrize("M,N,K", [(1, 1, 128), (8, 129, 256), (127, 255, 384), (129, 8, 128),
                                    (255, 127, 384), (130, 300, 640), (64, 512, 1024), (385, 264, 384)])
 def test_edge_shapes_exact(oracle_mod, fmt, flags, M, N, K):
-    if flags in (PAIR, MC) and (M < 128 or N < 128):
-        pytest.skip("cluster modes are for shapes with at least 128 rows on each side")
+    if flags == PAIR and (M < 128 or N < 128):
+        pytest.skip("pair tiles are for shapes with at least 128 rows on each side")
     rng = np.random.default_rng(M * 1000 + N + K)
     A, SA = small_int_codes(rng, M, K, fmt)
     B, SB = small_int_codes(rng, N, K, fmt)
@@ -167,8 +168,7 @@ def test_edge_shapes_exact(oracle_mod, fmt, flags, M, N, K):
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
 @pytest.mark.parametrize("flags", [0, 1 << 2, 1 << 3, (1 << 2) | 1, (1 << 2) | 2, (3 << 8), (1 << 3) | (5 << 8),
-                                   SINGLE, SINGLE | 2, PAIR | 1, PAIR | 2, PAIR | 1 | (3 << 8), PAIR | 2 | (2 << 8),
-                                   MC | 1, MC | 2, MC | 2 | (3 << 8)])
+                                   SINGLE, SINGLE | 2, PAIR | 1, PAIR | 2, PAIR | 1 | (3 << 8), PAIR | 2 | (2 << 8)])
 def test_plan_variants_agree_with_oracle(oracle_mod, fmt, flags):
     """Forced tile width / swap-AB / split-K variants all reproduce the oracle."""
     M, N, K = 200, 384, 2048
