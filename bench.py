@@ -255,6 +255,96 @@ def run_reference(args):
 
 # --------------------------------------------------------------- our arm --
 
+# Further workload shapes timed in the same run as the headline line, so that one
+# driver-run record carries both formats and both bounds: the 70B gate+up
+# projection at prefill (M = 16384 tokens) in MXFP8 and MXFP4, and the same
+# weight at decode (M = 8 tokens, weight-streaming, HBM-bound).
+EXTRA_SHAPES = [("llama33_70b gate+up prefill", "mxfp8", 16384, 57344, 8192),
+                ("llama33_70b gate+up prefill", "mxfp4", 16384, 57344, 8192),
+                ("llama33_70b gate+up decode", "mxfp8", 8, 57344, 8192)]
+
+
+def time_shape(mx, dev, fmt_name, M, N, K, reps, warmup=3, seed=0):
+    """GEMM time of one shape through mxgemm_run (scales pre-laid-out, as a
+    weight's are after loading and an activation's after the quantiser writes
+    them in the tile layout): device-side random codes (E4M3 NaN codes
+    excluded) and scale codes 120..134, rotating input/output sets whose total
+    exceeds twice the L2; `reps` back-to-back calls between CUDA events on the
+    launching stream, after `warmup` calls.  Returns (us per call, plan text,
+    number of input sets)."""
+    import torch
+    from mx_block_scaled_gb300.inputs import FMT_BY_NAME
+    fmt = FMT_BY_NAME[fmt_name]
+    rb = K if fmt_name == "mxfp8" else K // 2
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = (M + N) * rb + (M + N) * K // 32 + M * N * 2
+    nsets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+    nsets = min(nsets, max(2, int(40e9 // set_bytes)))
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def codes(rows):
+        c = torch.randint(0, 256, (rows, rb), dtype=torch.uint8, device=dev, generator=g)
+        if fmt_name == "mxfp8":
+            c = torch.where((c & 0x7F) == 0x7F, c & 0xFE, c)
+        return c
+
+    plan = mx.Plan(M, N, K, fmt, mx.MXGEMM_OUT_BF16, device=dev)
+    sets = []
+    for _ in range(nsets):
+        SA = torch.randint(120, 135, (M, K // 32), dtype=torch.uint8, device=dev, generator=g)
+        SB = torch.randint(120, 135, (N, K // 32), dtype=torch.uint8, device=dev, generator=g)
+        sets.append((codes(M), mx.relayout_scales(SA, M, K), codes(N), mx.relayout_scales(SB, N, K),
+                     torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
+        del SA, SB
+    pre = mx.MXGEMM_RUN_SA_PRELAYOUT | mx.MXGEMM_RUN_SB_PRELAYOUT
+
+    def one(i):
+        a, sa, b, sb, c = sets[i % nsets]
+        st = mx.mxgemm_run(plan.handle, a.data_ptr(), sa.data_ptr(), b.data_ptr(), sb.data_ptr(), c.data_ptr(),
+                           plan.workspace.data_ptr(), plan.ws_bytes, pre, stream.cuda_stream)
+        assert st == 0, mx.mxgemm_status_str(st)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(reps):
+        one(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    mx.check_device_status()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    desc = plan.describe()
+    del sets, plan
+    torch.cuda.empty_cache()
+    return us, desc, nsets
+
+
+def extra_shape_record(label, fmt_name, M, N, K, us, desc, nsets, hbm_gbs, bf16_tf, peak_src):
+    """One timed shape as a JSON object: TFLOP/s, GB/s and the roofline of its
+    bound (the slower of the MX tensor peak and the algorithmic bytes over the
+    measured HBM bandwidth)."""
+    flops = 2.0 * M * N * K
+    byts = algorithmic_bytes(M, N, K, fmt_name, 2)
+    peak = mx_peak_tflops(fmt_name, bf16_tf)
+    t = us / 1e6
+    tensor_bound = flops / (peak * 1e12) > byts / (hbm_gbs * 1e9)
+    tflops, gbs = flops / t / 1e12, byts / t / 1e9
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                "peak_source": f"{peak_src} bf16 burst {bf16_tf} TFLOP/s x nominal {fmt_name}/bf16 ratio "
+                               f"{NOMINAL_PF[fmt_name] / NOMINAL_PF['bf16']:g}"}
+    else:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
+                "algorithmic_bytes": byts, "peak_source": f"{peak_src} HBM copy bandwidth"}
+    return {"workload": f"{label}: {fmt_name} NT GEMM M={M} N={N} K={K}, BF16 out", "format": fmt_name,
+            "M": M, "N": N, "K": K, "us": us, "tflops": tflops, "gbs": gbs, "roofline": roof, "plan": desc,
+            "data": f"device-side random codes, scales 120..134, pre-laid-out; {nsets} rotating sets > 2x L2"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -436,6 +526,16 @@ def run_ours(args):
                "schedule": "copy-in / compute / copy-out streams, two buffer sets",
                "serial": {"value": job_tflops(flops, ws, serial_ms), "ms_per_step": serial_ms}}
 
+    # ---- further workload shapes (outside the timed region of the headline)
+    extras = []
+    if not args.no_extra_shapes:
+        hbm_gbs, bf16_tf, _, peak_src = load_peaks()
+        for label, fname, eM, eN, eK in EXTRA_SHAPES:
+            reps = 20 if eM >= 2048 else 100
+            us, edesc, ensets = time_shape(mx, dev, fname, eM, eN, eK, reps)
+            extras.append(extra_shape_record(label, fname, eM, eN, eK, us, edesc, ensets, hbm_gbs, bf16_tf,
+                                             peak_src))
+
     if rank != 0:
         dist.destroy_process_group()
         return 0
@@ -472,6 +572,7 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "extra_shapes": extras,
     }
     if not args.no_cpu_baseline:
         rows, dt, threads = oracle_sample_time(A, SA, B, SB, K, fmt, args.cpu_target_s, M)
@@ -923,6 +1024,8 @@ def main():
     ap.add_argument("--cpu-target-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra-shapes", action="store_true",
+                    help="skip the further workload shapes timed after the headline")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-workloads", default="")
     ap.add_argument("--sweep-reps", type=int, default=20)

@@ -8,7 +8,7 @@ half-integer operands); elsewhere within |C - C_ref| <= 1e-5 * sum|a*b|
 import numpy as np
 import pytest
 
-from gpu_util import OUT_BF16, OUT_F32, assert_within, lib, sample_indices
+from gpu_util import OUT_BF16, OUT_F32, assert_within, lib, tile_sample_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -93,7 +93,8 @@ def test_bf16_full_size_sampled(oracle_mod, M, N, K):
     C = plan.run(_dev(A), None, _dev(B), None)
     b.check_device_status()
     torch.cuda.synchronize()
-    rows, cols = sample_indices(M, M + 1), sample_indices(N, N + 2)
+    # every 128-row and every 128-column tile of the plan holds a sampled row / column
+    rows, cols = tile_sample_indices(M, M + 1), tile_sample_indices(N, N + 2)
     ref_r, S_r = oracle_mod.bf16_gemm(A, B, rows=rows)
     got_r = C[torch.from_numpy(rows).cuda()].float().double().cpu().numpy()
     assert_within(got_r, ref_r, S_r, OUT_BF16, f"rows {plan.describe()}")

@@ -310,15 +310,26 @@ def _weights(name, fmt, nki, N, K):
 @pytest.mark.parametrize("name,fmt,si,nki,M,N,K", _all_workload_cases(),
                          ids=[f"{c[0]}-{c[1]}-M{c[4]}-N{c[5]}-K{c[6]}" for c in _all_workload_cases()])
 def test_workload_full_size_sampled(oracle_mod, name, fmt, si, nki, M, N, K):
-    """Full-size model shapes in the default launch configuration: every output of
-    sampled rows (all columns) and of sampled columns (all rows) within the bound."""
+    """Full-size model shapes in the default launch configuration, within the bound:
+    for M <= 256 every element of C; otherwise one seeded row inside every 128-row
+    tile (all columns) and one seeded column inside every 128-column tile (all
+    rows), so that every output tile of the plan -- split-K slabs and stream-K
+    cut tiles included -- has elements compared with the oracle."""
     f = FMT_MXFP8 if fmt == "mxfp8" else FMT_MXFP4
     A, SA = make_operand(name, "A", si, M, K, f)
     B, SB = _weights(name, f, nki, N, K)
     import torch
     C = gpu_gemm_device(f, A, SA, B, SB, K, OUT_BF16)
-    rows = sample_indices(M, si, count=12) if M > 64 else np.arange(M)
-    cols = sample_indices(N, nki + 100, count=12)
+    if M <= 256:
+        got = C.double().cpu().numpy()
+        del C
+        ref, S = oracle_mod.gemm(f, A, SA, B, SB, K)
+        worst = assert_within(got, ref, S, OUT_BF16, f"{name} full C")
+        _record_parity_stat(name=name, format=fmt, M=M, N=N, K=K, rows=M, cols=N, full=True,
+                            worst_err_over_bound=worst)
+        return
+    rows = tile_sample_indices(M, si)
+    cols = tile_sample_indices(N, nki + 100)
     C_rows = C[torch.from_numpy(rows).cuda()].double().cpu().numpy()
     C_cols = C[:, torch.from_numpy(cols).cuda()].double().cpu().numpy()
     del C
@@ -326,7 +337,7 @@ def test_workload_full_size_sampled(oracle_mod, name, fmt, si, nki, M, N, K):
     worst_r = assert_within(C_rows, ref_r, S_r, OUT_BF16, f"{name} rows")
     ref_c, S_c = oracle_mod.gemm(f, A, SA, B, SB, K, cols=cols)
     worst_c = assert_within(C_cols, ref_c, S_c, OUT_BF16, f"{name} cols")
-    _record_parity_stat(name=name, format=fmt, M=M, N=N, K=K, rows=len(rows), cols=len(cols),
+    _record_parity_stat(name=name, format=fmt, M=M, N=N, K=K, rows=len(rows), cols=len(cols), full=False,
                         worst_err_over_bound=max(worst_r, worst_c))
 
 

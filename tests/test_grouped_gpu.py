@@ -188,12 +188,17 @@ def test_moe_workloads_full_size_sampled(oracle_mod, case):
     B, SB = quantize_mx(normal_f32(rng, G * N, K), fmt)
     offsets = list(group_offsets(sizes))
     C, desc = _run(fmt, offsets, A, SA, B, SB, N, K, OUT_BF16)
-    # sample: the first and last row of every non-empty group (capped) plus random rows
+    # sample: the first and last row of every non-empty group and one seeded row
+    # inside every 128-row token block of each group (all columns), so that every
+    # token tile of every group -- 64- or 128-row tiles starting at the group's
+    # first row -- has elements compared with the oracle
     rows = set()
     for e in range(G):
         if sizes[e]:
-            rows.update((offsets[e], offsets[e + 1] - 1))
-    rows = sorted(rows)[:48] + sorted(rng.integers(0, T, size=16).tolist())
-    rows = np.array(sorted(set(rows)), dtype=np.int64)
+            lo, hi = offsets[e], offsets[e + 1]
+            rows.update((lo, hi - 1))
+            for t0 in range(lo, hi, 64):
+                rows.add(int(t0 + rng.integers(0, min(64, hi - t0))))
+    rows = np.array(sorted(rows), dtype=np.int64)
     ref, S = oracle_mod.grouped_gemm(fmt, offsets, A, SA, B, SB, N, K, rows=rows)
     assert_within(C[rows], ref, S, OUT_BF16, f"{name} {fmt_name} {desc}")

@@ -9,7 +9,7 @@ codes and row-major scales.
 import numpy as np
 import pytest
 
-from gpu_util import OUT_BF16, OUT_F32, assert_within, lib, sample_indices, to_dev
+from gpu_util import OUT_BF16, OUT_F32, assert_within, lib, tile_sample_indices, to_dev
 from mx_block_scaled_gb300.inputs import FMT_MXFP4, FMT_MXFP8, with_outlier_blocks
 from test_gemm_gpu import relayout_reference
 from test_oracle_quantize import _wide_range_input
@@ -204,7 +204,7 @@ def test_activation_shapes_full_size_sampled(oracle_mod, name, M, K):
     bits = _bf16_bits(x)
     del x
     dx = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
-    rows = sample_indices(M, seed=M + K)
+    rows = tile_sample_indices(M, M + K)  # one row in every 128-row scale tile
     r = rows[:, None]
     j = np.arange(K // 32)[None, :]
     pos = ((r // 128) * (K // 128) + j // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + j % 4
