@@ -582,13 +582,15 @@ __device__ __noinline__ void sk_fixup_chunk(const GemmParams &p, int tile, int t
 }
 
 // The fixup warps: take jobs until the stop job (or an abort / time-out).
-// Warp fw adds column half fw of the CTA's 128 rows, four lane quarters.
+// Warp fw adds column half fw of the CTA's 128 rows, four lane quarters (a
+// tile of 32 columns has one half: warp 1 then only takes part in the hand-off).
 template <int BN, int kCols, int kChunks>
 __device__ __noinline__ void sk_fixup_warps(const GemmParams &p, const SkFix &slot, uint32_t bar_full,
                                                uint32_t bar_empty, int halves, int half, volatile int *abort,
                                                uint64_t lim)
 {
     const int fw = static_cast<int>(threadIdx.x >> 5) - kFixWarp0;
+    const bool has_cols = fw * kCols < BN;
     const int lane = static_cast<int>(threadIdx.x & 31);
     for (uint32_t j = 0;; ++j) {
         if (!warp_wait(bar_full, j & 1u, abort, lim)) {
@@ -601,6 +603,8 @@ __device__ __noinline__ void sk_fixup_warps(const GemmParams &p, const SkFix &sl
             mbar_arrive(bar_empty);  // this warp holds the job: the slot may be reused
         if (job.tile < 0)
             return;
+        if (!has_cols)
+            continue;
         __threadfence();  // the other segments' partials, published before their arrivals
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
@@ -622,16 +626,20 @@ __device__ __noinline__ void sk_fixup_warps(const GemmParams &p, const SkFix &sl
 
 // Stream-K epilogue of one CTA's 128-row share of a tile cut between CTAs (or
 // CTA pairs): publish this segment's FP32 partial sum; if it is the last
-// segment of the tile to arrive, post the tile's fixup to the fixup warps
-// (every segment's partial added in k order, this CTA's own re-read from its
-// slot).
+// segment of the tile to arrive, the tile's segments are added in k order --
+// by the fixup warps (the job is posted to them; this CTA's own partial is
+// re-read from its slot), or, for tiles of at most 64 columns (kEpiFix: the
+// weight-streaming decode tiles, whose partials are 16-32 KB), by these
+// epilogue warps themselves: 128-256 threads with two segments' loads in
+// flight at a time finish in one or two L2 round trips, where the two fixup
+// warps would take several.  Either way each element is ((0 + s_first) + ...) + s_last.
 //   unit:   the CTA's (or pair's) stream-K index; slots are numbered
 //           ((2 * unit + w.slot) * halves + half) -- `halves` 128-row shares
 //           per tile (1: single CTA, 2: CTA pair), `half` this CTA's share;
 //   row0:   first A-role row of this CTA's share.
 // Slot layout [h][chunk][4-column group][row]: each warp access is 32
 // consecutive 16-byte vectors (the rows of one TMEM lane quarter).
-template <int BN, int kCols, int kChunks>
+template <int BN, int kCols, int kChunks, bool kEpiFix = false>
 __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, const uint32_t (&r)[kChunks][32],
                                             int unit, int halves, int half, int row0, int h, int row_local,
                                             bool has_cols, int *sk_last, SkFix &fx, uint32_t fix_full,
@@ -667,6 +675,71 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
     epi_bar_sync();  // sk_last is read before the next segment may rewrite it
     if (!last)
         return;
+    if constexpr (kEpiFix) {
+        __threadfence();  // the other segments' partials, published before their arrivals
+        const int i = row0 + row_local;
+        if (!has_cols || i >= p.rows_a)
+            return;
+        const long long base_off = static_cast<long long>(i) * p.stride_i;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+            const int j0 = w.tn * BN + h * kCols + c * 32;
+            if (j0 >= p.rows_b)
+                break;
+            float sum[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                sum[e] = 0.0f;
+#pragma unroll 1
+            for (int cc0 = c_first; cc0 <= c_last; cc0 += 2) {
+                float4 x[2][8];
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int cc = cc0 + g;  // uniform over the CTA
+                    if (cc == unit) {         // this CTA's own segment: still in registers
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            x[g][v] = make_float4(__uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1]),
+                                                  __uint_as_float(r[c][4 * v + 2]), __uint_as_float(r[c][4 * v + 3]));
+                    } else if (cc <= c_last) {
+                        const long long beg = p.sk_stages * cc / p.sk_ctas;
+                        const int slot = (beg / p.kstages == w.tile - p.dp_tiles) ? 0 : 1;
+                        const float4 *src =
+                            reinterpret_cast<const float4 *>(
+                                p.sk_partials + static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
+                            (h * kChunks + c) * 8 * kBM + row_local;
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            x[g][v] = __ldcg(src + v * kBM);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            x[g][v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const bool keep = cc0 + g <= c_last;  // a select, not a product: partials may hold NaN
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        sum[4 * v] += keep ? x[g][v].x : 0.0f;
+                        sum[4 * v + 1] += keep ? x[g][v].y : 0.0f;
+                        sum[4 * v + 2] += keep ? x[g][v].z : 0.0f;
+                        sum[4 * v + 3] += keep ? x[g][v].w : 0.0f;
+                    }
+                }
+            }
+            uint32_t bits[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                bits[e] = __float_as_uint(sum[e]);
+            if (p.vec_ok && j0 + 32 <= p.rows_b)
+                store_row32_vec(p, base_off + j0, bits);
+            else
+                store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), bits);
+        }
+        return;
+    }
     if (threadIdx.x == 64) {
         __threadfence();
         const SkFix job{w.tile, w.tn, c_first, c_last, row0};
@@ -693,7 +766,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     __shared__ uint64_t fix_bars[2];  // stream-K fixup hand-off: full, empty
     __shared__ SkFix sk_fix;
     constexpr bool kSk = SK;  // this instantiation runs stream-K plans (fixup warps 10, 11)
-    static_assert(!SK || (!GROUPED && BN == 256), "stream-K: plain 128 x 256 tiles only");
+    static_assert(!SK || !GROUPED, "stream-K: plain (not grouped) tiles only");
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -739,6 +812,9 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         tmem_alloc(smem_addr(&tmem_base_holder), C::kTmemCols);
         tmem_relinquish();
     }
+    // Everything above overlaps the end of the preceding kernel (programmatic
+    // dependent launch); from here on global memory it wrote may be read.
+    griddep_wait();
     if constexpr (GROUPED) {
         if (warp == 2)
             build_group_table<BN>(p, gtab, lane);
@@ -987,9 +1063,9 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             if constexpr (kSk) {
                 if (w.kind == 1) {
                     // stream-K segment: publish, and queue the tile's fixup if this CTA is last
-                    sk_epilogue<BN, kCols, kChunks>(p, w, r, first_unit, 1, 0, tm * kBM, h, row_local, has_cols,
-                                                    &sk_last, sk_fix, smem_addr(&fix_bars[0]),
-                                                    smem_addr(&fix_bars[1]), sk_posted, abort, lim);
+                    sk_epilogue<BN, kCols, kChunks, (BN <= 64)>(p, w, r, first_unit, 1, 0, tm * kBM, h, row_local,
+                                                                has_cols, &sk_last, sk_fix, smem_addr(&fix_bars[0]),
+                                                                smem_addr(&fix_bars[1]), sk_posted, abort, lim);
                     continue;
                 }
             }
@@ -1024,7 +1100,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         // ------------------------------------------------- stream-K fixup
         if constexpr (kSk) {
             if (p.sk_ctas > 0) {
-                constexpr int kCols = BN / 2;
+                constexpr int kCols = BN / 2 >= 32 ? BN / 2 : 32;  // as in the epilogue
                 sk_fixup_warps<BN, kCols, kCols / 32>(p, sk_fix, smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]),
                                                       1, 0, abort, lim);
             }

@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         tmem_alloc_pair(smem_addr(&tmem_base_holder), C::kTmemCols);
         tmem_relinquish_pair();
     }
+    // Everything above overlaps the end of the preceding kernel (programmatic
+    // dependent launch); from here on global memory it wrote may be read.
+    griddep_wait();
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // barriers of both CTAs initialised before any cross-CTA arrive
@@ -140,6 +143,10 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         // Both CTAs load their own halves; every copy completes on the even CTA's
         // `full` barrier, which only the even CTA arms (with both CTAs' bytes).
         if (!p.test_stall) {
+            // Operands re-read by many tiles stay in L2 (evict-last); a streamed
+            // one (read by at most two tiles) is loaded evict-first.
+            const uint64_t pol_a = p.stream_a ? l2_policy_evict_first() : l2_policy_evict_last();
+            const uint64_t pol_b = p.stream_b ? l2_policy_evict_first() : l2_policy_evict_last();
             int st = 0;
             uint32_t ph = 0;
             uint32_t armed = 0, armed_ph = 0;
@@ -170,9 +177,9 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                         const uint32_t bar = map_to_cta(full_bar(st), 0);
                         if (leader)
                             mbar_arrive_expect_tx(full_bar(st), pair_bytes);
-                        tma_load_2d_pair(sA + st * C::kABytes, &map_a, bar, ks * kRowBytes, rb_a * kBM);
-                        tma_load_2d_pair(sB + st * C::kBBytes, &map_b, bar, ks * kRowBytes,
-                                         tn * BN + static_cast<int>(rank) * (BN / 2));
+                        tma_load_2d_pair_hint(sA + st * C::kABytes, &map_a, bar, ks * kRowBytes, rb_a * kBM, pol_a);
+                        tma_load_2d_pair_hint(sB + st * C::kBBytes, &map_b, bar, ks * kRowBytes,
+                                              tn * BN + static_cast<int>(rank) * (BN / 2), pol_b);
                         // scale chunks: rows of 256 bytes, two per 512-byte chunk
                         if (C::kScaled && has_sfa)
                             tma_load_2d_pair(sSFA + st * C::kSfaBytes, &map_sfa, bar, 0, (rb_a * p.num_kt + kt0) * 2);

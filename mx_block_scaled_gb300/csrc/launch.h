@@ -9,6 +9,34 @@
 
 namespace mxg {
 
+// Launch configuration: `grid` CTAs of `threads`, programmatic stream
+// serialization allowed, and clusters of `cluster` CTAs when cluster > 1.
+inline cudaLaunchConfig_t launch_config(int grid, int threads, int smem, cudaStream_t s, cudaLaunchAttribute (&attr)[2],
+                                        int cluster, bool pdl = true)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cfg;
+}
+
 // Set the shared-memory opt-in of every GEMM instantiation on the current
 // device.  Must run (once per device) before any launch below.
 cudaError_t prepare_gemm_fp8();

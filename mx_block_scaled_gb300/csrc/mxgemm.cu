@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(256)
     relayout_scales_kernel(RelayoutJob j0, RelayoutJob j1, int *zero, int nzero)
 {
     __shared__ uint32_t tile[128][kRelayoutKt + 1];
+    mxg::griddep_launch_dependents();  // the GEMM that follows may start its prologue
     int b = blockIdx.x;
     if (b == 0)
         for (int i = threadIdx.x; i < nzero; i += 256)
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(256)
     __shared__ int row0[mxg::kMaxGroups];
     __shared__ int rows[mxg::kMaxGroups];
     __shared__ uint32_t tile[128][kRelayoutKt + 1];
+    mxg::griddep_launch_dependents();  // the grouped GEMM that follows may start its prologue
     if (threadIdx.x < 32)
         mxg::group_scan(offsets, groups, total_rows, 128, 1, static_cast<int>(threadIdx.x), nullptr, tok_rb, row0,
                         rows);
@@ -226,6 +228,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
                                                              long long n, long long slab, void *out,
                                                              int out_kind)
 {
+    mxg::griddep_wait();  // launched as a programmatic dependent of the GEMM that wrote `part`
     const long long n4 = n / 4;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -424,20 +427,28 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     int bn = pick_bn(rows_b);
     if (flags & MXGEMM_PLAN_FORCE_BN128) bn = 128;
     if (flags & MXGEMM_PLAN_FORCE_BN256) bn = 256;
-    // Pair tiles need 128- or 256-wide N tiles.  Default: MXFP8
-    // with at least 128 rows on each side runs 256 x 256 pair tiles (measured
-    // faster from 128 tokens up); MXFP4, whose MMAs are issue-bound in both
-    // modes, and swapped decode shapes stay on single-CTA tiles.
+    // Pair tiles need 128- or 256-wide N tiles.  Default: MXFP8 and BF16 with
+    // at least 128 rows on each side run 256 x 256 pair tiles (measured faster
+    // from 128 tokens up).  An MXFP4 k-stage moves the same operand bytes as an
+    // MXFP8 one in the same MMA time, so it gains the same from the pair tile's
+    // halved B-operand loads -- measured +8-13% from four waves of pair tiles
+    // up (8192^3, 16384 x 8192 x 8192, 8192 x 4096 x 14336) but 2-4% slower at
+    // 3.4 waves (4096^3, 2048 x 4096 x 4096), so MXFP4 takes pair tiles from
+    // four waves on.  Swapped decode shapes stay on single-CTA tiles.
     int mode = 0;
-    if ((fmt == MXGEMM_FMT_MXFP8_E4M3 || bf16) && !swap && rows_a >= 128 && rows_b >= 256 &&
-        !(flags & MXGEMM_PLAN_FORCE_BN128) && ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0)
+    const bool pair_ok = !swap && rows_a >= 128 && rows_b >= 256 && !(flags & MXGEMM_PLAN_FORCE_BN128) &&
+                         ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0;
+    const int64_t pair_tiles = ceil_div(rows_a, 256) * ceil_div(rows_b, 256);
+    if (pair_ok && (fmt == MXGEMM_FMT_MXFP8_E4M3 || bf16))
+        mode = 1;
+    if (pair_ok && fmt == MXGEMM_FMT_MXFP4_E2M1 && pair_tiles >= 4 * (dev->num_sms / 2))
         mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_SINGLE) mode = 0;
     if (mode != 0 && bn < 128) bn = 128;
-    // Stream-K runs on 256-wide tiles only (the instantiations with fixup
-    // warps): a forced stream-K plan takes them.
-    if (flags & MXGEMM_PLAN_STREAMK) bn = 256;
+    // Stream-K on CTA pairs runs on 256-wide tiles only (the pair instantiation
+    // with fixup warps): a forced stream-K pair plan takes them.
+    if ((flags & MXGEMM_PLAN_STREAMK) && mode == 1) bn = 256;
     p->mode = mode;
     p->bn = bn;
     // tiles_m counts the work units along the A role: 128-row tiles (single),
@@ -491,10 +502,17 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         const int64_t full_waves = tiles / G;
         const bool spread = p->kstages >= 96 && full_waves >= 3;
         const bool halves = full_waves * p->kstages >= 96 && 2 * (tiles % G) <= G;
+        // Weight-streaming decode (swap-AB, single-CTA tiles of <= 64 tokens):
+        // every SM should stream an equal share of the weight from the start,
+        // so the k-stages of the tiles past the full waves are spread evenly
+        // over all SMs; the cut tiles' partial sums are small (128 x BN FP32)
+        // and are added by the fixup warps of the last CTA to arrive, which
+        // replaces the separate split-K reduce launch.
+        const bool decode = swap && mode == 0 && p->bn <= 64;
         const bool want = (flags & MXGEMM_PLAN_STREAMK)
                               ? dp_eff < 0.95
-                              : (!(flags & MXGEMM_PLAN_NO_STREAMK) && p->bn == 256 && dp_eff < 0.90 &&
-                                 (spread || halves));
+                              : (!(flags & MXGEMM_PLAN_NO_STREAMK) && dp_eff < 0.90 &&
+                                 ((p->bn == 256 && (spread || halves)) || decode));
         if (want) {
             const int64_t dp = (tiles / G) * G;
             const int64_t sk_stages = (tiles - dp) * p->kstages;
@@ -502,7 +520,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
             // Long k-loops spread the cut tiles' stages over every slot.  Short
             // ones cut each tile in at most two segments, so that the fixup adds
             // two partial sums (the fixup warps' fast path) and stays short.
-            const bool spread_units = (flags & MXGEMM_PLAN_STREAMK) ? p->kstages >= 96 : spread;
+            const bool spread_units = (flags & MXGEMM_PLAN_STREAMK) ? (p->kstages >= 96 || decode) : (spread || decode);
             const int64_t units = spread_units ? std::min<int64_t>(G, sk_stages / min_seg)
                                                : std::min<int64_t>(G, 2 * (tiles - dp));
             p->dp_tiles = static_cast<int>(dp);
@@ -812,10 +830,12 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
         const long long n4 = n / 4;
         int blocks = static_cast<int>(std::min<long long>(std::max<long long>(1, (n4 + 255) / 256),
                                                           static_cast<long long>(plan->num_sms) * 8));
-        splitk_reduce_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float *>(ws + plan->off_part),
-                                                    plan->splits, n, (n + 3) & ~3ll, C,
-                                                    plan->out == MXGEMM_OUT_BF16 ? mxg::OUT_BF16 : mxg::OUT_F32);
-        if (cudaGetLastError() != cudaSuccess)
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = mxg::launch_config(blocks, 256, 0, s, attr, 1);
+        if (cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, reinterpret_cast<const float *>(ws + plan->off_part),
+                               plan->splits, n, (n + 3) & ~3ll, static_cast<void *>(C),
+                               plan->out == MXGEMM_OUT_BF16 ? static_cast<int>(mxg::OUT_BF16)
+                                                            : static_cast<int>(mxg::OUT_F32)) != cudaSuccess)
             return MXGEMM_ERR_CUDA;
     }
     return MXGEMM_OK;

@@ -111,6 +111,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const v
     return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// ------------------------------------------ programmatic dependent launch --
+// Block until every grid this launch depends on (the preceding kernel in the
+// stream, when this one was launched with programmatic stream serialization)
+// has completed and its memory operations are visible.  A no-op otherwise.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the dependent launch that follows in the stream to be scheduled now
+// (it still waits in griddep_wait for this grid to complete).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------- cluster --
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
@@ -210,6 +220,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// The same with an L2 eviction-policy hint (createpolicy) for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
+                                                      int32_t y, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
 }
 

@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(QuantParams p)
 {
     using T = QTraits<FMT, IN>;
     constexpr int G = T::kG;
+    // a GEMM launched after this kernel (programmatic dependent launch) may run
+    // its prologue now; it waits for this grid to complete before reading
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t K = p.K;
     const int64_t units_per_row = (K + kChunk * G - 1) / (kChunk * G);

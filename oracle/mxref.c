@@ -38,7 +38,7 @@
  * 2i+1 the high nibble.  Decoding is by table (16 entries for E2M1, 256 for
  * E4M3 and E8M0); NaN codes decode to NaN and propagate through the sums.
  *
- * Built with: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (oracle/build.py).
+ * Built with: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (by build() in oracle/mxref.py).
  */
 #include <math.h>
 #include <stddef.h>

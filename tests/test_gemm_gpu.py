@@ -209,6 +209,27 @@ def test_stream_k_exact(oracle_mod, fmt, mode, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+@pytest.mark.parametrize("M,N,K", [(8, 1280, 4096), (64, 2048, 4096), (1, 384, 1024), (33, 8192, 1024),
+                                   (8, 20480, 1024)])
+def test_decode_default_plans_stream_k_exact(oracle_mod, fmt, M, N, K):
+    """Weight-streaming decode shapes (swap-AB, 32- or 64-token tiles): the
+    default plan spreads the k-stages of the tiles beyond the full waves over
+    every SM (stream-K), cutting tiles into up to ~8 segments whose partial
+    sums the fixup warps add in k order; the result is exact, FP32 and BF16 out."""
+    rng = np.random.default_rng([M, N, K, fmt])
+    A, SA = small_int_codes(rng, M, K, fmt)
+    B, SB = small_int_codes(rng, N, K, fmt)
+    ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
+    C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, return_plan=True)
+    assert "swap_ab=1" in desc and "/0 " not in desc.split("streamk=")[1][:16], desc
+    assert (C == ref).all(), desc
+    import torch
+    expect = torch.from_numpy(ref.astype(np.float32)).bfloat16().double().numpy()
+    C2 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16)
+    assert (C2 == expect).all(), desc
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
 def test_prelayout_scales_give_the_same_result(fmt):
     import torch
     b = lib()
