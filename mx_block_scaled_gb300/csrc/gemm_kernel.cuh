@@ -55,6 +55,14 @@ constexpr int kBM = 128;            // MMA M (rows of the A role per tile)
 constexpr int kRowBytes = 128;      // bytes of one operand row per k-stage
 constexpr int kSfChunk = 512;       // bytes of one scale chunk (128 rows x 4 K-blocks)
 constexpr int kSmemBudget = 232448; // 227 KiB opt-in shared memory per block
+// Scale factors travel in groups of kSfGroup k-stages: one copy per operand
+// brings a group's chunks into one of two shared-memory group slots, and the
+// MMA warp moves the whole group into TMEM at the group's first stage.  A TMA
+// or bulk copy has a fixed cost of its own, and per-stage scale copies (three
+// small ones per k-stage beside two operand tiles) cost more main-loop time
+// than the operand tiles themselves (measured: skipping them took a long-K
+// CTA-pair GEMM from 0.359 to 0.320 us per k-stage).
+constexpr int kSfGroup = 4;
 
 enum OutKind : int { OUT_F32 = 0, OUT_BF16 = 1 };
 
@@ -201,23 +209,28 @@ struct Cfg {
     static constexpr int kChunksB = BN >= 128 ? BN / 128 : 1; // 128-row scale chunks of B per K-tile
     static constexpr int kABytes = kBM * kRowBytes;
     static constexpr int kBBytes = BN * kRowBytes;
-    static constexpr int kSfaBytes = kScaled ? kKtPerStage * kSfChunk : 0;
-    static constexpr int kSfbBytes = kScaled ? kChunksB * kKtPerStage * kSfChunk : 0;
-    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-    static constexpr int kStagesRaw = (kSmemBudget - 1024 - 256) / kStageBytes;
+    static constexpr int kStageBytes = kABytes + kBBytes;     // operand ring slot
+    // scale group slot: SFA chunks [stage][K-tile], then SFB chunks [128-row block][stage][K-tile]
+    static constexpr int kSfaGrpBytes = kScaled ? kSfGroup * kKtPerStage * kSfChunk : 0;
+    static constexpr int kSfbGrpBytes = kScaled ? kChunksB * kSfGroup * kKtPerStage * kSfChunk : 0;
+    static constexpr int kSfGrpBytes = kSfaGrpBytes + kSfbGrpBytes;
+    static constexpr int kStagesRaw = (kSmemBudget - 1024 - 256 - 2 * kSfGrpBytes) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kSfaCols = kScaled ? 4 * kKtPerStage : 0;
     static constexpr int kSfbCols = kScaled ? 4 * kKtPerStage * kChunksB : 0;
-    static constexpr int kAccStages = (2 * BN + kSfaCols + kSfbCols <= 512) ? 2 : 1;
-    static constexpr int kTmemCols = 512;
-    // Scale columns: one (SFA, SFB) region per ring slot, so the tcgen05.cp of the
-    // next stage never overwrites scales that MMAs of the previous stage still read.
+    // Scale columns: one (SFA, SFB) region per stage of two scale groups, so the
+    // copies of a group never overwrite scales that MMAs of the group before
+    // still read (a group's regions are reused two groups later, after the MMAs
+    // that read them have completed).
     static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
+    static constexpr int kSfRegions = kScaled ? 2 * kSfGroup : 0;
+    static constexpr int kAccStages = (2 * BN + kSfRegions * kSfSlotCols <= 512) ? 2 : 1;
+    static constexpr int kTmemCols = 512;
     static constexpr int kSfCol0 = kAccStages * BN;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2 * kSfGrpBytes + 256;
     static constexpr uint32_t kIdesc = kScaled ? idesc_block_scaled(kFp4 ? 1u : 0u, kBM, BN) : idesc_bf16(kBM, BN);
     static_assert(kStages >= 2, "shared memory too small for two stages");
-    static_assert(kSfCol0 + kStages * kSfSlotCols <= kTmemCols, "TMEM overflow");
+    static_assert(kSfCol0 + kSfRegions * kSfSlotCols <= kTmemCols, "TMEM overflow");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be 32..256, multiple of 32");
 };
 
@@ -771,19 +784,24 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const gbase = smem_raw + (base - raw);
-    // Ring layout: [A x S][B x S][SFA x S][SFB x S][barriers]
+    // Layout: [A x S][B x S][scale group x 2][barriers]
     const uint32_t sA = base;
     const uint32_t sB = sA + S * C::kABytes;
-    const uint32_t sSFA = sB + S * C::kBBytes;
-    const uint32_t sSFB = sSFA + S * C::kSfaBytes;
-    const uint32_t sBar = sSFB + S * C::kSfbBytes;
+    const uint32_t sSF = sB + S * C::kBBytes;
+    const uint32_t sBar = sSF + 2 * C::kSfGrpBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + (sBar - base));
     (void)bars;
+    (void)gbase;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
     auto accf_bar = [&](int a) { return sBar + 8u * (2 * S + a); };
     auto acce_bar = [&](int a) { return sBar + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = sBar + 8u * (2 * S + 4);
+    // scale groups: slot landed (sfull), slot copied to TMEM (sempty), the
+    // group's TMEM regions read by all its MMAs (tfree)
+    auto sfull_bar = [&](int g) { return sBar + 8u * (2 * S + 5 + g); };
+    auto sempty_bar = [&](int g) { return sBar + 8u * (2 * S + 7 + g); };
+    auto tfree_bar = [&](int g) { return sBar + 8u * (2 * S + 9 + g); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -800,6 +818,9 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
             mbar_init(acce_bar(a), kEpiWarps);
+            mbar_init(sfull_bar(a), 1);
+            mbar_init(sempty_bar(a), 1);
+            mbar_init(tfree_bar(a), 1);
         }
         mbar_init(drain_bar, 1);
         mbar_init(smem_addr(&fix_bars[0]), 1);
@@ -847,6 +868,8 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             uint32_t ph = 0;
             uint32_t armed = 0;      // bit s: slot s armed at least once
             uint32_t armed_ph = 0;   // bit s: parity of slot s's last arm
+            int gi = 0;              // scale groups issued
+            uint32_t sarmed = 0, sarmed_ph = 0;  // the same for the two scale group slots
             bool ok = true;
             WorkIter wi;
             wi.init(p, first_unit, unit_step, gt, tok_tile);
@@ -861,29 +884,44 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 const int rb_b0 = g.sfb_rb0;
                 const int nchunk_b = g.nchunk_b;
                 for (int ks = ks0; ks < ks1; ++ks) {
+                    const int kt0 = ks * C::kKtPerStage;
+                    if (C::kScaled && (ks - ks0) % kSfGroup == 0) {
+                        // the scales of k-stages [ks, ks + kSfGroup) into group slot gs:
+                        // one bulk copy per operand (per 128-row block of the B role)
+                        const int gs = gi & 1;
+                        const uint32_t use = static_cast<uint32_t>(gi >> 1);
+                        if (gi >= 2 && !warp_wait(sempty_bar(gs), (use & 1u) ^ 1u, abort, lim)) {
+                            if (lane == 0) record_timeout(p, abort);
+                            ok = false;
+                            break;
+                        }
+                        const int nkt_g = min(kSfGroup * C::kKtPerStage, p.num_kt - kt0);
+                        const uint32_t gbytes = nkt_g * kSfChunk * ((has_sfa ? 1 : 0) + nchunk_b);
+                        const uint32_t dst = sSF + gs * C::kSfGrpBytes;
+                        if (elect_one()) {
+                            mbar_arrive_expect_tx(sfull_bar(gs), gbytes);
+                            if (has_sfa)
+                                bulk_load(dst, p.sfa + (static_cast<size_t>(g.sfa_rb) * p.num_kt + kt0) * kSfChunk,
+                                          nkt_g * kSfChunk, sfull_bar(gs));
+                            for (int c = 0; c < nchunk_b; ++c)
+                                bulk_load(dst + C::kSfaGrpBytes + c * kSfGroup * C::kKtPerStage * kSfChunk,
+                                          p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
+                                          nkt_g * kSfChunk, sfull_bar(gs));
+                        }
+                        __syncwarp();
+                        sarmed |= 1u << gs;
+                        sarmed_ph = (sarmed_ph & ~(1u << gs)) | ((use & 1u) << gs);
+                        ++gi;
+                    }
                     if (!warp_wait(empty_bar(st), ph ^ 1u, abort, lim)) {
                         if (lane == 0) record_timeout(p, abort);
                         ok = false;
                         break;
                     }
-                    const int kt0 = ks * C::kKtPerStage;
-                    const int nkt = min(C::kKtPerStage, p.num_kt - kt0);
-                    const uint32_t bytes =
-                        C::kABytes + C::kBBytes + (C::kScaled ? nkt * kSfChunk * ((has_sfa ? 1 : 0) + nchunk_b) : 0);
                     if (elect_one()) {
-                        mbar_arrive_expect_tx(full_bar(st), bytes);
+                        mbar_arrive_expect_tx(full_bar(st), C::kABytes + C::kBBytes);
                         tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, g.a_row, pol_a);
                         tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, g.b_row, pol_b);
-                        if constexpr (C::kScaled) {
-                            if (has_sfa)
-                                bulk_load(sSFA + st * C::kSfaBytes,
-                                          p.sfa + (static_cast<size_t>(g.sfa_rb) * p.num_kt + kt0) * kSfChunk,
-                                          nkt * kSfChunk, full_bar(st));
-                            for (int c = 0; c < nchunk_b; ++c)
-                                bulk_load(sSFB + st * C::kSfbBytes + c * C::kKtPerStage * kSfChunk,
-                                          p.sfb + (static_cast<size_t>(rb_b0 + c) * p.num_kt + kt0) * kSfChunk,
-                                          nkt * kSfChunk, full_bar(st));
-                        }
                     }
                     __syncwarp();
                     armed |= 1u << st;
@@ -895,10 +933,13 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 }
             }
             if (!ok) {
-                // Drain: let every armed stage finish landing before the CTA exits.
+                // Drain: let every armed stage and scale group finish landing before the CTA exits.
                 for (int s2 = 0; s2 < S; ++s2)
                     if (armed & (1u << s2))
                         warp_wait(full_bar(s2), (armed_ph >> s2) & 1u, no_abort, lim);
+                for (int g2 = 0; g2 < 2; ++g2)
+                    if (sarmed & (1u << g2))
+                        warp_wait(sfull_bar(g2), (sarmed_ph >> g2) & 1u, no_abort, lim);
             }
         }
     } else if (warp == 1) {
@@ -908,36 +949,51 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         int st = 0;
         uint32_t ph = 0;
         int it = 0;
+        int gi = 0;  // scale groups started
         bool ok = true;
         bool issued = false;
-        // Stage (slot s_, k-stage k_) in: wait until the slot has landed, then
-        // tcgen05.cp its scale chunks into the slot's own TMEM scale region.
-        auto stage_in = [&](int s_, uint32_t ph_, int k_) -> bool {
-            if (!warp_wait(full_bar(s_), ph_, abort, lim))
+        // Scale group in, at the group's first k-stage k_ (n_ stages of this work
+        // unit in the group): wait until the group slot has landed and the TMEM
+        // regions it goes to are no longer read (the MMAs of the group two
+        // before have completed), tcgen05.cp every stage's chunks into its own
+        // TMEM region, and commit so the producer may refill the slot.
+        auto group_in = [&](int k_, int n_) -> bool {
+            const int gs = gi & 1;
+            const uint32_t use = static_cast<uint32_t>(gi >> 1);
+            if (!warp_wait(sfull_bar(gs), use & 1u, abort, lim))
+                return false;
+            if (gi >= 2 && !warp_wait(tfree_bar(gs), (use & 1u) ^ 1u, abort, lim))
                 return false;
             tc_fence_after();
-            const int nkt_ = min(C::kKtPerStage, p.num_kt - k_ * C::kKtPerStage);
-            const uint32_t sfa_col_ = tmem + C::kSfCol0 + s_ * C::kSfSlotCols;
-            const uint32_t sfb_col_ = sfa_col_ + C::kSfaCols;
-            const uint32_t sfa_src = sSFA + s_ * C::kSfaBytes;
-            const uint32_t sfb_src = sSFB + s_ * C::kSfbBytes;
-            // one elected lane issues the stage's copies (and, below, its MMAs
-            // and commit) in one block: separate elect blocks per instruction
+            const uint32_t src = sSF + gs * C::kSfGrpBytes;
+            // one elected lane issues the group's copies (and, below, the MMAs
+            // and commits) in one block: separate elect blocks per instruction
             // measured up to 10% slower on long k-loops
             if (elect_one()) {
+#pragma unroll 1
+                for (int j = 0; j < n_; ++j) {
+                    const int nkt_ = min(C::kKtPerStage, p.num_kt - (k_ + j) * C::kKtPerStage);
+                    const uint32_t sfa_col_ = tmem + C::kSfCol0 + (gs * kSfGroup + j) * C::kSfSlotCols;
+                    const uint32_t sfb_col_ = sfa_col_ + C::kSfaCols;
 #pragma unroll
-                for (int t = 0; t < C::kKtPerStage; ++t) {
-                    if (C::kScaled && t < nkt_) {
-                        tc_cp_32x128b_warpx4(sfa_col_ + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
+                    for (int t = 0; t < C::kKtPerStage; ++t) {
+                        if (t < nkt_) {
+                            tc_cp_32x128b_warpx4(sfa_col_ + 4 * t,
+                                                 sdesc_sf_chunk(src + (j * C::kKtPerStage + t) * kSfChunk));
 #pragma unroll
-                        for (int c = 0; c < C::kChunksB; ++c)
-                            tc_cp_32x128b_warpx4(sfb_col_ + 4 * (t * C::kChunksB + c),
-                                                 sdesc_sf_chunk(sfb_src + (c * C::kKtPerStage + t) * kSfChunk));
+                            for (int c = 0; c < C::kChunksB; ++c)
+                                tc_cp_32x128b_warpx4(
+                                    sfb_col_ + 4 * (t * C::kChunksB + c),
+                                    sdesc_sf_chunk(src + C::kSfaGrpBytes +
+                                                   ((c * kSfGroup + j) * C::kKtPerStage + t) * kSfChunk));
+                        }
                     }
                 }
+                tc_commit(sempty_bar(gs));
             }
             __syncwarp();
             issued = true;
+            ++gi;
             return true;
         };
         WorkIter wi;
@@ -958,14 +1014,25 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             const int ks0 = w.ks0;
             const int ks1 = w.ks1;
             for (int ks = ks0; ks < ks1; ++ks) {
-                if (!stage_in(st, ph, ks)) {
+                const int rel = ks - ks0;
+                if (C::kScaled && rel % kSfGroup == 0 && !group_in(ks, min(kSfGroup, ks1 - ks))) {
                     if (lane == 0) record_timeout(p, abort);
                     ok = false;
                     break;
                 }
+                if (!warp_wait(full_bar(st), ph, abort, lim)) {
+                    if (lane == 0) record_timeout(p, abort);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issued = true;
                 const int nkt = min(C::kKtPerStage, p.num_kt - ks * C::kKtPerStage);
-                const uint32_t sfa_col = tmem + C::kSfCol0 + st * C::kSfSlotCols;
+                const int gcur = gi - 1;  // the group this stage belongs to
+                const uint32_t sfa_col =
+                    tmem + C::kSfCol0 + ((gcur & 1) * kSfGroup + rel % kSfGroup) * C::kSfSlotCols;
                 const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                const bool group_end = C::kScaled && (rel % kSfGroup == kSfGroup - 1 || ks == ks1 - 1);
                 const uint64_t adesc = sdesc_kmajor_sw128(sA + st * C::kABytes);
                 const uint64_t bdesc = sdesc_kmajor_sw128(sB + st * C::kBBytes);
                 const uint32_t acc0 = (ks > ks0) ? 1u : 0u;
@@ -992,6 +1059,8 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                         }
                     }
                     tc_commit(empty_bar(st));
+                    if (group_end)
+                        tc_commit(tfree_bar(gcur & 1));  // this group's TMEM scale regions are free again
                 }
                 __syncwarp();
                 if (++st == S) {

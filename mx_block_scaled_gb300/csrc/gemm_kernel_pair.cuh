@@ -39,20 +39,24 @@ struct CfgPair {
     static constexpr int kChunksB = BN / 128;                 // B-role scale chunks per K-tile (all BN rows)
     static constexpr int kABytes = kBM * kRowBytes;           // own 128 A-role rows
     static constexpr int kBBytes = (BN / 2) * kRowBytes;      // own half of the B-role tile
-    static constexpr int kSfaBytes = kScaled ? kKtPerStage * kSfChunk : 0;
-    static constexpr int kSfbBytes = kScaled ? kChunksB * kKtPerStage * kSfChunk : 0;
-    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-    static constexpr int kStagesRaw = (kSmemBudget - 1024 - 512) / kStageBytes;
+    static constexpr int kStageBytes = kABytes + kBBytes;     // operand ring slot
+    // scale group slot (see kSfGroup): SFA chunks of this CTA's 128 rows
+    // [stage][K-tile], then the SFB chunks of all BN rows [128-row block][stage][K-tile]
+    static constexpr int kSfaGrpBytes = kScaled ? kSfGroup * kKtPerStage * kSfChunk : 0;
+    static constexpr int kSfbGrpBytes = kScaled ? kChunksB * kSfGroup * kKtPerStage * kSfChunk : 0;
+    static constexpr int kSfGrpBytes = kSfaGrpBytes + kSfbGrpBytes;
+    static constexpr int kStagesRaw = (kSmemBudget - 1024 - 512 - 2 * kSfGrpBytes) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kSfaCols = kScaled ? 4 * kKtPerStage : 0;
     static constexpr int kSfbCols = kScaled ? 4 * kKtPerStage * kChunksB : 0;
     static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
-    static constexpr int kAccStages = (2 * BN + kStages * kSfSlotCols <= 512) ? 2 : 1;
+    static constexpr int kSfRegions = kScaled ? 2 * kSfGroup : 0;
+    static constexpr int kAccStages = (2 * BN + kSfRegions * kSfSlotCols <= 512) ? 2 : 1;
     static constexpr int kSfCol0 = kAccStages * BN;
-    static constexpr int kColsUsed = kSfCol0 + kStages * kSfSlotCols;
+    static constexpr int kColsUsed = kSfCol0 + kSfRegions * kSfSlotCols;
     static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128
                                    : kColsUsed <= 256 ? 256 : 512;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 512;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2 * kSfGrpBytes + 512;
     static constexpr uint32_t kIdesc =
         kScaled ? idesc_block_scaled(kFp4 ? 1u : 0u, 2 * kBM, BN) : idesc_bf16(2 * kBM, BN);
     static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
@@ -81,14 +85,17 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sA = base;
     const uint32_t sB = sA + S * C::kABytes;
-    const uint32_t sSFA = sB + S * C::kBBytes;
-    const uint32_t sSFB = sSFA + S * C::kSfaBytes;
-    const uint32_t sBar = sSFB + S * C::kSfbBytes;
+    const uint32_t sSF = sB + S * C::kBBytes;
+    const uint32_t sBar = sSF + 2 * C::kSfGrpBytes;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
     auto accf_bar = [&](int a) { return sBar + 8u * (3 * S + a); };
     auto acce_bar = [&](int a) { return sBar + 8u * (3 * S + 2 + a); };  // used in the even CTA
     const uint32_t drain_bar = sBar + 8u * (3 * S + 4);
+    // scale groups (sfull and tfree used in the even CTA, sempty in both)
+    auto sfull_bar = [&](int g) { return sBar + 8u * (3 * S + 5 + g); };
+    auto sempty_bar = [&](int g) { return sBar + 8u * (3 * S + 7 + g); };
+    auto tfree_bar = [&](int g) { return sBar + 8u * (3 * S + 9 + g); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -107,6 +114,9 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
             mbar_init(acce_bar(a), 2 * kEpiWarps);
+            mbar_init(sfull_bar(a), 1);
+            mbar_init(sempty_bar(a), 1);
+            mbar_init(tfree_bar(a), 1);
         }
         mbar_init(drain_bar, 1);
         mbar_init(smem_addr(&fix_bars[0]), 1);
@@ -136,7 +146,6 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     const int unit_step = static_cast<int>(cluster_count_x());
     const uint64_t lim = p.timeout_ns;
     const int nrb_a = (p.rows_a + 127) / 128;
-    const int nrb_b = (p.rows_b + 127) / 128;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -150,6 +159,8 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             int st = 0;
             uint32_t ph = 0;
             uint32_t armed = 0, armed_ph = 0;
+            int gi = 0;  // scale groups issued
+            uint32_t sarmed = 0, sarmed_ph = 0;
             bool ok = true;
             WorkIter wi;
             wi.init(p, first_unit, unit_step);
@@ -161,31 +172,49 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 const bool has_sfa = rb_a < nrb_a;
                 const bool peer_has_sfa = 2 * tm + 1 < nrb_a;
                 const int rb_b0 = (tn * BN) / 128;
-                const int nchunk_b = min(C::kChunksB, nrb_b - rb_b0);
-                // bytes of one CTA's copies, as counted by TMA (whole boxes)
-                const uint32_t common = C::kABytes + C::kBBytes + nchunk_b * C::kSfaBytes;
-                const uint32_t pair_bytes =
-                    2 * common + ((has_sfa ? 1 : 0) + (peer_has_sfa ? 1 : 0)) * C::kSfaBytes;
+                // bytes of both CTAs' copies, as counted by TMA (whole boxes; a box
+                // partly past the tensor is zero-filled and counted in full)
+                const uint32_t stage_bytes = 2 * (C::kABytes + C::kBBytes);
+                const uint32_t group_bytes =
+                    2 * C::kSfbGrpBytes + ((has_sfa ? 1 : 0) + (peer_has_sfa ? 1 : 0)) * C::kSfaGrpBytes;
                 for (int ks = ks0; ks < ks1; ++ks) {
+                    const int kt0 = ks * C::kKtPerStage;
+                    if (C::kScaled && (ks - ks0) % kSfGroup == 0) {
+                        // the scales of k-stages [ks, ks + kSfGroup): this CTA's A-role
+                        // rows and every B-role row, one 3-D box each (chunks of 2 rows x 256 B)
+                        const int gs = gi & 1;
+                        const uint32_t use = static_cast<uint32_t>(gi >> 1);
+                        if (gi >= 2 && !warp_wait_cluster(sempty_bar(gs), (use & 1u) ^ 1u, abort, lim)) {
+                            if (lane == 0) record_timeout(p, abort);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst = sSF + gs * C::kSfGrpBytes;
+                        if (elect_one()) {
+                            const uint32_t bar = map_to_cta(sfull_bar(gs), 0);
+                            if (leader)
+                                mbar_arrive_expect_tx(sfull_bar(gs), group_bytes);
+                            if (has_sfa)
+                                tma_load_3d_pair(dst, &map_sfa, bar, 0, 2 * kt0, rb_a);
+                            tma_load_3d_pair(dst + C::kSfaGrpBytes, &map_sfb, bar, 0, 2 * kt0, rb_b0);
+                        }
+                        __syncwarp();
+                        sarmed |= 1u << gs;
+                        sarmed_ph = (sarmed_ph & ~(1u << gs)) | ((use & 1u) << gs);
+                        ++gi;
+                    }
                     if (!warp_wait_cluster(empty_bar(st), ph ^ 1u, abort, lim)) {
                         if (lane == 0) record_timeout(p, abort);
                         ok = false;
                         break;
                     }
-                    const int kt0 = ks * C::kKtPerStage;
                     if (elect_one()) {
                         const uint32_t bar = map_to_cta(full_bar(st), 0);
                         if (leader)
-                            mbar_arrive_expect_tx(full_bar(st), pair_bytes);
+                            mbar_arrive_expect_tx(full_bar(st), stage_bytes);
                         tma_load_2d_pair_hint(sA + st * C::kABytes, &map_a, bar, ks * kRowBytes, rb_a * kBM, pol_a);
                         tma_load_2d_pair_hint(sB + st * C::kBBytes, &map_b, bar, ks * kRowBytes,
                                               tn * BN + static_cast<int>(rank) * (BN / 2), pol_b);
-                        // scale chunks: rows of 256 bytes, two per 512-byte chunk
-                        if (C::kScaled && has_sfa)
-                            tma_load_2d_pair(sSFA + st * C::kSfaBytes, &map_sfa, bar, 0, (rb_a * p.num_kt + kt0) * 2);
-                        for (int c = 0; c < (C::kScaled ? nchunk_b : 0); ++c)
-                            tma_load_2d_pair(sSFB + st * C::kSfbBytes + c * C::kSfaBytes, &map_sfb, bar, 0,
-                                             ((rb_b0 + c) * p.num_kt + kt0) * 2);
                     }
                     __syncwarp();
                     armed |= 1u << st;
@@ -200,6 +229,9 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 for (int s2 = 0; s2 < S; ++s2)
                     if (armed & (1u << s2))
                         warp_wait(full_bar(s2), (armed_ph >> s2) & 1u, no_abort, lim);
+                for (int g2 = 0; g2 < 2; ++g2)
+                    if (sarmed & (1u << g2))
+                        warp_wait(sfull_bar(g2), (sarmed_ph >> g2) & 1u, no_abort, lim);
             }
         }
     } else if (warp == 1 && leader) {
@@ -207,36 +239,52 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         int st = 0;
         uint32_t ph = 0;
         int it = 0;
+        int gi = 0;  // scale groups started
         bool ok = true;
         bool issued = false;
-        // Stage (slot s_, k-stage k_) in: wait until both CTAs' halves have
-        // landed, then copy each CTA's scale chunks into its own TMEM.
-        auto stage_in = [&](int s_, uint32_t ph_, int k_) -> bool {
-            if (!warp_wait_cluster(full_bar(s_), ph_, abort, lim))
+        // Scale group in, at the group's first k-stage k_ (n_ stages of this work
+        // unit in the group): wait until both CTAs' group slots have landed and
+        // the TMEM regions the group goes to are no longer read (the MMAs of the
+        // group two before have completed), copy each CTA's chunks into its own
+        // TMEM (one region per stage), and commit so both producers may refill
+        // their slot.
+        auto group_in = [&](int k_, int n_) -> bool {
+            const int gs = gi & 1;
+            const uint32_t use = static_cast<uint32_t>(gi >> 1);
+            if (!warp_wait_cluster(sfull_bar(gs), use & 1u, abort, lim))
+                return false;
+            if (gi >= 2 && !warp_wait(tfree_bar(gs), (use & 1u) ^ 1u, abort, lim))
                 return false;
             tc_fence_after();
-            const int nkt_ = min(C::kKtPerStage, p.num_kt - k_ * C::kKtPerStage);
-            const uint32_t sfa_col_ = tmem + C::kSfCol0 + s_ * C::kSfSlotCols;
-            const uint32_t sfb_col_ = sfa_col_ + C::kSfaCols;
-            const uint32_t sfa_src = sSFA + s_ * C::kSfaBytes;
-            const uint32_t sfb_src = sSFB + s_ * C::kSfbBytes;
-            // one elected lane issues the stage's copies (and, below, its MMAs
-            // and commit) in one block: separate elect blocks per instruction
+            const uint32_t src = sSF + gs * C::kSfGrpBytes;
+            // one elected lane issues the group's copies (and, below, the MMAs
+            // and commits) in one block: separate elect blocks per instruction
             // measured up to 10% slower on long k-loops
             if (elect_one()) {
+#pragma unroll 1
+                for (int j = 0; j < n_; ++j) {
+                    const int nkt_ = min(C::kKtPerStage, p.num_kt - (k_ + j) * C::kKtPerStage);
+                    const uint32_t sfa_col_ = tmem + C::kSfCol0 + (gs * kSfGroup + j) * C::kSfSlotCols;
+                    const uint32_t sfb_col_ = sfa_col_ + C::kSfaCols;
 #pragma unroll
-                for (int t = 0; t < C::kKtPerStage; ++t) {
-                    if (C::kScaled && t < nkt_) {
-                        tc_cp_pair_32x128b_warpx4(sfa_col_ + 4 * t, sdesc_sf_chunk(sfa_src + t * kSfChunk));
+                    for (int t = 0; t < C::kKtPerStage; ++t) {
+                        if (t < nkt_) {
+                            tc_cp_pair_32x128b_warpx4(sfa_col_ + 4 * t,
+                                                      sdesc_sf_chunk(src + (j * C::kKtPerStage + t) * kSfChunk));
 #pragma unroll
-                        for (int c = 0; c < C::kChunksB; ++c)
-                            tc_cp_pair_32x128b_warpx4(sfb_col_ + 4 * (t * C::kChunksB + c),
-                                                      sdesc_sf_chunk(sfb_src + (c * C::kKtPerStage + t) * kSfChunk));
+                            for (int c = 0; c < C::kChunksB; ++c)
+                                tc_cp_pair_32x128b_warpx4(
+                                    sfb_col_ + 4 * (t * C::kChunksB + c),
+                                    sdesc_sf_chunk(src + C::kSfaGrpBytes +
+                                                   ((c * kSfGroup + j) * C::kKtPerStage + t) * kSfChunk));
+                        }
                     }
                 }
+                tc_commit_pair(sempty_bar(gs), 0x3);
             }
             __syncwarp();
             issued = true;
+            ++gi;
             return true;
         };
         WorkIter wi;
@@ -254,14 +302,25 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             const uint32_t d_tmem = tmem + acc * BN;
             const int ks0 = w.ks0, ks1 = w.ks1;
             for (int ks = ks0; ks < ks1; ++ks) {
-                if (!stage_in(st, ph, ks)) {
+                const int rel = ks - ks0;
+                if (C::kScaled && rel % kSfGroup == 0 && !group_in(ks, min(kSfGroup, ks1 - ks))) {
                     if (lane == 0) record_timeout(p, abort);
                     ok = false;
                     break;
                 }
+                if (!warp_wait_cluster(full_bar(st), ph, abort, lim)) {
+                    if (lane == 0) record_timeout(p, abort);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issued = true;
                 const int nkt = min(C::kKtPerStage, p.num_kt - ks * C::kKtPerStage);
-                const uint32_t sfa_col = tmem + C::kSfCol0 + st * C::kSfSlotCols;
+                const int gcur = gi - 1;  // the group this stage belongs to
+                const uint32_t sfa_col =
+                    tmem + C::kSfCol0 + ((gcur & 1) * kSfGroup + rel % kSfGroup) * C::kSfSlotCols;
                 const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                const bool group_end = C::kScaled && (rel % kSfGroup == kSfGroup - 1 || ks == ks1 - 1);
                 const uint64_t adesc = sdesc_kmajor_sw128(sA + st * C::kABytes);
                 const uint64_t bdesc = sdesc_kmajor_sw128(sB + st * C::kBBytes);
                 const uint32_t acc0 = (ks > ks0) ? 1u : 0u;
@@ -286,6 +345,8 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                         }
                     }
                     tc_commit_pair(empty_bar(st), 0x3);
+                    if (group_end)
+                        tc_commit_pair(tfree_bar(gcur & 1), 0x1);  // the group's TMEM scale regions are free again
                 }
                 __syncwarp();
                 if (++st == S) {

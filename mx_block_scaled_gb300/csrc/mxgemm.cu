@@ -321,15 +321,20 @@ int encode_operand_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t 
     return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
 }
 
-// Tile-layout scales viewed as rows of 256 bytes (a 512-byte chunk is two
-// rows); box = one ring slot's chunks of one 128-row block.
-int encode_sf_map(CUtensorMap *map, const void *ptr, size_t bytes, int kt_per_stage)
+// Tile-layout scales of `rows` operand rows as a 3-D tensor: rows of 256 bytes
+// (a 512-byte chunk is two), 2 * (K/128) rows per 128-row block, then the row
+// blocks.  Box = one scale group (kSfGroup k-stages of kt_per_stage K-tiles)
+// of `blocks` consecutive 128-row blocks; a box reaching past the last K-tile
+// or row block is zero-filled (and those chunks are never read).
+int encode_sf_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int kt_per_stage, int blocks)
 {
-    cuuint64_t dims[2] = {256u, static_cast<cuuint64_t>(bytes / 256)};
-    cuuint64_t strides[1] = {256u};
-    cuuint32_t box[2] = {256u, static_cast<cuuint32_t>(2 * kt_per_stage)};
-    cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box,
+    const int64_t num_kt = K / 128;
+    cuuint64_t dims[3] = {256u, static_cast<cuuint64_t>(2 * num_kt), static_cast<cuuint64_t>(ceil_div(rows, 128))};
+    cuuint64_t strides[2] = {256u, static_cast<cuuint64_t>(num_kt * 512)};
+    cuuint32_t box[3] = {256u, static_cast<cuuint32_t>(2 * kt_per_stage * mxg::kSfGroup),
+                         static_cast<cuuint32_t>(blocks)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
@@ -803,12 +808,12 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     } else if (plan->mode == 1) {
         const int ktps = fp4 ? 2 : 1;
         if (plan->map_ptr_sfa != p.sfa) {
-            if (encode_sf_map(&plan->map_sfa, p.sfa, mxgemm_sf_bytes(rows_a, K), ktps) != MXGEMM_OK)
+            if (encode_sf_map(&plan->map_sfa, p.sfa, rows_a, K, ktps, 1) != MXGEMM_OK)
                 return MXGEMM_ERR_CUDA;
             plan->map_ptr_sfa = p.sfa;
         }
         if (plan->map_ptr_sfb != p.sfb) {
-            if (encode_sf_map(&plan->map_sfb, p.sfb, mxgemm_sf_bytes(rows_b, K), ktps) != MXGEMM_OK)
+            if (encode_sf_map(&plan->map_sfb, p.sfb, rows_b, K, ktps, plan->bn / 128) != MXGEMM_OK)
                 return MXGEMM_ERR_CUDA;
             plan->map_ptr_sfb = p.sfb;
         }
