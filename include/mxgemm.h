@@ -35,7 +35,8 @@
  *  - A plan is a host object; it is not thread-safe (one thread per plan).
  *  - On its first use on a device the library caches per-device state: the
  *    kernels' shared-memory opt-in, the device addresses of its own device
- *    variables (the status word, the mxgemm_run_noalloc scratch) and the
+ *    variables (the status word, the stream-K arrival counters, the
+ *    mxgemm_run_noalloc scratch) and the
  *    device's properties.  cudaDeviceReset discards what the cache refers to;
  *    a process that resets a device must not call this library on that
  *    device again (the cached addresses would be stale).
@@ -125,9 +126,18 @@ MXGEMM_API int mxgemm_plan_destroy(mxgemm_plan_t plan);
 /*
  * Bytes of device workspace mxgemm_run needs for this plan (0 for NULL plan):
  * the tile-layout copies of SA and SB (unless both are passed pre-laid-out),
- * split-K partial sums, and for stream-K plans the cut tiles' partial sums and
- * arrival counters (reset by every run, so the workspace holds nothing between
- * calls).  Alignment: 256 bytes.
+ * split-K partial sums, and for stream-K plans the cut tiles' partial sums.
+ * The workspace holds nothing between calls.  Alignment: 256 bytes.
+ * A stream-K plan's arrival counters live in a device array inside the
+ * library (64 Ki counters per device): each plan takes its own range when it
+ * is created and returns it when destroyed, and every completed launch leaves
+ * its counters at zero, so no launch zeroes anything first.  Consequences: two
+ * launches of the same plan must not overlap on the GPU (order them, as for a
+ * shared workspace); launches of different plans may.  If the array is full, a
+ * new plan keeps its counters in its workspace instead (zeroed by every run).
+ * A launch that gave up on a wait (MXGEMM_ERR_DEVICE_TIMEOUT) may leave
+ * counters nonzero: read the status with mxgemm_device_status(stream, 1),
+ * which then zeroes the array, before any further launch.
  */
 MXGEMM_API size_t mxgemm_workspace_bytes(mxgemm_plan_t plan);
 
@@ -253,9 +263,11 @@ MXGEMM_API int mxgemm_prepare(mxgemm_plan_t plan, const uint8_t *SA, const uint8
  * current device: MXGEMM_OK, or MXGEMM_ERR_DEVICE_TIMEOUT if any kernel since
  * the last reset gave up on a barrier wait (every wait in the kernels has a
  * time limit of MXGEMM_WAIT_LIMIT_NS, two seconds; on expiry the kernel records
- * the error, drains its own in-flight work and exits instead of hanging).  If `reset` is
- * nonzero the status is cleared after reading.  MXGEMM_ERR_CUDA if the
- * synchronisation itself fails.
+ * the error, drains its own in-flight work and exits instead of hanging).  If
+ * `reset` is nonzero the status is cleared after reading; if it was a timeout,
+ * the library's stream-K arrival counters are zeroed as well (call it with no
+ * other launch of this library in flight on the device).  MXGEMM_ERR_CUDA if
+ * the synchronisation itself fails.
  */
 MXGEMM_API int mxgemm_device_status(void *stream, int reset);
 

@@ -39,14 +39,20 @@ struct CfgPair {
     static constexpr int kChunksB = BN / 128;                 // B-role scale chunks per K-tile (all BN rows)
     static constexpr int kABytes = kBM * kRowBytes;           // own 128 A-role rows
     static constexpr int kBBytes = (BN / 2) * kRowBytes;      // own half of the B-role tile
-    static constexpr int kStageBytes = kABytes + kBBytes;     // operand ring slot
+    static constexpr int kStageBytes = kABytes + kBBytes;     // operands of one k-stage
+    // Operand ring slots hold two k-stages each, loaded by one 3-D box per
+    // operand: a CTA's TMA engine streams 32 KB boxes of two 128-byte K-slices
+    // at ~150 GB/s, one-slice 16 KB boxes at ~100 GB/s (measured, all SMs), and
+    // the MMAs of a 256 x 256 pair tile need ~125 GB/s per SM.
+    static constexpr int kSlotBytes = 2 * kStageBytes;
     // scale group slot (see kSfGroup): SFA chunks of this CTA's 128 rows
     // [stage][K-tile], then the SFB chunks of all BN rows [128-row block][stage][K-tile]
     static constexpr int kSfaGrpBytes = kScaled ? kSfGroup * kKtPerStage * kSfChunk : 0;
     static constexpr int kSfbGrpBytes = kScaled ? kChunksB * kSfGroup * kKtPerStage * kSfChunk : 0;
     static constexpr int kSfGrpBytes = kSfaGrpBytes + kSfbGrpBytes;
-    static constexpr int kStagesRaw = (kSmemBudget - 1024 - 512 - 2 * kSfGrpBytes) / kStageBytes;
-    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    static constexpr int kSlotsRaw = (kSmemBudget - 1024 - 512 - 2 * kSfGrpBytes) / kSlotBytes;
+    static constexpr int kSlots = kSlotsRaw > 4 ? 4 : kSlotsRaw;
+    static constexpr int kStages = 2 * kSlots;                // k-stages resident in the ring
     static constexpr int kSfaCols = kScaled ? 4 * kKtPerStage : 0;
     static constexpr int kSfbCols = kScaled ? 4 * kKtPerStage * kChunksB : 0;
     static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
@@ -56,11 +62,12 @@ struct CfgPair {
     static constexpr int kColsUsed = kSfCol0 + kSfRegions * kSfSlotCols;
     static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128
                                    : kColsUsed <= 256 ? 256 : 512;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2 * kSfGrpBytes + 512;
+    static constexpr int kSmemBytes = 1024 + kSlots * kSlotBytes + 2 * kSfGrpBytes + 512;
     static constexpr uint32_t kIdesc =
         kScaled ? idesc_block_scaled(kFp4 ? 1u : 0u, 2 * kBM, BN) : idesc_bf16(2 * kBM, BN);
     static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
-    static_assert(kStages >= 2, "shared memory too small for two stages");
+    static_assert(kSlots >= 2, "shared memory too small for two slots");
+    static_assert(kSfGroup % 2 == 0, "scale groups start on a slot boundary");
     static_assert(kColsUsed <= 512, "TMEM overflow");
 };
 
@@ -73,7 +80,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                         const __grid_constant__ CUtensorMap map_sfb)
 {
     using C = CfgPair<KIND, BN>;
-    constexpr int S = C::kStages;
+    constexpr int S = C::kSlots;  // ring slots, two k-stages each
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_holder;
@@ -83,9 +90,10 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
+    // Layout: [A: slot x 2 stages][B: slot x 2 stages][scale group x 2][barriers]
     const uint32_t sA = base;
-    const uint32_t sB = sA + S * C::kABytes;
-    const uint32_t sSF = sB + S * C::kBBytes;
+    const uint32_t sB = sA + S * 2 * C::kABytes;
+    const uint32_t sSF = sB + S * 2 * C::kBBytes;
     const uint32_t sBar = sSF + 2 * C::kSfGrpBytes;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
@@ -174,10 +182,12 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 const int rb_b0 = (tn * BN) / 128;
                 // bytes of both CTAs' copies, as counted by TMA (whole boxes; a box
                 // partly past the tensor is zero-filled and counted in full)
-                const uint32_t stage_bytes = 2 * (C::kABytes + C::kBBytes);
+                const uint32_t slot_bytes = 2 * C::kSlotBytes;
                 const uint32_t group_bytes =
                     2 * C::kSfbGrpBytes + ((has_sfa ? 1 : 0) + (peer_has_sfa ? 1 : 0)) * C::kSfaGrpBytes;
-                for (int ks = ks0; ks < ks1; ++ks) {
+                // one ring slot per two k-stages of the unit (the second may lie past
+                // ks1 -- or past K, zero-filled -- and is then loaded but not used)
+                for (int ks = ks0; ks < ks1; ks += 2) {
                     const int kt0 = ks * C::kKtPerStage;
                     if (C::kScaled && (ks - ks0) % kSfGroup == 0) {
                         // the scales of k-stages [ks, ks + kSfGroup): this CTA's A-role
@@ -209,12 +219,14 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                         break;
                     }
                     if (elect_one()) {
+                        // A: this CTA's 128 rows, B: its BN/2 rows, k-stages ks and ks + 1
+                        // (3-D maps: 128-byte K-slice x rows x slice index)
                         const uint32_t bar = map_to_cta(full_bar(st), 0);
                         if (leader)
-                            mbar_arrive_expect_tx(full_bar(st), stage_bytes);
-                        tma_load_2d_pair_hint(sA + st * C::kABytes, &map_a, bar, ks * kRowBytes, rb_a * kBM, pol_a);
-                        tma_load_2d_pair_hint(sB + st * C::kBBytes, &map_b, bar, ks * kRowBytes,
-                                              tn * BN + static_cast<int>(rank) * (BN / 2), pol_b);
+                            mbar_arrive_expect_tx(full_bar(st), slot_bytes);
+                        tma_load_3d_pair_hint(sA + st * 2 * C::kABytes, &map_a, bar, 0, rb_a * kBM, ks, pol_a);
+                        tma_load_3d_pair_hint(sB + st * 2 * C::kBBytes, &map_b, bar, 0,
+                                              tn * BN + static_cast<int>(rank) * (BN / 2), ks, pol_b);
                     }
                     __syncwarp();
                     armed |= 1u << st;
@@ -301,7 +313,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem + acc * BN;
             const int ks0 = w.ks0, ks1 = w.ks1;
-            for (int ks = ks0; ks < ks1; ++ks) {
+            for (int ks = ks0; ks < ks1; ks += 2) {
                 const int rel = ks - ks0;
                 if (C::kScaled && rel % kSfGroup == 0 && !group_in(ks, min(kSfGroup, ks1 - ks))) {
                     if (lane == 0) record_timeout(p, abort);
@@ -315,38 +327,47 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 }
                 tc_fence_after();
                 issued = true;
-                const int nkt = min(C::kKtPerStage, p.num_kt - ks * C::kKtPerStage);
-                const int gcur = gi - 1;  // the group this stage belongs to
-                const uint32_t sfa_col =
-                    tmem + C::kSfCol0 + ((gcur & 1) * kSfGroup + rel % kSfGroup) * C::kSfSlotCols;
-                const uint32_t sfb_col = sfa_col + C::kSfaCols;
-                const bool group_end = C::kScaled && (rel % kSfGroup == kSfGroup - 1 || ks == ks1 - 1);
-                const uint64_t adesc = sdesc_kmajor_sw128(sA + st * C::kABytes);
-                const uint64_t bdesc = sdesc_kmajor_sw128(sB + st * C::kBBytes);
-                const uint32_t acc0 = (ks > ks0) ? 1u : 0u;
+                const int nst = min(2, ks1 - ks);  // k-stages of the slot that belong to the unit
+                const int gcur = gi - 1;           // the scale group of the slot's stages
+                // the group's TMEM regions are free again after the MMAs of its last slot
+                const bool group_end = C::kScaled && ((rel + 2) % kSfGroup == 0 || ks + 2 >= ks1);
                 if (elect_one()) {
 #pragma unroll
-                    for (int s = 0; s < C::kKtPerStage * C::kSubPerKt; ++s) {
-                        const int t = s / C::kSubPerKt;
-                        if (t < nkt) {
-                            const uint32_t sf_id =
-                                C::kFp4 ? static_cast<uint32_t>((s % 2) * 2) : static_cast<uint32_t>(s % 4);
-                            const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, sf_id, sf_id);
-                            const uint32_t sfa_t = sfa_col + 4 * t;
-                            const uint32_t sfb_t = sfb_col + 4 * t * C::kChunksB;
-                            const uint64_t koff = static_cast<uint64_t>((s * 32) >> 4);
-                            const uint32_t accum = (s > 0) ? 1u : acc0;
-                            if constexpr (KIND == K_BF16)
-                                mma_pair_bf16(d_tmem, adesc + koff, bdesc + koff, C::kIdesc, accum);
-                            else if constexpr (C::kFp4)
-                                mma_pair_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
-                            else
-                                mma_pair_mxf8f6f4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
+                    for (int h = 0; h < 2; ++h) {
+                        if (h < nst) {
+                            const int kk = ks + h;
+                            const int nkt = min(C::kKtPerStage, p.num_kt - kk * C::kKtPerStage);
+                            const uint32_t sfa_col =
+                                tmem + C::kSfCol0 + ((gcur & 1) * kSfGroup + (rel + h) % kSfGroup) * C::kSfSlotCols;
+                            const uint32_t sfb_col = sfa_col + C::kSfaCols;
+                            const uint64_t adesc = sdesc_kmajor_sw128(sA + (st * 2 + h) * C::kABytes);
+                            const uint64_t bdesc = sdesc_kmajor_sw128(sB + (st * 2 + h) * C::kBBytes);
+                            const uint32_t acc0 = (kk > ks0) ? 1u : 0u;
+#pragma unroll
+                            for (int s = 0; s < C::kKtPerStage * C::kSubPerKt; ++s) {
+                                const int t = s / C::kSubPerKt;
+                                if (t < nkt) {
+                                    const uint32_t sf_id = C::kFp4 ? static_cast<uint32_t>((s % 2) * 2)
+                                                                   : static_cast<uint32_t>(s % 4);
+                                    const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, sf_id, sf_id);
+                                    const uint32_t sfa_t = sfa_col + 4 * t;
+                                    const uint32_t sfb_t = sfb_col + 4 * t * C::kChunksB;
+                                    const uint64_t koff = static_cast<uint64_t>((s * 32) >> 4);
+                                    const uint32_t accum = (s > 0) ? 1u : acc0;
+                                    if constexpr (KIND == K_BF16)
+                                        mma_pair_bf16(d_tmem, adesc + koff, bdesc + koff, C::kIdesc, accum);
+                                    else if constexpr (C::kFp4)
+                                        mma_pair_mxf4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t, accum);
+                                    else
+                                        mma_pair_mxf8f6f4(d_tmem, adesc + koff, bdesc + koff, idesc, sfa_t, sfb_t,
+                                                          accum);
+                                }
+                            }
                         }
                     }
                     tc_commit_pair(empty_bar(st), 0x3);
                     if (group_end)
-                        tc_commit_pair(tfree_bar(gcur & 1), 0x1);  // the group's TMEM scale regions are free again
+                        tc_commit_pair(tfree_bar(gcur & 1), 0x1);
                 }
                 __syncwarp();
                 if (++st == S) {

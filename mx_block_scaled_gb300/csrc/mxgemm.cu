@@ -5,6 +5,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -23,6 +25,17 @@ using mxg::GemmParams;
 // Sticky device status word, written by kernels that give up on a wait.
 __device__ int g_device_status;
 
+// Stream-K arrival counters.  They live in the library rather than in the
+// caller's workspace so that no launch needs a memset before it: the array is
+// zero when the module loads, and every completed launch leaves its counters
+// at zero (the last segment to arrive at a tile resets the tile's counter).
+// Each plan owns a disjoint range (taken at plan creation, returned when the
+// plan is destroyed), so plans running concurrently on different streams never
+// share a counter.  A launch that gave up on a wait (device timeout) may leave
+// counters nonzero; mxgemm_device_status(..., reset) then zeroes the array.
+constexpr int kCounterPool = 1 << 16;
+__device__ int g_sk_counters[kCounterPool];
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -31,9 +44,46 @@ struct DeviceInfo {
     bool is_sm103 = false;
     int num_sms = 0;
     int *status_ptr = nullptr;
+    int *counters_ptr = nullptr;                  // device address of g_sk_counters
+    std::vector<std::pair<int, int>> free_ranges; // unowned [offset, offset + length) of the counters
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
+
+// First-fit range of n counters on device dev, or -1 (the plan then keeps its
+// counters in the workspace, zeroed before each launch).
+int counters_take(int dev, int n)
+{
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    auto &fr = g_dev[dev].free_ranges;
+    for (size_t i = 0; i < fr.size(); ++i) {
+        if (fr[i].second >= n) {
+            const int off = fr[i].first;
+            fr[i].first += n;
+            fr[i].second -= n;
+            if (fr[i].second == 0)
+                fr.erase(fr.begin() + static_cast<long>(i));
+            return off;
+        }
+    }
+    return -1;
+}
+
+void counters_give_back(int dev, int off, int n)
+{
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    auto &fr = g_dev[dev].free_ranges;
+    fr.emplace_back(off, n);
+    std::sort(fr.begin(), fr.end());
+    std::vector<std::pair<int, int>> merged;
+    for (const auto &r : fr) {
+        if (!merged.empty() && merged.back().first + merged.back().second == r.first)
+            merged.back().second += r.second;
+        else
+            merged.push_back(r);
+    }
+    fr.swap(merged);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 
@@ -55,6 +105,10 @@ int device_info(DeviceInfo **out)
             if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess)
                 return MXGEMM_ERR_CUDA;
             d.status_ptr = static_cast<int *>(p);
+            if (cudaGetSymbolAddress(&p, g_sk_counters) != cudaSuccess)
+                return MXGEMM_ERR_CUDA;
+            d.counters_ptr = static_cast<int *>(p);
+            d.free_ranges.assign(1, std::make_pair(0, kCounterPool));
         }
         if (!g_encode_tiled) {
             void *fn = nullptr;
@@ -284,6 +338,8 @@ struct mxgemm_plan {
     int sk_halves;     // 128-row shares per tile (2 in pair mode): counters and slots per tile / unit
     int device;        // the device current when the plan was created; runs must use it
     size_t off_sfa, off_sfb, off_part, off_cnt, off_skp, ws_bytes;
+    int cnt_pool = -1;  // stream-K counters: offset in the library's counter array (-1: in the workspace)
+    int cnt_n = 0;      // counters of the plan (stream-K tiles x 128-row shares)
     // TMA descriptor cache (re-encoded when an operand pointer changes)
     const void *map_ptr_a = nullptr;
     const void *map_ptr_b = nullptr;
@@ -316,6 +372,24 @@ int encode_operand_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t 
     cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
+}
+
+// An operand (rows x row_bytes, row-major) as a 3-D tensor for the CTA-pair
+// kernel: the 128-byte K-slices of a row, the rows, then the slice index (the
+// innermost two dimensions make a k-stage tile, the third selects the stage).
+// Box = box_rows rows x two consecutive k-stages, landing as two 128-byte
+// swizzled tiles one after the other.  Needs row_bytes % 128 == 0, so that no
+// slice reaches past the end of a row.
+int encode_operand_map_2stage(CUtensorMap *map, const void *ptr, int64_t rows, int64_t row_bytes, int box_rows)
+{
+    cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(row_bytes / 128)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), 128u};
+    cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(box_rows), 2u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
@@ -450,6 +524,9 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_SINGLE) mode = 0;
+    // pair tiles load two 128-byte K-slices per box: MXFP4 rows must be a whole
+    // number of slices (K % 256 == 0), else single-CTA tiles
+    if (fmt == MXGEMM_FMT_MXFP4_E2M1 && K % 256 != 0) mode = 0;
     if (mode != 0 && bn < 128) bn = 128;
     // Stream-K on CTA pairs runs on 256-wide tiles only (the pair instantiation
     // with fixup warps): a forced stream-K pair plan takes them.
@@ -583,7 +660,10 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     p->off_cnt = off;
     p->off_skp = off;
     if (p->sk_ctas > 0) {
-        off = align256(off + static_cast<size_t>(p->sk_tiles) * p->sk_halves * sizeof(int));
+        p->cnt_n = p->sk_tiles * p->sk_halves;
+        p->cnt_pool = counters_take(p->device, p->cnt_n);
+        if (p->cnt_pool < 0)  // the library's counters are all taken: keep them in the workspace
+            off = align256(off + static_cast<size_t>(p->cnt_n) * sizeof(int));
         p->off_skp = off;
         off = align256(off + static_cast<size_t>(2) * p->sk_ctas * p->sk_halves * 128 * bn * sizeof(float));
     }
@@ -594,6 +674,8 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
 
 int mxgemm_plan_destroy(mxgemm_plan_t plan)
 {
+    if (plan && plan->cnt_pool >= 0)
+        counters_give_back(plan->device, plan->cnt_pool, plan->cnt_n);
     delete plan;
     return MXGEMM_OK;
 }
@@ -668,10 +750,11 @@ int mxgemm_quantize(int fmt, int in_dtype, const void *x, int64_t rows, int64_t 
 }
 
 // Phase 1 of a run: the relayout of whichever scales are not pre-laid-out into
-// the workspace, in one launch that also zeroes the stream-K arrival counters
-// (a memset when nothing is laid out).  The kernel leaves the counters zero
-// when it completes, but the workspace may be fresh or hold an aborted
-// launch's.  Arguments checked by the callers.
+// the workspace.  A plan whose stream-K counters had to go into the workspace
+// (the library's array was full) also has them zeroed here, by the same launch
+// (a memset when nothing is laid out): the kernel leaves them zero when it
+// completes, but the workspace may be fresh or hold an aborted launch's.
+// Arguments checked by the callers.
 static int prepare_impl(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB, uint8_t *ws, uint32_t run_flags,
                         cudaStream_t s)
 {
@@ -684,7 +767,7 @@ static int prepare_impl(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB
             jobs[njobs++] = make_job(SB, plan->N, plan->K, ws + plan->off_sfb);
     }
     int *const sk_counters = reinterpret_cast<int *>(ws + plan->off_cnt);
-    const int sk_ncnt = plan->sk_ctas > 0 ? plan->sk_tiles * plan->sk_halves : 0;
+    const int sk_ncnt = plan->cnt_pool < 0 ? plan->cnt_n : 0;
     if (njobs > 0) {
         if (launch_relayout(jobs[0], njobs > 1 ? &jobs[1] : nullptr, s, sk_counters, sk_ncnt) != cudaSuccess)
             return MXGEMM_ERR_CUDA;
@@ -748,14 +831,18 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     const void *pb = plan->swap ? A : B;
     const int64_t rows_a = plan->swap ? N : M;
     const int64_t rows_b = plan->swap ? M : N;
+    // single-CTA tiles: 2-D maps, one k-stage per box; CTA pairs: 3-D maps, two per box
     if (plan->map_ptr_a != pa) {
-        if (encode_operand_map(&plan->map_a, pa, rows_a, row_bytes, 128) != MXGEMM_OK)
+        const int r = plan->mode ? encode_operand_map_2stage(&plan->map_a, pa, rows_a, row_bytes, 128)
+                                 : encode_operand_map(&plan->map_a, pa, rows_a, row_bytes, 128);
+        if (r != MXGEMM_OK)
             return MXGEMM_ERR_CUDA;
         plan->map_ptr_a = pa;
     }
     if (plan->map_ptr_b != pb) {
-        if (encode_operand_map(&plan->map_b, pb, rows_b, row_bytes, plan->mode ? plan->bn / 2 : plan->bn) !=
-            MXGEMM_OK)
+        const int r = plan->mode ? encode_operand_map_2stage(&plan->map_b, pb, rows_b, row_bytes, plan->bn / 2)
+                                 : encode_operand_map(&plan->map_b, pb, rows_b, row_bytes, plan->bn);
+        if (r != MXGEMM_OK)
             return MXGEMM_ERR_CUDA;
         plan->map_ptr_b = pb;
     }
@@ -785,7 +872,7 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     p.dp_tiles = plan->dp_tiles;
     p.sk_ctas = plan->sk_ctas;
     p.sk_stages = static_cast<long long>(plan->sk_tiles) * plan->kstages;
-    p.sk_counters = sk_counters;
+    p.sk_counters = plan->cnt_pool >= 0 ? dev->counters_ptr + plan->cnt_pool : sk_counters;
     p.sk_partials = reinterpret_cast<float *>(ws + plan->off_skp);
     const bool split = plan->splits > 1;
     const int osize = split ? 4 : (plan->out == MXGEMM_OUT_BF16 ? 2 : 4);
@@ -1138,6 +1225,11 @@ int mxgemm_device_status(void *stream, int reset)
     if (reset) {
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess)
+            return MXGEMM_ERR_CUDA;
+        // a launch that gave up may have left stream-K arrival counters nonzero
+        if (v == MXGEMM_ERR_DEVICE_TIMEOUT &&
+            (cudaMemset(dev->counters_ptr, 0, sizeof(int) * kCounterPool) != cudaSuccess ||
+             cudaDeviceSynchronize() != cudaSuccess))
             return MXGEMM_ERR_CUDA;
     }
     return v;

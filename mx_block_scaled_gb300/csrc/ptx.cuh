@@ -235,6 +235,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// tma_load_3d_pair with an L2 eviction-policy hint (createpolicy) for the loaded lines.
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
+                                                      int32_t y, int32_t z, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // The same with an L2 eviction-policy hint (createpolicy) for the loaded lines.
 __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
                                                       int32_t y, uint64_t policy)

@@ -197,7 +197,8 @@ def test_stream_k_exact(oracle_mod, fmt, mode, M, N, K):
     B, SB = small_int_codes(rng, N, K, fmt)
     ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
     C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, flags=SK | mode, return_plan=True)
-    assert ("mode=pair" in desc) == (mode == PAIR), desc
+    # pair tiles need MXFP4 rows of whole 128-byte K-slices (K % 256 == 0)
+    assert ("mode=pair" in desc) == (mode == PAIR and (fmt != FMT_MXFP4 or K % 256 == 0)), desc
     assert "streamk=" in desc and "/0 " not in desc.split("streamk=")[1][:12], desc
     assert (C == ref).all(), desc
     C2, desc2 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16, return_plan=True)
