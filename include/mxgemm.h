@@ -222,7 +222,11 @@ MXGEMM_API int mxgemm_quantize(int fmt, int in_dtype, const void *x, int64_t row
  *       (may be NULL/0 if that is 0)
  * Enqueues (1) the relayout of whichever scales are not pre-laid-out and
  * (2) the persistent tcgen05 block-scaled GEMM kernel (3) a split-K reduce if
- * the plan splits K.  Inputs are read-only; C is fully overwritten.
+ * the plan splits K.  MXFP8 plans on 256-row CTA-pair tiles with
+ * K % 512 == 0 (their description says "sa=in-kernel") lay out row-major SA
+ * inside the GEMM kernel instead of step (1): one CTA of each pair loads the
+ * pair's row-major scales and writes the tile layout in shared memory.
+ * Inputs are read-only; C is fully overwritten.
  * A plan belongs to the device that was current when it was created; running
  * it with another device current returns MXGEMM_ERR_ARG.
  * Errors: MXGEMM_ERR_ARG, MXGEMM_ERR_ALIGN, MXGEMM_ERR_WORKSPACE,
@@ -235,13 +239,16 @@ MXGEMM_API int mxgemm_run(mxgemm_plan_t plan, const void *A, const uint8_t *SA,
 
 /*
  * Step (1) of mxgemm_run on its own: lays out whichever of SA / SB is not
- * flagged MXGEMM_RUN_S{A,B}_PRELAYOUT into `workspace` and resets the plan's
- * stream-K arrival counters there, in one launch on `stream` (a memset when
- * both scales are pre-laid-out).  A following mxgemm_run on the same
- * workspace and stream with MXGEMM_RUN_PREPARED (plus the same PRELAYOUT
- * flags) then enqueues only the GEMM (and its split-K reduce): the scales laid
- * out here are read from the workspace, so mxgemm_run's SA / SB arguments
- * without a PRELAYOUT flag are not read and may be NULL.  Lets a caller time
+ * flagged MXGEMM_RUN_S{A,B}_PRELAYOUT into `workspace` in one launch on
+ * `stream` (none when there is nothing to lay out); a plan whose stream-K
+ * counters did not fit in the library's array also has them reset here.  A
+ * following mxgemm_run on the same workspace and stream with
+ * MXGEMM_RUN_PREPARED (plus the same PRELAYOUT flags) then enqueues only the
+ * GEMM (and its split-K reduce): the scales laid out here are read from the
+ * workspace, so mxgemm_run's SA / SB arguments without a PRELAYOUT flag are
+ * not read and may be NULL -- except SA for a plan that lays it out inside the
+ * GEMM ("sa=in-kernel" in its description): mxgemm_prepare leaves SA alone
+ * and mxgemm_run reads it.  Lets a caller time
  * or schedule the two steps separately (the FlyDSL page's "layout copies" are
  * step (1)).  Nothing else may use the workspace in between.
  *   SA, SB:  row-major scales as for mxgemm_run (pre-laid-out ones not read;

@@ -17,9 +17,9 @@ cudaError_t launch_gemm_bf16(int bn, const GemmParams &p, const CUtensorMap &ma,
 }
 
 cudaError_t launch_gemm_pair_bf16(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
-                                  const CUtensorMap &msa, const CUtensorMap &msb, int clusters, cudaStream_t s)
+                                  const CUtensorMap &msa, const CUtensorMap &msb, const CUtensorMap &msarm, int clusters, cudaStream_t s)
 {
-    return L::launch_pair(bn, p, ma, mb, msa, msb, clusters, s);
+    return L::launch_pair(bn, p, ma, mb, msa, msb, msarm, clusters, s);
 }
 
 int gemm_pair_max_clusters_bf16(int bn) { return L::max_clusters(bn); }

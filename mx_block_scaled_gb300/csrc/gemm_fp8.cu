@@ -21,9 +21,9 @@ cudaError_t launch_gemm_grouped_fp8(int bn, const GemmParams &p, const CUtensorM
 }
 
 cudaError_t launch_gemm_pair_fp8(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
-                                 const CUtensorMap &msa, const CUtensorMap &msb, int clusters, cudaStream_t s)
+                                 const CUtensorMap &msa, const CUtensorMap &msb, const CUtensorMap &msarm, int clusters, cudaStream_t s)
 {
-    return L::launch_pair(bn, p, ma, mb, msa, msb, clusters, s);
+    return L::launch_pair(bn, p, ma, mb, msa, msb, msarm, clusters, s);
 }
 
 int gemm_pair_max_clusters_fp8(int bn) { return L::max_clusters(bn); }

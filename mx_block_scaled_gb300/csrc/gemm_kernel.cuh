@@ -78,6 +78,7 @@ struct GemmParams {
     int vec_ok;               // 1: stride_j == 1 and rows are 16-byte aligned
     int test_stall;           // self-test: the producer issues nothing (waits expire)
     int stream_a, stream_b;   // 1: that operand is read by at most two tiles (load it evict-first)
+    int sa_fused;             // CTA-pair kernel: 1 = A-role scales are row-major (laid out in the kernel)
     const uint8_t *sfa;       // tile-layout scales of the A role
     const uint8_t *sfb;       // tile-layout scales of the B role
     void *out;                // output base (C, or split-K partial slabs)

@@ -50,25 +50,38 @@ struct CfgPair {
     static constexpr int kSfaGrpBytes = kScaled ? kSfGroup * kKtPerStage * kSfChunk : 0;
     static constexpr int kSfbGrpBytes = kScaled ? kChunksB * kSfGroup * kKtPerStage * kSfChunk : 0;
     static constexpr int kSfGrpBytes = kSfaGrpBytes + kSfbGrpBytes;
-    static constexpr int kSlotsRaw = (kSmemBudget - 1024 - 512 - 2 * kSfGrpBytes) / kSlotBytes;
+    // Scale group slots (shared memory and TMEM regions): MXFP8 keeps three, so
+    // a group's copies and layout may start two groups ahead of its MMAs; MXFP4's
+    // scale columns leave TMEM room for two.
+    static constexpr int kGrp = (kScaled && !kFp4) ? 3 : 2;
+    // Row-major A-role scales laid out in the kernel (MXFP8): per group, a
+    // staging buffer for both CTAs' 256 rows x 4 bytes per K-tile, and the even
+    // CTA's chunks as built by the odd CTA.  (MXFP4 plans take pre-laid scales:
+    // their ring leaves no room for the buffers.)
+    static constexpr bool kFuseSa = kScaled && !kFp4;
+    static constexpr int kSaRawBytes = kFuseSa ? 2 * kBM * 4 * kSfGroup * kKtPerStage : 0;
+    static constexpr int kSaLeadBytes = kFuseSa ? kSfaGrpBytes : 0;
+    static constexpr int kSaBytes = 2 * kSaRawBytes + kGrp * kSaLeadBytes;
+    static constexpr int kSlotsRaw = (kSmemBudget - 1024 - 512 - kGrp * kSfGrpBytes - kSaBytes) / kSlotBytes;
     static constexpr int kSlots = kSlotsRaw > 4 ? 4 : kSlotsRaw;
     static constexpr int kStages = 2 * kSlots;                // k-stages resident in the ring
     static constexpr int kSfaCols = kScaled ? 4 * kKtPerStage : 0;
     static constexpr int kSfbCols = kScaled ? 4 * kKtPerStage * kChunksB : 0;
     static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
-    static constexpr int kSfRegions = kScaled ? 2 * kSfGroup : 0;
+    static constexpr int kSfRegions = kScaled ? kGrp * kSfGroup : 0;
     static constexpr int kAccStages = (2 * BN + kSfRegions * kSfSlotCols <= 512) ? 2 : 1;
     static constexpr int kSfCol0 = kAccStages * BN;
     static constexpr int kColsUsed = kSfCol0 + kSfRegions * kSfSlotCols;
     static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128
                                    : kColsUsed <= 256 ? 256 : 512;
-    static constexpr int kSmemBytes = 1024 + kSlots * kSlotBytes + 2 * kSfGrpBytes + 512;
+    static constexpr int kSmemBytes = 1024 + kSlots * kSlotBytes + kGrp * kSfGrpBytes + kSaBytes + 512;
     static constexpr uint32_t kIdesc =
         kScaled ? idesc_block_scaled(kFp4 ? 1u : 0u, 2 * kBM, BN) : idesc_bf16(2 * kBM, BN);
     static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
     static_assert(kSlots >= 2, "shared memory too small for two slots");
     static_assert(kSfGroup % 2 == 0, "scale groups start on a slot boundary");
     static_assert(kColsUsed <= 512, "TMEM overflow");
+    static_assert(!kFuseSa || kSfGroup * kKtPerStage == 4, "the fused layout moves one 16-byte row word per chunk");
 };
 
 // SK = true: the instantiation for stream-K plans, with the two fixup warps
@@ -77,7 +90,7 @@ template <int KIND, int BN, bool SK = false>
 __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
-                        const __grid_constant__ CUtensorMap map_sfb)
+                        const __grid_constant__ CUtensorMap map_sfb, const __grid_constant__ CUtensorMap map_sarm)
 {
     using C = CfgPair<KIND, BN>;
     constexpr int S = C::kSlots;  // ring slots, two k-stages each
@@ -90,20 +103,25 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    // Layout: [A: slot x 2 stages][B: slot x 2 stages][scale group x 2][barriers]
+    // Layout: [A: slot x 2 stages][B: slot x 2 stages][scale group x kGrp]
+    //         [row-major A-role scale staging x 2][even CTA's A-role chunks x kGrp][barriers]
     const uint32_t sA = base;
     const uint32_t sB = sA + S * 2 * C::kABytes;
     const uint32_t sSF = sB + S * 2 * C::kBBytes;
-    const uint32_t sBar = sSF + 2 * C::kSfGrpBytes;
+    const uint32_t sRaw = sSF + C::kGrp * C::kSfGrpBytes;
+    const uint32_t sLead = sRaw + 2 * C::kSaRawBytes;
+    const uint32_t sBar = sLead + C::kGrp * C::kSaLeadBytes;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (S + s); };
     auto accf_bar = [&](int a) { return sBar + 8u * (3 * S + a); };
     auto acce_bar = [&](int a) { return sBar + 8u * (3 * S + 2 + a); };  // used in the even CTA
     const uint32_t drain_bar = sBar + 8u * (3 * S + 4);
     // scale groups (sfull and tfree used in the even CTA, sempty in both)
+    constexpr int G = C::kGrp;
     auto sfull_bar = [&](int g) { return sBar + 8u * (3 * S + 5 + g); };
-    auto sempty_bar = [&](int g) { return sBar + 8u * (3 * S + 7 + g); };
-    auto tfree_bar = [&](int g) { return sBar + 8u * (3 * S + 9 + g); };
+    auto sempty_bar = [&](int g) { return sBar + 8u * (3 * S + 5 + G + g); };
+    auto tfree_bar = [&](int g) { return sBar + 8u * (3 * S + 5 + 2 * G + g); };
+    auto araw_bar = [&](int b) { return sBar + 8u * (3 * S + 5 + 3 * G + b); };  // staging landed (odd CTA)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -122,9 +140,12 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
             mbar_init(acce_bar(a), 2 * kEpiWarps);
-            mbar_init(sfull_bar(a), 1);
-            mbar_init(sempty_bar(a), 1);
-            mbar_init(tfree_bar(a), 1);
+            mbar_init(araw_bar(a), 1);
+        }
+        for (int g = 0; g < G; ++g) {
+            mbar_init(sfull_bar(g), 1);
+            mbar_init(sempty_bar(g), 1);
+            mbar_init(tfree_bar(g), 1);
         }
         mbar_init(drain_bar, 1);
         mbar_init(smem_addr(&fix_bars[0]), 1);
@@ -134,6 +155,8 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         tma_prefetch_map(&map_b);
         tma_prefetch_map(&map_sfa);
         tma_prefetch_map(&map_sfb);
+        if (p.sa_fused)
+            tma_prefetch_map(&map_sarm);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_addr(&tmem_base_holder), C::kTmemCols);
@@ -155,6 +178,12 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     const uint64_t lim = p.timeout_ns;
     const int nrb_a = (p.rows_a + 127) / 128;
 
+    // Slots and scale groups are aligned to absolute k-stage indices: slot =
+    // k-stages (2j, 2j+1), scale group = k-stages [4g, 4g+4).  A work unit that
+    // starts or ends inside one (stream-K segments, split-K slabs) loads the
+    // whole of it and uses its own stages only.  The alignment keeps the
+    // row-major scale box of a group on a 16-byte boundary.
+    auto group_start = [&](int kb, int kb0) { return C::kScaled && (kb % kSfGroup == 0 || kb == kb0); };
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         // Both CTAs load their own halves; every copy completes on the even CTA's
@@ -181,20 +210,22 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 const bool peer_has_sfa = 2 * tm + 1 < nrb_a;
                 const int rb_b0 = (tn * BN) / 128;
                 // bytes of both CTAs' copies, as counted by TMA (whole boxes; a box
-                // partly past the tensor is zero-filled and counted in full)
+                // partly or wholly past the tensor is zero-filled and counted in full)
                 const uint32_t slot_bytes = 2 * C::kSlotBytes;
+                // (fused: the even CTA's A-role chunks, sent by the odd CTA)
                 const uint32_t group_bytes =
-                    2 * C::kSfbGrpBytes + ((has_sfa ? 1 : 0) + (peer_has_sfa ? 1 : 0)) * C::kSfaGrpBytes;
-                // one ring slot per two k-stages of the unit (the second may lie past
-                // ks1 -- or past K, zero-filled -- and is then loaded but not used)
-                for (int ks = ks0; ks < ks1; ks += 2) {
-                    const int kt0 = ks * C::kKtPerStage;
-                    if (C::kScaled && (ks - ks0) % kSfGroup == 0) {
-                        // the scales of k-stages [ks, ks + kSfGroup): this CTA's A-role
-                        // rows and every B-role row, one 3-D box each (chunks of 2 rows x 256 B)
-                        const int gs = gi & 1;
-                        const uint32_t use = static_cast<uint32_t>(gi >> 1);
-                        if (gi >= 2 && !warp_wait_cluster(sempty_bar(gs), (use & 1u) ^ 1u, abort, lim)) {
+                    2 * C::kSfbGrpBytes +
+                    (p.sa_fused ? 1u : ((has_sfa ? 1u : 0u) + (peer_has_sfa ? 1u : 0u))) * C::kSfaGrpBytes;
+                const int kb0 = ks0 & ~1;
+                for (int kb = kb0; kb < ks1; kb += 2) {
+                    if (group_start(kb, kb0)) {
+                        // the scales of the group holding k-stage kb: every B-role row, one
+                        // 3-D box (chunks of 2 rows x 256 B), and this CTA's A-role rows, a
+                        // 3-D box of tile-layout chunks (unless the odd CTA lays them out)
+                        const int gkt0 = (kb - kb % kSfGroup) * C::kKtPerStage;
+                        const int gs = gi % G;
+                        const uint32_t use = static_cast<uint32_t>(gi / G);
+                        if (gi >= G && !warp_wait_cluster(sempty_bar(gs), (use & 1u) ^ 1u, abort, lim)) {
                             if (lane == 0) record_timeout(p, abort);
                             ok = false;
                             break;
@@ -204,9 +235,9 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                             const uint32_t bar = map_to_cta(sfull_bar(gs), 0);
                             if (leader)
                                 mbar_arrive_expect_tx(sfull_bar(gs), group_bytes);
-                            if (has_sfa)
-                                tma_load_3d_pair(dst, &map_sfa, bar, 0, 2 * kt0, rb_a);
-                            tma_load_3d_pair(dst + C::kSfaGrpBytes, &map_sfb, bar, 0, 2 * kt0, rb_b0);
+                            if (!p.sa_fused && has_sfa)
+                                tma_load_3d_pair(dst, &map_sfa, bar, 0, 2 * gkt0, rb_a);
+                            tma_load_3d_pair(dst + C::kSfaGrpBytes, &map_sfb, bar, 0, 2 * gkt0, rb_b0);
                         }
                         __syncwarp();
                         sarmed |= 1u << gs;
@@ -219,14 +250,14 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                         break;
                     }
                     if (elect_one()) {
-                        // A: this CTA's 128 rows, B: its BN/2 rows, k-stages ks and ks + 1
+                        // A: this CTA's 128 rows, B: its BN/2 rows, k-stages kb and kb + 1
                         // (3-D maps: 128-byte K-slice x rows x slice index)
                         const uint32_t bar = map_to_cta(full_bar(st), 0);
                         if (leader)
                             mbar_arrive_expect_tx(full_bar(st), slot_bytes);
-                        tma_load_3d_pair_hint(sA + st * 2 * C::kABytes, &map_a, bar, 0, rb_a * kBM, ks, pol_a);
+                        tma_load_3d_pair_hint(sA + st * 2 * C::kABytes, &map_a, bar, 0, rb_a * kBM, kb, pol_a);
                         tma_load_3d_pair_hint(sB + st * 2 * C::kBBytes, &map_b, bar, 0,
-                                              tn * BN + static_cast<int>(rank) * (BN / 2), ks, pol_b);
+                                              tn * BN + static_cast<int>(rank) * (BN / 2), kb, pol_b);
                     }
                     __syncwarp();
                     armed |= 1u << st;
@@ -237,13 +268,121 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                     }
                 }
             }
-            if (!ok && leader) {
+            if (!ok) {
+                // let every armed copy finish landing before the CTA exits
                 for (int s2 = 0; s2 < S; ++s2)
-                    if (armed & (1u << s2))
+                    if (leader && (armed & (1u << s2)))
                         warp_wait(full_bar(s2), (armed_ph >> s2) & 1u, no_abort, lim);
-                for (int g2 = 0; g2 < 2; ++g2)
-                    if (sarmed & (1u << g2))
+                for (int g2 = 0; g2 < G; ++g2)
+                    if (leader && (sarmed & (1u << g2)))
                         warp_wait(sfull_bar(g2), (sarmed_ph >> g2) & 1u, no_abort, lim);
+            }
+        }
+    } else if (warp == 1 && !leader) {
+        // ------------ odd CTA: lays out the pair's row-major A-role scales
+        // Per scale group one 2-D box brings both CTAs' 256 rows x 16 bytes into
+        // a staging buffer (loaded one group ahead).  The warp writes this CTA's
+        // rows as tensor-core chunks into its group slot and the even CTA's rows
+        // into a side buffer, orders those writes before its async-proxy
+        // operations, and sends the side buffer to the even CTA's group slot by
+        // a bulk copy that completes on the even CTA's sfull barrier, so the
+        // barrier also covers this CTA's own chunks.  (A thread's arrive on the
+        // other CTA's barrier measured ~0.9 us per group here; the copy is
+        // asynchronous, and the even CTA's MMA warp does no layout work.)
+        if constexpr (C::kFuseSa) {
+            if (p.sa_fused && !p.test_stall) {
+                const uint64_t pol_a = p.stream_a ? l2_policy_evict_first() : l2_policy_evict_last();
+                WorkIter wi;
+                wi.init(p, first_unit, unit_step);
+                Work w;
+                bool in_unit = false;
+                int kb = 0, kb0 = 0;
+                // the next scale group in the order the producer and MMA warps meet them
+                auto next_group = [&](int &kt0, int &row0) -> bool {
+                    for (;;) {
+                        if (!in_unit) {
+                            if (!wi.next(p, w))
+                                return false;
+                            in_unit = true;
+                            kb0 = w.ks0 & ~1;
+                            kb = kb0;
+                        }
+                        while (kb < w.ks1) {
+                            const int k = kb;
+                            kb += 2;
+                            if (group_start(k, kb0)) {
+                                kt0 = (k - k % kSfGroup) * C::kKtPerStage;
+                                row0 = 2 * w.tm * kBM;
+                                return true;
+                            }
+                        }
+                        in_unit = false;
+                    }
+                };
+                uint32_t armed = 0, armed_ph = 0;  // staging loads in flight
+                auto load_raw = [&](int b, uint32_t use, int kt0, int row0) {
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(araw_bar(b), C::kSaRawBytes);
+                        tma_load_2d(sRaw + b * C::kSaRawBytes, &map_sarm, araw_bar(b), 4 * kt0, row0, pol_a);
+                    }
+                    __syncwarp();
+                    armed |= 1u << b;
+                    armed_ph = (armed_ph & ~(1u << b)) | ((use & 1u) << b);
+                };
+                int kt_cur = 0, row_cur = 0, kt_nxt = 0, row_nxt = 0;
+                bool has_cur = next_group(kt_cur, row_cur);
+                if (has_cur)
+                    load_raw(0, 0u, kt_cur, row_cur);
+                bool ok = true;
+                for (int gi = 0; has_cur; ++gi) {
+                    const int rb = gi & 1;  // staging buffer
+                    const int gs = gi % G;  // group slot and side buffer
+                    const uint32_t use = static_cast<uint32_t>(gi / G);
+                    // prefetch the next group (its staging buffer was last read by the
+                    // layout of group gi - 1, already done)
+                    const bool has_nxt = next_group(kt_nxt, row_nxt);
+                    if (has_nxt)
+                        load_raw(rb ^ 1, static_cast<uint32_t>((gi + 1) >> 1), kt_nxt, row_nxt);
+                    // staging landed; group slot gs (and side buffer gs) no longer read:
+                    // the MMA warp's copies of group gi - G have completed
+                    if (!warp_wait(araw_bar(rb), static_cast<uint32_t>(gi >> 1) & 1u, abort, lim) ||
+                        (gi >= G && !warp_wait_cluster(sempty_bar(gs), (use & 1u) ^ 1u, abort, lim))) {
+                        if (lane == 0) record_timeout(p, abort);
+                        ok = false;
+                        break;
+                    }
+                    armed &= ~(1u << rb);
+                    // chunk u (K-tile u of the group), byte 16p + 4q + c = row 32q + p,
+                    // K-block c; staging row r = the pair's row r (even CTA: 0..127)
+                    const uint8_t *src = smem_raw + (sRaw - raw) + rb * C::kSaRawBytes;
+                    uint8_t *own = smem_raw + (sSF - raw) + gs * C::kSfGrpBytes;
+                    uint8_t *lead = smem_raw + (sLead - raw) + gs * C::kSaLeadBytes;
+                    uint4 rowv[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        rowv[q] = reinterpret_cast<const uint4 *>(src)[32 * q + lane];
+#pragma unroll
+                    for (int u = 0; u < kSfGroup; ++u) {
+                        auto word = [&](const uint4 &x) { return u == 0 ? x.x : u == 1 ? x.y : u == 2 ? x.z : x.w; };
+                        reinterpret_cast<uint4 *>(lead + u * kSfChunk)[lane] =
+                            make_uint4(word(rowv[0]), word(rowv[1]), word(rowv[2]), word(rowv[3]));
+                        reinterpret_cast<uint4 *>(own + u * kSfChunk)[lane] =
+                            make_uint4(word(rowv[4]), word(rowv[5]), word(rowv[6]), word(rowv[7]));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (elect_one())
+                        bulk_copy_s2s_cluster(map_to_cta(sSF + gs * C::kSfGrpBytes, 0), sLead + gs * C::kSaLeadBytes,
+                                              C::kSaLeadBytes, map_to_cta(sfull_bar(gs), 0));
+                    __syncwarp();
+                    kt_cur = kt_nxt;
+                    row_cur = row_nxt;
+                    has_cur = has_nxt;
+                }
+                if (!ok)
+                    for (int b2 = 0; b2 < 2; ++b2)
+                        if (armed & (1u << b2))
+                            warp_wait(araw_bar(b2), (armed_ph >> b2) & 1u, no_abort, lim);
             }
         }
     } else if (warp == 1 && leader) {
@@ -254,28 +393,31 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         int gi = 0;  // scale groups started
         bool ok = true;
         bool issued = false;
-        // Scale group in, at the group's first k-stage k_ (n_ stages of this work
-        // unit in the group): wait until both CTAs' group slots have landed and
-        // the TMEM regions the group goes to are no longer read (the MMAs of the
-        // group two before have completed), copy each CTA's chunks into its own
-        // TMEM (one region per stage), and commit so both producers may refill
-        // their slot.
-        auto group_in = [&](int k_, int n_) -> bool {
-            const int gs = gi & 1;
-            const uint32_t use = static_cast<uint32_t>(gi >> 1);
+        // Scale group in, for the group holding k-stage kb, whose stages
+        // [lo, hi) belong to the work unit: wait until both CTAs' group slots
+        // are complete (copies landed, fused layouts done) and the TMEM
+        // regions the group goes to are no longer read (the MMAs of the group
+        // kGrp before have completed); copy each CTA's chunks of the unit's stages
+        // into its own TMEM (one region per stage); commit so both producers may
+        // refill their slot.
+        auto group_in = [&](int kb, int lo, int hi) -> bool {
+            const int gs = gi % G;
+            const uint32_t use = static_cast<uint32_t>(gi / G);
             if (!warp_wait_cluster(sfull_bar(gs), use & 1u, abort, lim))
                 return false;
-            if (gi >= 2 && !warp_wait(tfree_bar(gs), (use & 1u) ^ 1u, abort, lim))
+            if (gi >= G && !warp_wait(tfree_bar(gs), (use & 1u) ^ 1u, abort, lim))
                 return false;
             tc_fence_after();
             const uint32_t src = sSF + gs * C::kSfGrpBytes;
+            const int g0 = kb - kb % kSfGroup;
             // one elected lane issues the group's copies (and, below, the MMAs
             // and commits) in one block: separate elect blocks per instruction
             // measured up to 10% slower on long k-loops
             if (elect_one()) {
 #pragma unroll 1
-                for (int j = 0; j < n_; ++j) {
-                    const int nkt_ = min(C::kKtPerStage, p.num_kt - (k_ + j) * C::kKtPerStage);
+                for (int k = lo; k < hi; ++k) {
+                    const int j = k - g0;
+                    const int nkt_ = min(C::kKtPerStage, p.num_kt - k * C::kKtPerStage);
                     const uint32_t sfa_col_ = tmem + C::kSfCol0 + (gs * kSfGroup + j) * C::kSfSlotCols;
                     const uint32_t sfb_col_ = sfa_col_ + C::kSfaCols;
 #pragma unroll
@@ -313,12 +455,15 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem + acc * BN;
             const int ks0 = w.ks0, ks1 = w.ks1;
-            for (int ks = ks0; ks < ks1; ks += 2) {
-                const int rel = ks - ks0;
-                if (C::kScaled && rel % kSfGroup == 0 && !group_in(ks, min(kSfGroup, ks1 - ks))) {
-                    if (lane == 0) record_timeout(p, abort);
-                    ok = false;
-                    break;
+            const int kb0 = ks0 & ~1;
+            for (int kb = kb0; kb < ks1; kb += 2) {
+                if (group_start(kb, kb0)) {
+                    const int g0 = kb - kb % kSfGroup;
+                    if (!group_in(kb, max(ks0, g0), min(ks1, g0 + kSfGroup))) {
+                        if (lane == 0) record_timeout(p, abort);
+                        ok = false;
+                        break;
+                    }
                 }
                 if (!warp_wait_cluster(full_bar(st), ph, abort, lim)) {
                     if (lane == 0) record_timeout(p, abort);
@@ -327,18 +472,17 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 }
                 tc_fence_after();
                 issued = true;
-                const int nst = min(2, ks1 - ks);  // k-stages of the slot that belong to the unit
-                const int gcur = gi - 1;           // the scale group of the slot's stages
+                const int gcur = gi - 1;  // the scale group of the slot's stages
                 // the group's TMEM regions are free again after the MMAs of its last slot
-                const bool group_end = C::kScaled && ((rel + 2) % kSfGroup == 0 || ks + 2 >= ks1);
+                const bool group_end = C::kScaled && ((kb + 2) % kSfGroup == 0 || kb + 2 >= ks1);
                 if (elect_one()) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        if (h < nst) {
-                            const int kk = ks + h;
+                        const int kk = kb + h;
+                        if (kk >= ks0 && kk < ks1) {
                             const int nkt = min(C::kKtPerStage, p.num_kt - kk * C::kKtPerStage);
                             const uint32_t sfa_col =
-                                tmem + C::kSfCol0 + ((gcur & 1) * kSfGroup + (rel + h) % kSfGroup) * C::kSfSlotCols;
+                                tmem + C::kSfCol0 + ((gcur % G) * kSfGroup + kk % kSfGroup) * C::kSfSlotCols;
                             const uint32_t sfb_col = sfa_col + C::kSfaCols;
                             const uint64_t adesc = sdesc_kmajor_sw128(sA + (st * 2 + h) * C::kABytes);
                             const uint64_t bdesc = sdesc_kmajor_sw128(sB + (st * 2 + h) * C::kBBytes);
@@ -367,7 +511,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                     }
                     tc_commit_pair(empty_bar(st), 0x3);
                     if (group_end)
-                        tc_commit_pair(tfree_bar(gcur & 1), 0x1);
+                        tc_commit_pair(tfree_bar(gcur % G), 0x1);
                 }
                 __syncwarp();
                 if (++st == S) {

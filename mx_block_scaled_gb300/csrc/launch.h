@@ -58,13 +58,14 @@ cudaError_t launch_gemm_grouped_fp4(int bn, const GemmParams &p, const CUtensorM
                                     int grid, cudaStream_t stream);
 
 // CTA-pair kernel (cluster of 2, cta_group::2), pair tile 256 x bn (bn = 128 or
-// 256), on `clusters` clusters; it also takes 2-D maps of the two tile-layout
-// scale tensors (rows of 256 bytes).  And the largest co-resident cluster count.
+// 256), on `clusters` clusters; it also takes 3-D maps of the two tile-layout
+// scale tensors and, for p.sa_fused, a 2-D map of the row-major A-role scales.
+// And the largest co-resident cluster count.
 cudaError_t launch_gemm_pair_fp8(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                 const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, int clusters,
+                                 const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, const CUtensorMap &map_sarm, int clusters,
                                  cudaStream_t stream);
 cudaError_t launch_gemm_pair_fp4(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                 const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, int clusters,
+                                 const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, const CUtensorMap &map_sarm, int clusters,
                                  cudaStream_t stream);
 int gemm_pair_max_clusters_fp8(int bn);
 int gemm_pair_max_clusters_fp4(int bn);
@@ -74,7 +75,7 @@ int gemm_pair_max_clusters_fp4(int bn);
 cudaError_t launch_gemm_bf16(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
                              int grid, cudaStream_t stream);
 cudaError_t launch_gemm_pair_bf16(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                  const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, int clusters,
+                                  const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, const CUtensorMap &map_sarm, int clusters,
                                   cudaStream_t stream);
 int gemm_pair_max_clusters_bf16(int bn);
 

@@ -42,18 +42,18 @@ struct Launchers {
     // 256 x BN tiles on CTA pairs (clusters of two).
     template <int BN>
     static cudaError_t pair(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &msa,
-                            const CUtensorMap &msb, int clusters, cudaStream_t s)
+                            const CUtensorMap &msb, const CUtensorMap &msarm, int clusters, cudaStream_t s)
     {
         cudaLaunchAttribute attr[2];
         if constexpr (BN == 256) {
             if (p.sk_ctas > 0) {
                 cudaLaunchConfig_t cfg =
                     launch_config(2 * clusters, kThreadsSk, CfgPair<KIND, BN>::kSmemBytes, s, attr, 2);
-                return cudaLaunchKernelEx(&cfg, mx_gemm_pair_kernel<KIND, BN, true>, p, ma, mb, msa, msb);
+                return cudaLaunchKernelEx(&cfg, mx_gemm_pair_kernel<KIND, BN, true>, p, ma, mb, msa, msb, msarm);
             }
         }
         cudaLaunchConfig_t cfg = launch_config(2 * clusters, kThreads, CfgPair<KIND, BN>::kSmemBytes, s, attr, 2);
-        return cudaLaunchKernelEx(&cfg, mx_gemm_pair_kernel<KIND, BN>, p, ma, mb, msa, msb);
+        return cudaLaunchKernelEx(&cfg, mx_gemm_pair_kernel<KIND, BN>, p, ma, mb, msa, msb, msarm);
     }
 
     // Co-resident clusters of two of the pair kernel (its work slots).
@@ -130,11 +130,12 @@ struct Launchers {
     }
 
     static cudaError_t launch_pair(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
-                                   const CUtensorMap &msa, const CUtensorMap &msb, int clusters, cudaStream_t s)
+                                   const CUtensorMap &msa, const CUtensorMap &msb, const CUtensorMap &msarm, int clusters,
+                                   cudaStream_t s)
     {
         switch (bn) {
-        case 128: return pair<128>(p, ma, mb, msa, msb, clusters, s);
-        case 256: return pair<256>(p, ma, mb, msa, msb, clusters, s);
+        case 128: return pair<128>(p, ma, mb, msa, msb, msarm, clusters, s);
+        case 256: return pair<256>(p, ma, mb, msa, msb, msarm, clusters, s);
         default: return cudaErrorInvalidValue;
         }
     }

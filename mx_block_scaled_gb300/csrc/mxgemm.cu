@@ -338,6 +338,7 @@ struct mxgemm_plan {
     int sk_halves;     // 128-row shares per tile (2 in pair mode): counters and slots per tile / unit
     int device;        // the device current when the plan was created; runs must use it
     size_t off_sfa, off_sfb, off_part, off_cnt, off_skp, ws_bytes;
+    int sa_fuse;        // 1: row-major A scales are laid out inside the GEMM (pair tiles, K % 512 == 0)
     int cnt_pool = -1;  // stream-K counters: offset in the library's counter array (-1: in the workspace)
     int cnt_n = 0;      // counters of the plan (stream-K tiles x 128-row shares)
     // TMA descriptor cache (re-encoded when an operand pointer changes)
@@ -345,7 +346,8 @@ struct mxgemm_plan {
     const void *map_ptr_b = nullptr;
     const void *map_ptr_sfa = nullptr;
     const void *map_ptr_sfb = nullptr;
-    CUtensorMap map_a, map_b, map_sfa, map_sfb;
+    const void *map_ptr_sarm = nullptr;
+    CUtensorMap map_a, map_b, map_sfa, map_sfb, map_sarm;
 };
 
 struct mxgemm_grouped_plan {
@@ -391,6 +393,23 @@ int encode_operand_map_2stage(CUtensorMap *map, const void *ptr, int64_t rows, i
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
+}
+
+// Row-major scales (rows x K/32 bytes) as a 2-D tensor for the CTA-pair kernel's
+// fused layout: box = one scale group (kSfGroup k-stages of kt_per_stage
+// K-tiles: 4 bytes each) of a pair tile's 256 rows (rows past the end read as
+// zero).  Needs (K/32) % 16 == 0 (row pitch) and group starts on 16-byte
+// boundaries (the kernel aligns its groups to them).
+int encode_rowmajor_sf_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int kt_per_stage)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 32), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 32)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(4 * kt_per_stage * mxg::kSfGroup), 256u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
 }
@@ -527,6 +546,10 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     // pair tiles load two 128-byte K-slices per box: MXFP4 rows must be a whole
     // number of slices (K % 256 == 0), else single-CTA tiles
     if (fmt == MXGEMM_FMT_MXFP4_E2M1 && K % 256 != 0) mode = 0;
+    // The activation scales' relayout (the FlyDSL page's "layout copy") runs
+    // inside the MXFP8 pair kernel when their row pitch K/32 allows 16-byte TMA
+    // rows.
+    p->sa_fuse = (mode == 1 && fmt == MXGEMM_FMT_MXFP8_E4M3 && !swap && K % 512 == 0) ? 1 : 0;
     if (mode != 0 && bn < 128) bn = 128;
     // Stream-K on CTA pairs runs on 256-wide tiles only (the pair instantiation
     // with fixup warps): a forced stream-K pair plan takes them.
@@ -696,12 +719,12 @@ int mxgemm_plan_describe(mxgemm_plan_t plan, char *buf, size_t len)
                                                 : bf16 ? mxg::gemm_info_bf16(plan->bn) : mxg::gemm_info_fp8(plan->bn));
     snprintf(buf, len,
              "fmt=%s out=%s tile=%dx%d mode=%s swap_ab=%d split_k=%d streamk=%d+%d/%d units=%dx%d kstages=%d grid=%d%s "
-             "stages=%d acc_stages=%d smem=%d",
+             "stages=%d acc_stages=%d smem=%d sa=%s",
              fp4 ? "mxfp4" : bf16 ? "bf16" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32",
              plan->mode == 1 ? 256 : 128,
              plan->bn, kModes[plan->mode], plan->swap, plan->splits, plan->dp_tiles, plan->sk_tiles, plan->sk_ctas,
              plan->tiles_m, plan->tiles_n, plan->kstages, plan->grid, plan->mode ? "x2" : "", ki.stages, ki.acc_stages,
-             ki.smem_bytes);
+             ki.smem_bytes, plan->sa_fuse ? "in-kernel" : "relayout");
     return MXGEMM_OK;
 }
 
@@ -761,7 +784,7 @@ static int prepare_impl(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB
     RelayoutJob jobs[2];
     int njobs = 0;
     if (plan->fmt != MXGEMM_FMT_BF16) {
-        if (!(run_flags & MXGEMM_RUN_SA_PRELAYOUT))
+        if (!(run_flags & MXGEMM_RUN_SA_PRELAYOUT) && !plan->sa_fuse)
             jobs[njobs++] = make_job(SA, plan->M, plan->K, ws + plan->off_sfa);
         if (!(run_flags & MXGEMM_RUN_SB_PRELAYOUT))
             jobs[njobs++] = make_job(SB, plan->N, plan->K, ws + plan->off_sfb);
@@ -787,9 +810,11 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     const bool bf16 = plan->fmt == MXGEMM_FMT_BF16;  // no scales: SA and SB are not read
     if (run_flags & ~(MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT | MXGEMM_RUN_PREPARED))
         return MXGEMM_ERR_ARG;
-    // after mxgemm_prepare, scales that were not pre-laid-out are in the workspace
+    // after mxgemm_prepare, scales that were not pre-laid-out are in the workspace --
+    // except row-major SA of a plan that lays it out inside the GEMM
     const bool prepared = (run_flags & MXGEMM_RUN_PREPARED) != 0;
-    const bool read_sa = !bf16 && (!prepared || (run_flags & MXGEMM_RUN_SA_PRELAYOUT));
+    const bool fused = plan->sa_fuse && !(run_flags & MXGEMM_RUN_SA_PRELAYOUT);
+    const bool read_sa = !bf16 && (!prepared || (run_flags & MXGEMM_RUN_SA_PRELAYOUT) || fused);
     const bool read_sb = !bf16 && (!prepared || (run_flags & MXGEMM_RUN_SB_PRELAYOUT));
     if ((read_sa && !SA) || (read_sb && !SB))
         return MXGEMM_ERR_ARG;
@@ -890,8 +915,8 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     cudaError_t e;
     if (plan->mode == 1 && bf16) {
         // the kernel reads no scale maps for BF16; pass valid descriptors anyway
-        e = mxg::launch_gemm_pair_bf16(plan->bn, p, plan->map_a, plan->map_b, plan->map_a, plan->map_b, plan->grid,
-                                       s);
+        e = mxg::launch_gemm_pair_bf16(plan->bn, p, plan->map_a, plan->map_b, plan->map_a, plan->map_b, plan->map_a,
+                                       plan->grid, s);
     } else if (plan->mode == 1) {
         const int ktps = fp4 ? 2 : 1;
         if (plan->map_ptr_sfa != p.sfa) {
@@ -904,10 +929,17 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
                 return MXGEMM_ERR_CUDA;
             plan->map_ptr_sfb = p.sfb;
         }
+        if (fused && plan->map_ptr_sarm != SA) {
+            if (encode_rowmajor_sf_map(&plan->map_sarm, SA, M, K, ktps) != MXGEMM_OK)
+                return MXGEMM_ERR_CUDA;
+            plan->map_ptr_sarm = SA;
+        }
+        p.sa_fused = fused ? 1 : 0;
+        const CUtensorMap &msarm = fused ? plan->map_sarm : plan->map_sfa;  // not read unless fused
         e = fp4 ? mxg::launch_gemm_pair_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->map_sfa, plan->map_sfb,
-                                            plan->grid, s)
+                                            msarm, plan->grid, s)
                 : mxg::launch_gemm_pair_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->map_sfa, plan->map_sfb,
-                                            plan->grid, s);
+                                            msarm, plan->grid, s);
     } else if (bf16)
         e = mxg::launch_gemm_bf16(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
     else

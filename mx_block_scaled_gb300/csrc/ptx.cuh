@@ -112,6 +112,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const v
 }
 
 // ------------------------------------------ programmatic dependent launch --
+// Order this thread's earlier generic-proxy writes to shared memory before
+// later async-proxy reads of it (tcgen05.cp, tcgen05.mma, TMA stores).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Block until every grid this launch depends on (the preceding kernel in the
 // stream, when this one was launched with programmatic stream serialization)
 // has completed and its memory operations are visible.  A no-op otherwise.
@@ -264,6 +268,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// Bulk copy from this CTA's shared memory to the shared memory of a CTA of
+// the cluster (dst and bar: shared::cluster addresses in that CTA), completing
+// on that CTA's barrier.  Addresses and size are multiples of 16 bytes.
+__device__ __forceinline__ void bulk_copy_s2s_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last()

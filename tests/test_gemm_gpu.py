@@ -248,6 +248,33 @@ def test_prelayout_scales_give_the_same_result(fmt):
     assert torch.equal(C1, C2) and torch.equal(C1, C3)
 
 
+@pytest.mark.parametrize("M,N,K,flags", [(136, 256, 512, PAIR), (383, 640, 1536, PAIR), (520, 1024, 4096, PAIR),
+                                         (520, 1024, 4096, PAIR | SK), (300, 768, 2048, PAIR | 3),
+                                         (1000, 512, 3072, PAIR | SK)])
+def test_in_kernel_scale_layout_exact(oracle_mod, M, N, K, flags):
+    """MXFP8 pair plans with K % 512 == 0 lay out the row-major activation
+    scales inside the GEMM (the odd CTA of each pair builds both CTAs' chunks):
+    ragged pair tiles (rows past M), many scale groups per tile, stream-K
+    segments and split-K slabs that start inside a group all give the oracle's
+    result, bit-identical to the pre-laid-out path."""
+    import torch
+    b = lib()
+    rng = np.random.default_rng([M, N, K, flags])
+    A, SA = small_int_codes(rng, M, K, FMT_MXFP8)
+    B, SB = small_int_codes(rng, N, K, FMT_MXFP8)
+    ref, _ = oracle_mod.gemm(FMT_MXFP8, A, SA, B, SB, K)
+    plan = b.Plan(M, N, K, FMT_MXFP8, OUT_F32, flags)
+    assert "sa=in-kernel" in plan.describe(), plan.describe()
+    dA, dB, dSA, dSB = to_dev(A), to_dev(B), to_dev(SA), to_dev(SB)
+    C1 = plan.run(dA, dSA, dB, dSB)
+    tSA = b.relayout_scales(dSA, M, K)
+    C2 = plan.run(dA, tSA, dB, dSB, run_flags=b.MXGEMM_RUN_SA_PRELAYOUT)
+    b.check_device_status()
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2), plan.describe()
+    assert (C1.double().cpu().numpy() == ref).all(), plan.describe()
+
+
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
 def test_nan_scale_makes_its_rows_nan(oracle_mod, fmt):
     """E8M0 code 0xFF is NaN: every output fed by such a block is NaN, the rest is exact."""
@@ -427,8 +454,9 @@ def test_prepare_then_run_equals_run(oracle_mod, fmt, plan_flags):
         sb_pre = rf & b.MXGEMM_RUN_SB_PRELAYOUT
         for _ in range(2):
             plan.prepare(None if sa_pre else dSA, None if sb_pre else dSB, rf)
-            C = plan.run(dA, tSA if sa_pre else None, dB, tSB if sb_pre else None,
-                         run_flags=rf | b.MXGEMM_RUN_PREPARED)
+            # a plan that lays out row-major SA inside the GEMM (sa=in-kernel) reads SA in run
+            sa_arg = tSA if sa_pre else (dSA if "sa=in-kernel" in plan.describe() else None)
+            C = plan.run(dA, sa_arg, dB, tSB if sb_pre else None, run_flags=rf | b.MXGEMM_RUN_PREPARED)
             b.check_device_status()
             torch.cuda.synchronize()
             assert (C.double().cpu().numpy() == ref).all(), (rf, plan.describe())
