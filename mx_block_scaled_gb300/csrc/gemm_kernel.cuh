@@ -834,6 +834,28 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         tmem_alloc(smem_addr(&tmem_base_holder), C::kTmemCols);
         tmem_relinquish();
     }
+    // The kernel that follows in the stream may be scheduled as SMs free up
+    // (it waits for this grid before it touches memory).
+    griddep_launch_dependents();
+    if constexpr (!GROUPED) {
+        if (warp == 0 && !p.test_stall) {
+            // Warm L2 with the first ring's worth of this CTA's operand boxes while
+            // the preceding kernel drains: a prefetch is only a hint and L2 is where
+            // that kernel's writes land, so no stale data can be read by it.
+            WorkIter wi0;
+            wi0.init(p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
+            Work w0;
+            if (wi0.next(p, w0) && elect_one()) {
+                TileGeom g0;
+                tile_geom<BN, C::kChunksB>(p, nullptr, w0, g0);
+                for (int ks = w0.ks0; ks < w0.ks1 && ks < w0.ks0 + S; ++ks) {
+                    tma_prefetch_2d(&map_a, ks * kRowBytes, g0.a_row);
+                    tma_prefetch_2d(&map_b, ks * kRowBytes, g0.b_row);
+                }
+            }
+            __syncwarp();
+        }
+    }
     // Everything above overlaps the end of the preceding kernel (programmatic
     // dependent launch); from here on global memory it wrote may be read.
     griddep_wait();

@@ -162,6 +162,25 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         tmem_alloc_pair(smem_addr(&tmem_base_holder), C::kTmemCols);
         tmem_relinquish_pair();
     }
+    // The kernel that follows in the stream may be scheduled as SMs free up
+    // (it waits for this grid before it touches memory).
+    griddep_launch_dependents();
+    if (warp == 0 && !p.test_stall) {
+        // Warm L2 with the first ring's worth of this CTA's operand boxes while
+        // the preceding kernel drains: a prefetch is only a hint and L2 is where
+        // that kernel's writes land, so no stale data can be read by it.
+        WorkIter wi0;
+        wi0.init(p, static_cast<int>(cluster_id_x()), static_cast<int>(cluster_count_x()));
+        Work w0;
+        if (wi0.next(p, w0) && elect_one()) {
+            const int kb0 = w0.ks0 & ~1;
+            for (int kb = kb0; kb < w0.ks1 && kb < kb0 + 2 * S; kb += 2) {
+                tma_prefetch_3d(&map_a, 0, (2 * w0.tm + static_cast<int>(rank)) * kBM, kb);
+                tma_prefetch_3d(&map_b, 0, w0.tn * BN + static_cast<int>(rank) * (BN / 2), kb);
+            }
+        }
+        __syncwarp();
+    }
     // Everything above overlaps the end of the preceding kernel (programmatic
     // dependent launch); from here on global memory it wrote may be read.
     griddep_wait();

@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
                                                              int out_kind)
 {
     mxg::griddep_wait();  // launched as a programmatic dependent of the GEMM that wrote `part`
+    mxg::griddep_launch_dependents();
     const long long n4 = n / 4;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;

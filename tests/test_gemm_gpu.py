@@ -249,7 +249,7 @@ def test_prelayout_scales_give_the_same_result(fmt):
 
 
 @pytest.mark.parametrize("M,N,K,flags", [(136, 256, 512, PAIR), (383, 640, 1536, PAIR), (520, 1024, 4096, PAIR),
-                                         (520, 1024, 4096, PAIR | SK), (300, 768, 2048, PAIR | 3),
+                                         (520, 1024, 4096, PAIR | SK), (300, 768, 2048, PAIR | (3 << 8)),
                                          (1000, 512, 3072, PAIR | SK)])
 def test_in_kernel_scale_layout_exact(oracle_mod, M, N, K, flags):
     """MXFP8 pair plans with K % 512 == 0 lay out the row-major activation
