@@ -75,7 +75,7 @@ struct GemmParams {
     int tiles_m, tiles_n, splits;
     int group_m;              // raster: tiles of the A role walked together
     int out_kind;             // OutKind
-    int vec_ok;               // 1: stride_j == 1 and rows are 16-byte aligned
+    int vec_ok;               // stride_j == 1 and rows 16-byte (1) or 32-byte (2) aligned; else 0
     int test_stall;           // self-test: the producer issues nothing (waits expire)
     int stream_a, stream_b;   // 1: that operand is read by at most two tiles (load it evict-first)
     int sa_fused;             // CTA-pair kernel: 1 = A-role scales are row-major (laid out in the kernel)
@@ -424,8 +424,42 @@ __device__ __forceinline__ void record_timeout(const GemmParams &p, volatile int
 }
 
 // Store 32 consecutive B-role values of one A-role row: out[off .. off+32).
+__device__ __forceinline__ void st_global_v8(void *dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                             uint32_t f, uint32_t g, uint32_t h)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a), "r"(b), "r"(c), "r"(d),
+                 "r"(e), "r"(f), "r"(g), "r"(h)
+                 : "memory");
+}
+
+// kWide: 32-byte stores where rows are 32-byte aligned.  The epilogue's stores
+// are one row per thread, so each store instruction touches 32 rows; 32-byte
+// stores fill whole sectors with half the instructions.  The stream-K fixup
+// paths (out-of-line functions) keep 16-byte stores: there the 32-byte form
+// stored only its first word in a GPU test.
+template <bool kWide = false>
 __device__ __forceinline__ void store_row32_vec(const GemmParams &p, long long off, const uint32_t (&r)[32])
 {
+    if (kWide && p.vec_ok == 2) {
+        if (p.out_kind == OUT_BF16) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                w[e] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            uint32_t *dst = reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(p.out) + off);
+            st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            st_global_v8(dst + 8, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+        } else {
+            uint32_t *dst = reinterpret_cast<uint32_t *>(static_cast<float *>(p.out) + off);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                st_global_v8(dst + 8 * v, r[8 * v], r[8 * v + 1], r[8 * v + 2], r[8 * v + 3], r[8 * v + 4],
+                             r[8 * v + 5], r[8 * v + 6], r[8 * v + 7]);
+        }
+        return;
+    }
     if (p.out_kind == OUT_BF16) {
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + off);
 #pragma unroll
@@ -1175,7 +1209,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                     const int j0 = tn * BN + h * kCols + c * 32;
                     if (j0 >= g.lim_j) break;
                     if (p.vec_ok && j0 + 32 <= g.lim_j)
-                        store_row32_vec(p, base_off + j0, r[c]);
+                        store_row32_vec<true>(p, base_off + j0, r[c]);
                     else
                         store_row32_masked(p, base_off, j0, min(32, g.lim_j - j0), r[c]);
                 }

@@ -460,10 +460,28 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             ++gi;
             return true;
         };
+        // A unit's first scale group is copied in before the accumulator wait:
+        // its TMEM regions are not the accumulator's, so the copies overlap the
+        // previous tile's drain and epilogue instead of delaying the first MMAs
+        // (at a tile start the group's waits and copies took ~1.5 us).
+        auto first_group_in = [&](const Work &u) -> bool {
+            if constexpr (!C::kScaled) {
+                return true;
+            } else {
+                const int kb0 = u.ks0 & ~1;
+                const int g0 = kb0 - kb0 % kSfGroup;
+                return group_in(kb0, max(u.ks0, g0), min(u.ks1, g0 + kSfGroup));
+            }
+        };
         WorkIter wi;
         wi.init(p, first_unit, unit_step);
         Work w;
-        for (; ok && wi.next(p, w); ++it) {
+        bool have = wi.next(p, w);
+        if (have && !first_group_in(w)) {
+            if (lane == 0) record_timeout(p, abort);
+            ok = false;
+        }
+        for (; ok && have; ++it) {
             const int acc = it % C::kAccStages;
             const uint32_t acc_par = static_cast<uint32_t>((it / C::kAccStages) & 1);
             if (!warp_wait_cluster(acce_bar(acc), acc_par ^ 1u, abort, lim)) {
@@ -476,7 +494,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             const int ks0 = w.ks0, ks1 = w.ks1;
             const int kb0 = ks0 & ~1;
             for (int kb = kb0; kb < ks1; kb += 2) {
-                if (group_start(kb, kb0)) {
+                if (kb != kb0 && group_start(kb, kb0)) {
                     const int g0 = kb - kb % kSfGroup;
                     if (!group_in(kb, max(ks0, g0), min(ks1, g0 + kSfGroup))) {
                         if (lane == 0) record_timeout(p, abort);
@@ -542,6 +560,11 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             if (elect_one())
                 tc_commit_pair(accf_bar(acc), 0x3);
             __syncwarp();
+            have = wi.next(p, w);
+            if (have && !first_group_in(w)) {
+                if (lane == 0) record_timeout(p, abort);
+                ok = false;
+            }
         }
         if (!ok && issued) {
             if (elect_one())
@@ -609,7 +632,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                     const int j0 = tn * BN + h * kCols + c * 32;
                     if (j0 >= p.rows_b) break;
                     if (p.vec_ok && j0 + 32 <= p.rows_b)
-                        store_row32_vec(p, base_off + j0, r[c]);
+                        store_row32_vec<true>(p, base_off + j0, r[c]);
                     else
                         store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), r[c]);
                 }

@@ -132,6 +132,16 @@ int device_info(DeviceInfo **out)
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Vector width of the epilogue's row stores: 2 = 32-byte stores (row pitch and
+// base 32-byte aligned), 1 = 16-byte stores, 0 = element stores (transposed
+// output, or rows not 16-byte aligned).
+inline int vec_level(bool rows_contiguous, int64_t row_bytes, const void *base)
+{
+    if (!rows_contiguous || row_bytes % 16 != 0 || !aligned16(base))
+        return 0;
+    return (row_bytes % 32 == 0 && (reinterpret_cast<uintptr_t>(base) & 31u) == 0) ? 2 : 1;
+}
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -680,7 +690,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     off = align256(off + (bf16 ? 0 : mxgemm_sf_bytes(N, K)));
     p->off_part = off;
     if (p->splits > 1)
-        off = align256(off + static_cast<size_t>(p->splits) * ((M * N + 3) & ~3ll) * sizeof(float));
+        off = align256(off + static_cast<size_t>(p->splits) * ((M * N + 7) & ~7ll) * sizeof(float));
     p->off_cnt = off;
     p->off_skp = off;
     if (p->sk_ctas > 0) {
@@ -905,13 +915,13 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     if (split) {
         p.out = ws + plan->off_part;
         p.out_kind = mxg::OUT_F32;
-        p.split_stride = (M * N + 3) & ~3ll;  // keeps every slab 16-byte aligned
+        p.split_stride = (M * N + 7) & ~7ll;  // keeps every slab 32-byte aligned
     } else {
         p.out = C;
         p.out_kind = plan->out == MXGEMM_OUT_BF16 ? mxg::OUT_BF16 : mxg::OUT_F32;
         p.split_stride = 0;
     }
-    p.vec_ok = (!plan->swap && (N * osize) % 16 == 0 && aligned16(p.out)) ? 1 : 0;
+    p.vec_ok = vec_level(!plan->swap, N * osize, p.out);
 
     cudaError_t e;
     if (plan->mode == 1 && bf16) {
@@ -958,7 +968,7 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
         cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = mxg::launch_config(blocks, 256, 0, s, attr, 1);
         if (cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, reinterpret_cast<const float *>(ws + plan->off_part),
-                               plan->splits, n, (n + 3) & ~3ll, static_cast<void *>(C),
+                               plan->splits, n, (n + 7) & ~7ll, static_cast<void *>(C),
                                plan->out == MXGEMM_OUT_BF16 ? static_cast<int>(mxg::OUT_BF16)
                                                             : static_cast<int>(mxg::OUT_F32)) != cudaSuccess)
             return MXGEMM_ERR_CUDA;
@@ -1200,7 +1210,7 @@ int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *group_offsets,
     const int osize = plan->out == MXGEMM_OUT_BF16 ? 2 : 4;
     p.stride_i = plan->swap ? 1 : N;
     p.stride_j = plan->swap ? N : 1;
-    p.vec_ok = (!plan->swap && (N * osize) % 16 == 0 && aligned16(C)) ? 1 : 0;
+    p.vec_ok = vec_level(!plan->swap, N * osize, C);
     // the weights are streamed when each group has at most two token tiles
     const int64_t avg = std::max<int64_t>(1, T / G);
     const bool stream_w = ceil_div(avg, plan->swap ? plan->bn : 128) <= 2;
