@@ -178,6 +178,19 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 tma_prefetch_3d(&map_a, 0, (2 * w0.tm + static_cast<int>(rank)) * kBM, kb);
                 tma_prefetch_3d(&map_b, 0, w0.tn * BN + static_cast<int>(rank) * (BN / 2), kb);
             }
+            if constexpr (C::kScaled) {
+                // and the first scale group (the first MMAs wait for it)
+                const int gkt0 = (kb0 - kb0 % kSfGroup) * C::kKtPerStage;
+                const int rb_a0 = 2 * w0.tm + static_cast<int>(rank);
+                if (rank == 0)
+                    tma_prefetch_3d(&map_sfb, 0, 2 * gkt0, (w0.tn * BN) / 128);
+                if (p.sa_fused) {
+                    if (rank == 1)
+                        tma_prefetch_2d(&map_sarm, 4 * gkt0, 2 * w0.tm * kBM);
+                } else if (rb_a0 < (p.rows_a + 127) / 128) {
+                    tma_prefetch_3d(&map_sfa, 0, 2 * gkt0, rb_a0);
+                }
+            }
         }
         __syncwarp();
     }
