@@ -394,7 +394,10 @@ def run_ours(args):
         assert mx.mxgemm_relayout_scales(s["SB"].data_ptr(), N, K, s["tSB"].data_ptr(), sh) == 0
     torch.cuda.synchronize()
 
+    launch = {"sh": sh}  # the stream the steps launch on (a side stream while a graph is captured)
+
     def step(i, ev=None):
+        sh = launch["sh"]
         s = sets[i % nsets]
         if ev is not None:
             ev[0].record(stream)
@@ -452,10 +455,13 @@ def run_ours(args):
     # replayed (how a serving loop launches them: no per-launch host work between
     # the kernels, programmatic-dependent-launch edges kept in the graph).  The
     # headline is the faster of the two launch modes; both are reported.
+    capture = torch.cuda.Stream(device=dev)  # graphs are captured off the default stream
     graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
+    launch["sh"] = capture.cuda_stream
+    with torch.cuda.graph(graph, stream=capture):
         for k in range(args.steps):
             step(k)
+    launch["sh"] = sh
     graph.replay()
     torch.cuda.synchronize()
     if ws > 1:
@@ -473,6 +479,7 @@ def run_ours(args):
     # back to back on the prepared workspace of each rotating set, events only at
     # the ends (the kernel's average duration as a stream runs it).
     def gemm_only(i):
+        sh = launch["sh"]
         s = sets[i % nsets]
         st = mx.mxgemm_run(plan.handle, s["A"].data_ptr(), s["SA"].data_ptr(), s["B"].data_ptr(),
                            s["tSB"].data_ptr(), s["C"].data_ptr(), plan.workspace.data_ptr(), plan.ws_bytes,
@@ -487,9 +494,11 @@ def run_ours(args):
     g_end.record(stream)
     torch.cuda.synchronize()
     gemm_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gemm_graph, stream=stream):
+    launch["sh"] = capture.cuda_stream
+    with torch.cuda.graph(gemm_graph, stream=capture):
         for k in range(args.steps):
             gemm_only(k)
+    launch["sh"] = sh
     gemm_graph.replay()
     torch.cuda.synchronize()
     gg_start, gg_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
