@@ -536,22 +536,28 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     int bn = pick_bn(rows_b);
     if (flags & MXGEMM_PLAN_FORCE_BN128) bn = 128;
     if (flags & MXGEMM_PLAN_FORCE_BN256) bn = 256;
-    // Pair tiles need 128- or 256-wide N tiles.  Default: MXFP8 and BF16 with
-    // at least 128 rows on each side run 256 x 256 pair tiles (measured faster
-    // from 128 tokens up).  An MXFP4 k-stage moves the same operand bytes as an
-    // MXFP8 one in the same MMA time, so it gains the same from the pair tile's
-    // halved B-operand loads -- measured +8-13% from four waves of pair tiles
-    // up (8192^3, 16384 x 8192 x 8192, 8192 x 4096 x 14336) but 2-4% slower at
-    // 3.4 waves (4096^3, 2048 x 4096 x 4096), so MXFP4 takes pair tiles from
-    // four waves on.  Swapped decode shapes stay on single-CTA tiles.
+    // Pair tiles need 128- or 256-wide N tiles.  Default: every format with at
+    // least 128 rows on each side runs 256 x 256 pair tiles (measured faster from
+    // 128 tokens up): an MXFP4 k-stage moves the same operand bytes as an MXFP8
+    // one in the same MMA time, so it gains the same from the pair tile's halved
+    // B-operand loads (2048 x 4096 x 14336: 56.5 -> 43.8 us; 4096^3: 35.9 ->
+    // 28.7 us; 256 x 28672 x 4096: 21.5 -> 19.7 us).  MXFP4 with fewer pair
+    // tiles than half the pairs stays on single-CTA tiles, which need fewer
+    // K-splits (128 x 5120 x 25600: pair 31.4 us, single 22.2 us); MXFP8 keeps
+    // the pair tiles there, whose in-kernel activation-scale layout saves the
+    // relayout launch.  Swapped decode shapes stay on single-CTA tiles.
     int mode = 0;
     const bool pair_ok = !swap && rows_a >= 128 && rows_b >= 256 && !(flags & MXGEMM_PLAN_FORCE_BN128) &&
                          ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0;
     const int64_t pair_tiles = ceil_div(rows_a, 256) * ceil_div(rows_b, 256);
-    if (pair_ok && (fmt == MXGEMM_FMT_MXFP8_E4M3 || bf16))
+    if (pair_ok && (fmt != MXGEMM_FMT_MXFP4_E2M1 || pair_tiles >= dev->num_sms / 4))
         mode = 1;
-    if (pair_ok && fmt == MXGEMM_FMT_MXFP4_E2M1 && pair_tiles >= 4 * (dev->num_sms / 2))
-        mode = 1;
+    // BF16 runs its MMAs at half the MX rate per operand byte, so it is bound by
+    // the tensor pipe where MX formats wait on memory: with at most 128 tokens a
+    // pair tile's M = 256 MMAs would compute half empty rows (128 x 10240 x 5120:
+    // pair 30.5 us, 128 x 128 tiles 23.9 us) -- unless the narrower tiles need
+    // more than one wave (128 x 51200 x 5120: pair 95.0 us, single 97.5 us).
+    if (bf16 && rows_a <= 128 && ceil_div(rows_b, 128) <= dev->num_sms) mode = 0;
     if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_SINGLE) mode = 0;
     // pair tiles load two 128-byte K-slices per box: MXFP4 rows must be a whole
@@ -562,6 +568,18 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     // rows.
     p->sa_fuse = (mode == 1 && fmt == MXGEMM_FMT_MXFP8_E4M3 && !swap && K % 512 == 0) ? 1 : 0;
     if (mode != 0 && bn < 128) bn = 128;
+    // BF16 with few tiles: 128-wide N tiles rather than a 256-wide tile count
+    // below the work slots (which leaves SMs idle or needs split-K and its reduce
+    // pass), as long as the narrower tiles still fit in one wave.  Measured
+    // (256 tokens, K = 4096-8192): N = 6144 20.8 -> 17.4 us, N = 8192 35.7 ->
+    // 31.8 us; 128 tokens: N = 5120 25.9 -> 20.5 us.
+    if (bf16 && bn == 256 &&
+        !(flags & (MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_STREAMK))) {
+        const int64_t units_m = mode == 0 ? ceil_div(rows_a, 128) : ceil_div(rows_a, 256);
+        const int64_t slots_est = mode == 0 ? dev->num_sms : dev->num_sms / 2;
+        if (units_m * ceil_div(rows_b, 256) < slots_est && units_m * ceil_div(rows_b, 128) <= slots_est)
+            bn = 128;
+    }
     // Stream-K on CTA pairs runs on 256-wide tiles only (the pair instantiation
     // with fixup warps): a forced stream-K pair plan takes them.
     if ((flags & MXGEMM_PLAN_STREAMK) && mode == 1) bn = 256;
