@@ -194,13 +194,14 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         }
         __syncwarp();
     }
-    // Everything above overlaps the end of the preceding kernel (programmatic
-    // dependent launch); from here on global memory it wrote may be read.
-    griddep_wait();
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // barriers of both CTAs initialised before any cross-CTA arrive
     tc_fence_after();
+    // Everything above (the cluster barrier included) overlaps the end of the
+    // preceding kernel (programmatic dependent launch); from here on global
+    // memory it wrote may be read.
+    griddep_wait();
     const uint32_t tmem = tmem_base_holder;
 
     // Work of this pair (tiles_m counts 256-row pair tiles): stream-K segments,
