@@ -460,3 +460,31 @@ def test_prepare_then_run_equals_run(oracle_mod, fmt, plan_flags):
             b.check_device_status()
             torch.cuda.synchronize()
             assert (C.double().cpu().numpy() == ref).all(), (rf, plan.describe())
+
+
+@pytest.mark.parametrize("fmt,M,N,K,expect", [
+    ("mxfp8", 4096, 4096, 4096, ["tile=256x256", "mode=pair", "streamk=228+28/56", "sa=in-kernel"]),
+    ("mxfp8", 16384, 8192, 8192, ["tile=256x256", "mode=pair", "sa=in-kernel"]),
+    ("mxfp8", 8, 10240, 8192, ["tile=128x32", "mode=single", "swap_ab=1", "streamk=0+80/152"]),
+    ("mxfp8", 64, 8192, 8192, ["tile=128x64", "swap_ab=1"]),
+    ("mxfp4", 4096, 4096, 4096, ["tile=256x256", "mode=pair", "sa=relayout"]),
+    ("mxfp4", 256, 6144, 4096, ["tile=128x256", "mode=single"]),
+    ("mxfp4", 256, 10240, 8192, ["mode=pair"]),
+    ("bf16", 128, 10240, 5120, ["tile=128x128", "mode=single"]),
+    ("bf16", 128, 51200, 5120, ["mode=pair"]),
+    ("bf16", 256, 6144, 4096, ["tile=256x128", "mode=pair"]),
+    ("bf16", 256, 10240, 8192, ["tile=256x256", "mode=pair"]),
+])
+def test_default_plans_follow_the_heuristic(fmt, M, N, K, expect):
+    """The planner's choices on representative shapes, as the design documents them
+    (pair tiles for MXFP8 from 128 tokens, MXFP4 pair tiles from half a wave,
+    BF16 small-token tile rules, swap-AB decode with stream-K over every SM)."""
+    b = lib()
+    f = {"mxfp8": FMT_MXFP8, "mxfp4": FMT_MXFP4, "bf16": b.MXGEMM_FMT_BF16}[fmt]
+    plan = b.Plan(M, N, K, f, OUT_BF16)
+    d = plan.describe()
+    sms = __import__("torch").cuda.get_device_properties(0).multi_processor_count
+    for e in expect:
+        if "streamk=" in e and sms != 152:
+            continue  # the stream-K split depends on the SM count
+        assert e in d, (e, d)
