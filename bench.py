@@ -24,7 +24,9 @@ has no exchange step); value = all ranks' FLOPs / the slowest rank's time.
 same result here) on a bounded sample of the same workload.
 --sweep prints one line per shape of the model workloads (not the headline);
 --quant-sweep one line per activation shape for the MX quantiser; --grouped-sweep
-one line per grouped (mixture-of-experts) case.
+one line per grouped (mixture-of-experts) case; --tensor-probe one line per MMA
+kind and tile of the tensor pipe's own rate (operands resident in shared memory),
+the ceiling the GEMM lines are compared with.
 """
 from __future__ import annotations
 
@@ -1047,6 +1049,34 @@ def run_placement_sweep(args):
     return 0
 
 
+def run_tensor_probe(args):
+    """Tensor-pipe rate probe: back-to-back tcgen05.mma from shared-memory operands
+    on every SM (or CTA pair), no loads.  One JSON line per (format, cta_group, N,
+    scale copies): cycles per MMA, the SM clock the kernel itself saw (clock64 over
+    globaltimer: each run lasts milliseconds, too short for nvidia-smi sampling),
+    whole-GPU dense PFLOP/s, and that rate against the measured-peak roofline the
+    GEMM lines use."""
+    import torch
+    from mx_block_scaled_gb300 import binding as mx
+    torch.cuda.set_device(0)
+    _, bf16_tf, _, peak_src = load_peaks()
+    fmts = [("mxfp8", mx.MXGEMM_FMT_MXFP8_E4M3), ("mxfp4", mx.MXGEMM_FMT_MXFP4_E2M1), ("bf16", mx.MXGEMM_FMT_BF16)]
+    for name, fmt in fmts:
+        for cg in (1, 2):
+            for n in (128, 256):
+                for cp in ((0, 1) if fmt != mx.MXGEMM_FMT_BF16 else (0,)):
+                    r = mx.mxgemm_probe_tensor_rate(fmt, cg, n, cp, args.probe_stages)
+                    peak = mx_peak_tflops(name, bf16_tf) / 1e3
+                    rec = {"kernel": "tensor_rate_probe", "fmt": name, "cta_group": cg, "n": n,
+                           "scale_copies": bool(cp), "stages": args.probe_stages,
+                           "m_per_mma": 128 * cg, "cycles_per_mma": round(r["cycles_per_mma"], 2),
+                           "sm_ghz": round(r["sm_ghz"], 3), "units": r["units"], "pflops": round(r["pflops"], 3),
+                           "peak_pflops": round(peak, 3), "frac_of_peak": round(r["pflops"] / peak, 3),
+                           "peak_src": f"{peak_src} bf16 x nominal {name}/bf16"}
+                    print(json.dumps(rec), flush=True)
+    return 0
+
+
 def _cpu_model() -> str:
     try:
         out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
@@ -1131,6 +1161,9 @@ def main():
     ap.add_argument("--out-dir", default="", help="--placement-sweep: save the per-pair counts here (.npz)")
     ap.add_argument("--placement-sweep", action="store_true",
                     help="run the scale-placement checker over every scale pair for k = 1, 2, 3")
+    ap.add_argument("--tensor-probe", action="store_true",
+                    help="measure the tensor pipe's own MMA rate (operands resident in shared memory)")
+    ap.add_argument("--probe-stages", type=int, default=16384, help="k-stages per unit for --tensor-probe")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -1146,6 +1179,8 @@ def main():
         return run_placement_sweep(args)
     if args.oracle_sweep:
         return run_oracle_sweep(args)
+    if args.tensor_probe:
+        return run_tensor_probe(args)
     if args.sweep or args.shape:
         return run_sweep(args)
     return run_ours(args)

@@ -411,6 +411,36 @@ MXGEMM_API int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *gro
 MXGEMM_API int mxgemm_placement_scan(int k, const int *sa, const int *sb, int npairs, long long *counts,
                                      long long *first_diff, void *stream);
 
+/*
+ * Tensor-pipe rate probe: the ceiling the GEMM kernels are measured against.
+ * Every SM (cta_group 1) or CTA pair (cta_group 2, clusters of 2) holds four
+ * operand sets in shared memory and issues `stages` k-stages of back-to-back
+ * tcgen05.mma into one TMEM accumulator, with no global loads; each k-stage
+ * is 128 bytes of K per row (4 MMAs: K = 32 for MXFP8, 64 for MXFP4 (two per
+ * 128-element scale tile), 16 for BF16), M = 128 per CTA (256 per pair) and
+ * N = `n` (128 or 256) columns.  scale_copies = 1 also issues, per k-stage,
+ * the tcgen05.cp copies of the stage's scale chunks into TMEM that a GEMM
+ * k-stage issues (ignored for BF16).  The operand values are fixed finite
+ * codes with scale 1; the products are not read.
+ *   fmt:     MXGEMM_FMT_MXFP8_E4M3, MXGEMM_FMT_MXFP4_E2M1 or MXGEMM_FMT_BF16
+ *   stages:  16 .. 2^22 (4 * stages MMAs per unit; ~4096 lasts ~1 ms)
+ *   result:  host double[4], written on success:
+ *            [0] cycles per MMA (SM clock, mean over units),
+ *            [1] SM clock during the run in GHz (clock64 over globaltimer),
+ *            [2] dense PFLOP/s of the whole GPU (all units' MMAs over the
+ *                span from the first unit's start to the last unit's end),
+ *            [3] units that ran (SMs, or pairs).
+ * Synchronous: launches a short warm-up and the measured kernel on `stream`
+ * and waits for them.  Uses a static device array of the library (no
+ * allocation); calls must not overlap.  Each unit waits for its MMAs with a
+ * two-second limit.
+ * Errors: MXGEMM_ERR_ARG (NULL result, fmt / cta_group / n / scale_copies /
+ * stages out of range), MXGEMM_ERR_ARCH, MXGEMM_ERR_CUDA,
+ * MXGEMM_ERR_DEVICE_TIMEOUT (a unit's wait expired).
+ */
+MXGEMM_API int mxgemm_probe_tensor_rate(int fmt, int cta_group, int n, int scale_copies, int stages,
+                                        double *result, void *stream);
+
 /* Static, human-readable name of a status code. */
 MXGEMM_API const char *mxgemm_status_str(int status);
 

@@ -71,6 +71,8 @@ SIGNATURES = [
     ("mxgemm_grouped_plan_describe", ctypes.c_int, [_P, ctypes.c_char_p, ctypes.c_size_t]),
     ("mxgemm_grouped_run", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     ("mxgemm_placement_scan", ctypes.c_int, [ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P]),
+    ("mxgemm_probe_tensor_rate", ctypes.c_int,
+     [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double), _P]),
     ("mxgemm_status_str", ctypes.c_char_p, [ctypes.c_int]),
     ("mxgemm_version", ctypes.c_int, []),
 ]
@@ -346,6 +348,17 @@ def placement_scan(k: int, sa, sb, stream=None):
     _check(mxgemm_placement_scan(k, sa.data_ptr(), sb.data_ptr(), n, counts.data_ptr(), first.data_ptr(),
                                  _stream_handle(stream)), "mxgemm_placement_scan")
     return counts, first
+
+
+def mxgemm_probe_tensor_rate(fmt: int, cta_group: int, n: int, scale_copies: int, stages: int,
+                             stream=None) -> dict:
+    """Tensor-pipe rate probe (tcgen05.mma from shared-memory operands, no loads) on
+    the current device.  Synchronous.  Returns cycles per MMA, the SM clock in GHz,
+    the whole-GPU dense PFLOP/s and the number of SMs or CTA pairs that ran."""
+    out = (ctypes.c_double * 4)()
+    _check(_lib.mxgemm_probe_tensor_rate(fmt, cta_group, n, scale_copies, stages, out, _stream_handle(stream)),
+           "mxgemm_probe_tensor_rate")
+    return {"cycles_per_mma": out[0], "sm_ghz": out[1], "pflops": out[2], "units": int(out[3])}
 
 
 def check_device_status(stream=None) -> None:

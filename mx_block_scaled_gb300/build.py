@@ -20,7 +20,7 @@ OBJ_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmxgemm.so")
 
-SOURCES = ["mxgemm.cu", "gemm_fp8.cu", "gemm_fp4.cu", "gemm_bf16.cu", "quantize.cu", "placement.cu"]
+SOURCES = ["mxgemm.cu", "gemm_fp8.cu", "gemm_fp4.cu", "gemm_bf16.cu", "quantize.cu", "placement.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I" + INCLUDE, "-I" + CSRC]

@@ -187,3 +187,18 @@ def test_binding_constants_match_the_header(lib):
             assert getattr(lib, name) == val, name
             checked += 1
     assert checked >= 15
+
+
+@pytest.mark.parametrize("fmt,cg,n,cp,stages", [
+    (0, 1, 256, 0, 1024),     # unknown format
+    (1, 3, 256, 0, 1024),     # cta_group not 1 or 2
+    (1, 1, 192, 0, 1024),     # N not 128 or 256
+    (1, 1, 256, 2, 1024),     # scale_copies not 0 or 1
+    (1, 1, 256, 0, 8),        # too few k-stages
+    (2, 2, 128, 1, 1 << 23),  # too many k-stages
+])
+def test_tensor_probe_validates_before_touching_the_device(lib, fmt, cg, n, cp, stages):
+    import ctypes
+    out = (ctypes.c_double * 4)()
+    assert lib._lib.mxgemm_probe_tensor_rate(fmt, cg, n, cp, stages, out, None) == lib.MXGEMM_ERR_ARG
+    assert lib._lib.mxgemm_probe_tensor_rate(1, 1, 256, 0, 1024, None, None) == lib.MXGEMM_ERR_ARG
