@@ -675,12 +675,16 @@ __device__ __noinline__ void sk_fixup_warps(const GemmParams &p, const SkFix &sl
 // Stream-K epilogue of one CTA's 128-row share of a tile cut between CTAs (or
 // CTA pairs): publish this segment's FP32 partial sum; if it is the last
 // segment of the tile to arrive, the tile's segments are added in k order --
-// by the fixup warps (the job is posted to them; this CTA's own partial is
-// re-read from its slot), or, for tiles of at most 64 columns (kEpiFix: the
-// weight-streaming decode tiles, whose partials are 16-32 KB), by these
-// epilogue warps themselves: 128-256 threads with two segments' loads in
-// flight at a time finish in one or two L2 round trips, where the two fixup
-// warps would take several.  Either way each element is ((0 + s_first) + ...) + s_last.
+// by the fixup warps (the job is posted through `fx`; this CTA's own partial is
+// re-read from its slot), or, with kEpiFix, by these epilogue warps themselves:
+// 256 threads with two segments' loads in flight at a time take a quarter of
+// the L2 round trips of the two fixup warps.  kEpiFix serves the single-CTA
+// weight-streaming decode tiles (at most 64 columns, partials of 16-32 KB) and
+// every CTA-pair tile (the pair kernel has no fixup warps; the epilogue has
+// handed its accumulator back before the fixup, so the next tile's MMAs go on
+// meanwhile).  The own segment comes from registers for tiles of at most 64
+// columns per column half, else from its slot (fewer live registers).  Either
+// way each element is ((0 + s_first) + ...) + s_last.
 //   unit:   the CTA's (or pair's) stream-K index; slots are numbered
 //           ((2 * unit + w.slot) * halves + half) -- `halves` 128-row shares
 //           per tile (1: single CTA, 2: CTA pair), `half` this CTA's share;
@@ -690,8 +694,8 @@ __device__ __noinline__ void sk_fixup_warps(const GemmParams &p, const SkFix &sl
 template <int BN, int kCols, int kChunks, bool kEpiFix = false>
 __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, const uint32_t (&r)[kChunks][32],
                                             int unit, int halves, int half, int row0, int h, int row_local,
-                                            bool has_cols, int *sk_last, SkFix &fx, uint32_t fix_full,
-                                            uint32_t fix_empty, uint32_t &posted, volatile int *abort, uint64_t lim)
+                                            bool has_cols, int *sk_last, SkFix *fx, uint32_t fix_full,
+                                            uint32_t fix_empty, uint32_t *posted, volatile int *abort, uint64_t lim)
 {
     constexpr size_t kSlot = static_cast<size_t>(kBM) * BN;
     uint4 *const mine =
@@ -744,7 +748,7 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     const int cc = cc0 + g;  // uniform over the CTA
-                    if (cc == unit) {         // this CTA's own segment: still in registers
+                    if (kChunks <= 2 && cc == unit) {  // this CTA's own segment: still in registers
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
                             x[g][v] = make_float4(__uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1]),
@@ -786,13 +790,13 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
             else
                 store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), bits);
         }
-        return;
-    }
-    if (threadIdx.x == 64) {
-        __threadfence();
-        const SkFix job{w.tile, w.tn, c_first, c_last, row0};
-        if (!sk_post(fx, job, fix_full, fix_empty, posted, abort, lim))
-            record_timeout(p, abort);
+    } else {
+        if (threadIdx.x == 64) {
+            __threadfence();
+            const SkFix job{w.tile, w.tn, c_first, c_last, row0};
+            if (!sk_post(*fx, job, fix_full, fix_empty, *posted, abort, lim))
+                record_timeout(p, abort);
+        }
     }
 }
 
@@ -1190,8 +1194,8 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 if (w.kind == 1) {
                     // stream-K segment: publish, and queue the tile's fixup if this CTA is last
                     sk_epilogue<BN, kCols, kChunks, (BN <= 64)>(p, w, r, first_unit, 1, 0, tm * kBM, h, row_local,
-                                                                has_cols, &sk_last, sk_fix, smem_addr(&fix_bars[0]),
-                                                                smem_addr(&fix_bars[1]), sk_posted, abort, lim);
+                                                                has_cols, &sk_last, &sk_fix, smem_addr(&fix_bars[0]),
+                                                                smem_addr(&fix_bars[1]), &sk_posted, abort, lim);
                     continue;
                 }
             }

@@ -21,7 +21,8 @@
 //     epilogue stores those rows.
 //   * with stream-K, a pair's segment of a cut tile is published per CTA (each
 //     its 128 rows, its own arrival counter), and the last pair to arrive adds
-//     the segments in k order, each CTA for its own rows.
+//     the segments in k order, each CTA for its own rows, in its epilogue warps
+//     (there are no fixup warps: 4096^3 MXFP8 49.2 -> 48.2 us per call).
 // All waits are bounded as in the single-CTA kernel; the CTAs meet at a cluster
 // barrier before TMEM is released.
 #pragma once
@@ -84,10 +85,10 @@ struct CfgPair {
     static_assert(!kFuseSa || kSfGroup * kKtPerStage == 4, "the fused layout moves one 16-byte row word per chunk");
 };
 
-// SK = true: the instantiation for stream-K plans, with the two fixup warps
-// (384 threads); plans without cut tiles run the 320-thread form.
+// SK = true: the instantiation for stream-K plans (the epilogue publishes and
+// adds the cut tiles' segments); plans without cut tiles run the other form.
 template <int KIND, int BN, bool SK = false>
-__global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
                         const __grid_constant__ CUtensorMap map_sfb, const __grid_constant__ CUtensorMap map_sarm)
@@ -98,8 +99,6 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_holder;
     __shared__ int abort_flag;
-    __shared__ uint64_t fix_bars[2];  // stream-K fixup hand-off: full, empty
-    __shared__ SkFix sk_fix;
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -148,8 +147,6 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             mbar_init(tfree_bar(g), 1);
         }
         mbar_init(drain_bar, 1);
-        mbar_init(smem_addr(&fix_bars[0]), 1);
-        mbar_init(smem_addr(&fix_bars[1]), kFixWarps);
         fence_mbar_init();
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b);
@@ -586,14 +583,13 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             __syncwarp();
             warp_wait(drain_bar, 0, no_abort, lim);
         }
-    } else if (warp >= 2 && warp < kFixWarp0) {
+    } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         constexpr int kCols = BN / 2;
         constexpr int kChunks = kCols / 32;
         __shared__ int sk_last;
-        uint32_t sk_posted = 0;  // jobs posted to the fixup warps (thread 64)
         int it = 0;
         WorkIter wi;
         wi.init(p, first_unit, unit_step);
@@ -630,10 +626,10 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             const int row0 = (2 * tm + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
             if constexpr (SK) {
                 if (w.kind == 1) {
-                    // stream-K segment: publish, and queue the tile's fixup if this pair is last
-                    sk_epilogue<BN, kCols, kChunks>(p, w, r, first_unit, 2, static_cast<int>(rank), row0, h,
-                                                    q * 32 + lane, true, &sk_last, sk_fix, smem_addr(&fix_bars[0]),
-                                                    smem_addr(&fix_bars[1]), sk_posted, abort, lim);
+                    // stream-K segment: publish, and add the tile's segments if this pair is last
+                    sk_epilogue<BN, kCols, kChunks, true>(p, w, r, first_unit, 2, static_cast<int>(rank), row0, h,
+                                                          q * 32 + lane, true, &sk_last, nullptr, 0u, 0u, nullptr,
+                                                          abort, lim);
                     continue;
                 }
             }
@@ -651,18 +647,6 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                         store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), r[c]);
                 }
             }
-        }
-        if (SK && p.sk_ctas > 0 && threadIdx.x == 64) {
-            const SkFix stop{-1, 0, 0, 0, 0};
-            if (!sk_post(sk_fix, stop, smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]), sk_posted, abort, lim))
-                record_timeout(p, abort);
-        }
-    } else if (warp >= kFixWarp0) {
-        // ------------------------------------------------- stream-K fixup
-        if (SK && p.sk_ctas > 0) {
-            constexpr int kCols = BN / 2;
-            sk_fixup_warps<BN, kCols, kCols / 32>(p, sk_fix, smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]), 2,
-                                                  static_cast<int>(rank), abort, lim);
         }
     }
 

@@ -48,7 +48,7 @@ struct Launchers {
         if constexpr (BN == 256) {
             if (p.sk_ctas > 0) {
                 cudaLaunchConfig_t cfg =
-                    launch_config(2 * clusters, kThreadsSk, CfgPair<KIND, BN>::kSmemBytes, s, attr, 2);
+                    launch_config(2 * clusters, kThreads, CfgPair<KIND, BN>::kSmemBytes, s, attr, 2);
                 return cudaLaunchKernelEx(&cfg, mx_gemm_pair_kernel<KIND, BN, true>, p, ma, mb, msa, msb, msarm);
             }
         }

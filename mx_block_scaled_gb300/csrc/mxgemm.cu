@@ -580,8 +580,8 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         if (units_m * ceil_div(rows_b, 256) < slots_est && units_m * ceil_div(rows_b, 128) <= slots_est)
             bn = 128;
     }
-    // Stream-K on CTA pairs runs on 256-wide tiles only (the pair instantiation
-    // with fixup warps): a forced stream-K pair plan takes them.
+    // Stream-K on CTA pairs runs on 256-wide tiles only (the pair kernel's
+    // stream-K instantiation): a forced stream-K pair plan takes them.
     if ((flags & MXGEMM_PLAN_STREAMK) && mode == 1) bn = 256;
     p->mode = mode;
     p->bn = bn;
@@ -622,9 +622,9 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         const int64_t waves = ceil_div(tiles, G);
         const double dp_eff = static_cast<double>(tiles) / static_cast<double>(waves * G);
         // Default (256-wide tiles, last wave under 90% full): the fixup of a cut
-        // tile (run by the CTA's fixup warps, ~30 us with every SM streaming
-        // operands into L2; longer for three or more partials) must hide behind
-        // the whole tiles each slot computes after its segment, so
+        // tile (L2 round trips of the partial sums, several us with every SM
+        // streaming operands into L2; longer for three or more partials) must
+        // hide behind the whole tiles each slot computes after its segment, so
         //  - halves: each tile of the last wave cut into two segments (2 x its
         //    tiles <= slots), when the whole tiles give every slot >= 96
         //    k-stages (MXFP8 4096^3: +6.5%; MXFP4 4096^3 at 48: a loss);
@@ -643,10 +643,19 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         // and are added by the fixup warps of the last CTA to arrive, which
         // replaces the separate split-K reduce launch.
         const bool decode = swap && mode == 0 && p->bn <= 64;
+        // By default decode takes stream-K where its fixed cost (the fixup of
+        // the cut tiles after the last segment) is paid back: k-loops of at
+        // least 64 stages, and either tiles that a uniform 2-way split-K would
+        // spread over more than one wave, or long k-loops.  Otherwise split-K
+        // with its reduce launch is faster (MXFP8 8 x 8192 x 8192: stream-K
+        // 19.4 us, split 2 17.6; MXFP4 8 x 10240 x 8192: 18.1 vs split 5 15.7;
+        // MXFP8 8 x 10240 x 8192: stream-K 22.0 vs split 8 24.4; 8 x 8192 x
+        // 28672: 44.6 vs split 2 47.1).
+        const bool decode_sk = decode && p->kstages >= 64 && (tiles * 2 > G || p->kstages >= 128);
         const bool want = (flags & MXGEMM_PLAN_STREAMK)
                               ? dp_eff < 0.95
                               : (!(flags & MXGEMM_PLAN_NO_STREAMK) && dp_eff < 0.90 &&
-                                 ((p->bn == 256 && (spread || halves)) || decode));
+                                 ((p->bn == 256 && (spread || halves)) || decode_sk));
         if (want) {
             const int64_t dp = (tiles / G) * G;
             const int64_t sk_stages = (tiles - dp) * p->kstages;

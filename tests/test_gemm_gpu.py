@@ -210,24 +210,33 @@ def test_stream_k_exact(oracle_mod, fmt, mode, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
-@pytest.mark.parametrize("M,N,K", [(8, 1280, 4096), (64, 2048, 4096), (1, 384, 1024), (33, 8192, 1024),
-                                   (8, 20480, 1024)])
-def test_decode_default_plans_stream_k_exact(oracle_mod, fmt, M, N, K):
-    """Weight-streaming decode shapes (swap-AB, 32- or 64-token tiles): the
-    default plan spreads the k-stages of the tiles beyond the full waves over
-    every SM (stream-K), cutting tiles into up to ~8 segments whose partial
-    sums the fixup warps add in k order; the result is exact, FP32 and BF16 out."""
+@pytest.mark.parametrize("M,N,K,forced", [(8, 1280, 4096, True), (64, 2048, 4096, True), (1, 384, 1024, True),
+                                          (33, 8192, 1024, True), (8, 20480, 1024, True),
+                                          (8, 10240, 16384, False), (8, 1280, 32768, False)])
+def test_decode_stream_k_exact(oracle_mod, fmt, M, N, K, forced):
+    """Weight-streaming decode shapes (swap-AB, 32- or 64-token tiles) with the
+    k-stages of the tiles beyond the full waves spread over every SM (stream-K),
+    cutting tiles into up to ~8 segments whose partial sums the epilogue of the
+    last CTA adds in k order: exact, FP32 and BF16 out.  Short k-loops get
+    stream-K from the plan flag (their default plan splits K); 80 tiles of 64
+    k-stages and 10 tiles of 128 k-stages get it by default.  The default plan
+    of every shape is exact too."""
     rng = np.random.default_rng([M, N, K, fmt])
     A, SA = small_int_codes(rng, M, K, fmt)
     B, SB = small_int_codes(rng, N, K, fmt)
     ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
-    C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, return_plan=True)
-    assert "swap_ab=1" in desc and "/0 " not in desc.split("streamk=")[1][:16], desc
-    assert (C == ref).all(), desc
     import torch
     expect = torch.from_numpy(ref.astype(np.float32)).bfloat16().double().numpy()
-    C2 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16)
+    flags = SK if forced else 0
+    C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, flags=flags, return_plan=True)
+    assert "swap_ab=1" in desc and "/0 " not in desc.split("streamk=")[1][:16], desc
+    assert (C == ref).all(), desc
+    C2 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16, flags=flags)
     assert (C2 == expect).all(), desc
+    if forced:
+        C3, desc3 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, return_plan=True)
+        assert "swap_ab=1" in desc3, desc3
+        assert (C3 == ref).all(), desc3
 
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
@@ -466,7 +475,9 @@ def test_prepare_then_run_equals_run(oracle_mod, fmt, plan_flags):
     ("mxfp8", 4096, 4096, 4096, ["tile=256x256", "mode=pair", "streamk=228+28/56", "sa=in-kernel"]),
     ("mxfp8", 16384, 8192, 8192, ["tile=256x256", "mode=pair", "sa=in-kernel"]),
     ("mxfp8", 8, 10240, 8192, ["tile=128x32", "mode=single", "swap_ab=1", "streamk=0+80/152"]),
-    ("mxfp8", 64, 8192, 8192, ["tile=128x64", "swap_ab=1"]),
+    ("mxfp8", 64, 8192, 8192, ["tile=128x64", "swap_ab=1", "split_k=2", "streamk=64+0/0"]),
+    ("mxfp8", 8, 8192, 28672, ["tile=128x32", "swap_ab=1", "streamk=0+64/152"]),
+    ("mxfp4", 8, 10240, 8192, ["tile=128x32", "swap_ab=1", "streamk=80+0/0"]),
     ("mxfp4", 4096, 4096, 4096, ["tile=256x256", "mode=pair", "sa=relayout"]),
     ("mxfp4", 256, 6144, 4096, ["tile=128x256", "mode=single"]),
     ("mxfp4", 256, 10240, 8192, ["mode=pair"]),
@@ -478,7 +489,8 @@ def test_prepare_then_run_equals_run(oracle_mod, fmt, plan_flags):
 def test_default_plans_follow_the_heuristic(fmt, M, N, K, expect):
     """The planner's choices on representative shapes, as the design documents them
     (pair tiles for MXFP8 from 128 tokens, MXFP4 pair tiles from half a wave,
-    BF16 small-token tile rules, swap-AB decode with stream-K over every SM)."""
+    BF16 small-token tile rules, swap-AB decode with stream-K over every SM on wide
+    or long k-loops and split-K otherwise)."""
     b = lib()
     f = {"mxfp8": FMT_MXFP8, "mxfp4": FMT_MXFP4, "bf16": b.MXGEMM_FMT_BF16}[fmt]
     plan = b.Plan(M, N, K, f, OUT_BF16)
