@@ -80,6 +80,7 @@ typedef enum {
 #define MXGEMM_ERR_CUDA            -6  /* a CUDA runtime/driver call failed        */
 #define MXGEMM_ERR_DEVICE_TIMEOUT  -7  /* a kernel gave up waiting (see below)     */
 #define MXGEMM_ERR_UNSUPPORTED     -8  /* valid request this build does not serve  */
+#define MXGEMM_ERR_DEVICE_BOUNDS   -9  /* debug build: a kernel skipped an access  */
 
 /* Plan flags (mxgemm_plan_create).  0 = the library's per-shape heuristic. */
 #define MXGEMM_PLAN_FORCE_BN128     (1u << 0)  /* force a 128-wide N tile             */
@@ -290,6 +291,39 @@ MXGEMM_API int mxgemm_device_status(void *stream, int reset);
 MXGEMM_API int mxgemm_selftest_stall(mxgemm_plan_t plan, const void *A, const uint8_t *SA,
                           const void *B, const uint8_t *SB, void *C,
                           void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Debug build.  The library is also built with MXGEMM_DEBUG defined
+ * (libmxgemm_debug.so beside libmxgemm.so; the Python binding loads it when
+ * the environment variable MXGEMM_DEBUG=1).  Same entry points; in it
+ *   - every plain global load and store of the GEMM kernels (C or the split-K
+ *     slabs, the stream-K partial sums and arrival counters) is checked
+ *     against its buffer's extent, vector stores also against their
+ *     alignment; a failing access is skipped and MXGEMM_ERR_DEVICE_BOUNDS is
+ *     written to the device status word (no trap);
+ *   - mxgemm_run and mxgemm_run_noalloc fill C with NaN (all-ones bytes)
+ *     before the GEMM, so an element no kernel writes reads back as NaN;
+ *   - mxgemm_run, mxgemm_run_noalloc and mxgemm_grouped_run synchronise their
+ *     stream and return the device status word (so they cannot be captured in
+ *     a CUDA graph).
+ * mxgemm_debug_build() returns 1 in the debug build, 0 in the release build.
+ */
+MXGEMM_API int mxgemm_debug_build(void);
+
+/*
+ * Self-test of the debug build's bounds checks: runs `plan` (arguments as for
+ * mxgemm_run) with the GEMM kernel told that C ends one row early, so the
+ * stores of the last row are out of its range.  The debug build skips them
+ * (the last row of C keeps the NaN fill; with swap-AB tiles, whose stores run
+ * down the columns of C, every 32-row group of stores that touches it) and
+ * returns MXGEMM_ERR_DEVICE_BOUNDS, the rest of C being the product; clear
+ * the status afterwards with mxgemm_device_status(stream, 1).  Plans that
+ * split K (C written by the reduce pass) give MXGEMM_ERR_UNSUPPORTED, and so
+ * does the release build.
+ */
+MXGEMM_API int mxgemm_selftest_bounds(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B,
+                                      const uint8_t *SB, void *C, void *workspace, size_t ws_bytes,
+                                      uint32_t run_flags, void *stream);
 
 /*
  * mxgemm_run without a workspace argument, for callers that cannot allocate

@@ -3,14 +3,16 @@
 Argument marshalling only: every step of the GEMM (scale relayout, the tcgen05
 GEMM, the split-K reduce) runs in the library's CUDA kernels.  PyTorch is used
 for device memory and streams.  If the library is missing this module raises
-at import time; there is no fallback implementation.
+at import time; there is no fallback implementation.  With the environment
+variable MXGEMM_DEBUG=1 the module loads the debug build (libmxgemm_debug.so:
+bounds-checked kernels, NaN-filled C, synchronous status) instead.
 """
 from __future__ import annotations
 
 import ctypes
 import os
 
-from .build import LIB_PATH
+from .build import DEBUG_LIB_PATH, LIB_PATH
 
 MXGEMM_FMT_MXFP8_E4M3 = 1
 MXGEMM_FMT_MXFP4_E2M1 = 2
@@ -27,6 +29,7 @@ MXGEMM_ERR_ARCH = -5
 MXGEMM_ERR_CUDA = -6
 MXGEMM_ERR_DEVICE_TIMEOUT = -7
 MXGEMM_ERR_UNSUPPORTED = -8
+MXGEMM_ERR_DEVICE_BOUNDS = -9
 
 MXGEMM_PLAN_FORCE_BN128 = 1 << 0
 MXGEMM_PLAN_FORCE_BN256 = 1 << 1
@@ -64,6 +67,8 @@ SIGNATURES = [
     ("mxgemm_run_noalloc", ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_uint32, _P]),
     ("mxgemm_device_status", ctypes.c_int, [_P, ctypes.c_int]),
     ("mxgemm_selftest_stall", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    ("mxgemm_selftest_bounds", ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_uint32, _P]),
+    ("mxgemm_debug_build", ctypes.c_int, []),
     ("mxgemm_grouped_plan_create", ctypes.c_int,
      [ctypes.POINTER(ctypes.c_void_p), _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32]),
     ("mxgemm_grouped_plan_destroy", ctypes.c_int, [_P]),
@@ -91,7 +96,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     return lib
 
 
-_lib = load_library()
+_lib = load_library(DEBUG_LIB_PATH if os.environ.get("MXGEMM_DEBUG", "0") == "1" else LIB_PATH)
 
 
 class MxGemmError(RuntimeError):
@@ -192,6 +197,14 @@ def mxgemm_device_status(stream: int, reset: bool = True) -> int:
 
 def mxgemm_selftest_stall(plan, A_ptr, SA_ptr, B_ptr, SB_ptr, C_ptr, ws_ptr, ws_bytes, stream) -> int:
     return _lib.mxgemm_selftest_stall(plan, A_ptr, SA_ptr, B_ptr, SB_ptr, C_ptr, ws_ptr, ws_bytes, stream)
+
+
+def mxgemm_selftest_bounds(plan, A_ptr, SA_ptr, B_ptr, SB_ptr, C_ptr, ws_ptr, ws_bytes, run_flags, stream) -> int:
+    return _lib.mxgemm_selftest_bounds(plan, A_ptr, SA_ptr, B_ptr, SB_ptr, C_ptr, ws_ptr, ws_bytes, run_flags, stream)
+
+
+def mxgemm_debug_build() -> int:
+    return _lib.mxgemm_debug_build()
 
 
 def mxgemm_status_str(status: int) -> str:

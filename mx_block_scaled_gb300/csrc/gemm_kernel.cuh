@@ -108,6 +108,12 @@ struct GemmParams {
     int rows_total;           // T: rows of A and C
     int tok_sf_cap;           // 128-row blocks in the tokens' tile-layout scale region
     const long long *group_offsets;  // G + 1 row offsets (device)
+    // Extents of the buffers the kernels reach with plain loads and stores,
+    // set for every launch; a debug build (MXGEMM_DEBUG) checks each such
+    // access against them (dbg_ok below).
+    long long dbg_out_elems;  // elements addressable from out
+    long long dbg_skp_elems;  // floats in sk_partials
+    long long dbg_counters;   // ints in sk_counters
 };
 
 constexpr int kMaxGroups = 512;
@@ -423,6 +429,36 @@ __device__ __forceinline__ void record_timeout(const GemmParams &p, volatile int
     atomicExch(p.status, -7 /* MXGEMM_ERR_DEVICE_TIMEOUT */);
 }
 
+// Debug build (compiled with MXGEMM_DEBUG): every plain global store and load
+// of the GEMM kernels -- C or the split-K slabs, the stream-K partial slots
+// and arrival counters -- is checked against its buffer's extent (and the
+// vector stores against their alignment) before it is made.  An access that
+// fails is skipped (a load then reads nothing, a fixup gives up) and
+// MXGEMM_ERR_DEVICE_BOUNDS is recorded in the status word; nothing traps.
+// Tensor-map (TMA) loads are bounded by their maps and need no check.  In the
+// release build the checks compile to nothing.
+#ifdef MXGEMM_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+__device__ __forceinline__ bool dbg_fail(const GemmParams &p)
+{
+    atomicCAS(p.status, 0, -9 /* MXGEMM_ERR_DEVICE_BOUNDS */);
+    return false;
+}
+
+// [lo, hi) inside [0, cap)
+__device__ __forceinline__ bool dbg_ok(const GemmParams &p, long long lo, long long hi, long long cap)
+{
+    if constexpr (!kDebugChecks)
+        return true;
+    if (lo >= 0 && lo <= hi && hi <= cap)
+        return true;
+    return dbg_fail(p);
+}
+
 // Store 32 consecutive B-role values of one A-role row: out[off .. off+32).
 __device__ __forceinline__ void st_global_v8(void *dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
                                              uint32_t f, uint32_t g, uint32_t h)
@@ -440,6 +476,17 @@ __device__ __forceinline__ void st_global_v8(void *dst, uint32_t a, uint32_t b, 
 template <bool kWide = false>
 __device__ __forceinline__ void store_row32_vec(const GemmParams &p, long long off, const uint32_t (&r)[32])
 {
+    if constexpr (kDebugChecks) {
+        const unsigned long long esz = p.out_kind == OUT_BF16 ? 2u : 4u;
+        const unsigned long long a = reinterpret_cast<unsigned long long>(p.out) + static_cast<unsigned long long>(off) * esz;
+        const unsigned long long need = (kWide && p.vec_ok == 2) ? 32u : 16u;
+        if (!dbg_ok(p, off, off + 32, p.dbg_out_elems))
+            return;
+        if (a % need != 0) {
+            dbg_fail(p);
+            return;
+        }
+    }
     if (kWide && p.vec_ok == 2) {
         if (p.out_kind == OUT_BF16) {
             uint32_t w[16];
@@ -485,6 +532,11 @@ __device__ __forceinline__ void store_row32_vec(const GemmParams &p, long long o
 __device__ __forceinline__ void store_row32_masked(const GemmParams &p, long long base, int j0, int n,
                                                    const uint32_t (&r)[32])
 {
+    if constexpr (kDebugChecks) {  // stride_j >= 1: the first and last element bound the run
+        if (n > 0 && !dbg_ok(p, base + static_cast<long long>(j0) * p.stride_j,
+                             base + static_cast<long long>(j0 + n - 1) * p.stride_j + 1, p.dbg_out_elems))
+            return;
+    }
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
         if (e < n) {
@@ -535,9 +587,10 @@ __device__ __noinline__ void sk_fixup_two(const GemmParams &p, int tile, int tn,
         const int cc = c_first + g;
         const long long beg = p.sk_stages * cc / p.sk_ctas;
         const int slot = (beg / p.kstages == tile - p.dp_tiles) ? 0 : 1;
-        src[g] = reinterpret_cast<const float4 *>(p.sk_partials +
-                                                  static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
-                 row_local;
+        const long long so = static_cast<long long>((2 * cc + slot) * halves + half) * kSlot;
+        if (!dbg_ok(p, so, so + static_cast<long long>(kSlot), p.dbg_skp_elems))
+            return;
+        src[g] = reinterpret_cast<const float4 *>(p.sk_partials + so) + row_local;
     }
     float4 x[2][2][8];  // [segment][chunk][4-column group]
 #pragma unroll
@@ -594,8 +647,10 @@ __device__ __noinline__ void sk_fixup_chunk(const GemmParams &p, int tile, int t
             const int cc = min(cc0 + g, c_last);
             const long long beg = p.sk_stages * cc / p.sk_ctas;
             const int slot = (beg / p.kstages == tile - p.dp_tiles) ? 0 : 1;
-            const float4 *src = reinterpret_cast<const float4 *>(
-                                    p.sk_partials + static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
+            const long long so = static_cast<long long>((2 * cc + slot) * halves + half) * kSlot;
+            if (!dbg_ok(p, so, so + static_cast<long long>(kSlot), p.dbg_skp_elems))
+                return;
+            const float4 *src = reinterpret_cast<const float4 *>(p.sk_partials + so) +
                                 (h * kChunks + c) * 8 * kBM + row_local;
             if (cc0 + g <= c_last) {  // uniform over the CTA: no load past the last segment
 #pragma unroll
@@ -698,9 +753,9 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
                                             uint32_t fix_empty, uint32_t *posted, volatile int *abort, uint64_t lim)
 {
     constexpr size_t kSlot = static_cast<size_t>(kBM) * BN;
-    uint4 *const mine =
-        reinterpret_cast<uint4 *>(p.sk_partials + static_cast<size_t>((2 * unit + w.slot) * halves + half) * kSlot);
-    if (has_cols) {
+    const long long mine_off = static_cast<long long>((2 * unit + w.slot) * halves + half) * kSlot;
+    uint4 *const mine = reinterpret_cast<uint4 *>(p.sk_partials + mine_off);
+    if (has_cols && dbg_ok(p, mine_off, mine_off + static_cast<long long>(kSlot), p.dbg_skp_elems)) {
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
@@ -714,13 +769,18 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
     const long long t0 = static_cast<long long>(w.tile - p.dp_tiles) * p.kstages;
     const int c_first = sk_cta_of(p, t0);
     const int c_last = sk_cta_of(p, t0 + p.kstages - 1);
-    int *const counter = p.sk_counters + (w.tile - p.dp_tiles) * halves + half;
+    const int cidx = (w.tile - p.dp_tiles) * halves + half;
+    int *const counter = p.sk_counters + cidx;
     if (threadIdx.x == 64) {
-        const int old = atomicAdd(counter, 1);
-        const int last = old == c_last - c_first;
-        if (last)
-            *counter = 0;  // ready for the next launch
-        *sk_last = last;
+        if (!dbg_ok(p, cidx, cidx + 1, p.dbg_counters)) {
+            *sk_last = 0;
+        } else {
+            const int old = atomicAdd(counter, 1);
+            const int last = old == c_last - c_first;
+            if (last)
+                *counter = 0;  // ready for the next launch
+            *sk_last = last;
+        }
     }
     epi_bar_sync();
     const bool last = *sk_last != 0;
@@ -756,13 +816,18 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
                     } else if (cc <= c_last) {
                         const long long beg = p.sk_stages * cc / p.sk_ctas;
                         const int slot = (beg / p.kstages == w.tile - p.dp_tiles) ? 0 : 1;
-                        const float4 *src =
-                            reinterpret_cast<const float4 *>(
-                                p.sk_partials + static_cast<size_t>((2 * cc + slot) * halves + half) * kSlot) +
-                            (h * kChunks + c) * 8 * kBM + row_local;
+                        const long long so = static_cast<long long>((2 * cc + slot) * halves + half) * kSlot;
+                        const float4 *src = reinterpret_cast<const float4 *>(p.sk_partials + so) +
+                                            (h * kChunks + c) * 8 * kBM + row_local;
+                        if (dbg_ok(p, so, so + static_cast<long long>(kSlot), p.dbg_skp_elems)) {
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            x[g][v] = __ldcg(src + v * kBM);
+                            for (int v = 0; v < 8; ++v)
+                                x[g][v] = __ldcg(src + v * kBM);
+                        } else {
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                x[g][v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        }
                     } else {
 #pragma unroll
                         for (int v = 0; v < 8; ++v)

@@ -473,6 +473,7 @@ const char *mxgemm_status_str(int status)
     case MXGEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
     case MXGEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on a barrier (device timeout)";
     case MXGEMM_ERR_UNSUPPORTED: return "request not supported by this build";
+    case MXGEMM_ERR_DEVICE_BOUNDS: return "a debug-build kernel skipped an out-of-range load or store";
     default: return "unknown status";
     }
 }
@@ -839,9 +840,29 @@ static int prepare_impl(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB
     return MXGEMM_OK;
 }
 
+// Debug build (MXGEMM_DEBUG): a run synchronises its stream and returns the
+// device status word, so that a kernel's bounds check or timeout is reported
+// by the call that caused it.  Release build: nothing (calls stay asynchronous).
+static int debug_finish(cudaStream_t s)
+{
+#ifdef MXGEMM_DEBUG
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return MXGEMM_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess)
+        return MXGEMM_ERR_CUDA;
+    return v;
+#else
+    (void)s;
+    return MXGEMM_OK;
+#endif
+}
+
+// dbg_short_rows: self-test of the debug build's bounds checks -- the GEMM
+// kernel is told that C ends that many rows early.
 static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB, void *C,
                     void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream, int test_stall,
-                    unsigned long long timeout_ns)
+                    unsigned long long timeout_ns, int dbg_short_rows = 0)
 {
     if (!plan || !A || !B || !C)
         return MXGEMM_ERR_ARG;
@@ -949,6 +970,17 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
         p.split_stride = 0;
     }
     p.vec_ok = vec_level(!plan->swap, N * osize, p.out);
+    p.dbg_out_elems = split ? static_cast<long long>(plan->splits) * p.split_stride : M * N;
+    p.dbg_out_elems -= static_cast<long long>(dbg_short_rows) * N;
+    p.dbg_skp_elems = plan->sk_ctas > 0 ? 2ll * plan->sk_ctas * plan->sk_halves * 128 * plan->bn : 0;
+    p.dbg_counters = plan->sk_ctas > 0 ? plan->cnt_n : 0;
+#ifdef MXGEMM_DEBUG
+    // C pre-filled with NaN (all-ones bytes in BF16 and FP32): an element that
+    // no kernel writes reads back as NaN
+    if (cudaMemsetAsync(C, 0xFF, static_cast<size_t>(M * N) * (plan->out == MXGEMM_OUT_BF16 ? 2 : 4), s) !=
+        cudaSuccess)
+        return MXGEMM_ERR_CUDA;
+#endif
 
     cudaError_t e;
     if (plan->mode == 1 && bf16) {
@@ -1000,7 +1032,7 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
                                                             : static_cast<int>(mxg::OUT_F32)) != cudaSuccess)
             return MXGEMM_ERR_CUDA;
     }
-    return MXGEMM_OK;
+    return debug_finish(s);
 }
 
 int mxgemm_prepare(mxgemm_plan_t plan, const uint8_t *SA, const uint8_t *SB, void *workspace, size_t ws_bytes,
@@ -1042,6 +1074,31 @@ int mxgemm_selftest_stall(mxgemm_plan_t plan, const void *A, const uint8_t *SA, 
 {
     return run_impl(plan, A, SA, B, SB, C, workspace, ws_bytes, MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT,
                     stream, 1, 20000000ull);
+}
+
+int mxgemm_selftest_bounds(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const void *B, const uint8_t *SB,
+                           void *C, void *workspace, size_t ws_bytes, uint32_t run_flags, void *stream)
+{
+#ifdef MXGEMM_DEBUG
+    if (!plan)
+        return MXGEMM_ERR_ARG;
+    if (plan->splits > 1)
+        return MXGEMM_ERR_UNSUPPORTED;  // C is written by the reduce pass, not the GEMM kernel
+    return run_impl(plan, A, SA, B, SB, C, workspace, ws_bytes, run_flags, stream, 0, MXGEMM_WAIT_LIMIT_NS, 1);
+#else
+    (void)plan, (void)A, (void)SA, (void)B, (void)SB, (void)C, (void)workspace, (void)ws_bytes, (void)run_flags,
+        (void)stream;
+    return MXGEMM_ERR_UNSUPPORTED;
+#endif
+}
+
+int mxgemm_debug_build(void)
+{
+#ifdef MXGEMM_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 // ------------------------------------------------------------- no-alloc --
@@ -1256,9 +1313,10 @@ int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *group_offsets,
     p.group_offsets = offs;
     const CUtensorMap &ma = plan->swap ? plan->map_w : plan->map_tok;
     const CUtensorMap &mb = plan->swap ? plan->map_tok : plan->map_w;
+    p.dbg_out_elems = static_cast<long long>(T) * N;
     const cudaError_t e = fp4 ? mxg::launch_gemm_grouped_fp4(plan->bn, p, ma, mb, plan->num_sms, s)
                               : mxg::launch_gemm_grouped_fp8(plan->bn, p, ma, mb, plan->num_sms, s);
-    return e == cudaSuccess ? MXGEMM_OK : MXGEMM_ERR_CUDA;
+    return e == cudaSuccess ? debug_finish(s) : MXGEMM_ERR_CUDA;
 }
 
 int mxgemm_placement_scan(int k, const int *sa, const int *sb, int npairs, long long *counts, long long *first_diff,

@@ -3,7 +3,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from mx_block_scaled_gb300.inputs import FMT_MXFP4, FMT_MXFP8
+from mx_block_scaled_gb300.inputs import FMT_MXFP4, FMT_MXFP8, pack_fp4
 
 OUT_F32 = 1
 OUT_BF16 = 2
@@ -14,6 +14,18 @@ def lib():
     build.build()
     from mx_block_scaled_gb300 import binding
     return binding
+
+
+def small_int_codes(rng, rows, K, fmt):
+    """Codes of values in {0, +-0.5, +-1, +-2} with scales in [125, 129]: every partial
+    sum of a K <= 2048 product is exact in FP32, so the GPU must match bit for bit."""
+    vals = np.array([0x00, 0x30, 0x38, 0x40, 0xB0, 0xB8, 0xC0], np.uint8) if fmt == FMT_MXFP8 else \
+        np.array([0x0, 0x1, 0x2, 0x4, 0x9, 0xA, 0xC], np.uint8)
+    codes = vals[rng.integers(0, len(vals), size=(rows, K))]
+    if fmt == FMT_MXFP4:
+        codes = pack_fp4(codes)
+    scales = rng.integers(125, 130, size=(rows, K // 32), dtype=np.uint8)
+    return codes, scales
 
 
 def to_dev(x):

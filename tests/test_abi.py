@@ -39,6 +39,20 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(declared_entry_points()) == bound
 
 
+def test_debug_library_exports_every_declared_symbol(lib):
+    """The debug build (MXGEMM_DEBUG) has the same entry points, and says which
+    build it is; the release build's bounds self-test is refused on the host."""
+    dbg = lib.load_library(lib.DEBUG_LIB_PATH)
+    for name in declared_entry_points():
+        assert hasattr(dbg, name), f"{name} declared in mxgemm.h but not exported by the debug build"
+    assert dbg.mxgemm_debug_build() == 1
+    assert lib._lib.mxgemm_debug_build() == 0
+    assert lib._lib.mxgemm_selftest_bounds(None, None, None, None, None, None, None, 0, 0, None) == \
+        lib.MXGEMM_ERR_UNSUPPORTED
+    assert dbg.mxgemm_selftest_bounds(None, None, None, None, None, None, None, 0, 0, None) == lib.MXGEMM_ERR_ARG
+    assert dbg.mxgemm_status_str(lib.MXGEMM_ERR_DEVICE_BOUNDS).decode().startswith("a debug-build kernel")
+
+
 def test_sf_bytes(lib):
     assert lib.mxgemm_sf_bytes(1, 128) == 128 * 4
     assert lib.mxgemm_sf_bytes(129, 256) == 256 * 8

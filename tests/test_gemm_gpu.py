@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 from golden_io import load_handworked
-from gpu_util import (OUT_BF16, OUT_F32, assert_within, gpu_gemm, gpu_gemm_device, lib,
+from gpu_util import (OUT_BF16, OUT_F32, assert_within, gpu_gemm, gpu_gemm_device, lib, small_int_codes,
                       tile_sample_indices, to_dev)
 from mx_block_scaled_gb300.inputs import (FMT_MXFP4, FMT_MXFP8, finite_uniform_codes, make_operand,
                                           pack_fp4, workload_cases)
@@ -110,18 +110,6 @@ def test_identity_b_returns_dequantised_a(oracle_mod, fmt):
     C = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32)
     ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
     assert (C == ref).all()
-
-
-def small_int_codes(rng, rows, K, fmt):
-    """Codes of values in {0, +-0.5, +-1, +-2} with scales in [125, 129]: every partial
-    sum of a K <= 2048 product is exact in FP32, so the GPU must match bit for bit."""
-    vals = np.array([0x00, 0x30, 0x38, 0x40, 0xB0, 0xB8, 0xC0], np.uint8) if fmt == FMT_MXFP8 else \
-        np.array([0x0, 0x1, 0x2, 0x4, 0x9, 0xA, 0xC], np.uint8)
-    codes = vals[rng.integers(0, len(vals), size=(rows, K))]
-    if fmt == FMT_MXFP4:
-        codes = pack_fp4(codes)
-    scales = rng.integers(125, 130, size=(rows, K // 32), dtype=np.uint8)
-    return codes, scales
 
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
