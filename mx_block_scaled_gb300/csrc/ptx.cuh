@@ -162,6 +162,16 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t local, uint32_t rank)
 // the tcgen05 fences around the hand-off, and no memory data travels with it.
 // A release at cluster scope measured ~0.9 us per arrive in the GEMM's
 // epilogue (the warp stalls until it is performed), this form ~0.1 us.
+// Atomic add with acquire-release semantics at GPU scope: releases the writes
+// ordered before it (including other threads' writes ordered by a CTA barrier)
+// and acquires those released by earlier adds on the same word.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *addr, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
