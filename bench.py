@@ -579,7 +579,9 @@ def run_ours(args):
                 hC[b].copy_(d["C"], non_blocking=True)
                 done_out[b].record(s_out)
 
-        n_e2e = max(5, min(args.steps, 20))
+        # a serving loop runs many steps: time up to 50 so that the pipeline's
+        # fill and drain (one upload, one download) weigh little
+        n_e2e = max(5, min(args.steps, 50))
 
         def timed(fn, pipelined):
             for i in range(3):
@@ -602,10 +604,47 @@ def run_ours(args):
         serial_ms = timed(e2e_step_serial, False)
         e2e_ms = timed(e2e_step_pipelined, True)
         mx.check_device_status()
+
+        # The host link's own rates for the same tensors (one direction alone,
+        # then both at once), which bound the pipelined step from below.
+        def link_ms(fn, reps=5):
+            fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        def up():
+            bufs[0]["A"].copy_(hA, non_blocking=True)
+            bufs[0]["B"].copy_(hB, non_blocking=True)
+
+        def down():
+            hC[0].copy_(bufs[1]["C"], non_blocking=True)
+
+        def both():
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            s_out.wait_event(ev)
+            up()
+            with torch.cuda.stream(s_out):
+                down()
+            stream.wait_stream(s_out)
+
+        up_b, down_b = A.nbytes + B.nbytes, M * N * out_bytes
+        up_ms, down_ms, both_ms = link_ms(up), link_ms(down), link_ms(both)
+        h2d_b = A.nbytes + B.nbytes + SA.nbytes + SB.nbytes
+        link = {"h2d_gbs": up_b / up_ms / 1e6, "d2h_gbs": down_b / down_ms / 1e6,
+                "both_dirs_ms": both_ms,
+                "bound_ms_per_step": both_ms * h2d_b / up_b}  # + the scales' upload
         e2e = {"value": job_tflops(flops, ws, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(A.nbytes + B.nbytes + SA.nbytes + SB.nbytes),
                "d2h_bytes_per_step": int(M * N * out_bytes), "ms_per_step": e2e_ms,
                "schedule": "copy-in / compute / copy-out streams, two buffer sets",
+               "steps": n_e2e, "link": link,
                "serial": {"value": job_tflops(flops, ws, serial_ms), "ms_per_step": serial_ms}}
 
     # ---- further workload shapes (outside the timed region of the headline)
