@@ -653,6 +653,7 @@ def run_ours(args):
         hbm_gbs, bf16_tf, _, peak_src = load_peaks()
         for label, fname, eM, eN, eK in EXTRA_SHAPES:
             reps = 20 if eM >= 2048 else 100
+            cool_down(args)
             us, edesc, ensets = time_shape(mx, dev, fname, eM, eN, eK, reps)
             extras.append(extra_shape_record(label, fname, eM, eN, eK, us, edesc, ensets, hbm_gbs, bf16_tf,
                                              peak_src))
@@ -716,6 +717,17 @@ def run_ours(args):
 
 # ------------------------------------------------------------------- sweep --
 
+def cool_down(args):
+    """Idle before timing the next sweep shape: after seconds of a power-capped
+    prefill GEMM the GPU keeps its clocks down for a while, and a short kernel
+    timed right after measured up to 1.5x slower (MXFP4 8 x 10240 x 8192: 15.5
+    us alone, 23.3 us right after 16384 x 57344 x 8192)."""
+    if args.sweep_cooldown > 0:
+        import torch
+        torch.cuda.synchronize()
+        time.sleep(args.sweep_cooldown)
+
+
 def run_sweep(args):
     """Per-shape GEMM time for the model workloads (device-side random codes)."""
     import torch
@@ -738,6 +750,7 @@ def run_sweep(args):
             if (fmt_name, M, N, K) in seen:
                 continue
             seen.add((fmt_name, M, N, K))
+            cool_down(args)
             fmt = FMT_BY_NAME[fmt_name]
             rb = K if fmt_name == "mxfp8" else K // 2
             out = mx.MXGEMM_OUT_BF16 if name == "shape" or WORKLOADS[name]["out"] == "bf16" else mx.MXGEMM_OUT_F32
@@ -897,6 +910,7 @@ def run_grouped_sweep(args):
             set_bytes = T * rb + T * K // 32 + G * N * rb + mx.mxgemm_sf_bytes(G * N, K) + T * N * 2
             nsets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
             nsets = min(nsets, max(2, int(30e9 // set_bytes)))
+            cool_down(args)
             plan = mx.GroupedPlan(G, T, N, K, fmt, mx.MXGEMM_OUT_BF16, device=dev)
             g = torch.Generator(device=dev)
             g.manual_seed(G * 131 + N + K)
@@ -983,6 +997,7 @@ def run_bf16_sweep(args):
         byts = (M + N) * K * 2 + M * N * 2
         nsets = max(2, math.ceil(2 * l2 / byts) + 1)
         nsets = min(nsets, max(2, int(30e9 // byts)))
+        cool_down(args)
         g = torch.Generator(device=dev)
         g.manual_seed(M + N + K)
         sets = [(torch.randn((M, K), device=dev, generator=g).to(torch.bfloat16),
@@ -1187,6 +1202,8 @@ def main():
     ap.add_argument("--sweep-workloads", default="")
     ap.add_argument("--sweep-reps", type=int, default=20)
     ap.add_argument("--sweep-flags", type=int, default=0, help="mxgemm_plan_create flags for --sweep")
+    ap.add_argument("--sweep-cooldown", type=float, default=3.0,
+                    help="seconds of idle before each sweep shape (lets the clocks recover from the last one)")
     ap.add_argument("--shape", default="", help="M,N,K: sweep this one shape (BF16 out)")
     ap.add_argument("--fmt", default="mxfp8", choices=["mxfp8", "mxfp4"], help="format for --shape")
     ap.add_argument("--quant-sweep", action="store_true",
