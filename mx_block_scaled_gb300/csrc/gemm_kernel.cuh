@@ -792,6 +792,17 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
     if (!last)
         return;
     if constexpr (kEpiFix) {
+        // The own segment's values stay in registers for tiles of at most 64
+        // columns per column half; wider ones re-read it from its slot (fewer
+        // live registers), which makes it one more load of a batch.
+        constexpr bool kOwnRegs = kChunks <= 2;
+        constexpr int kBatch = kOwnRegs ? 2 : 3;
+        auto own = [&](int c, float4 (&x)[8]) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                x[v] = make_float4(__uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1]),
+                                   __uint_as_float(r[c][4 * v + 2]), __uint_as_float(r[c][4 * v + 3]));
+        };
         const int i = row0 + row_local;
         if (!has_cols || i >= p.rows_a)
             return;
@@ -805,49 +816,69 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
 #pragma unroll
             for (int e = 0; e < 32; ++e)
                 sum[e] = 0.0f;
-#pragma unroll 1
-            for (int cc0 = c_first; cc0 <= c_last; cc0 += 2) {
-                float4 x[2][8];
+            auto add = [&](const float4 (&x)[8], bool keep) {  // a select, not a product: partials may hold NaN
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const int cc = cc0 + g;  // uniform over the CTA
-                    if (kChunks <= 2 && cc == unit) {  // this CTA's own segment: still in registers
+                for (int v = 0; v < 8; ++v) {
+                    sum[4 * v] += keep ? x[v].x : 0.0f;
+                    sum[4 * v + 1] += keep ? x[v].y : 0.0f;
+                    sum[4 * v + 2] += keep ? x[v].z : 0.0f;
+                    sum[4 * v + 3] += keep ? x[v].w : 0.0f;
+                }
+            };
+            // Batches of kBatch loaded segments (uniform over the CTA): all of a
+            // batch's loads are issued before its adds, so a tile of up to
+            // kBatch other segments costs one L2 round trip per chunk; the adds
+            // then follow k order, the own segment (from registers) in its place.
+            int cc = c_first;
+            bool own_added = !kOwnRegs;
+#pragma unroll 1
+            while (cc <= c_last) {
+                float4 x[kBatch][8];
+                int seg[kBatch];
+                int nxt = cc;
+#pragma unroll
+                for (int g = 0; g < kBatch; ++g) {
+                    if (kOwnRegs && nxt == unit)
+                        ++nxt;
+                    seg[g] = nxt <= c_last ? nxt : -1;
+                    const int sg = seg[g] < 0 ? c_first : seg[g];
+                    const long long beg = p.sk_stages * sg / p.sk_ctas;
+                    const int slot = (beg / p.kstages == w.tile - p.dp_tiles) ? 0 : 1;
+                    const long long so = static_cast<long long>((2 * sg + slot) * halves + half) * kSlot;
+                    const float4 *src = reinterpret_cast<const float4 *>(p.sk_partials + so) +
+                                        (h * kChunks + c) * 8 * kBM + row_local;
+                    if (seg[g] >= 0 && dbg_ok(p, so, so + static_cast<long long>(kSlot), p.dbg_skp_elems)) {
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            x[g][v] = make_float4(__uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1]),
-                                                  __uint_as_float(r[c][4 * v + 2]), __uint_as_float(r[c][4 * v + 3]));
-                    } else if (cc <= c_last) {
-                        const long long beg = p.sk_stages * cc / p.sk_ctas;
-                        const int slot = (beg / p.kstages == w.tile - p.dp_tiles) ? 0 : 1;
-                        const long long so = static_cast<long long>((2 * cc + slot) * halves + half) * kSlot;
-                        const float4 *src = reinterpret_cast<const float4 *>(p.sk_partials + so) +
-                                            (h * kChunks + c) * 8 * kBM + row_local;
-                        if (dbg_ok(p, so, so + static_cast<long long>(kSlot), p.dbg_skp_elems)) {
-#pragma unroll
-                            for (int v = 0; v < 8; ++v)
-                                x[g][v] = __ldcg(src + v * kBM);
-                        } else {
-#pragma unroll
-                            for (int v = 0; v < 8; ++v)
-                                x[g][v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                        }
+                            x[g][v] = __ldcg(src + v * kBM);
                     } else {
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
                             x[g][v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                     }
+                    ++nxt;
                 }
+                // segments [cc, stop) are added now
+                int stop = seg[kBatch - 1] >= 0 ? seg[kBatch - 1] + 1 : c_last + 1;
+                if (kOwnRegs && stop == unit)
+                    ++stop;
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const bool keep = cc0 + g <= c_last;  // a select, not a product: partials may hold NaN
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        sum[4 * v] += keep ? x[g][v].x : 0.0f;
-                        sum[4 * v + 1] += keep ? x[g][v].y : 0.0f;
-                        sum[4 * v + 2] += keep ? x[g][v].z : 0.0f;
-                        sum[4 * v + 3] += keep ? x[g][v].w : 0.0f;
+                for (int g = 0; g < kBatch; ++g) {
+                    if (kOwnRegs && !own_added && seg[g] >= 0 && unit < seg[g]) {
+                        float4 y[8];
+                        own(c, y);
+                        add(y, true);
+                        own_added = true;
                     }
+                    add(x[g], seg[g] >= 0);
                 }
+                if (kOwnRegs && !own_added && unit < stop) {
+                    float4 y[8];
+                    own(c, y);
+                    add(y, true);
+                    own_added = true;
+                }
+                cc = stop;
             }
             uint32_t bits[32];
 #pragma unroll
