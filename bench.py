@@ -304,7 +304,9 @@ def time_shape(mx, dev, fmt_name, M, N, K, reps, warmup=3, seed=0):
         sets.append((codes(M), mx.relayout_scales(SA, M, K), codes(N), mx.relayout_scales(SB, N, K),
                      torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
         del SA, SB
-    pre = mx.MXGEMM_RUN_SA_PRELAYOUT | mx.MXGEMM_RUN_SB_PRELAYOUT
+    # weights are only read: MXGEMM_RUN_B_STATIC lets the decode plans start
+    # loading them before the preceding call has finished
+    pre = mx.MXGEMM_RUN_SA_PRELAYOUT | mx.MXGEMM_RUN_SB_PRELAYOUT | mx.MXGEMM_RUN_B_STATIC
 
     def one(i):
         a, sa, b, sb, c = sets[i % nsets]
@@ -774,7 +776,9 @@ def run_sweep(args):
                 SB = torch.randint(120, 135, (N, K // 32), dtype=torch.uint8, device=dev, generator=g)
                 sets.append((codes(M), mx.relayout_scales(SA, M, K), codes(N), mx.relayout_scales(SB, N, K),
                              torch.empty((M, N), dtype=torch.bfloat16 if ob == 2 else torch.float32, device=dev)))
-            pre = mx.MXGEMM_RUN_SA_PRELAYOUT | mx.MXGEMM_RUN_SB_PRELAYOUT
+            # weights are only read: MXGEMM_RUN_B_STATIC lets the decode plans start
+            # loading them before the preceding call has finished
+            pre = mx.MXGEMM_RUN_SA_PRELAYOUT | mx.MXGEMM_RUN_SB_PRELAYOUT | mx.MXGEMM_RUN_B_STATIC
 
             def one(i):
                 a, sa, b, sb, c = sets[i % nsets]

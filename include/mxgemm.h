@@ -98,6 +98,7 @@ typedef enum {
 #define MXGEMM_RUN_SA_PRELAYOUT     (1u << 0)  /* SA is already in the tile layout    */
 #define MXGEMM_RUN_SB_PRELAYOUT     (1u << 1)  /* SB is already in the tile layout    */
 #define MXGEMM_RUN_PREPARED         (1u << 2)  /* mxgemm_prepare ran on this workspace */
+#define MXGEMM_RUN_B_STATIC         (1u << 3)  /* no kernel still running writes B    */
 
 typedef struct mxgemm_plan *mxgemm_plan_t;
 
@@ -228,6 +229,13 @@ MXGEMM_API int mxgemm_quantize(int fmt, int in_dtype, const void *x, int64_t row
  * inside the GEMM kernel instead of step (1): one CTA of each pair loads the
  * pair's row-major scales and writes the tile layout in shared memory.
  * Inputs are read-only; C is fully overwritten.
+ * MXGEMM_RUN_B_STATIC: the caller promises that B (the weight) is not written
+ * by any kernel that may still be running on `stream` when this call starts
+ * (weights loaded once and only read; the preceding kernels produce A).  The
+ * GEMM's CTAs may then start loading B before the preceding kernel completes
+ * (programmatic dependent launch); A, SA and SB are still read only after it.
+ * Used by the weight-streaming decode plans ("lean" in their description);
+ * other plans ignore it.  Breaking the promise gives wrong results, not a fault.
  * A plan belongs to the device that was current when it was created; running
  * it with another device current returns MXGEMM_ERR_ARG.
  * Errors: MXGEMM_ERR_ARG, MXGEMM_ERR_ALIGN, MXGEMM_ERR_WORKSPACE,

@@ -44,6 +44,7 @@ MXGEMM_PLAN_NO_STREAMK = 1 << 16
 MXGEMM_RUN_SA_PRELAYOUT = 1 << 0
 MXGEMM_RUN_SB_PRELAYOUT = 1 << 1
 MXGEMM_RUN_PREPARED = 1 << 2
+MXGEMM_RUN_B_STATIC = 1 << 3
 
 MXGEMM_IN_F32 = 1
 MXGEMM_IN_BF16 = 2

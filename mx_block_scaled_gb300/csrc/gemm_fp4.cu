@@ -8,10 +8,10 @@ using L = Launchers<K_MXFP4>;
 
 cudaError_t prepare_gemm_fp4() { return L::prepare(); }
 
-cudaError_t launch_gemm_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid,
-                            cudaStream_t s)
+cudaError_t launch_gemm_fp4(int bn, bool lean, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
+                             int grid, cudaStream_t s)
 {
-    return L::launch_single(bn, p, ma, mb, grid, s);
+    return L::launch_single(bn, lean, p, ma, mb, grid, s);
 }
 
 cudaError_t launch_gemm_grouped_fp4(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
@@ -30,6 +30,6 @@ int gemm_pair_max_clusters_fp4(int bn) { return L::max_clusters(bn); }
 
 KernelInfo gemm_pair_info_fp4(int bn) { return L::pair_info(bn); }
 
-KernelInfo gemm_info_fp4(int bn) { return L::info(bn); }
+KernelInfo gemm_info_fp4(int bn, bool lean) { return L::info(bn, lean); }
 
 }  // namespace mxg

@@ -55,6 +55,14 @@ constexpr int kBM = 128;            // MMA M (rows of the A role per tile)
 constexpr int kRowBytes = 128;      // bytes of one operand row per k-stage
 constexpr int kSfChunk = 512;       // bytes of one scale chunk (128 rows x 4 K-blocks)
 constexpr int kSmemBudget = 232448; // 227 KiB opt-in shared memory per block
+// The lean form of the single-CTA kernel (weight-streaming decode tiles of 32
+// or 64 columns; the planner uses it for 32): four epilogue warps, no fixup
+// warps, a ring that leaves room for a second CTA on the SM and at most 256
+// TMEM columns, so that the next GEMM's CTAs can be resident (allocated, L2
+// warmed, waiting on the grid dependency) while this one drains.
+constexpr int kLeanEpiWarps = 4;
+constexpr int kLeanThreads = 64 + 32 * kLeanEpiWarps;
+constexpr int kLeanSmemBudget = 112 * 1024;
 // Scale factors travel in groups of kSfGroup k-stages: one copy per operand
 // brings a group's chunks into one of two shared-memory group slots, and the
 // MMA warp moves the whole group into TMEM at the group's first stage.  A TMA
@@ -79,6 +87,8 @@ struct GemmParams {
     int test_stall;           // self-test: the producer issues nothing (waits expire)
     int stream_a, stream_b;   // 1: that operand is read by at most two tiles (load it evict-first)
     int sa_fused;             // CTA-pair kernel: 1 = A-role scales are row-major (laid out in the kernel)
+    int early_a;              // lean form: 1 = no preceding kernel writes the A-role operand, so the
+                              // first ring of its tiles is loaded before the grid dependency wait
     const uint8_t *sfa;       // tile-layout scales of the A role
     const uint8_t *sfb;       // tile-layout scales of the B role
     void *out;                // output base (C, or split-K partial slabs)
@@ -206,7 +216,7 @@ __device__ __forceinline__ void build_group_table(const GemmParams &p, GroupTabl
 // Element kind of the operands: MX block-scaled E4M3 or E2M1, or plain BF16.
 enum ElemKind : int { K_MXFP8 = 0, K_MXFP4 = 1, K_BF16 = 2 };
 
-template <int KIND, int BN>
+template <int KIND, int BN, bool LEAN = false>
 struct Cfg {
     static constexpr bool kFp4 = KIND == K_MXFP4;
     static constexpr bool kScaled = KIND != K_BF16;           // MX kinds carry E8M0 scales
@@ -221,7 +231,7 @@ struct Cfg {
     static constexpr int kSfaGrpBytes = kScaled ? kSfGroup * kKtPerStage * kSfChunk : 0;
     static constexpr int kSfbGrpBytes = kScaled ? kChunksB * kSfGroup * kKtPerStage * kSfChunk : 0;
     static constexpr int kSfGrpBytes = kSfaGrpBytes + kSfbGrpBytes;
-    static constexpr int kStagesRaw = (kSmemBudget - 1024 - 256 - 2 * kSfGrpBytes) / kStageBytes;
+    static constexpr int kStagesRaw = ((LEAN ? kLeanSmemBudget : kSmemBudget) - 1024 - 256 - 2 * kSfGrpBytes) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kSfaCols = kScaled ? 4 * kKtPerStage : 0;
     static constexpr int kSfbCols = kScaled ? 4 * kKtPerStage * kChunksB : 0;
@@ -232,13 +242,15 @@ struct Cfg {
     static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
     static constexpr int kSfRegions = kScaled ? 2 * kSfGroup : 0;
     static constexpr int kAccStages = (2 * BN + kSfRegions * kSfSlotCols <= 512) ? 2 : 1;
-    static constexpr int kTmemCols = 512;
     static constexpr int kSfCol0 = kAccStages * BN;
+    static constexpr int kColsUsed = kSfCol0 + kSfRegions * kSfSlotCols;
+    static constexpr int kTmemCols = LEAN ? (kColsUsed <= 128 ? 128 : 256) : 512;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2 * kSfGrpBytes + 256;
     static constexpr uint32_t kIdesc = kScaled ? idesc_block_scaled(kFp4 ? 1u : 0u, kBM, BN) : idesc_bf16(kBM, BN);
     static_assert(kStages >= 2, "shared memory too small for two stages");
     static_assert(kSfCol0 + kSfRegions * kSfSlotCols <= kTmemCols, "TMEM overflow");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be 32..256, multiple of 32");
+    static_assert(!LEAN || (BN <= 64 && kColsUsed <= 256), "the lean form is for tiles of at most 64 columns");
 };
 
 __device__ __forceinline__ void tile_coords(const GemmParams &p, int unit, int &tm, int &tn, int &split)
@@ -421,7 +433,11 @@ __device__ __forceinline__ int sk_cta_of(const GemmParams &p, long long x)
     return static_cast<int>(((x + 1) * p.sk_ctas + p.sk_stages - 1) / p.sk_stages - 1);
 }
 
-__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
+template <int kEpi = kEpiWarps>
+__device__ __forceinline__ void epi_bar_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpi) : "memory");
+}
 
 __device__ __forceinline__ void record_timeout(const GemmParams &p, volatile int *abort)
 {
@@ -746,7 +762,7 @@ __device__ __noinline__ void sk_fixup_warps(const GemmParams &p, const SkFix &sl
 //   row0:   first A-role row of this CTA's share.
 // Slot layout [h][chunk][4-column group][row]: each warp access is 32
 // consecutive 16-byte vectors (the rows of one TMEM lane quarter).
-template <int BN, int kCols, int kChunks, bool kEpiFix = false>
+template <int BN, int kCols, int kChunks, bool kEpiFix = false, int kEpi = kEpiWarps>
 __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, const uint32_t (&r)[kChunks][32],
                                             int unit, int halves, int half, int row0, int h, int row_local,
                                             bool has_cols, int *sk_last, SkFix *fx, uint32_t fix_full,
@@ -769,7 +785,7 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
     // GPU scope and, for the last arrival, makes the other segments' partials
     // (published the same way) visible to the loads after the next barrier.
     // One atomic round trip instead of a fence on each side of a relaxed add.
-    epi_bar_sync();
+    epi_bar_sync<kEpi>();
     const long long t0 = static_cast<long long>(w.tile - p.dp_tiles) * p.kstages;
     const int c_first = sk_cta_of(p, t0);
     const int c_last = sk_cta_of(p, t0 + p.kstages - 1);
@@ -786,9 +802,9 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
             *sk_last = last;
         }
     }
-    epi_bar_sync();
+    epi_bar_sync<kEpi>();
     const bool last = *sk_last != 0;
-    epi_bar_sync();  // sk_last is read before the next segment may rewrite it
+    epi_bar_sync<kEpi>();  // sk_last is read before the next segment may rewrite it
     if (!last)
         return;
     if constexpr (kEpiFix) {
@@ -902,13 +918,16 @@ __device__ __forceinline__ void sk_epilogue(const GemmParams &p, const Work &w, 
 // GROUPED = true: the grouped (mixture-of-experts) form, tiles of all groups
 // walked through the per-CTA group table (p.grouped must be 1); plain GEMMs
 // use GROUPED = false, so none of its code or shared memory is in them.
-template <int KIND, int BN, bool GROUPED = false, bool SK = false>
-__global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
+// LEAN = true: the lean decode form (kLeanEpiWarps epilogue warps, which also
+// add stream-K segments; two CTAs fit on an SM).
+template <int KIND, int BN, bool GROUPED = false, bool SK = false, bool LEAN = false>
+__global__ void __launch_bounds__(LEAN ? kLeanThreads : (SK ? kThreadsSk : kThreads), LEAN ? 2 : 1)
     mx_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b)
 {
-    using C = Cfg<KIND, BN>;
+    using C = Cfg<KIND, BN, LEAN>;
     constexpr int S = C::kStages;
+    constexpr int kEpi = LEAN ? kLeanEpiWarps : kEpiWarps;  // epilogue warps 2 .. 2 + kEpi - 1
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_holder;
@@ -916,8 +935,10 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     __shared__ GroupTable gtab;  // grouped GEMM only
     __shared__ uint64_t fix_bars[2];  // stream-K fixup hand-off: full, empty
     __shared__ SkFix sk_fix;
-    constexpr bool kSk = SK;  // this instantiation runs stream-K plans (fixup warps 10, 11)
+    constexpr bool kSk = SK;  // this instantiation runs stream-K plans (fixup warps 10, 11 unless lean)
+    constexpr bool kFixW = SK && !LEAN;
     static_assert(!SK || !GROUPED, "stream-K: plain (not grouped) tiles only");
+    static_assert(!LEAN || !GROUPED, "the lean form is for plain tiles");
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -955,7 +976,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
-            mbar_init(acce_bar(a), kEpiWarps);
+            mbar_init(acce_bar(a), kEpi);
             mbar_init(sfull_bar(a), 1);
             mbar_init(sempty_bar(a), 1);
             mbar_init(tfree_bar(a), 1);
@@ -974,20 +995,50 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
     // The kernel that follows in the stream may be scheduled as SMs free up
     // (it waits for this grid before it touches memory).
     griddep_launch_dependents();
+    int npre = 0;         // k-stages of the first unit whose A-role tile was loaded before the grid wait
+    bool sfa_pre = false;  // and its first scale group's A-role chunks
     if constexpr (!GROUPED) {
         if (warp == 0 && !p.test_stall) {
-            // Warm L2 with the first ring's worth of this CTA's operand boxes while
-            // the preceding kernel drains: a prefetch is only a hint and L2 is where
-            // that kernel's writes land, so no stale data can be read by it.
             WorkIter wi0;
             wi0.init(p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
             Work w0;
-            if (wi0.next(p, w0) && elect_one()) {
+            if (wi0.next(p, w0)) {
                 TileGeom g0;
                 tile_geom<BN, C::kChunksB>(p, nullptr, w0, g0);
-                for (int ks = w0.ks0; ks < w0.ks1 && ks < w0.ks0 + S; ++ks) {
-                    tma_prefetch_2d(&map_a, ks * kRowBytes, g0.a_row);
-                    tma_prefetch_2d(&map_b, ks * kRowBytes, g0.b_row);
+                const int n0 = min(S, w0.ks1 - w0.ks0);
+                if (LEAN && p.early_a) {
+                    // The A-role operand is static (the caller's promise): arm the
+                    // first ring slots for both tiles and load the A-role tiles now,
+                    // while the preceding kernel drains; the B-role tiles follow the
+                    // grid wait.  (The barriers were initialised by thread 0 of this warp.)
+                    __syncwarp();
+                    const uint64_t pol_a0 = p.stream_a ? l2_policy_evict_first() : l2_policy_evict_last();
+                    if (elect_one()) {
+                        if (C::kScaled && g0.has_sfa) {
+                            // the first scale group: arm for both operands, copy the A-role chunks
+                            const int kt0 = w0.ks0 * C::kKtPerStage;
+                            const int nkt_g = min(kSfGroup * C::kKtPerStage, p.num_kt - kt0);
+                            mbar_arrive_expect_tx(sfull_bar(0), nkt_g * kSfChunk * (1 + g0.nchunk_b));
+                            bulk_load(sSF, p.sfa + (static_cast<size_t>(g0.sfa_rb) * p.num_kt + kt0) * kSfChunk,
+                                      nkt_g * kSfChunk, sfull_bar(0));
+                        }
+                        for (int j = 0; j < n0; ++j) {
+                            mbar_arrive_expect_tx(full_bar(j), C::kABytes + C::kBBytes);
+                            tma_load_2d(sA + j * C::kABytes, &map_a, full_bar(j), (w0.ks0 + j) * kRowBytes, g0.a_row,
+                                        pol_a0);
+                        }
+                    }
+                    npre = n0;
+                    sfa_pre = C::kScaled && g0.has_sfa;
+                } else if (elect_one()) {
+                    // Warm L2 with the first ring's worth of this CTA's operand boxes
+                    // while the preceding kernel drains: a prefetch is only a hint and
+                    // L2 is where that kernel's writes land, so no stale data can be
+                    // read by it.
+                    for (int j = 0; j < n0; ++j) {
+                        tma_prefetch_2d(&map_a, (w0.ks0 + j) * kRowBytes, g0.a_row);
+                        tma_prefetch_2d(&map_b, (w0.ks0 + j) * kRowBytes, g0.b_row);
+                    }
                 }
             }
             __syncwarp();
@@ -1031,6 +1082,8 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             int gi = 0;              // scale groups issued
             uint32_t sarmed = 0, sarmed_ph = 0;  // the same for the two scale group slots
             bool ok = true;
+            int pre_left = npre;     // first-unit stages whose slot is armed and A-role tile loading
+            armed = npre > 0 ? (1u << npre) - 1u : 0u;  // (phase 0)
             WorkIter wi;
             wi.init(p, first_unit, unit_step, gt, tok_tile);
             Work w;
@@ -1058,9 +1111,12 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                         const int nkt_g = min(kSfGroup * C::kKtPerStage, p.num_kt - kt0);
                         const uint32_t gbytes = nkt_g * kSfChunk * ((has_sfa ? 1 : 0) + nchunk_b);
                         const uint32_t dst = sSF + gs * C::kSfGrpBytes;
+                        // the first group's A-role chunks may have gone out before the grid wait
+                        const bool pre = gi == 0 && sfa_pre;
                         if (elect_one()) {
-                            mbar_arrive_expect_tx(sfull_bar(gs), gbytes);
-                            if (has_sfa)
+                            if (!pre)
+                                mbar_arrive_expect_tx(sfull_bar(gs), gbytes);
+                            if (has_sfa && !pre)
                                 bulk_load(dst, p.sfa + (static_cast<size_t>(g.sfa_rb) * p.num_kt + kt0) * kSfChunk,
                                           nkt_g * kSfChunk, sfull_bar(gs));
                             for (int c = 0; c < nchunk_b; ++c)
@@ -1073,15 +1129,22 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                         sarmed_ph = (sarmed_ph & ~(1u << gs)) | ((use & 1u) << gs);
                         ++gi;
                     }
-                    if (!warp_wait(empty_bar(st), ph ^ 1u, abort, lim)) {
-                        if (lane == 0) record_timeout(p, abort);
-                        ok = false;
-                        break;
-                    }
-                    if (elect_one()) {
-                        mbar_arrive_expect_tx(full_bar(st), C::kABytes + C::kBBytes);
-                        tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, g.a_row, pol_a);
-                        tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, g.b_row, pol_b);
+                    if (pre_left > 0) {
+                        // slot st was armed and its A-role tile loaded before the grid wait
+                        if (elect_one())
+                            tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, g.b_row, pol_b);
+                        --pre_left;
+                    } else {
+                        if (!warp_wait(empty_bar(st), ph ^ 1u, abort, lim)) {
+                            if (lane == 0) record_timeout(p, abort);
+                            ok = false;
+                            break;
+                        }
+                        if (elect_one()) {
+                            mbar_arrive_expect_tx(full_bar(st), C::kABytes + C::kBBytes);
+                            tma_load_2d(sA + st * C::kABytes, &map_a, full_bar(st), ks * kRowBytes, g.a_row, pol_a);
+                            tma_load_2d(sB + st * C::kBBytes, &map_b, full_bar(st), ks * kRowBytes, g.b_row, pol_b);
+                        }
                     }
                     __syncwarp();
                     armed |= 1u << st;
@@ -1240,11 +1303,11 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             __syncwarp();
             warp_wait(drain_bar, 0, no_abort, lim);
         }
-    } else if (warp >= 2 && warp < kFixWarp0) {
+    } else if (warp >= 2 && warp < 2 + kEpi) {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;         // TMEM lane quarter this warp may access
-        const int h = (warp - 2) >> 2;  // column half
-        constexpr int kCols = BN / 2 >= 32 ? BN / 2 : 32;
+        const int q = warp & 3;                     // TMEM lane quarter this warp may access
+        const int h = LEAN ? 0 : (warp - 2) >> 2;   // column half (the lean form: all columns)
+        constexpr int kCols = LEAN ? BN : (BN / 2 >= 32 ? BN / 2 : 32);
         constexpr int kChunks = kCols / 32;
         const bool has_cols = h * kCols < BN;
         __shared__ int sk_last;
@@ -1292,9 +1355,9 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
             if constexpr (kSk) {
                 if (w.kind == 1) {
                     // stream-K segment: publish, and queue the tile's fixup if this CTA is last
-                    sk_epilogue<BN, kCols, kChunks, (BN <= 64)>(p, w, r, first_unit, 1, 0, tm * kBM, h, row_local,
-                                                                has_cols, &sk_last, &sk_fix, smem_addr(&fix_bars[0]),
-                                                                smem_addr(&fix_bars[1]), &sk_posted, abort, lim);
+                    sk_epilogue<BN, kCols, kChunks, (LEAN || BN <= 64), kEpi>(
+                        p, w, r, first_unit, 1, 0, tm * kBM, h, row_local, has_cols, &sk_last, &sk_fix,
+                        smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]), &sk_posted, abort, lim);
                     continue;
                 }
             }
@@ -1318,7 +1381,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
                 }
             }
         }
-        if constexpr (kSk) {
+        if constexpr (kFixW) {
             if (p.sk_ctas > 0 && threadIdx.x == 64) {
                 const SkFix stop{-1, 0, 0, 0, 0};
                 if (!sk_post(sk_fix, stop, smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]), sk_posted, abort, lim))
@@ -1327,7 +1390,7 @@ __global__ void __launch_bounds__(SK ? kThreadsSk : kThreads, 1)
         }
     } else if (warp >= kFixWarp0) {
         // ------------------------------------------------- stream-K fixup
-        if constexpr (kSk) {
+        if constexpr (kFixW) {
             if (p.sk_ctas > 0) {
                 constexpr int kCols = BN / 2 >= 32 ? BN / 2 : 32;  // as in the epilogue
                 sk_fixup_warps<BN, kCols, kCols / 32>(p, sk_fix, smem_addr(&fix_bars[0]), smem_addr(&fix_bars[1]),

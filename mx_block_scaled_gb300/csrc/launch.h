@@ -44,11 +44,12 @@ cudaError_t prepare_gemm_fp4();
 cudaError_t prepare_gemm_bf16();
 
 // Launch the persistent GEMM kernel for tile width `bn` (32, 64, 128, 256) on
-// `grid` CTAs.  Returns cudaErrorInvalidValue for an unsupported bn.
-cudaError_t launch_gemm_fp8(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                            int grid, cudaStream_t stream);
-cudaError_t launch_gemm_fp4(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                            int grid, cudaStream_t stream);
+// `grid` CTAs; `lean` selects the lean decode form (bn 32 or 64).  Returns
+// cudaErrorInvalidValue for an unsupported bn.
+cudaError_t launch_gemm_fp8(int bn, bool lean, const GemmParams &p, const CUtensorMap &map_a,
+                            const CUtensorMap &map_b, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_fp4(int bn, bool lean, const GemmParams &p, const CUtensorMap &map_a,
+                            const CUtensorMap &map_b, int grid, cudaStream_t stream);
 
 // Grouped (mixture-of-experts) form of the single-CTA kernel, bn = 64, 128 or
 // 256 (p.grouped = 1), on `grid` CTAs.
@@ -72,8 +73,8 @@ int gemm_pair_max_clusters_fp4(int bn);
 
 // BF16 (kind::f16, no scales) GEMM: single-CTA tiles (bn 32..256) and CTA-pair
 // tiles (bn 128, 256; the scale maps are not read).
-cudaError_t launch_gemm_bf16(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                             int grid, cudaStream_t stream);
+cudaError_t launch_gemm_bf16(int bn, bool lean, const GemmParams &p, const CUtensorMap &map_a,
+                             const CUtensorMap &map_b, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_pair_bf16(int bn, const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
                                   const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, const CUtensorMap &map_sarm, int clusters,
                                   cudaStream_t stream);
@@ -85,11 +86,11 @@ struct KernelInfo {
     int acc_stages;
     int smem_bytes;
 };
-KernelInfo gemm_info_fp8(int bn);
-KernelInfo gemm_info_fp4(int bn);
+KernelInfo gemm_info_fp8(int bn, bool lean = false);
+KernelInfo gemm_info_fp4(int bn, bool lean = false);
 KernelInfo gemm_pair_info_fp8(int bn);
 KernelInfo gemm_pair_info_fp4(int bn);
-KernelInfo gemm_info_bf16(int bn);
+KernelInfo gemm_info_bf16(int bn, bool lean = false);
 KernelInfo gemm_pair_info_bf16(int bn);
 
 }  // namespace mxg

@@ -17,17 +17,19 @@ namespace mxg {
 template <int KIND>
 struct Launchers {
     // Single-CTA 128 x BN tiles; plans with stream-K segments run the
-    // instantiation with the two fixup warps.
-    template <int BN>
+    // instantiation with the two fixup warps (the lean form adds them in its
+    // epilogue warps).
+    template <int BN, bool LEAN = false>
     static cudaError_t single(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid, cudaStream_t s)
     {
         cudaLaunchAttribute attr[2];
+        constexpr int kSmem = Cfg<KIND, BN, LEAN>::kSmemBytes;
         if (p.sk_ctas > 0) {
-            cudaLaunchConfig_t cfg = launch_config(grid, kThreadsSk, Cfg<KIND, BN>::kSmemBytes, s, attr, 1);
-            return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<KIND, BN, false, true>, p, ma, mb);
+            cudaLaunchConfig_t cfg = launch_config(grid, LEAN ? kLeanThreads : kThreadsSk, kSmem, s, attr, 1);
+            return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<KIND, BN, false, true, LEAN>, p, ma, mb);
         }
-        cudaLaunchConfig_t cfg = launch_config(grid, kThreads, Cfg<KIND, BN>::kSmemBytes, s, attr, 1);
-        return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<KIND, BN>, p, ma, mb);
+        cudaLaunchConfig_t cfg = launch_config(grid, LEAN ? kLeanThreads : kThreads, kSmem, s, attr, 1);
+        return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<KIND, BN, false, false, LEAN>, p, ma, mb);
     }
 
     template <int BN>
@@ -95,6 +97,10 @@ struct Launchers {
         chk(opt_in(mx_gemm_kernel<KIND, 64, false, true>, Cfg<KIND, 64>::kSmemBytes));
         chk(opt_in(mx_gemm_kernel<KIND, 128, false, true>, Cfg<KIND, 128>::kSmemBytes));
         chk(opt_in(mx_gemm_kernel<KIND, 256, false, true>, Cfg<KIND, 256>::kSmemBytes));
+        chk(opt_in(mx_gemm_kernel<KIND, 32, false, false, true>, Cfg<KIND, 32, true>::kSmemBytes));
+        chk(opt_in(mx_gemm_kernel<KIND, 64, false, false, true>, Cfg<KIND, 64, true>::kSmemBytes));
+        chk(opt_in(mx_gemm_kernel<KIND, 32, false, true, true>, Cfg<KIND, 32, true>::kSmemBytes));
+        chk(opt_in(mx_gemm_kernel<KIND, 64, false, true, true>, Cfg<KIND, 64, true>::kSmemBytes));
         chk(opt_in(mx_gemm_pair_kernel<KIND, 128>, CfgPair<KIND, 128>::kSmemBytes));
         chk(opt_in(mx_gemm_pair_kernel<KIND, 256>, CfgPair<KIND, 256>::kSmemBytes));
         chk(opt_in(mx_gemm_pair_kernel<KIND, 256, true>, CfgPair<KIND, 256>::kSmemBytes));
@@ -106,9 +112,16 @@ struct Launchers {
         return e;
     }
 
-    static cudaError_t launch_single(int bn, const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid,
-                                     cudaStream_t s)
+    static cudaError_t launch_single(int bn, bool lean, const GemmParams &p, const CUtensorMap &ma,
+                                     const CUtensorMap &mb, int grid, cudaStream_t s)
     {
+        if (lean) {
+            switch (bn) {
+            case 32: return single<32, true>(p, ma, mb, grid, s);
+            case 64: return single<64, true>(p, ma, mb, grid, s);
+            default: return cudaErrorInvalidValue;
+            }
+        }
         switch (bn) {
         case 32: return single<32>(p, ma, mb, grid, s);
         case 64: return single<64>(p, ma, mb, grid, s);
@@ -142,14 +155,17 @@ struct Launchers {
 
     static int max_clusters(int bn) { return bn == 128 ? pair_max_clusters<128>() : pair_max_clusters<256>(); }
 
-    template <int BN>
+    template <int BN, bool LEAN = false>
     static KernelInfo single_info()
     {
-        return KernelInfo{Cfg<KIND, BN>::kStages, Cfg<KIND, BN>::kAccStages, Cfg<KIND, BN>::kSmemBytes};
+        using C = Cfg<KIND, BN, LEAN>;
+        return KernelInfo{C::kStages, C::kAccStages, C::kSmemBytes};
     }
 
-    static KernelInfo info(int bn)
+    static KernelInfo info(int bn, bool lean)
     {
+        if (lean)
+            return bn == 32 ? single_info<32, true>() : single_info<64, true>();
         switch (bn) {
         case 32: return single_info<32>();
         case 64: return single_info<64>();

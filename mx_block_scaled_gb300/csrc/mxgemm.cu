@@ -350,6 +350,7 @@ struct mxgemm_plan {
     int device;        // the device current when the plan was created; runs must use it
     size_t off_sfa, off_sfb, off_part, off_cnt, off_skp, ws_bytes;
     int sa_fuse;        // 1: row-major A scales are laid out inside the GEMM (pair tiles, K % 512 == 0)
+    int lean;           // 1: the lean single-CTA form (weight-streaming decode tiles, two CTAs per SM)
     int cnt_pool = -1;  // stream-K counters: offset in the library's counter array (-1: in the workspace)
     int cnt_n = 0;      // counters of the plan (stream-K tiles x 128-row shares)
     // TMA descriptor cache (re-encoded when an operand pointer changes)
@@ -586,6 +587,15 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     if ((flags & MXGEMM_PLAN_STREAMK) && mode == 1) bn = 256;
     p->mode = mode;
     p->bn = bn;
+    // Weight-streaming decode with at most 32 tokens (swap-AB single-CTA MX
+    // tiles of 32 columns) runs the lean form: two of its CTAs fit on an SM, so
+    // the next GEMM's CTAs are resident (TMEM allocated, first ring warmed in
+    // L2) while this one drains.  Measured: MXFP8 8 x 8192 x 8192 17.8 -> 16.9
+    // us, 8 x 10240 x 8192 21.2 -> 20.1; MXFP4 8 x 8192 x 8192 13.7 -> 11.6.
+    // Its ring is smaller (5 stages), which costs the 64-token tiles (4 stages:
+    // 64 x 10240 x 8192 22.7 -> 26.3 us) and BF16 (8 x 8192 x 8192 26.2 ->
+    // 27.2), so those keep the full form.
+    p->lean = (swap && mode == 0 && bn == 32 && !bf16) ? 1 : 0;
     // tiles_m counts the work units along the A role: 128-row tiles (single),
     // 256-row tiles (pair).
     p->tiles_m = static_cast<int>(mode == 0 ? ceil_div(rows_a, 128) : ceil_div(rows_a, 256));
@@ -751,19 +761,21 @@ int mxgemm_plan_describe(mxgemm_plan_t plan, char *buf, size_t len)
     const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
     const bool bf16 = plan->fmt == MXGEMM_FMT_BF16;
     static const char *const kModes[2] = {"single", "pair"};
+    const bool lean = plan->lean != 0;
     mxg::KernelInfo ki = plan->mode == 1 ? (fp4 ? mxg::gemm_pair_info_fp4(plan->bn)
                                                 : bf16 ? mxg::gemm_pair_info_bf16(plan->bn)
                                                        : mxg::gemm_pair_info_fp8(plan->bn))
-                                         : (fp4 ? mxg::gemm_info_fp4(plan->bn)
-                                                : bf16 ? mxg::gemm_info_bf16(plan->bn) : mxg::gemm_info_fp8(plan->bn));
+                                         : (fp4    ? mxg::gemm_info_fp4(plan->bn, lean)
+                                            : bf16 ? mxg::gemm_info_bf16(plan->bn, lean)
+                                                   : mxg::gemm_info_fp8(plan->bn, lean));
     snprintf(buf, len,
              "fmt=%s out=%s tile=%dx%d mode=%s swap_ab=%d split_k=%d streamk=%d+%d/%d units=%dx%d kstages=%d grid=%d%s "
-             "stages=%d acc_stages=%d smem=%d sa=%s",
+             "stages=%d acc_stages=%d smem=%d sa=%s%s",
              fp4 ? "mxfp4" : bf16 ? "bf16" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32",
              plan->mode == 1 ? 256 : 128,
              plan->bn, kModes[plan->mode], plan->swap, plan->splits, plan->dp_tiles, plan->sk_tiles, plan->sk_ctas,
              plan->tiles_m, plan->tiles_n, plan->kstages, plan->grid, plan->mode ? "x2" : "", ki.stages, ki.acc_stages,
-             ki.smem_bytes, plan->sa_fuse ? "in-kernel" : "relayout");
+             ki.smem_bytes, plan->sa_fuse ? "in-kernel" : "relayout", lean ? " lean" : "");
     return MXGEMM_OK;
 }
 
@@ -867,7 +879,7 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
     if (!plan || !A || !B || !C)
         return MXGEMM_ERR_ARG;
     const bool bf16 = plan->fmt == MXGEMM_FMT_BF16;  // no scales: SA and SB are not read
-    if (run_flags & ~(MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT | MXGEMM_RUN_PREPARED))
+    if (run_flags & ~(MXGEMM_RUN_SA_PRELAYOUT | MXGEMM_RUN_SB_PRELAYOUT | MXGEMM_RUN_PREPARED | MXGEMM_RUN_B_STATIC))
         return MXGEMM_ERR_ARG;
     // after mxgemm_prepare, scales that were not pre-laid-out are in the workspace --
     // except row-major SA of a plan that lays it out inside the GEMM
@@ -970,6 +982,8 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
         p.split_stride = 0;
     }
     p.vec_ok = vec_level(!plan->swap, N * osize, p.out);
+    // the lean decode form may load the weight (B, its A role) before the grid wait
+    p.early_a = (plan->lean && plan->swap && (run_flags & MXGEMM_RUN_B_STATIC)) ? 1 : 0;
     p.dbg_out_elems = split ? static_cast<long long>(plan->splits) * p.split_stride : M * N;
     p.dbg_out_elems -= static_cast<long long>(dbg_short_rows) * N;
     p.dbg_skp_elems = plan->sk_ctas > 0 ? 2ll * plan->sk_ctas * plan->sk_halves * 128 * plan->bn : 0;
@@ -1011,10 +1025,10 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
                 : mxg::launch_gemm_pair_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->map_sfa, plan->map_sfb,
                                             msarm, plan->grid, s);
     } else if (bf16)
-        e = mxg::launch_gemm_bf16(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
+        e = mxg::launch_gemm_bf16(plan->bn, plan->lean != 0, p, plan->map_a, plan->map_b, plan->grid, s);
     else
-        e = fp4 ? mxg::launch_gemm_fp4(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s)
-                : mxg::launch_gemm_fp8(plan->bn, p, plan->map_a, plan->map_b, plan->grid, s);
+        e = fp4 ? mxg::launch_gemm_fp4(plan->bn, plan->lean != 0, p, plan->map_a, plan->map_b, plan->grid, s)
+                : mxg::launch_gemm_fp8(plan->bn, plan->lean != 0, p, plan->map_a, plan->map_b, plan->grid, s);
     if (e != cudaSuccess)
         return MXGEMM_ERR_CUDA;
 

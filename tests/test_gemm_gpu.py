@@ -462,8 +462,9 @@ def test_prepare_then_run_equals_run(oracle_mod, fmt, plan_flags):
 @pytest.mark.parametrize("fmt,M,N,K,expect", [
     ("mxfp8", 4096, 4096, 4096, ["tile=256x256", "mode=pair", "streamk=228+28/56", "sa=in-kernel"]),
     ("mxfp8", 16384, 8192, 8192, ["tile=256x256", "mode=pair", "sa=in-kernel"]),
-    ("mxfp8", 8, 10240, 8192, ["tile=128x32", "mode=single", "swap_ab=1", "streamk=0+80/152"]),
-    ("mxfp8", 64, 8192, 8192, ["tile=128x64", "swap_ab=1", "split_k=2", "streamk=64+0/0"]),
+    ("mxfp8", 8, 10240, 8192, ["tile=128x32", "mode=single", "swap_ab=1", "streamk=0+80/152", "lean"]),
+    ("mxfp8", 64, 8192, 8192, ["tile=128x64", "swap_ab=1", "split_k=2", "streamk=64+0/0", "!lean"]),
+    ("bf16", 8, 8192, 8192, ["tile=128x32", "swap_ab=1", "!lean"]),
     ("mxfp8", 8, 8192, 28672, ["tile=128x32", "swap_ab=1", "streamk=0+64/152"]),
     ("mxfp4", 8, 10240, 8192, ["tile=128x32", "swap_ab=1", "streamk=80+0/0"]),
     ("mxfp4", 4096, 4096, 4096, ["tile=256x256", "mode=pair", "sa=relayout"]),
@@ -478,7 +479,8 @@ def test_default_plans_follow_the_heuristic(fmt, M, N, K, expect):
     """The planner's choices on representative shapes, as the design documents them
     (pair tiles for MXFP8 from 128 tokens, MXFP4 pair tiles from half a wave,
     BF16 small-token tile rules, swap-AB decode with stream-K over every SM on wide
-    or long k-loops and split-K otherwise)."""
+    or long k-loops and split-K otherwise, the lean kernel form for MX decode of at
+    most 32 tokens)."""
     b = lib()
     f = {"mxfp8": FMT_MXFP8, "mxfp4": FMT_MXFP4, "bf16": b.MXGEMM_FMT_BF16}[fmt]
     plan = b.Plan(M, N, K, f, OUT_BF16)
@@ -487,4 +489,42 @@ def test_default_plans_follow_the_heuristic(fmt, M, N, K, expect):
     for e in expect:
         if "streamk=" in e and sms != 152:
             continue  # the stream-K split depends on the SM count
-        assert e in d, (e, d)
+        if e.startswith("!"):
+            assert e[1:] not in d, (e, d)
+        else:
+            assert e in d, (e, d)
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+@pytest.mark.parametrize("M,N,K", [(8, 1280, 4096), (8, 10240, 2048), (1, 384, 1024), (32, 2048, 8192)])
+def test_static_weight_early_loads_exact(oracle_mod, fmt, M, N, K):
+    """MXGEMM_RUN_B_STATIC on the lean decode form (the weight's first ring and
+    first scale group loaded before the grid-dependency wait): back-to-back calls,
+    each the programmatic dependent of the one before, and a CUDA-graph replay of
+    them give the oracle's product exactly, as does a call without the flag."""
+    import torch
+    b = lib()
+    rng = np.random.default_rng([M, N, K, fmt, 5])
+    A, SA = small_int_codes(rng, M, K, fmt)
+    B, SB = small_int_codes(rng, N, K, fmt)
+    ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
+    plan = b.Plan(M, N, K, fmt, OUT_F32)
+    assert "lean" in plan.describe(), plan.describe()
+    dA, dSA, dB, dSB = to_dev(A), to_dev(SA), to_dev(B), to_dev(SB)
+    flags = b.MXGEMM_RUN_B_STATIC
+    outs = [plan.run(dA, dSA, dB, dSB, run_flags=flags) for _ in range(4)]
+    outs.append(plan.run(dA, dSA, dB, dSB))
+    b.check_device_status()
+    torch.cuda.synchronize()
+    for C in outs:
+        assert (C.double().cpu().numpy() == ref).all(), plan.describe()
+    Cs = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for _ in range(3)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for C in Cs:
+            plan.run(dA, dSA, dB, dSB, C=C, run_flags=flags)
+    g.replay()
+    torch.cuda.synchronize()
+    b.check_device_status()
+    for C in Cs:
+        assert (C.double().cpu().numpy() == ref).all(), plan.describe()
