@@ -93,6 +93,7 @@ typedef enum {
 #define MXGEMM_PLAN_STREAMK         (1u << 7)  /* spread the last wave's k-stages     */
 #define MXGEMM_PLAN_SPLITK_SHIFT    8          /* bits 8..15: forced split-K (0=auto) */
 #define MXGEMM_PLAN_NO_STREAMK      (1u << 16) /* whole tiles only (no stream-K)      */
+#define MXGEMM_PLAN_FORCE_BN192     (1u << 17) /* 256 x 192 tiles on CTA pairs        */
 
 /* Run flags (mxgemm_run). */
 #define MXGEMM_RUN_SA_PRELAYOUT     (1u << 0)  /* SA is already in the tile layout    */
@@ -118,6 +119,11 @@ typedef struct mxgemm_plan *mxgemm_plan_t;
  * tile's partial sums are added in k order inside the kernel (the result does
  * not depend on the run); MXGEMM_PLAN_STREAMK forces it where the last wave is
  * under 95% full, MXGEMM_PLAN_NO_STREAMK keeps whole tiles.
+ * 256 x 192 CTA-pair tiles are planned where 256-wide pair tiles would fill
+ * less than a wave of pairs and could not be split two ways within one;
+ * MXGEMM_PLAN_FORCE_BN192 forces them (MXGEMM_ERR_UNSUPPORTED where pair tiles
+ * cannot serve the shape: MXFP4 with K % 256 != 0; MXGEMM_ERR_ARG together
+ * with another tile-width, single-CTA or stream-K flag).
  */
 MXGEMM_API int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
                        int fmt, int out, uint32_t flags);

@@ -40,6 +40,7 @@ MXGEMM_PLAN_FORCE_SINGLE = 1 << 5
 MXGEMM_PLAN_STREAMK = 1 << 7
 MXGEMM_PLAN_SPLITK_SHIFT = 8
 MXGEMM_PLAN_NO_STREAMK = 1 << 16
+MXGEMM_PLAN_FORCE_BN192 = 1 << 17
 
 MXGEMM_RUN_SA_PRELAYOUT = 1 << 0
 MXGEMM_RUN_SB_PRELAYOUT = 1 << 1

@@ -37,7 +37,10 @@ struct CfgPair {
     static constexpr bool kScaled = KIND != K_BF16;
     static constexpr int kKtPerStage = kFp4 ? 2 : 1;
     static constexpr int kSubPerKt = kFp4 ? 2 : 4;
-    static constexpr int kChunksB = BN / 128;                 // B-role scale chunks per K-tile (all BN rows)
+    // B-role scale chunks per K-tile: all BN rows.  A 192-wide tile starts 0 or 64
+    // rows into a 128-row chunk, so it spans two chunks and its MMAs read the B
+    // scales from TMEM column 0 or 2 of them (an even column, as required).
+    static constexpr int kChunksB = (BN + 127) / 128;
     static constexpr int kABytes = kBM * kRowBytes;           // own 128 A-role rows
     static constexpr int kBBytes = (BN / 2) * kRowBytes;      // own half of the B-role tile
     static constexpr int kStageBytes = kABytes + kBBytes;     // operands of one k-stage
@@ -78,7 +81,7 @@ struct CfgPair {
     static constexpr int kSmemBytes = 1024 + kSlots * kSlotBytes + kGrp * kSfGrpBytes + kSaBytes + 512;
     static constexpr uint32_t kIdesc =
         kScaled ? idesc_block_scaled(kFp4 ? 1u : 0u, 2 * kBM, BN) : idesc_bf16(2 * kBM, BN);
-    static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
+    static_assert(BN == 128 || BN == 192 || BN == 256, "pair tiles are 256 x 128, 256 x 192 or 256 x 256");
     static_assert(kSlots >= 2, "shared memory too small for two slots");
     static_assert(kSfGroup % 2 == 0, "scale groups start on a slot boundary");
     static_assert(kColsUsed <= 512, "TMEM overflow");
@@ -504,6 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t d_tmem = tmem + acc * BN;
             const int ks0 = w.ks0, ks1 = w.ks1;
             const int kb0 = ks0 & ~1;
+            // 32-row group of the tile's first B-role row in its scale chunk (0 unless BN = 192)
+            const uint32_t sub_b = static_cast<uint32_t>(((w.tn * BN) & 127) >> 5);
             for (int kb = kb0; kb < ks1; kb += 2) {
                 if (kb != kb0 && group_start(kb, kb0)) {
                     const int g0 = kb - kb % kSfGroup;
@@ -543,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                    : static_cast<uint32_t>(s % 4);
                                     const uint32_t idesc = idesc_with_sf_ids(C::kIdesc, sf_id, sf_id);
                                     const uint32_t sfa_t = sfa_col + 4 * t;
-                                    const uint32_t sfb_t = sfb_col + 4 * t * C::kChunksB;
+                                    const uint32_t sfb_t = sfb_col + 4 * t * C::kChunksB + sub_b;
                                     const uint64_t koff = static_cast<uint64_t>((s * 32) >> 4);
                                     const uint32_t accum = (s > 0) ? 1u : acc0;
                                     if constexpr (KIND == K_BF16)

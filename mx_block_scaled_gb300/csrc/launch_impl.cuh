@@ -102,6 +102,7 @@ struct Launchers {
         chk(opt_in(mx_gemm_kernel<KIND, 32, false, true, true>, Cfg<KIND, 32, true>::kSmemBytes));
         chk(opt_in(mx_gemm_kernel<KIND, 64, false, true, true>, Cfg<KIND, 64, true>::kSmemBytes));
         chk(opt_in(mx_gemm_pair_kernel<KIND, 128>, CfgPair<KIND, 128>::kSmemBytes));
+        chk(opt_in(mx_gemm_pair_kernel<KIND, 192>, CfgPair<KIND, 192>::kSmemBytes));
         chk(opt_in(mx_gemm_pair_kernel<KIND, 256>, CfgPair<KIND, 256>::kSmemBytes));
         chk(opt_in(mx_gemm_pair_kernel<KIND, 256, true>, CfgPair<KIND, 256>::kSmemBytes));
         if constexpr (KIND != K_BF16) {
@@ -148,12 +149,16 @@ struct Launchers {
     {
         switch (bn) {
         case 128: return pair<128>(p, ma, mb, msa, msb, msarm, clusters, s);
+        case 192: return pair<192>(p, ma, mb, msa, msb, msarm, clusters, s);
         case 256: return pair<256>(p, ma, mb, msa, msb, msarm, clusters, s);
         default: return cudaErrorInvalidValue;
         }
     }
 
-    static int max_clusters(int bn) { return bn == 128 ? pair_max_clusters<128>() : pair_max_clusters<256>(); }
+    static int max_clusters(int bn)
+    {
+        return bn == 128 ? pair_max_clusters<128>() : bn == 192 ? pair_max_clusters<192>() : pair_max_clusters<256>();
+    }
 
     template <int BN, bool LEAN = false>
     static KernelInfo single_info()
@@ -174,12 +179,15 @@ struct Launchers {
         }
     }
 
+    template <int BN>
+    static KernelInfo pair_info_of()
+    {
+        return KernelInfo{CfgPair<KIND, BN>::kStages, CfgPair<KIND, BN>::kAccStages, CfgPair<KIND, BN>::kSmemBytes};
+    }
+
     static KernelInfo pair_info(int bn)
     {
-        return bn == 128 ? KernelInfo{CfgPair<KIND, 128>::kStages, CfgPair<KIND, 128>::kAccStages,
-                                      CfgPair<KIND, 128>::kSmemBytes}
-                         : KernelInfo{CfgPair<KIND, 256>::kStages, CfgPair<KIND, 256>::kAccStages,
-                                      CfgPair<KIND, 256>::kSmemBytes};
+        return bn == 128 ? pair_info_of<128>() : bn == 192 ? pair_info_of<192>() : pair_info_of<256>();
     }
 };
 

@@ -497,9 +497,11 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     const bool bf16 = fmt == MXGEMM_FMT_BF16;
     const uint32_t known = MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_NOSWAP |
                            MXGEMM_PLAN_FORCE_SWAP | MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE |
-                           MXGEMM_PLAN_STREAMK | MXGEMM_PLAN_NO_STREAMK |
+                           MXGEMM_PLAN_STREAMK | MXGEMM_PLAN_NO_STREAMK | MXGEMM_PLAN_FORCE_BN192 |
                            (0xFFu << MXGEMM_PLAN_SPLITK_SHIFT);
     if ((flags & ~known) != 0 || ((flags & MXGEMM_PLAN_FORCE_SWAP) && (flags & MXGEMM_PLAN_FORCE_NOSWAP)) ||
+        ((flags & MXGEMM_PLAN_FORCE_BN192) &&
+         (flags & (MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_SINGLE | MXGEMM_PLAN_STREAMK))) ||
         ((flags & MXGEMM_PLAN_STREAMK) && (flags & MXGEMM_PLAN_NO_STREAMK)) ||
         ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)) ||
         ((flags & MXGEMM_PLAN_FORCE_PAIR) && (flags & MXGEMM_PLAN_FORCE_SINGLE)))
@@ -560,11 +562,15 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     // pair 30.5 us, 128 x 128 tiles 23.9 us) -- unless the narrower tiles need
     // more than one wave (128 x 51200 x 5120: pair 95.0 us, single 97.5 us).
     if (bf16 && rows_a <= 128 && ceil_div(rows_b, 128) <= dev->num_sms) mode = 0;
-    if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 1;
+    if (flags & (MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_BN192)) mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_SINGLE) mode = 0;
     // pair tiles load two 128-byte K-slices per box: MXFP4 rows must be a whole
     // number of slices (K % 256 == 0), else single-CTA tiles
     if (fmt == MXGEMM_FMT_MXFP4_E2M1 && K % 256 != 0) mode = 0;
+    if ((flags & MXGEMM_PLAN_FORCE_BN192) && mode != 1) {  // 192-wide tiles exist on CTA pairs only
+        delete p;
+        return MXGEMM_ERR_UNSUPPORTED;
+    }
     // The activation scales' relayout (the FlyDSL page's "layout copy") runs
     // inside the MXFP8 pair kernel when their row pitch K/32 allows 16-byte TMA
     // rows.
@@ -582,6 +588,22 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         if (units_m * ceil_div(rows_b, 256) < slots_est && units_m * ceil_div(rows_b, 128) <= slots_est)
             bn = 128;
     }
+    // 192-wide pair tiles where the 256-wide ones fill less than a wave of pairs,
+    // cannot be split two ways within one (the split-K rule below would then
+    // split them), and the narrower ones still fit in one wave: more pairs at
+    // work, each k-stage shorter.  Measured: 256 x 10240 x 8192 MXFP8 (40 -> 54
+    // of 76 pairs) 27.8 -> 25.6 us, MXFP4 18.1 -> 16.7, BF16 45.9 -> 37.1;
+    // where two-way split-K fits, 192-wide tiles without it lost (256 x 8192 x
+    // 28672: 55.3 -> 72.0 us).
+    if (mode == 1 && bn == 256 &&
+        !(flags & (MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_STREAMK))) {
+        const int64_t units_m = ceil_div(rows_a, 256);
+        const int64_t pairs_est = dev->num_sms / 2;
+        const int64_t t256 = units_m * ceil_div(rows_b, 256), t192 = units_m * ceil_div(rows_b, 192);
+        if (t256 < pairs_est && 2 * t256 > pairs_est && t192 <= pairs_est && t192 > t256)
+            bn = 192;
+    }
+    if (flags & MXGEMM_PLAN_FORCE_BN192) bn = 192;
     // Stream-K on CTA pairs runs on 256-wide tiles only (the pair kernel's
     // stream-K instantiation): a forced stream-K pair plan takes them.
     if ((flags & MXGEMM_PLAN_STREAMK) && mode == 1) bn = 256;
@@ -1009,7 +1031,8 @@ static int run_impl(mxgemm_plan_t plan, const void *A, const uint8_t *SA, const 
             plan->map_ptr_sfa = p.sfa;
         }
         if (plan->map_ptr_sfb != p.sfb) {
-            if (encode_sf_map(&plan->map_sfb, p.sfb, rows_b, K, ktps, plan->bn / 128) != MXGEMM_OK)
+            if (encode_sf_map(&plan->map_sfb, p.sfb, rows_b, K, ktps, static_cast<int>(ceil_div(plan->bn, 128))) !=
+                MXGEMM_OK)
                 return MXGEMM_ERR_CUDA;
             plan->map_ptr_sfb = p.sfb;
         }

@@ -80,6 +80,8 @@ def test_status_strings(lib):
     (16, 16, 128, 1, 2, (1 << 7) | (1 << 16), -1),  # stream-K forced on and off
     (16, 16, 128, 1, 2, 1 << 6, -1),  # bit 6 is not a plan flag
     (16, 16, 128, 1, 2, (1 << 4) | (1 << 5), -1),  # pair and single tiles at once
+    (16, 16, 128, 1, 2, (1 << 17) | (1 << 1), -1),  # 192- and 256-wide tiles at once
+    (16, 16, 128, 1, 2, (1 << 17) | (1 << 7), -1),  # 192-wide tiles with stream-K
 ])
 def test_plan_create_validates_before_touching_the_device(lib, M, N, K, fmt, out, flags, expect):
     st, h = lib.mxgemm_plan_create(M, N, K, fmt, out, flags)

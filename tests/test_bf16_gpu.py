@@ -101,3 +101,18 @@ def test_bf16_full_size_sampled(oracle_mod, M, N, K):
     ref_c, S_c = oracle_mod.bf16_gemm(A, B, cols=cols)
     got_c = C[:, torch.from_numpy(cols).cuda()].float().double().cpu().numpy()
     assert_within(got_c, ref_c, S_c, OUT_BF16, f"cols {plan.describe()}")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 1000, 512), (300, 2000, 1024)])
+def test_bf16_pair_192_wide_tiles_exact(oracle_mod, M, N, K):
+    """BF16 on 256 x 192 CTA-pair tiles (MXGEMM_PLAN_FORCE_BN192), exact against the
+    oracle in FP32 and BF16 out."""
+    rng = np.random.default_rng(M + N + K + 192)
+    A, B = _small(rng, M, K), _small(rng, N, K)
+    ref, _ = oracle_mod.bf16_gemm(A, B)
+    for out in (OUT_F32, OUT_BF16):
+        C, desc = _gemm(A, B, out, (1 << 17) | (1 << 8))
+        expect = ref if out == OUT_F32 else _bf16_round(ref)
+        assert "tile=256x192" in desc, desc
+        assert (C == expect).all(), f"{M}x{N}x{K} {desc}"
+

@@ -473,11 +473,14 @@ def test_prepare_then_run_equals_run(oracle_mod, fmt, plan_flags):
     ("bf16", 128, 10240, 5120, ["tile=128x128", "mode=single"]),
     ("bf16", 128, 51200, 5120, ["mode=pair"]),
     ("bf16", 256, 6144, 4096, ["tile=256x128", "mode=pair"]),
-    ("bf16", 256, 10240, 8192, ["tile=256x256", "mode=pair"]),
+    ("bf16", 256, 10240, 8192, ["tile=256x192", "mode=pair"]),
+    ("mxfp8", 256, 10240, 8192, ["tile=256x192", "mode=pair", "split_k=1"]),
+    ("mxfp8", 256, 8192, 8192, ["tile=256x256", "mode=pair", "split_k=2"]),
 ])
 def test_default_plans_follow_the_heuristic(fmt, M, N, K, expect):
     """The planner's choices on representative shapes, as the design documents them
-    (pair tiles for MXFP8 from 128 tokens, MXFP4 pair tiles from half a wave,
+    (pair tiles for MXFP8 from 128 tokens, MXFP4 pair tiles from half a wave, 192-wide
+    pair tiles where 256-wide ones fill less than a wave and cannot split two ways,
     BF16 small-token tile rules, swap-AB decode with stream-K over every SM on wide
     or long k-loops and split-K otherwise, the lean kernel form for MX decode of at
     most 32 tokens)."""
@@ -528,3 +531,27 @@ def test_static_weight_early_loads_exact(oracle_mod, fmt, M, N, K):
     b.check_device_status()
     for C in Cs:
         assert (C.double().cpu().numpy() == ref).all(), plan.describe()
+
+
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
+@pytest.mark.parametrize("M,N,K", [(256, 1000, 1536), (300, 2000, 1152), (200, 4096, 2048), (129, 776, 4096)])
+def test_pair_192_wide_tiles_exact(oracle_mod, fmt, M, N, K):
+    """256 x 192 CTA-pair tiles (MXGEMM_PLAN_FORCE_BN192; planned by default where
+    256-wide pair tiles fill less than a wave and cannot split two ways): every
+    other tile starts 64 rows into a 128-row scale chunk, so its MMAs
+    read the B scales two TMEM columns in, and the last tile's second chunk lies
+    past the end of B; ragged M and N, in-kernel and relayout activation scales."""
+    if fmt == FMT_MXFP4 and K % 256 != 0:
+        pytest.skip("MXFP4 pair tiles need K % 256 == 0")
+    rng = np.random.default_rng([M, N, K, fmt, 192])
+    A, SA = small_int_codes(rng, M, K, fmt)
+    B, SB = small_int_codes(rng, N, K, fmt)
+    ref, _ = oracle_mod.gemm(fmt, A, SA, B, SB, K)
+    flags = (1 << 17) | ((1 << 8) if fmt == FMT_MXFP8 else 0)  # FORCE_BN192; MXFP8: one split
+    C, desc = gpu_gemm(fmt, A, SA, B, SB, K, OUT_F32, flags=flags, return_plan=True)
+    assert "tile=256x192" in desc, desc
+    assert (C == ref).all(), desc
+    C2, desc2 = gpu_gemm(fmt, A, SA, B, SB, K, OUT_BF16, flags=1 << 17, return_plan=True)
+    import torch
+    expect = torch.from_numpy(ref.astype(np.float32)).bfloat16().double().numpy()
+    assert (C2 == expect).all(), desc2
