@@ -554,8 +554,21 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     const bool pair_ok = !swap && rows_a >= 128 && rows_b >= 256 && !(flags & MXGEMM_PLAN_FORCE_BN128) &&
                          ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0;
     const int64_t pair_tiles = ceil_div(rows_a, 256) * ceil_div(rows_b, 256);
-    if (pair_ok && (fmt != MXGEMM_FMT_MXFP4_E2M1 || pair_tiles >= dev->num_sms / 4))
+    const int64_t pair_tiles192 = ceil_div(rows_a, 256) * ceil_div(rows_b, 192);
+    // MXFP4 whose 256-wide pair tiles stay under half the pairs but whose
+    // 192-wide ones reach half and fit in a wave, with k-loops of at most 32
+    // stages: 192-wide pair tiles (256 x 8192 x 8192: single-CTA split-K 18.2
+    // us, 256 x 192 pair tiles 16.2 us; with 112 k-stages, 256 x 8192 x 28672,
+    // the single-CTA split-K plan stays faster: 37.0 against 41.5 us).
+    bool fp4_192 = false;
+    if (pair_ok && (fmt != MXGEMM_FMT_MXFP4_E2M1 || pair_tiles >= dev->num_sms / 4)) {
         mode = 1;
+    } else if (pair_ok && fmt == MXGEMM_FMT_MXFP4_E2M1 && pair_tiles192 >= dev->num_sms / 4 &&
+               pair_tiles192 <= dev->num_sms / 2 && ceil_div(K, 256) <= 32 &&
+               !(flags & (MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_STREAMK))) {
+        mode = 1;
+        fp4_192 = true;
+    }
     // BF16 runs its MMAs at half the MX rate per operand byte, so it is bound by
     // the tensor pipe where MX formats wait on memory: with at most 128 tokens a
     // pair tile's M = 256 MMAs would compute half empty rows (128 x 10240 x 5120:
@@ -603,7 +616,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         if (t256 < pairs_est && 2 * t256 > pairs_est && t192 <= pairs_est && t192 > t256)
             bn = 192;
     }
-    if (flags & MXGEMM_PLAN_FORCE_BN192) bn = 192;
+    if ((flags & MXGEMM_PLAN_FORCE_BN192) || (fp4_192 && mode == 1)) bn = 192;
     // Stream-K on CTA pairs runs on 256-wide tiles only (the pair kernel's
     // stream-K instantiation): a forced stream-K pair plan takes them.
     if ((flags & MXGEMM_PLAN_STREAMK) && mode == 1) bn = 256;

@@ -469,7 +469,8 @@ def test_prepare_then_run_equals_run(oracle_mod, fmt, plan_flags):
     ("mxfp4", 8, 10240, 8192, ["tile=128x32", "swap_ab=1", "streamk=80+0/0"]),
     ("mxfp4", 4096, 4096, 4096, ["tile=256x256", "mode=pair", "sa=relayout"]),
     ("mxfp4", 256, 6144, 4096, ["tile=128x256", "mode=single"]),
-    ("mxfp4", 256, 10240, 8192, ["mode=pair"]),
+    ("mxfp4", 256, 10240, 8192, ["tile=256x192", "mode=pair"]),
+    ("mxfp4", 256, 8192, 8192, ["tile=256x192", "mode=pair", "split_k=1"]),
     ("bf16", 128, 10240, 5120, ["tile=128x128", "mode=single"]),
     ("bf16", 128, 51200, 5120, ["mode=pair"]),
     ("bf16", 256, 6144, 4096, ["tile=256x128", "mode=pair"]),
