@@ -532,6 +532,18 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
 
     // Operand roles: small token counts put the weight (B) in the 128-row MMA dimension.
     int swap = (M <= 64 && N >= 128) ? 1 : 0;
+    // MXFP8 with 65..128 tokens and a long k-loop: the weight in the 256-row role
+    // of CTA-pair tiles and the tokens as one 128-wide tile, which computes no
+    // empty rows and fits an 8-stage ring (scales pre-laid-out: 128 x 5120 x
+    // 8192 19.6 -> 16.5 us, 128 x 5120 x 25600 35.0 -> 29.3 us; no gain at K =
+    // 5120).  Row-major activation scales then take a relayout launch (~2.4 us).
+    const bool swap_pair =
+        fmt == MXGEMM_FMT_MXFP8_E4M3 && M > 64 && M <= 128 && N >= 256 && K >= 8192 &&
+        !(flags & (MXGEMM_PLAN_FORCE_SWAP | MXGEMM_PLAN_FORCE_NOSWAP | MXGEMM_PLAN_FORCE_SINGLE |
+                   MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 |
+                   MXGEMM_PLAN_FORCE_BN192 | MXGEMM_PLAN_STREAMK)) &&
+        ((flags >> MXGEMM_PLAN_SPLITK_SHIFT) & 0xFFu) == 0;
+    if (swap_pair) swap = 1;
     if (flags & MXGEMM_PLAN_FORCE_SWAP) swap = 1;
     if (flags & MXGEMM_PLAN_FORCE_NOSWAP) swap = 0;
     p->swap = swap;
@@ -575,7 +587,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     // pair 30.5 us, 128 x 128 tiles 23.9 us) -- unless the narrower tiles need
     // more than one wave (128 x 51200 x 5120: pair 95.0 us, single 97.5 us).
     if (bf16 && rows_a <= 128 && ceil_div(rows_b, 128) <= dev->num_sms) mode = 0;
-    if (flags & (MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_BN192)) mode = 1;
+    if (swap_pair || (flags & (MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_BN192))) mode = 1;
     if (flags & MXGEMM_PLAN_FORCE_SINGLE) mode = 0;
     // pair tiles load two 128-byte K-slices per box: MXFP4 rows must be a whole
     // number of slices (K % 256 == 0), else single-CTA tiles

@@ -156,7 +156,8 @@ def test_edge_shapes_exact(oracle_mod, fmt, flags, M, N, K):
 
 @pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_MXFP4])
 @pytest.mark.parametrize("flags", [0, 1 << 2, 1 << 3, (1 << 2) | 1, (1 << 2) | 2, (3 << 8), (1 << 3) | (5 << 8),
-                                   SINGLE, SINGLE | 2, PAIR | 1, PAIR | 2, PAIR | 1 | (3 << 8), PAIR | 2 | (2 << 8)])
+                                   SINGLE, SINGLE | 2, PAIR | 1, PAIR | 2, PAIR | 1 | (3 << 8), PAIR | 2 | (2 << 8),
+                                   PAIR | (1 << 3), PAIR | (1 << 3) | 1])
 def test_plan_variants_agree_with_oracle(oracle_mod, fmt, flags):
     """Forced tile width / swap-AB / split-K variants all reproduce the oracle."""
     M, N, K = 200, 384, 2048
@@ -466,6 +467,8 @@ def test_prepare_then_run_equals_run(oracle_mod, fmt, plan_flags):
     ("mxfp8", 64, 8192, 8192, ["tile=128x64", "swap_ab=1", "split_k=2", "streamk=64+0/0", "!lean"]),
     ("bf16", 8, 8192, 8192, ["tile=128x32", "swap_ab=1", "!lean"]),
     ("mxfp8", 8, 8192, 28672, ["tile=128x32", "swap_ab=1", "streamk=0+64/152"]),
+    ("mxfp8", 128, 5120, 8192, ["tile=256x128", "mode=pair", "swap_ab=1"]),
+    ("mxfp8", 128, 10240, 5120, ["tile=256x192", "mode=pair", "swap_ab=0"]),
     ("mxfp4", 8, 10240, 8192, ["tile=128x32", "swap_ab=1", "streamk=80+0/0"]),
     ("mxfp4", 4096, 4096, 4096, ["tile=256x256", "mode=pair", "sa=relayout"]),
     ("mxfp4", 256, 6144, 4096, ["tile=128x256", "mode=single"]),
@@ -556,3 +559,28 @@ def test_pair_192_wide_tiles_exact(oracle_mod, fmt, M, N, K):
     import torch
     expect = torch.from_numpy(ref.astype(np.float32)).bfloat16().double().numpy()
     assert (C2 == expect).all(), desc2
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 640, 8192), (100, 1000, 8192), (65, 384, 16384)])
+def test_swap_pair_default_for_mid_token_counts_exact(oracle_mod, M, N, K):
+    """MXFP8 with 65-128 tokens and K >= 8192 plans swap-AB on CTA pairs (the weight
+    in the 256-row role, the tokens as one 128-wide tile): exact against the oracle,
+    row-major and pre-laid-out scales, FP32 and BF16 out."""
+    b = lib()
+    rng = np.random.default_rng([M, N, K, 65])
+    A, SA = small_int_codes(rng, M, K, FMT_MXFP8)
+    B, SB = small_int_codes(rng, N, K, FMT_MXFP8)
+    ref, _ = oracle_mod.gemm(FMT_MXFP8, A, SA, B, SB, K)
+    C, desc = gpu_gemm(FMT_MXFP8, A, SA, B, SB, K, OUT_F32, return_plan=True)
+    assert "mode=pair" in desc and "swap_ab=1" in desc and "tile=256x128" in desc, desc
+    assert (C == ref).all(), desc
+    import torch
+    plan = b.Plan(M, N, K, FMT_MXFP8, OUT_BF16)
+    tSA = b.relayout_scales(to_dev(SA), M, K)
+    tSB = b.relayout_scales(to_dev(SB), N, K)
+    C2 = plan.run(to_dev(A), tSA, to_dev(B), tSB,
+                  run_flags=b.MXGEMM_RUN_SA_PRELAYOUT | b.MXGEMM_RUN_SB_PRELAYOUT)
+    b.check_device_status()
+    expect = torch.from_numpy(ref.astype(np.float32)).bfloat16().double().numpy()
+    assert (C2.double().cpu().numpy() == expect).all(), desc
+
