@@ -29,7 +29,11 @@
 //               the stores overlap the next tile's MMAs.
 //   warps 10,11 stream-K fixup: add the partial sums of a tile cut between CTAs
 //               (posted by the epilogue when this CTA's segment arrived last)
-//               and store it, concurrently with everything else.
+//               and store it, concurrently with everything else.  Tiles of at
+//               most 64 columns have the epilogue warps add them instead.
+// The lean form (weight-streaming decode, 192 threads) keeps warps 0 and 1 and
+// four epilogue warps that own all the tile's columns and add cut tiles
+// themselves; its ring fits two CTAs on an SM.
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // MXGEMM_ERR_DEVICE_TIMEOUT in *status, drains its in-flight copies and MMAs,
 // frees its TMEM and exits.
