@@ -393,9 +393,12 @@ typedef struct mxgemm_grouped_plan *mxgemm_grouped_plan_t;
  * (the row count of A and C: T), N weight rows per group (a multiple of 128,
  * so that every group's weight scales start on a 128-row scale tile) and K
  * (a multiple of 128).  fmt / out as for mxgemm_plan_create; flags: any of
- * MXGEMM_PLAN_FORCE_{SWAP,NOSWAP,BN128,BN256} (others: MXGEMM_ERR_ARG).  By
- * default the weights fill the 128-row MMA dimension (swap-AB) when the
- * expected tokens per group, rows / groups, are at most 64.  Host memory only.
+ * MXGEMM_PLAN_FORCE_{SWAP,NOSWAP,BN128,BN256,PAIR,SINGLE} (others:
+ * MXGEMM_ERR_ARG).  By default the weights fill the 128-row MMA dimension
+ * (swap-AB) when the expected tokens per group, rows / groups, are at most
+ * 64, and groups of at least 512 tokens on average run 256 x 256 CTA-pair
+ * tiles (token tiles of 256 rows inside each group; not swapped, N >= 256,
+ * MXFP4 with K % 256 == 0).  Host memory only.
  * Errors: MXGEMM_ERR_ARG, MXGEMM_ERR_SHAPE, MXGEMM_ERR_UNSUPPORTED (sizes past
  * the kernel's 32-bit indices), MXGEMM_ERR_ARCH.
  */

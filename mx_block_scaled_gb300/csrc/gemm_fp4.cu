@@ -28,6 +28,20 @@ cudaError_t launch_gemm_pair_fp4(int bn, const GemmParams &p, const CUtensorMap 
 
 int gemm_pair_max_clusters_fp4(int bn) { return L::max_clusters(bn); }
 
+cudaError_t launch_gemm_grouped_pair_fp4(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
+                                         const CUtensorMap &msa, const CUtensorMap &msb, int clusters, cudaStream_t s)
+{
+    return L::grouped_pair(p, ma, mb, msa, msb, clusters, s);
+}
+
+int gemm_grouped_pair_max_clusters_fp4() { return L::pair_max_clusters<256, true>(); }
+
+KernelInfo gemm_grouped_pair_info_fp4()
+{
+    using C = CfgPair<K_MXFP4, 256, true>;
+    return KernelInfo{C::kStages, C::kAccStages, C::kSmemBytes};
+}
+
 KernelInfo gemm_pair_info_fp4(int bn) { return L::pair_info(bn); }
 
 KernelInfo gemm_info_fp4(int bn, bool lean) { return L::info(bn, lean); }

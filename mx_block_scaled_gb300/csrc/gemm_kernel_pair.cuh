@@ -31,7 +31,10 @@
 
 namespace mxg {
 
-template <int KIND, int BN>
+// GROUPED = true: the grouped (mixture-of-experts) form: token tiles of 256 rows
+// inside each group, the group table in static shared memory, no in-kernel
+// scale layout (the tokens' scales are laid out per group before the GEMM).
+template <int KIND, int BN, bool GROUPED = false>
 struct CfgPair {
     static constexpr bool kFp4 = KIND == K_MXFP4;
     static constexpr bool kScaled = KIND != K_BF16;
@@ -62,11 +65,13 @@ struct CfgPair {
     // staging buffer for both CTAs' 256 rows x 4 bytes per K-tile, and the even
     // CTA's chunks as built by the odd CTA.  (MXFP4 plans take pre-laid scales:
     // their ring leaves no room for the buffers.)
-    static constexpr bool kFuseSa = kScaled && !kFp4;
+    static constexpr bool kFuseSa = kScaled && !kFp4 && !GROUPED;
     static constexpr int kSaRawBytes = kFuseSa ? 2 * kBM * 4 * kSfGroup * kKtPerStage : 0;
     static constexpr int kSaLeadBytes = kFuseSa ? kSfaGrpBytes : 0;
     static constexpr int kSaBytes = 2 * kSaRawBytes + kGrp * kSaLeadBytes;
-    static constexpr int kSlotsRaw = (kSmemBudget - 1024 - 512 - kGrp * kSfGrpBytes - kSaBytes) / kSlotBytes;
+    static constexpr int kStaticBytes = GROUPED ? static_cast<int>(sizeof(GroupTable)) : 0;
+    static constexpr int kSlotsRaw =
+        (kSmemBudget - kStaticBytes - 1024 - 512 - kGrp * kSfGrpBytes - kSaBytes) / kSlotBytes;
     static constexpr int kSlots = kSlotsRaw > 4 ? 4 : kSlotsRaw;
     static constexpr int kStages = 2 * kSlots;                // k-stages resident in the ring
     static constexpr int kSfaCols = kScaled ? 4 * kKtPerStage : 0;
@@ -88,20 +93,66 @@ struct CfgPair {
     static_assert(!kFuseSa || kSfGroup * kKtPerStage == 4, "the fused layout moves one 16-byte row word per chunk");
 };
 
+// Where one CTA of a pair works on tile w: the TMA rows of its A-role rows and
+// of its half of the B-role tile, its A-role scale block (and the odd CTA's, for
+// the even CTA's byte count), the tile's first B-role scale block, and the
+// output rows and limits of its 128 rows.  Grouped tiles are group-local: the
+// tokens' rows and scale blocks start at the group's, the weights' at e * N.
+struct PairGeom {
+    int a_row, b_row;
+    int sfa_rb;
+    bool has_sfa, peer_has_sfa;
+    int rb_b0;
+    int row0;              // first output row (within the group) of this CTA's 128 rows
+    int lim_i, lim_j;
+    long long out_base;
+};
+
+template <int BN>
+__device__ __forceinline__ void pair_geom(const GemmParams &p, const GroupTable *g, const Work &w, int rank,
+                                          PairGeom &t)
+{
+    int base_rb = 0, a0 = 0, b0 = 0, nrb = (p.rows_a + 127) / 128;
+    t.lim_i = p.rows_a;
+    t.lim_j = p.rows_b;
+    t.out_base = 0;
+    if (g != nullptr) {
+        const int e = w.grp;
+        base_rb = g->tok_rb[e];
+        a0 = g->row0[e];
+        b0 = e * p.group_n;
+        nrb = p.tok_sf_cap;
+        t.lim_i = g->rows[e];
+        t.lim_j = p.group_n;
+        t.out_base = static_cast<long long>(a0) * p.group_n;
+    }
+    t.row0 = (2 * w.tm + rank) * kBM;
+    t.a_row = a0 + t.row0;
+    t.sfa_rb = base_rb + 2 * w.tm + rank;
+    t.has_sfa = t.sfa_rb >= 0 && t.sfa_rb < nrb;
+    const int peer_rb = base_rb + 2 * w.tm + 1;
+    t.peer_has_sfa = peer_rb >= 0 && peer_rb < nrb;
+    t.b_row = b0 + w.tn * BN + rank * (BN / 2);
+    t.rb_b0 = (b0 + w.tn * BN) / 128;
+}
+
 // SK = true: the instantiation for stream-K plans (the epilogue publishes and
 // adds the cut tiles' segments); plans without cut tiles run the other form.
-template <int KIND, int BN, bool SK = false>
+// GROUPED = true: the grouped form (p.grouped = 1, non-swapped, BN = 256).
+template <int KIND, int BN, bool SK = false, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
                         const __grid_constant__ CUtensorMap map_sfb, const __grid_constant__ CUtensorMap map_sarm)
 {
-    using C = CfgPair<KIND, BN>;
+    using C = CfgPair<KIND, BN, GROUPED>;
     constexpr int S = C::kSlots;  // ring slots, two k-stages each
+    static_assert(!(SK && GROUPED), "the grouped form has no stream-K");
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_base_holder;
     __shared__ int abort_flag;
+    __shared__ GroupTable gtab;  // grouped form only
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -165,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The kernel that follows in the stream may be scheduled as SMs free up
     // (it waits for this grid before it touches memory).
     griddep_launch_dependents();
-    if (warp == 0 && !p.test_stall) {
+    if (!GROUPED && warp == 0 && !p.test_stall) {
         // Warm L2 with the first ring's worth of this CTA's operand boxes while
         // the preceding kernel drains: a prefetch is only a hint and L2 is where
         // that kernel's writes land, so no stale data can be read by it.
@@ -202,14 +253,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // preceding kernel (programmatic dependent launch); from here on global
     // memory it wrote may be read.
     griddep_wait();
+    // Grouped: one warp reads the offsets (written by the preceding kernel) into
+    // this CTA's group table; both CTAs of a pair build the same table.
+    if constexpr (GROUPED) {
+        if (warp == 2)
+            group_scan(p.group_offsets, p.groups, p.rows_total, 2 * kBM, (p.group_n + BN - 1) / BN, lane,
+                       gtab.tile_start, gtab.tok_rb, gtab.row0, gtab.rows);
+        __syncthreads();
+    }
     const uint32_t tmem = tmem_base_holder;
+    const GroupTable *gt = nullptr;  // grouped form only (a constant null pointer otherwise)
+    if constexpr (GROUPED)
+        gt = &gtab;
 
     // Work of this pair (tiles_m counts 256-row pair tiles): stream-K segments,
     // then whole tiles (or split-K slabs) round-robin over the clusters.
     const int first_unit = static_cast<int>(cluster_id_x());
     const int unit_step = static_cast<int>(cluster_count_x());
     const uint64_t lim = p.timeout_ns;
-    const int nrb_a = (p.rows_a + 127) / 128;
 
     // Slots and scale groups are aligned to absolute k-stage indices: slot =
     // k-stages (2j, 2j+1), scale group = k-stages [4g, 4g+4).  A work unit that
@@ -233,15 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sarmed = 0, sarmed_ph = 0;
             bool ok = true;
             WorkIter wi;
-            wi.init(p, first_unit, unit_step);
+            wi.init(p, first_unit, unit_step, gt, 2 * kBM);
             Work w;
             while (ok && wi.next(p, w)) {
-                const int tm = w.tm, tn = w.tn;
                 const int ks0 = w.ks0, ks1 = w.ks1;
-                const int rb_a = 2 * tm + static_cast<int>(rank);      // own 128-row block of the A role
-                const bool has_sfa = rb_a < nrb_a;
-                const bool peer_has_sfa = 2 * tm + 1 < nrb_a;
-                const int rb_b0 = (tn * BN) / 128;
+                PairGeom pg;
+                pair_geom<BN>(p, gt, w, static_cast<int>(rank), pg);
+                const int rb_a = pg.sfa_rb;  // own 128-row block of the A-role scales
+                const bool has_sfa = pg.has_sfa;
+                const bool peer_has_sfa = pg.peer_has_sfa;
+                const int rb_b0 = pg.rb_b0;
                 // bytes of both CTAs' copies, as counted by TMA (whole boxes; a box
                 // partly or wholly past the tensor is zero-filled and counted in full)
                 const uint32_t slot_bytes = 2 * C::kSlotBytes;
@@ -288,9 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t bar = map_to_cta(full_bar(st), 0);
                         if (leader)
                             mbar_arrive_expect_tx(full_bar(st), slot_bytes);
-                        tma_load_3d_pair_hint(sA + st * 2 * C::kABytes, &map_a, bar, 0, rb_a * kBM, kb, pol_a);
-                        tma_load_3d_pair_hint(sB + st * 2 * C::kBBytes, &map_b, bar, 0,
-                                              tn * BN + static_cast<int>(rank) * (BN / 2), kb, pol_b);
+                        tma_load_3d_pair_hint(sA + st * 2 * C::kABytes, &map_a, bar, 0, pg.a_row, kb, pol_a);
+                        tma_load_3d_pair_hint(sB + st * 2 * C::kBBytes, &map_b, bar, 0, pg.b_row, kb, pol_b);
                     }
                     __syncwarp();
                     armed |= 1u << st;
@@ -326,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.sa_fused && !p.test_stall) {
                 const uint64_t pol_a = p.stream_a ? l2_policy_evict_first() : l2_policy_evict_last();
                 WorkIter wi;
-                wi.init(p, first_unit, unit_step);
+                wi.init(p, first_unit, unit_step, gt, 2 * kBM);
                 Work w;
                 bool in_unit = false;
                 int kb = 0, kb0 = 0;
@@ -488,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         WorkIter wi;
-        wi.init(p, first_unit, unit_step);
+        wi.init(p, first_unit, unit_step, gt, 2 * kBM);
         Work w;
         bool have = wi.next(p, w);
         if (have && !first_group_in(w)) {
@@ -597,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __shared__ int sk_last;
         int it = 0;
         WorkIter wi;
-        wi.init(p, first_unit, unit_step);
+        wi.init(p, first_unit, unit_step, gt, 2 * kBM);
         Work w;
         for (; wi.next(p, w); ++it) {
             const int tm = w.tm, tn = w.tn;
@@ -638,18 +699,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
             }
+            // Output limits and origin (plain: the whole C; grouped: the group's rows)
+            int lim_i = p.rows_a, lim_j = p.rows_b;
+            long long out0 = 0;
+            if constexpr (GROUPED) {
+                PairGeom pg;
+                pair_geom<BN>(p, gt, w, static_cast<int>(rank), pg);
+                lim_i = pg.lim_i;
+                lim_j = pg.lim_j;
+                out0 = pg.out_base;
+            }
             const int i = row0 + q * 32 + lane;
-            if (i < p.rows_a) {
-                const long long base_off = (w.kind == 2 ? static_cast<long long>(w.slot) * p.split_stride : 0ll) +
+            if (i < lim_i) {
+                const long long base_off = out0 +
+                                           (w.kind == 2 ? static_cast<long long>(w.slot) * p.split_stride : 0ll) +
                                            static_cast<long long>(i) * p.stride_i;
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
                     const int j0 = tn * BN + h * kCols + c * 32;
-                    if (j0 >= p.rows_b) break;
-                    if (p.vec_ok && j0 + 32 <= p.rows_b)
+                    if (j0 >= lim_j) break;
+                    if (p.vec_ok && j0 + 32 <= lim_j)
                         store_row32_vec<true>(p, base_off + j0, r[c]);
                     else
-                        store_row32_masked(p, base_off, j0, min(32, p.rows_b - j0), r[c]);
+                        store_row32_masked(p, base_off, j0, min(32, lim_j - j0), r[c]);
                 }
             }
         }

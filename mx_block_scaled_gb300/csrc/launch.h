@@ -71,6 +71,17 @@ cudaError_t launch_gemm_pair_fp4(int bn, const GemmParams &p, const CUtensorMap 
 int gemm_pair_max_clusters_fp8(int bn);
 int gemm_pair_max_clusters_fp4(int bn);
 
+// Grouped GEMM on 256 x 256 CTA-pair tiles (p.grouped = 1, tokens in the A
+// role), on `clusters` clusters; its co-resident cluster count and pipeline facts.
+cudaError_t launch_gemm_grouped_pair_fp8(const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                         const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, int clusters,
+                                         cudaStream_t stream);
+cudaError_t launch_gemm_grouped_pair_fp4(const GemmParams &p, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                         const CUtensorMap &map_sfa, const CUtensorMap &map_sfb, int clusters,
+                                         cudaStream_t stream);
+int gemm_grouped_pair_max_clusters_fp8();
+int gemm_grouped_pair_max_clusters_fp4();
+
 // BF16 (kind::f16, no scales) GEMM: single-CTA tiles (bn 32..256) and CTA-pair
 // tiles (bn 128, 256; the scale maps are not read).
 cudaError_t launch_gemm_bf16(int bn, bool lean, const GemmParams &p, const CUtensorMap &map_a,
@@ -91,6 +102,8 @@ KernelInfo gemm_info_fp4(int bn, bool lean = false);
 KernelInfo gemm_pair_info_fp8(int bn);
 KernelInfo gemm_pair_info_fp4(int bn);
 KernelInfo gemm_info_bf16(int bn, bool lean = false);
+KernelInfo gemm_grouped_pair_info_fp8();
+KernelInfo gemm_grouped_pair_info_fp4();
 KernelInfo gemm_pair_info_bf16(int bn);
 
 }  // namespace mxg

@@ -58,16 +58,27 @@ struct Launchers {
         return cudaLaunchKernelEx(&cfg, mx_gemm_pair_kernel<KIND, BN>, p, ma, mb, msa, msb, msarm);
     }
 
+    // Grouped (mixture-of-experts) GEMM on 256 x 256 CTA-pair tiles (the
+    // tokens' 256-row tiles inside each group), on `clusters` clusters.
+    static cudaError_t grouped_pair(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
+                                    const CUtensorMap &msa, const CUtensorMap &msb, int clusters, cudaStream_t s)
+    {
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg =
+            launch_config(2 * clusters, kThreads, CfgPair<KIND, 256, true>::kSmemBytes, s, attr, 2);
+        return cudaLaunchKernelEx(&cfg, mx_gemm_pair_kernel<KIND, 256, false, true>, p, ma, mb, msa, msb, msa);
+    }
+
     // Co-resident clusters of two of the pair kernel (its work slots).
-    template <int BN>
+    template <int BN, bool GROUPED = false>
     static int pair_max_clusters()
     {
-        auto kern = mx_gemm_pair_kernel<KIND, BN>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgPair<KIND, BN>::kSmemBytes) !=
-            cudaSuccess)
+        auto kern = mx_gemm_pair_kernel<KIND, BN, false, GROUPED>;
+        constexpr int kSmem = CfgPair<KIND, BN, GROUPED>::kSmemBytes;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
             return 0;
         cudaLaunchAttribute attr[2];
-        cudaLaunchConfig_t cfg = launch_config(2, kThreads, CfgPair<KIND, BN>::kSmemBytes, nullptr, attr, 2, false);
+        cudaLaunchConfig_t cfg = launch_config(2, kThreads, kSmem, nullptr, attr, 2, false);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
             return 0;
@@ -106,6 +117,7 @@ struct Launchers {
         chk(opt_in(mx_gemm_pair_kernel<KIND, 256>, CfgPair<KIND, 256>::kSmemBytes));
         chk(opt_in(mx_gemm_pair_kernel<KIND, 256, true>, CfgPair<KIND, 256>::kSmemBytes));
         if constexpr (KIND != K_BF16) {
+            chk(opt_in(mx_gemm_pair_kernel<KIND, 256, false, true>, CfgPair<KIND, 256, true>::kSmemBytes));
             chk(opt_in(mx_gemm_kernel<KIND, 64, true>, Cfg<KIND, 64>::kSmemBytes));
             chk(opt_in(mx_gemm_kernel<KIND, 128, true>, Cfg<KIND, 128>::kSmemBytes));
             chk(opt_in(mx_gemm_kernel<KIND, 256, true>, Cfg<KIND, 256>::kSmemBytes));

@@ -371,10 +371,15 @@ struct mxgemm_grouped_plan {
     int num_sms;
     int device;
     int tok_sf_cap;      // 128-row blocks of the tokens' tile-layout scale region
+    int mode = 0;        // 1: 256 x 256 CTA-pair tiles (tokens in the A role, 256-row tiles per group)
+    int clusters = 0;    // pair mode: co-resident clusters of two (the grid)
     size_t off_tok_sf, off_w_sf, ws_bytes;
     const void *map_ptr_tok = nullptr;
     const void *map_ptr_w = nullptr;
     CUtensorMap map_tok, map_w;
+    // pair mode: 3-D operand maps (two k-stages a box) and the scale maps
+    const void *map_ptr_tok3 = nullptr, *map_ptr_w3 = nullptr, *map_ptr_sftok = nullptr, *map_ptr_sfw = nullptr;
+    CUtensorMap map_tok3, map_w3, map_sftok, map_sfw;
 };
 
 namespace {
@@ -1211,10 +1216,11 @@ int mxgemm_grouped_plan_create(mxgemm_grouped_plan_t *plan, int64_t groups, int6
     if ((fmt != MXGEMM_FMT_MXFP8_E4M3 && fmt != MXGEMM_FMT_MXFP4_E2M1) ||
         (out != MXGEMM_OUT_F32 && out != MXGEMM_OUT_BF16))
         return MXGEMM_ERR_ARG;
-    const uint32_t known =
-        MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_NOSWAP | MXGEMM_PLAN_FORCE_SWAP;
+    const uint32_t known = MXGEMM_PLAN_FORCE_BN128 | MXGEMM_PLAN_FORCE_BN256 | MXGEMM_PLAN_FORCE_NOSWAP |
+                           MXGEMM_PLAN_FORCE_SWAP | MXGEMM_PLAN_FORCE_PAIR | MXGEMM_PLAN_FORCE_SINGLE;
     if ((flags & ~known) != 0 || ((flags & MXGEMM_PLAN_FORCE_SWAP) && (flags & MXGEMM_PLAN_FORCE_NOSWAP)) ||
-        ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)))
+        ((flags & MXGEMM_PLAN_FORCE_BN128) && (flags & MXGEMM_PLAN_FORCE_BN256)) ||
+        ((flags & MXGEMM_PLAN_FORCE_PAIR) && (flags & MXGEMM_PLAN_FORCE_SINGLE)))
         return MXGEMM_ERR_ARG;
     if (groups < 1 || groups > mxg::kMaxGroups || rows < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0)
         return MXGEMM_ERR_SHAPE;
@@ -1248,6 +1254,20 @@ int mxgemm_grouped_plan_create(mxgemm_grouped_plan_t *plan, int64_t groups, int6
     int bn = swap ? std::min(std::max(pick_bn(avg), 64), 128) : (N >= 256 ? 256 : 128);
     if (flags & MXGEMM_PLAN_FORCE_BN128) bn = 128;
     if (flags & MXGEMM_PLAN_FORCE_BN256) bn = 256;
+    // Prefill-sized groups (>= 512 tokens on average) run 256 x 256 CTA-pair
+    // tiles: half the B-role operand bytes per FLOP of a 128 x 256 tile.
+    int mode = (!swap && avg >= 512) ? 1 : 0;
+    if (flags & MXGEMM_PLAN_FORCE_PAIR) mode = 1;
+    if (flags & (MXGEMM_PLAN_FORCE_SINGLE | MXGEMM_PLAN_FORCE_BN128)) mode = 0;
+    if (swap || N < 256 || (fmt == MXGEMM_FMT_MXFP4_E2M1 && K % 256 != 0)) mode = 0;
+    if (mode == 1) {
+        bn = 256;
+        p->clusters = fmt == MXGEMM_FMT_MXFP4_E2M1 ? mxg::gemm_grouped_pair_max_clusters_fp4()
+                                                   : mxg::gemm_grouped_pair_max_clusters_fp8();
+        if (p->clusters < 1)
+            mode = 0;
+    }
+    p->mode = mode;
     p->bn = bn;
     p->kstages = static_cast<int>(fmt == MXGEMM_FMT_MXFP4_E2M1 ? ceil_div(K, 256) : K / 128);
     p->tok_sf_cap = static_cast<int>(ceil_div(rows, 128) + groups);
@@ -1271,13 +1291,16 @@ int mxgemm_grouped_plan_describe(mxgemm_grouped_plan_t plan, char *buf, size_t l
     if (!plan || !buf || len == 0)
         return MXGEMM_ERR_ARG;
     const bool fp4 = plan->fmt == MXGEMM_FMT_MXFP4_E2M1;
-    mxg::KernelInfo ki = fp4 ? mxg::gemm_info_fp4(plan->bn) : mxg::gemm_info_fp8(plan->bn);
+    const bool pair = plan->mode == 1;
+    mxg::KernelInfo ki = pair ? (fp4 ? mxg::gemm_grouped_pair_info_fp4() : mxg::gemm_grouped_pair_info_fp8())
+                              : (fp4 ? mxg::gemm_info_fp4(plan->bn) : mxg::gemm_info_fp8(plan->bn));
     snprintf(buf, len,
-             "grouped fmt=%s out=%s groups=%lld rows=%lld N=%lld K=%lld tile=128x%d swap_ab=%d kstages=%d grid=%d "
-             "stages=%d acc_stages=%d smem=%d",
+             "grouped fmt=%s out=%s groups=%lld rows=%lld N=%lld K=%lld tile=%dx%d mode=%s swap_ab=%d kstages=%d "
+             "grid=%d%s stages=%d acc_stages=%d smem=%d",
              fp4 ? "mxfp4" : "mxfp8", plan->out == MXGEMM_OUT_BF16 ? "bf16" : "f32", static_cast<long long>(plan->G),
              static_cast<long long>(plan->T), static_cast<long long>(plan->N), static_cast<long long>(plan->K),
-             plan->bn, plan->swap, plan->kstages, plan->num_sms, ki.stages, ki.acc_stages, ki.smem_bytes);
+             pair ? 256 : 128, plan->bn, pair ? "pair" : "single", plan->swap, plan->kstages,
+             pair ? plan->clusters : plan->num_sms, pair ? "x2" : "", ki.stages, ki.acc_stages, ki.smem_bytes);
     return MXGEMM_OK;
 }
 
@@ -1373,9 +1396,43 @@ int mxgemm_grouped_run(mxgemm_grouped_plan_t plan, const int64_t *group_offsets,
     p.rows_total = static_cast<int>(T);
     p.tok_sf_cap = plan->tok_sf_cap;
     p.group_offsets = offs;
+    p.dbg_out_elems = static_cast<long long>(T) * N;
+    if (plan->mode == 1) {
+        // CTA-pair tiles: 3-D operand maps (two 128-byte K-slices a box; 128
+        // token rows, 128 weight rows a box) and 3-D maps of both scale regions
+        const int ktps = fp4 ? 2 : 1;
+        if (plan->map_ptr_tok3 != A) {
+            if (encode_operand_map_2stage(&plan->map_tok3, A, T, row_bytes, 128) != MXGEMM_OK)
+                return MXGEMM_ERR_CUDA;
+            plan->map_ptr_tok3 = A;
+        }
+        if (plan->map_ptr_w3 != B) {
+            if (encode_operand_map_2stage(&plan->map_w3, B, G * N, row_bytes, 128) != MXGEMM_OK)
+                return MXGEMM_ERR_CUDA;
+            plan->map_ptr_w3 = B;
+        }
+        if (plan->map_ptr_sftok != tok_sf) {
+            if (encode_sf_map(&plan->map_sftok, tok_sf, static_cast<int64_t>(plan->tok_sf_cap) * 128, K, ktps, 1) !=
+                MXGEMM_OK)
+                return MXGEMM_ERR_CUDA;
+            plan->map_ptr_sftok = tok_sf;
+        }
+        if (plan->map_ptr_sfw != w_sf) {
+            if (encode_sf_map(&plan->map_sfw, w_sf, G * N, K, ktps, 2) != MXGEMM_OK)
+                return MXGEMM_ERR_CUDA;
+            plan->map_ptr_sfw = w_sf;
+        }
+        p.stream_a = 0;
+        p.stream_b = stream_w ? 1 : 0;
+        const cudaError_t e =
+            fp4 ? mxg::launch_gemm_grouped_pair_fp4(p, plan->map_tok3, plan->map_w3, plan->map_sftok, plan->map_sfw,
+                                                    plan->clusters, s)
+                : mxg::launch_gemm_grouped_pair_fp8(p, plan->map_tok3, plan->map_w3, plan->map_sftok, plan->map_sfw,
+                                                    plan->clusters, s);
+        return e == cudaSuccess ? debug_finish(s) : MXGEMM_ERR_CUDA;
+    }
     const CUtensorMap &ma = plan->swap ? plan->map_w : plan->map_tok;
     const CUtensorMap &mb = plan->swap ? plan->map_tok : plan->map_w;
-    p.dbg_out_elems = static_cast<long long>(T) * N;
     const cudaError_t e = fp4 ? mxg::launch_gemm_grouped_fp4(plan->bn, p, ma, mb, plan->num_sms, s)
                               : mxg::launch_gemm_grouped_fp8(plan->bn, p, ma, mb, plan->num_sms, s);
     return e == cudaSuccess ? debug_finish(s) : MXGEMM_ERR_CUDA;

@@ -140,7 +140,8 @@ def test_quantize_validates_before_touching_the_device(lib, fmt, in_dtype, x, ro
     (4, 64, 128, 96, 1, 2, 0, -2),         # K not a multiple of 128
     (4, 64, 128, 128, 3, 2, 0, -1),        # unknown format
     (4, 64, 128, 128, 1, 9, 0, -1),        # unknown output type
-    (4, 64, 128, 128, 1, 2, 1 << 4, -1),   # CTA-pair tiles are not offered for grouped GEMMs
+    (4, 64, 128, 128, 1, 2, (1 << 4) | (1 << 5), -1),  # pair and single tiles at once
+    (4, 64, 128, 128, 1, 2, 1 << 7, -1),   # stream-K is not offered for grouped GEMMs
     (4, 64, 128, 128, 1, 2, (1 << 2) | (1 << 3), -1),
 ])
 def test_grouped_plan_validates_before_touching_the_device(lib, groups, rows, N, K, fmt, out, flags, expect):

@@ -88,6 +88,11 @@ CASES = [
     (FMT_MXFP4, 64, 2048, 4096, SK, "swap_ab=1"),
     (FMT_BF16, 264, 392, 512, 0, "fmt=bf16"),
     (FMT_BF16, 300, 768, 1024, PAIR, "mode=pair"),
+    (FMT_MXFP8, 256, 1000, 1536, 1 << 17, "tile=256x192"),
+    (FMT_MXFP4, 300, 2000, 2048, 1 << 17, "tile=256x192"),
+    (FMT_MXFP8, 100, 1000, 8192, 0, "swap_ab=1"),
+    (FMT_MXFP8, 8, 10240, 2048, 0, " lean"),
+    (FMT_MXFP4, 8, 1280, 16384, 0, " lean"),
 ]
 
 

@@ -17,7 +17,7 @@ from test_gemm_gpu import small_int_codes
 
 pytestmark = pytest.mark.gpu
 
-BN128, BN256, NOSWAP, SWAP = 1 << 0, 1 << 1, 1 << 2, 1 << 3
+BN128, BN256, NOSWAP, SWAP, PAIR = 1 << 0, 1 << 1, 1 << 2, 1 << 3, 1 << 4
 FMTS = [FMT_MXFP8, FMT_MXFP4]
 
 
@@ -71,7 +71,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("flags", [0, SWAP, NOSWAP, NOSWAP | BN128, SWAP | BN128, SWAP | BN256])
+@pytest.mark.parametrize("flags", [0, SWAP, NOSWAP, NOSWAP | BN128, SWAP | BN128, SWAP | BN256, PAIR])
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_grouped_exact(oracle_mod, fmt, flags, case):
     sizes, N, K, lead, trail = CASES[case]
@@ -202,3 +202,31 @@ def test_moe_workloads_full_size_sampled(oracle_mod, case):
     rows = np.array(sorted(rows), dtype=np.int64)
     ref, S = oracle_mod.grouped_gemm(fmt, offsets, A, SA, B, SB, N, K, rows=rows)
     assert_within(C[rows], ref, S, OUT_BF16, f"{name} {fmt_name} {desc}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("sizes,N,K,lead,trail", [([700, 1200, 0, 900], 512, 512, 0, 0),
+                                                   ([513, 1, 256, 1030], 384, 1024, 5, 3),
+                                                   ([2048], 256, 256, 0, 0)])
+def test_grouped_pair_tiles_exact(oracle_mod, fmt, sizes, N, K, lead, trail):
+    """Prefill-sized groups (>= 512 tokens on average, or forced) run 256 x 256
+    CTA-pair tiles: token tiles of 256 rows inside each group (the odd CTA's rows
+    may run past the group's end into the next group, and the last weight tile
+    of a group of 384 rows into the next group's weights), exact against the
+    oracle; rows outside every group untouched."""
+    offsets = list(lead + group_offsets(sizes))
+    T = offsets[-1] + trail
+    G = len(sizes)
+    rng = np.random.default_rng([sum(sizes), N, K, fmt])
+    A, SA = small_int_codes(rng, T, K, fmt)
+    B, SB = small_int_codes(rng, G * N, K, fmt)
+    ref, _ = oracle_mod.grouped_gemm(fmt, offsets, A, SA, B, SB, N, K)
+    inside = _in_groups(offsets, T)
+    for out, flags in ((OUT_F32, PAIR), (OUT_BF16, 0)):
+        C, desc = _run(fmt, offsets, A, SA, B, SB, N, K, out, flags)
+        if flags == PAIR or sum(sizes) // G >= 512:
+            assert "mode=pair" in desc, desc
+        expect = ref if out == OUT_F32 else _bf16(ref)
+        assert (C[inside] == expect[inside]).all(), desc
+        assert np.isnan(C[~inside]).all(), f"rows outside every group were written: {desc}"
+
