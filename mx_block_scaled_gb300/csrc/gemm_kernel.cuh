@@ -111,10 +111,11 @@ struct GemmParams {
     long long sk_stages;      // (tiles - dp_tiles) * kstages
     int *sk_counters;         // one arrival counter per stream-K tile and 128-row share, zero at launch
     float *sk_partials;       // two 128 x BN FP32 slots per stream-K CTA (per CTA of a pair)
-    // Grouped (mixture-of-experts) GEMM, single-CTA kernel only: group e owns the
-    // token rows [off[e], off[e+1]) of A and C and the weight rows
-    // [e*group_n, (e+1)*group_n) of B.  Offsets are read on the device and
-    // sanitised (clamped to [0, rows_total], end >= start) before use.
+    // Grouped (mixture-of-experts) GEMM (single-CTA kernel, or the pair kernel
+    // with the tokens in the A role): group e owns the token rows
+    // [off[e], off[e+1]) of A and C and the weight rows [e*group_n,
+    // (e+1)*group_n) of B.  Offsets are read on the device and sanitised
+    // (clamped to [0, rows_total], end >= start) before use.
     int grouped;              // 0: plain GEMM
     int groups;               // G <= kMaxGroups
     int tok_b;                // 1: the tokens are the B role (swap-AB), 0: the A role
