@@ -120,3 +120,51 @@ def test_bounds_check_skips_and_reports_an_out_of_range_store(dbg, oracle_mod, f
     assert (C[: M - 1] == ref[: M - 1]).all(), desc
     assert dbg.mxgemm_device_status(None, 1) == -9  # sticky until cleared
     assert dbg.mxgemm_device_status(None, 1) == 0
+
+
+SWAP = 1 << 3
+GROUPED_CASES = [
+    # (fmt, group sizes, N, K, leading gap rows, plan flags, expected plan text)
+    (FMT_MXFP8, [0, 1, 127, 128, 129, 300], 384, 512, 3, 0, "mode=single"),
+    (FMT_MXFP8, [5, 0, 33, 0, 200], 128, 1024, 7, SWAP, "swap_ab=1"),
+    (FMT_MXFP8, [300, 0, 600, 37], 256, 1024, 0, PAIR, "mode=pair"),
+    (FMT_MXFP4, [300, 0, 600, 37], 512, 1024, 5, PAIR, "mode=pair"),
+]
+
+
+@pytest.mark.parametrize("fmt,sizes,N,K,lead,flags,expect", GROUPED_CASES)
+def test_debug_build_grouped_runs_clean(dbg, oracle_mod, fmt, sizes, N, K, lead, flags, expect):
+    """The grouped GEMM (single-CTA, swap-AB and CTA-pair tiles) in the debug
+    build: no bounds check fires, every row inside a group equals the oracle's
+    grouped product, and rows outside every group keep their NaN fill."""
+    import torch
+    from mx_block_scaled_gb300.inputs import group_offsets
+    offsets = [lead + int(o) for o in group_offsets(sizes)]
+    T, G = offsets[-1] + 4, len(sizes)
+    rng = np.random.default_rng([fmt, T, N, K])
+    A, SA = small_int_codes(rng, T, K, fmt)
+    B, SB = small_int_codes(rng, G * N, K, fmt)
+    ref, _ = oracle_mod.grouped_gemm(fmt, offsets, A, SA, B, SB, N, K)
+    h = ctypes.c_void_p()
+    assert dbg.mxgemm_grouped_plan_create(ctypes.byref(h), G, T, N, K, fmt, OUT_F32, flags) == 0
+    buf = ctypes.create_string_buffer(512)
+    dbg.mxgemm_grouped_plan_describe(h, buf, 512)
+    desc = buf.value.decode()
+    ws_bytes = dbg.mxgemm_grouped_workspace_bytes(h)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    d_off = torch.tensor(np.asarray(offsets, dtype=np.int64), device="cuda")
+    dA, dSA, dB, dSB = to_dev(A), to_dev(SA), to_dev(B), to_dev(SB)
+    C = torch.full((T, N), float("nan"), dtype=torch.float32, device="cuda")
+    st = dbg.mxgemm_grouped_run(h, d_off.data_ptr(), dA.data_ptr(), dSA.data_ptr(), dB.data_ptr(), dSB.data_ptr(),
+                                C.data_ptr(), ws.data_ptr(), ws_bytes, 0, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    dbg.mxgemm_grouped_plan_destroy(h)
+    assert expect in desc, desc
+    assert st == 0, (st, desc)
+    got = C.double().cpu().numpy()
+    inside = np.zeros(T, bool)
+    for e in range(G):
+        inside[offsets[e]:offsets[e + 1]] = True
+    assert (got[inside] == ref[inside]).all(), desc
+    assert np.isnan(got[~inside]).all(), desc
+    assert dbg.mxgemm_device_status(None, 1) == 0
