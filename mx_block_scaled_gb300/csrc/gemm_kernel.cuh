@@ -339,8 +339,8 @@ struct WorkIter {
         w.tn = p.tok_b ? tok_i : w_i;
     }
 
-    // Stream-K segments come first, so that the fixup of a cut tile (run by the
-    // fixup warps of its last CTA) overlaps the whole tiles computed after it.
+    // Stream-K segments come first, so that the fixup of a cut tile (run by its
+    // last CTA's epilogue or fixup warps) overlaps the whole tiles computed after it.
     __device__ bool next(const GemmParams &p, Work &w)
     {
         if (pos < end) {

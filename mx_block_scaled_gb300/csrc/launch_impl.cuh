@@ -17,7 +17,8 @@ namespace mxg {
 template <int KIND>
 struct Launchers {
     // Single-CTA 128 x BN tiles; plans with stream-K segments run the
-    // instantiation with the two fixup warps (the lean form adds them in its
+    // instantiation with the two fixup warps, which add the segments of 128-
+    // and 256-wide tiles (narrower tiles and the lean form add them in their
     // epilogue warps).
     template <int BN, bool LEAN = false>
     static cudaError_t single(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int grid, cudaStream_t s)

@@ -703,7 +703,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         // every SM should stream an equal share of the weight from the start,
         // so the k-stages of the tiles past the full waves are spread evenly
         // over all SMs; the cut tiles' partial sums are small (128 x BN FP32)
-        // and are added by the fixup warps of the last CTA to arrive, which
+        // and are added by the epilogue warps of the last CTA to arrive, which
         // replaces the separate split-K reduce launch.
         const bool decode = swap && mode == 0 && p->bn <= 64;
         // By default decode takes stream-K where its fixed cost (the fixup of
@@ -725,7 +725,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
             const int64_t min_seg = 4;  // k-stages per stream-K unit, at least
             // Long k-loops spread the cut tiles' stages over every slot.  Short
             // ones cut each tile in at most two segments, so that the fixup adds
-            // two partial sums (the fixup warps' fast path) and stays short.
+            // two partial sums (one batch of loads) and stays short.
             const bool spread_units = (flags & MXGEMM_PLAN_STREAMK) ? (p->kstages >= 96 || decode) : (spread || decode);
             const int64_t units = spread_units ? std::min<int64_t>(G, sk_stages / min_seg)
                                                : std::min<int64_t>(G, 2 * (tiles - dp));
