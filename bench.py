@@ -77,7 +77,7 @@ def slowest_rank_ms(ms: float, ws: int, device) -> float:
 
 def versions() -> dict:
     """Library, CUDA, driver, PyTorch and numpy versions of the run and the hash of the
-    kernel sources (recorded beside the plan; the GPU machine gets no git history)."""
+    kernel sources (recorded beside the plan; a copy of the sources may carry no git history)."""
     import numpy
     import torch
     out = {"torch": torch.__version__, "numpy": numpy.__version__, "cuda_runtime": torch.version.cuda,
