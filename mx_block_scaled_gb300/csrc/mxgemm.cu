@@ -652,6 +652,14 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
     // 256-row tiles (pair).
     p->tiles_m = static_cast<int>(mode == 0 ? ceil_div(rows_a, 128) : ceil_div(rows_a, 256));
     p->tiles_n = static_cast<int>(ceil_div(rows_b, bn));
+    // The MMA reads a B-role tile's scales from TMEM column (tn*BN % 128) / 32 of
+    // its scale chunk, which must be even: a 32-wide tile other than the first
+    // would start at an odd column (a misaligned-address fault).  BN = 32 is
+    // picked only for at most 32 B-role rows; refuse anything else outright.
+    if (bn == 32 && p->tiles_n > 1) {
+        delete p;
+        return MXGEMM_ERR_UNSUPPORTED;
+    }
     p->kstages = static_cast<int>(fmt == MXGEMM_FMT_MXFP4_E2M1 ? ceil_div(K, 256) : bf16 ? K / 64 : K / 128);
 
     // Concurrent work units: SMs, or co-resident clusters of two.
