@@ -50,7 +50,8 @@ NOMINAL_PF = {"bf16": 2.25, "mxfp8": 4.5, "mxfp4": 13.5}
 # the GEMM kernels and the host code that plans them (tile, stream-K split)
 KERNEL_SOURCES = ["mx_block_scaled_gb300/csrc/gemm_kernel.cuh", "mx_block_scaled_gb300/csrc/ptx.cuh",
                   "mx_block_scaled_gb300/csrc/gemm_fp8.cu", "mx_block_scaled_gb300/csrc/gemm_fp4.cu",
-                  "mx_block_scaled_gb300/csrc/gemm_kernel_pair.cuh", "mx_block_scaled_gb300/csrc/mxgemm.cu"]
+                  "mx_block_scaled_gb300/csrc/gemm_kernel_pair.cuh", "mx_block_scaled_gb300/csrc/mxgemm.cu",
+                  "mx_block_scaled_gb300/csrc/launch_impl.cuh", "mx_block_scaled_gb300/csrc/launch.h"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
 
