@@ -17,7 +17,7 @@
  *    MXFP4 scaled GEMMs are timed from already-quantised inputs; quantisation,
  *    compilation and initial tuning are outside the measurement.
  *  - AI-compiler daily digest of 2026-10-22, item 1 (FlyDSL): the scaled GEMMs
- *    are "BlockWise1x32, E8M0 scale, FP32 accumulation".
+ *    scale blocks of 1 x 32 values with E8M0 scales and accumulate in FP32.
  *  - Element encodings (not printed on the pages; OCP MX): MXFP8 elements are
  *    E4M3 (bias 7, max 448, 0x7F/0xFF NaN), MXFP4 elements are E2M1 packed two
  *    per byte (element 2i in the low nibble), E8M0 is 2^(code-127) with 0xFF NaN.
@@ -264,8 +264,8 @@ MXGEMM_API int mxgemm_run(mxgemm_plan_t plan, const void *A, const uint8_t *SA,
  * not read and may be NULL -- except SA for a plan that lays it out inside the
  * GEMM ("sa=in-kernel" in its description): mxgemm_prepare leaves SA alone
  * and mxgemm_run reads it.  Lets a caller time
- * or schedule the two steps separately (the FlyDSL page's "layout copies" are
- * step (1)).  Nothing else may use the workspace in between.
+ * or schedule the two steps separately (the extra layout copies the FlyDSL page
+ * warns about are step (1)).  Nothing else may use the workspace in between.
  *   SA, SB:  row-major scales as for mxgemm_run (pre-laid-out ones not read;
  *            all ignored for MXGEMM_FMT_BF16)
  * Errors: MXGEMM_ERR_ARG (NULL plan, unknown flag, missing scales, another

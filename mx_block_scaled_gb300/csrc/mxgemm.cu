@@ -601,7 +601,7 @@ int mxgemm_plan_create(mxgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int
         delete p;
         return MXGEMM_ERR_UNSUPPORTED;
     }
-    // The activation scales' relayout (the FlyDSL page's "layout copy") runs
+    // The activation scales' relayout (the FlyDSL page's extra layout copy) runs
     // inside the MXFP8 pair kernel when their row pitch K/32 allows 16-byte TMA
     // rows.
     p->sa_fuse = (mode == 1 && fmt == MXGEMM_FMT_MXFP8_E4M3 && !swap && K % 512 == 0) ? 1 : 0;

@@ -18,7 +18,7 @@
  *    "API compatibility is not universal input coverage": MXFP scaled GEMM takes
  *    one E8M0 scale per 32 values along K, and K divisible by 128.
  *  - AI-compiler daily digest of 2026-10-22, item 1 (FlyDSL): MXFP8/MXFP4 scaled
- *    GEMM is "BlockWise1x32, E8M0 scale, FP32 accumulation".
+ *    GEMM uses scale blocks of 1 x 32 values, E8M0 scales and FP32 accumulation.
  *  - Same digest, item 2 ("Deciding Scale Placement in MXFP4 Dot Products"):
  *    applying the scale before or after the dot product can round differently.
  *    This oracle evaluates each 32-block's inner sum exactly (see below), so both
